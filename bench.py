@@ -1,0 +1,494 @@
+"""Benchmark of the GDP prefill hot path on GB300 (one JSON line on rank 0).
+
+A step is one pass of the prefill path over the bf16 prefill workload
+(B=2, T=4096, H=HV=16, K=V=128, M=2, chunk 64): gdp_prefill_prepare on the
+post-conv activations (G=H: one key/query group per head) followed by
+gdp_chunk_fwd with the in-kernel L2 norm of q and k, producing o [B,T,HV,V]
+fp32 and the final state. Inputs are synthetic (seeded N(0,1) activations,
+the pages' gate-input distributions) and resident in HBM before the timed
+region; L2 is flushed (a 256 MiB write) before every timed step.
+
+value = expanded tokens (B*T*M) per second over all ranks; e2e = the same
+through the C ABI with the step's inputs copied from pinned host memory and
+o copied back inside the timed region. roofline = the dominant kernel's
+achieved bandwidth (or flop rate) against the measured peak. Per-kernel times
+come from CUDA events recorded on the launching stream (the library's
+stage-event hook). Multi-GPU: each rank runs its own copy of the workload, no
+collective on the data path (weak scaling).
+
+--impl reference times the CPU oracle (the plain fp64 walk that the tests use
+as ground truth) on a bounded sample per step of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "GDP prefill tokens/sec (T·M) and % of bf16 TC peak; prepare GB/s vs HBM"
+WORKLOAD = dict(B=2, T=4096, H=16, HV=16, G=16, K=128, V=128, M=2, BT=64)
+DECODE = dict(n=256, S=4, M=2, H=32, G=8, P=128, N=128)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------------
+# algorithmic work (per step), stated in the design doc
+# ----------------------------------------------------------------------------------
+
+def algorithmic(w=WORKLOAD):
+    B, T, H, HV, G, K, V, M, BT = (w[k] for k in ("B", "T", "H", "HV", "G", "K", "V", "M", "BT"))
+    E = B * T * M  # expanded tokens
+    D = M * H * V + M * G * K + G * K
+    prep_bytes = (B * T * D * 2 + B * T * (M * H + H) * 2          # x, ba read
+                  + B * T * H * K * 2 + E * H * K * 2 + E * H * V * 2  # q, k, v written
+                  + E * H * 4 + B * T * H * 4)                       # beta, g written
+    # chunked forward, fused floor: read q, k, v (bf16), beta, g; write o, final state (fp32)
+    chunk_bytes = (B * T * H * K * 2 + E * H * K * 2 + E * HV * V * 2 + E * HV * 4
+                   + B * T * HV * 4 + B * T * HV * V * 4 + B * HV * K * V * 4)
+    per_tok = (2 * BT * (2 * K + V) + 4 * K * V + 2 * BT * (K + V) + 2 * K * V / M)
+    flops = {
+        "wy": E * HV * 2 * BT * (2 * K + V),
+        "h": E * HV * 4 * K * V,
+        "o": E * HV * (2 * BT * (K + V) + 2 * K * V / M),
+    }
+    flops["chunk"] = E * HV * per_tok
+    return {"E": E, "prepare_bytes": prep_bytes, "chunk_bytes": chunk_bytes, "flops": flops}
+
+
+# ----------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------
+
+def make_inputs(dev, seed=0):
+    import synth_inputs as si
+    w = WORKLOAD
+    d = si.prepare_inputs(w["B"], w["T"], w["M"], w["H"], w["G"], w["V"], w["K"], seed=seed)
+    return d
+
+
+class Prefill:
+    """Buffers and one step of the prefill path, all on `dev`."""
+
+    def __init__(self, gdp, d, dev):
+        w = WORKLOAD
+        self.gdp = gdp
+        B, T, H, G, K, V, M = w["B"], w["T"], w["H"], w["G"], w["K"], w["V"], w["M"]
+        self.x = d["x"].to(dev)
+        self.ba = d["ba"].to(dev)
+        self.A_log = d["A_log"].to(dev)
+        self.dt_bias = d["dt_bias"].to(dev)
+        bf = torch.bfloat16
+        self.pre = (torch.empty(B, T, H, K, dtype=bf, device=dev),
+                    torch.empty(B, T * M, H, K, dtype=bf, device=dev),
+                    torch.empty(B, T * M, H, V, dtype=bf, device=dev),
+                    torch.empty(B, T * M, H, dtype=torch.float32, device=dev),
+                    torch.empty(B, T, H, dtype=torch.float32, device=dev))
+        self.o = torch.empty(B, T, H, V, dtype=torch.float32, device=dev)
+        self.fs = torch.empty(B, H, K, V, dtype=torch.float32, device=dev)
+        need = gdp.gdp_chunk_fwd_workspace_size(B, T, B, H, H, K, V, M, w["BT"], bf)
+        self.ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.path = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, H, K, V, M, w["BT"], bf)[5]
+
+    def step(self, ev_prep=None):
+        w = WORKLOAD
+        if ev_prep is not None:
+            ev_prep[0].record()
+        self.gdp.gdp_prefill_prepare(self.x, self.ba, self.A_log, self.dt_bias, w["M"], w["H"],
+                                     w["G"], w["V"], w["K"], out=self.pre)
+        if ev_prep is not None:
+            ev_prep[1].record()
+        q, k, v, beta, g = self.pre
+        self.gdp.gdp_chunk_fwd(q, k, v, beta, g, chunk_size=w["BT"], num_householder=w["M"],
+                               use_qk_l2norm=True, workspace=self.ws, out=(self.o, self.fs))
+
+
+def launches_per_step(path: int) -> int:
+    # prepare + tables + chunk kernels (generic: wy, h, o; tensor-core path: see the design doc)
+    return 1 + 1 + (3 if path == 0 else 3)
+
+
+def run_ours(args, rank, world, dev):
+    import linear_attention_ssm_gdp_gb300 as gdp
+    gdp.load()
+    pk, pk_src = peaks()
+    alg = algorithmic()
+    d = make_inputs(dev)
+    pf = Prefill(gdp, d, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(gdp.GDP_STAGE_EVENTS)]
+    prep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    gdp.gdp_set_stage_events(stage)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        pf.step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device() if dev.index is None else dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    times = {"step": [], "prepare": [], "tables": [], "wy": [], "h": [], "o": []}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        step_ev[0].record()
+        pf.step(prep_ev)
+        step_ev[1].record()
+        torch.cuda.synchronize()
+        times["step"].append(step_ev[0].elapsed_time(step_ev[1]))
+        times["prepare"].append(prep_ev[0].elapsed_time(prep_ev[1]))
+        times["tables"].append(stage[0].elapsed_time(stage[1]))
+        times["wy"].append(stage[1].elapsed_time(stage[2]))
+        times["h"].append(stage[2].elapsed_time(stage[3]))
+        times["o"].append(stage[3].elapsed_time(stage[4]))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    # keep the GPU busy a little longer so the sampler sees load, then stop
+    extra_t0 = time.time()
+    while time.time() - extra_t0 < 0.5:
+        pf.step()
+    torch.cuda.synchronize()
+    sampler.stop()
+    gdp.gdp_set_stage_events(None)
+
+    ms = statistics.mean(times["step"])
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    units = alg["E"] * world
+    value = units / (ms * 1e-3)
+
+    # per-kernel rooflines
+    kern = {}
+    hbm = pk["hbm_gbs"]
+    tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    prep_ms = statistics.mean(times["prepare"])
+    kern["prepare"] = {"ms": prep_ms, "bound": "hbm",
+                       "GBps": alg["prepare_bytes"] / (prep_ms * 1e-3) / 1e9}
+    kern["prepare"]["frac"] = kern["prepare"]["GBps"] / hbm
+    for name in ("wy", "h", "o"):
+        kms = statistics.mean(times[name])
+        tf = alg["flops"][name] / (kms * 1e-3) / 1e12
+        kern[name] = {"ms": kms, "bound": "tensor", "TFLOPs": tf, "frac": tf / tc}
+    kern["tables"] = {"ms": statistics.mean(times["tables"])}
+    chunk_ms = sum(kern[n]["ms"] for n in ("tables", "wy", "h", "o"))
+    chunk_tf = alg["flops"]["chunk"] / (chunk_ms * 1e-3) / 1e12
+    chunk_gbs = alg["chunk_bytes"] / (chunk_ms * 1e-3) / 1e9
+    dominant = max(("prepare", "wy", "h", "o"), key=lambda n: kern[n]["ms"])
+    dk = kern[dominant]
+    if dk["bound"] == "hbm":
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": dk["GBps"], "peak": hbm,
+                "unit": "GB/s", "frac": dk["frac"],
+                "traffic": None, "peak_source": pk_src}
+    else:
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": dk["TFLOPs"], "peak": tc,
+                "unit": "TFLOP/s", "frac": dk["frac"], "traffic": None,
+                "peak_source": pk_src + " (sustained bf16)"}
+    roof["traffic"] = args.traffic
+
+    e2e = run_e2e(args, gdp, d, dev, pf)
+    decode = run_decode(args, gdp, dev, pk)
+    clocks = sampler.summary()
+    w = WORKLOAD
+    line = {
+        "metric": METRIC, "value": value, "unit": "expanded tokens/s (B*T*M)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations and gate inputs)",
+        "config": {"workload": "prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64 "
+                               "(prepare + chunk_fwd, G=16, in-kernel qk L2 norm)",
+                   "B": w["B"], "T": w["T"], "H": w["H"], "HV": w["HV"], "G": w["G"],
+                   "K": w["K"], "V": w["V"], "M": w["M"], "chunk_size": w["BT"],
+                   "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "chunk_path": "tensor-core" if pf.path == 1 else "generic"},
+        "roofline": roof,
+        "chunk": {"ms": chunk_ms, "TFLOPs": chunk_tf, "tc_frac": chunk_tf / tc,
+                  "GBps_fused_floor": chunk_gbs, "hbm_frac": chunk_gbs / hbm},
+        "prepare": {"ms": prep_ms, "GBps": kern["prepare"]["GBps"],
+                    "hbm_frac": kern["prepare"]["frac"]},
+        "kernels": kern,
+        "decode": decode,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(pf.path) * args.steps,
+        "clocks": clocks,
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tc, "source": pk_src},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, max_seconds=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, gdp, d, dev, pf):
+    """Same step through the C ABI with host buffers: H2D of x and ba from pinned
+    memory, the two calls, D2H of o and the final state, all inside the timing."""
+    w = WORKLOAD
+    hx = d["x"].pin_memory()
+    hba = d["ba"].pin_memory()
+    ho = torch.empty(pf.o.shape, dtype=torch.float32).pin_memory()
+    hfs = torch.empty(pf.fs.shape, dtype=torch.float32).pin_memory()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def one():
+        pf.x.copy_(hx, non_blocking=True)
+        pf.ba.copy_(hba, non_blocking=True)
+        pf.step()
+        ho.copy_(pf.o, non_blocking=True)
+        hfs.copy_(pf.fs, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    ts = []
+    for _ in range(n):
+        ev[0].record()
+        one()
+        ev[1].record()
+        torch.cuda.synchronize()
+        ts.append(ev[0].elapsed_time(ev[1]))
+    ms = statistics.mean(ts)
+    bi = hx.numel() * hx.element_size() + hba.numel() * hba.element_size()
+    bo = ho.numel() * 4 + hfs.numel() * 4
+    return {"value": WORKLOAD["B"] * WORKLOAD["T"] * WORKLOAD["M"] / (ms * 1e-3),
+            "unit": "expanded tokens/s (B*T*M)", "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def run_decode(args, gdp, dev, pk):
+    """Decode step (prepare + recurrent update), n=256 S=4 M=2 H=32 G=8 P=N=128."""
+    import synth_inputs as si
+    w = DECODE
+    n, S, M, H, G, P, N = w["n"], w["S"], w["M"], w["H"], w["G"], w["P"], w["N"]
+    d = si.prepare_inputs(n, S, M, H, G, P, N, seed=1)
+    x, ba = d["x"].to(dev), d["ba"].to(dev)
+    A_log, dt_bias = d["A_log"].to(dev), d["dt_bias"].to(dev)
+    state = si.decode_state(n, H, N, P).to(dev)
+    outs = gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N)
+    o = torch.empty(n, S * M, H, P, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(3):
+        gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
+        gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True, out=o)
+    torch.cuda.synchronize()
+    tp, tr = [], []
+    for _ in range(max(5, min(args.steps, 50))):
+        flush.fill_(1.0)
+        ev[0].record()
+        gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
+        ev[1].record()
+        gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True, out=o)
+        ev[2].record()
+        torch.cuda.synchronize()
+        tp.append(ev[0].elapsed_time(ev[1]))
+        tr.append(ev[1].elapsed_time(ev[2]))
+    D = M * H * P + M * G * N + G * N
+    L = S * M
+    prep_bytes = (n * S * D * 2 + n * S * (M * H + H) * 2 + n * L * H * (2 * N + P) * 2
+                  + 2 * n * L * H * 4)
+    rec_bytes = (2 * n * H * N * P * 4 + n * L * H * (2 * N + P) * 2 + 2 * n * L * H * 4
+                 + n * L * H * P * 4)
+    mp, mr = statistics.mean(tp), statistics.mean(tr)
+    hbm = pk["hbm_gbs"]
+    return {"workload": "decode n256 S4 M2 H32 G8 P128 N128 (fp32 state)",
+            "prepare_us": mp * 1e3, "prepare_GBps": prep_bytes / (mp * 1e-3) / 1e9,
+            "prepare_hbm_frac": prep_bytes / (mp * 1e-3) / 1e9 / hbm,
+            "update_us": mr * 1e3, "update_GBps": rec_bytes / (mr * 1e-3) / 1e9,
+            "update_hbm_frac": rec_bytes / (mr * 1e-3) / 1e9 / hbm,
+            "requests_per_s": n / ((mp + mr) * 1e-3)}
+
+
+# ----------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ----------------------------------------------------------------------------------
+
+def _oracle_sample(d, heads, t_len):
+    """Oracle prepare + fp64 walk over batch row 0, `heads` value heads, first t_len tokens."""
+    import oracle
+    w = WORKLOAD
+    x = d["x"][:1, :t_len]
+    ba = d["ba"][:1, :t_len]
+    q, k, v, beta, g = oracle.prepare(x, ba, d["A_log"], d["dt_bias"], w["M"], w["H"], w["G"],
+                                      w["V"], w["K"], decode=False)
+    hs = slice(0, heads)
+    oracle.walk(q[:, :, hs], k[:, :, hs], v[:, :, hs], beta[:, :, hs], g[:, :, hs], w["M"],
+                w["K"] ** -0.5, l2norm=True)
+    return t_len * w["M"] * heads  # expanded token-heads
+
+
+def cpu_baseline(d, max_seconds=20.0):
+    import oracle
+    oracle.build()
+    w = WORKLOAD
+    heads, t_len = w["HV"], w["T"]
+    t0 = time.perf_counter()
+    done = _oracle_sample(d, 2, 256)  # calibration
+    dt = time.perf_counter() - t0
+    rate = done / max(dt, 1e-9)
+    target = rate * max_seconds * 0.5
+    t_len = int(min(w["T"], max(64, target / (w["M"] * heads))))
+    t0 = time.perf_counter()
+    done = _oracle_sample(d, heads, t_len)
+    dt = time.perf_counter() - t0
+    per_head_tokens_per_s = done / dt  # expanded token-heads per second
+    value = per_head_tokens_per_s / w["HV"]  # expanded tokens (all heads) per second
+    return {"value": value, "unit": "expanded tokens/s (B*T*M)", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"batch row 0, {heads} heads, first {t_len} tokens (x{w['M']} copies): "
+                      f"oracle prepare + fp64 walk, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    d = make_inputs(torch.device("cpu"))
+    w = WORKLOAD
+    heads, t_len = w["HV"], 256
+    for _ in range(args.warmup):
+        _oracle_sample(d, heads, t_len)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_sample(d, heads, t_len)
+        ts.append(time.perf_counter() - t0)
+    per_step = statistics.mean(ts)
+    # each step is a bounded sample: scale its throughput to whole-workload tokens/s
+    value = (t_len * w["M"] * heads / w["HV"]) / per_step
+    sample = (f"per step: batch row 0, {heads} of {w['HV']} heads, first {t_len} tokens: "
+              f"oracle prepare + fp64 walk")
+    cores = oracle.max_threads()
+    return {"metric": METRIC, "value": value, "unit": "expanded tokens/s (B*T*M)",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64 "
+                                   "(prepare + chunk_fwd, G=16, in-kernel qk L2 norm)"},
+            "impl": "reference",
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": value},
+            "e2e": {"value": value, "unit": "expanded tokens/s (B*T*M)",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu DRAM bytes per launch of the dominant kernel, if measured")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

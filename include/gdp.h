@@ -1,0 +1,214 @@
+/*
+ * gdp.h - C ABI of the Gated Delta Product (GDP) forward-pass library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow three Megatron-core API pages:
+ *   "core.ssm.ops.gdp.prepare"  (gdp_prepare_kernel, gdp_decode_prepare,
+ *                                gdp_prefill_prepare, softplus)
+ *   "core.ssm.ops.gdp.wy_fast"  (recompute_w_u_fwd: WY factors w, u from the
+ *                                inverted transition block of solve_tril)
+ *   "core.ssm.ops.gdp.chunk_o"  (chunk_gated_delta_product_fwd_o: output from
+ *                                the chunk-boundary state of chunk_h plus the
+ *                                causal within-chunk attention over the copies)
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is a DEVICE pointer owned by the caller, unless a comment
+ *     says otherwise. The library allocates no device memory: scratch comes
+ *     from a caller-provided workspace whose size a query function returns.
+ *   - Every call is asynchronous on `stream`, performs no host
+ *     synchronisation (except gdp_read_status, which is for debugging) and
+ *     validates all scalar arguments before launching anything. On a
+ *     validation error nothing is launched.
+ *   - Tensors are row-major with the shapes given; strides, where a call takes
+ *     them, are in elements. Only x and ba may be strided (rows), and their
+ *     last dimension must be contiguous.
+ *   - Returns GDP_OK, or an error code; gdp_status_string() describes it.
+ *     GDP_ERR_CUDA means a CUDA runtime call failed (the CUDA error is left
+ *     for the caller to read with cudaGetLastError()).
+ */
+#ifndef GDP_H_
+#define GDP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdp_status {
+  GDP_OK = 0,
+  GDP_ERR_INVALID_ARG = 1,     /* a pointer, size or stride is invalid */
+  GDP_ERR_UNSUPPORTED = 2,     /* valid, but this combination is not built */
+  GDP_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
+  GDP_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait gave up */
+  GDP_ERR_WORKSPACE = 5        /* workspace too small or misaligned (256 B) */
+} gdp_status;
+
+typedef enum gdp_dtype { GDP_BF16 = 0, GDP_F16 = 1, GDP_F32 = 2 } gdp_dtype;
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* gdp_status_string(gdp_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int gdp_version(void);
+
+/*
+ * gdp_prefill_prepare - split, reshape and gate one prefill step's post-conv
+ * activations in one launch (prepare page, module overview and
+ * gdp_prefill_prepare).
+ *
+ *   x       [n, T, M*H*P + M*G*N + G*N] value | key | query, dtype `dt`;
+ *           element strides x_sn (per request) and x_st (per token); the last
+ *           dimension is contiguous.
+ *   ba      [n, T, M*H + H]: M*H beta logits b (copy-major), then H decay
+ *           inputs a; strides ba_sn, ba_st; last dimension contiguous.
+ *   A_log   [H] fp32 log decay rates.   dt_bias [H] fp32 softplus bias.
+ * Outputs (contiguous, caller-allocated):
+ *   q [n, T, H, N] (dt), k [n, T*M, H, N] (dt), v [n, T*M, H, P] (dt),
+ *   beta [n, T*M, H] fp32 = sigmoid(b), g [n, T, H] fp32 =
+ *   -exp(A_log) * softplus(a + dt_bias), softplus(x) = x > 20 ? x : log1p(exp(x)).
+ * Copy j of token t sits at expanded position t*M + j. Key/query group
+ * grp = h / (H/G) feeds head h. Requires H % G == 0. q/k/v are bit copies;
+ * beta and g use the CUDA math library's expf/log1pf with IEEE division,
+ * operation by operation in fp32.
+ * Errors: GDP_ERR_INVALID_ARG (null pointer, non-positive size, H % G != 0,
+ * row strides shorter than a row), GDP_ERR_UNSUPPORTED (dtype), GDP_ERR_CUDA.
+ */
+gdp_status gdp_prefill_prepare(const void* x, int64_t x_sn, int64_t x_st, const void* ba,
+                               int64_t ba_sn, int64_t ba_st, const float* A_log,
+                               const float* dt_bias, int n, int T, int M, int H, int G, int P,
+                               int N, gdp_dtype dt, void* q, void* k, void* v, float* beta,
+                               float* g, cudaStream_t stream);
+
+/*
+ * gdp_decode_prepare - the same map for one decode step of S = 1 + drafts
+ * tokens per request (prepare page, gdp_decode_prepare), with query and
+ * decay placed on the copies: the query on the last copy, g on the first,
+ * +0.0 on the others.
+ * Inputs as gdp_prefill_prepare with T replaced by S (S in 1..16).
+ * Outputs: q [n, S*M, H, N], k [n, S*M, H, N], v [n, S*M, H, P] (dt),
+ *          beta [n, S*M, H], g [n, S*M, H] fp32.
+ */
+gdp_status gdp_decode_prepare(const void* x, int64_t x_sn, int64_t x_st, const void* ba,
+                              int64_t ba_sn, int64_t ba_st, const float* A_log,
+                              const float* dt_bias, int n, int S, int M, int H, int G, int P,
+                              int N, gdp_dtype dt, void* q, void* k, void* v, float* beta,
+                              float* g, cudaStream_t stream);
+
+/*
+ * gdp_chunk_fwd_workspace_size - bytes of device workspace gdp_chunk_fwd
+ * needs for these sizes (pure host arithmetic; 0 if the sizes are invalid).
+ * N_seq is the number of packed sequences when cu_seqlens is used, else B.
+ */
+size_t gdp_chunk_fwd_workspace_size(int B, int T, int N_seq, int H, int HV, int K, int V, int M,
+                                    int chunk_size, gdp_dtype dt);
+
+/*
+ * gdp_chunk_fwd - chunked Gated Delta Product forward (wy_fast page:
+ * recompute_w_u_fwd; chunk_o page: chunk_gated_delta_product_fwd_o), from
+ * the prepared tensors to the outputs and the final state:
+ *   per (sequence, value head hv), with key/query head kh = hv / (HV/H), the
+ *   state S (V x K) walks the expanded stream, copy j of token t at t*M + j:
+ *     S <- exp(g_e) S (I - beta_e k_e k_e^T) + beta_e v_e k_e^T,
+ *   g_e = g_t on a token's first copy and 0 on the others, and
+ *   o_t = scale * S q_t after the token's last copy.
+ * computed chunk-wise: transition block and its inverse (solve_tril), WY
+ * factors w and u, chunk-boundary state recurrence with corrected values
+ * v_new = u - w h, then output = q h + causal within-chunk attention summed
+ * over the M copies.
+ *
+ *   q [B, T, H, K], k [B, T*M, H, K], v [B, T*M, HV, V]   dtype dt
+ *   beta [B, T*M, HV] fp32; g [B, T, HV] fp32 natural-log decay per token, or
+ *   NULL (ungated: g = 0)
+ *   initial_state [N_seq, HV, K, V] fp32 or NULL (zeros)
+ *   cu_seqlens [N_seq + 1] int32 token offsets on the unexpanded stream, or
+ *   NULL (then N_seq must equal B). With cu_seqlens, B must be 1, offsets must
+ *   be non-decreasing with cu_seqlens[0] = 0 and cu_seqlens[N_seq] <= T; they
+ *   are read on the device only (no host synchronisation).
+ *   chunk_size: 16, 32 or 64. scale: score scale (the pages' default is
+ *   K^-0.5; the caller passes it). use_qk_l2norm: 1 to L2-normalise q and k
+ *   per (position, head) as x / sqrt(sum x^2 + 1e-6) before use.
+ * Outputs: o [B, T, HV, V] fp32; final_state [N_seq, HV, K, V] fp32 or NULL.
+ * workspace: device scratch of at least gdp_chunk_fwd_workspace_size() bytes,
+ * 256-byte aligned; its first 256 bytes hold the device status word that
+ * gdp_read_status() reads back. Calls that share a workspace must not overlap
+ * on the GPU.
+ * Requires HV % H == 0, K <= 256, V <= 1024, M in 1..8.
+ */
+gdp_status gdp_chunk_fwd(const void* q, const void* k, const void* v, const float* beta,
+                         const float* g, const float* initial_state, const int32_t* cu_seqlens,
+                         int N_seq, int B, int T, int H, int HV, int K, int V, int M,
+                         int chunk_size, float scale, int use_qk_l2norm, gdp_dtype dt, float* o,
+                         float* final_state, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
+ * gdp_recurrent_update - fused recurrent update for decode (prepare page,
+ * decode bullet: the copies are walked as a sequence). For each request r
+ * and value head hv the fp32 state h = S^T [K, V] is updated in place over
+ * L = S*M steps, each step e using its own inputs:
+ *   S <- exp(g_e) S (I - beta_e k_e k_e^T) + beta_e v_e k_e^T;
+ *   o_e = scale * S q_e.
+ *   q [n, L, H, K], k [n, L, H, K], v [n, L, HV, V] dtype dt (q is zero on all
+ *   but a token's last copy when it comes from gdp_decode_prepare);
+ *   beta [n, L, HV], g [n, L, HV] fp32 (natural log);
+ *   state [n, HV, K, V] fp32, read and written in place;
+ *   o [n, L, HV, V] fp32.
+ * Requires HV % H == 0, K in {32, 64, 128, 256}, V % 8 == 0, V <= 1024.
+ * No scratch, no host synchronisation, fixed launch shape for fixed sizes.
+ */
+gdp_status gdp_recurrent_update(const void* q, const void* k, const void* v, const float* beta,
+                                const float* g, float* state, int n, int L, int H, int HV, int K,
+                                int V, float scale, int use_qk_l2norm, gdp_dtype dt, float* o,
+                                cudaStream_t stream);
+
+/*
+ * gdp_read_status - synchronise `stream` and return the device status word
+ * in the first bytes of a gdp_chunk_fwd workspace: GDP_OK, or
+ * GDP_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel gave up.
+ * Debugging aid; it does synchronise.
+ */
+gdp_status gdp_read_status(const void* workspace, cudaStream_t stream);
+
+/*
+ * gdp_chunk_fwd_stage_offsets - byte offsets, inside a gdp_chunk_fwd
+ * workspace for these sizes, of the intermediate stages the last call left
+ * there (for stage-by-stage checks), or SIZE_MAX for a stage the selected
+ * path does not materialise. `out` (HOST pointer, 8 entries) receives:
+ *   [0] A      fp32 [B*T*M, HV, BT]  inverted transition blocks (row p = its
+ *                                    chunk row, zero-padded)
+ *   [1] w      fp32 [B*T*M, HV, K]
+ *   [2] u      fp32 [B*T*M, HV, V]
+ *   [3] v_new  fp32 [B*T*M, HV, V]   corrected values
+ *   [4] h      fp32 [n_tok_chunks, HV, K, V] state at each token-chunk start,
+ *                                    sequences in order
+ *   [5] path   not an offset: 0 = generic fp32 path, 1 = tensor-core path
+ *   [6], [7]   reserved (SIZE_MAX)
+ * Returns GDP_ERR_INVALID_ARG on invalid sizes.
+ */
+gdp_status gdp_chunk_fwd_stage_offsets(int B, int T, int N_seq, int H, int HV, int K, int V,
+                                       int M, int chunk_size, gdp_dtype dt, size_t* out);
+
+/* Number of stage-boundary events gdp_set_stage_events takes. */
+#define GDP_STAGE_EVENTS 5
+
+/*
+ * gdp_set_stage_events - profiling hook. When `events` (HOST array of n >=
+ * GDP_STAGE_EVENTS caller-created cudaEvent_t) is non-NULL, every later
+ * gdp_chunk_fwd call records events[i] on its stream at its stage
+ * boundaries: [0] entry, [1] after the chunk tables, [2] after the WY stage
+ * (transition block, solve_tril, w and u), [3] after the chunk-boundary state
+ * recurrence, [4] after the output stage. A path that fuses stages records
+ * the fused boundaries back to back. NULL switches the hook off. The hook is
+ * process-wide and not thread-safe; the events stay owned by the caller.
+ */
+gdp_status gdp_set_stage_events(cudaEvent_t* events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDP_H_ */

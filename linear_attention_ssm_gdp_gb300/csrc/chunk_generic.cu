@@ -1,0 +1,551 @@
+// Generic chunked Gated Delta Product forward: fp32 arithmetic on CUDA cores,
+// any input dtype (bf16/fp16/fp32), any K <= 256, V <= 1024, chunk 16/32/64.
+// Used for fp32/fp16 inputs and for shapes outside the tensor-core path, and
+// keeps every intermediate stage in the workspace for stage-by-stage checks.
+//
+// Stages (Megatron-core API pages "core.ssm.ops.gdp.wy_fast" and
+// "core.ssm.ops.gdp.chunk_o"; the chunk algebra is the WY form of the gated
+// delta rule over the Householder-expanded stream, copy j of token t at t*M+j):
+//   tables   device-built chunk descriptors from cu_seqlens (no host sync)
+//   wy       per expanded chunk of BT positions: Gam = inclusive cumsum of the
+//            per-position decay in log2 units (g_t on a token's first copy),
+//            L[p,i] = beta_p 2^(Gam_p-Gam_i) k_p.k_i (i<p), A = (I+L)^-1
+//            (solve_tril, forward substitution), w = A(beta 2^Gam k),
+//            u = A(beta v)  (recompute_w_u)
+//   chunk_h  per (sequence, value head, value slice), sequential over chunks:
+//            v_new = u - w h ; h <- 2^Gam_last h + (k 2^(Gam_last-Gam))^T v_new;
+//            the state at each token-chunk start is stored for chunk_o
+//   chunk_o  per token chunk of BT tokens: o_t = scale (2^Gt_t q_t.h_c +
+//            sum_{s<=t} sum_j 2^(Gt_t-Gt_s) (q_t.k_{s,j}) v_new_{s,j}), the
+//            token chunk c starting at expanded chunk c*M.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gdp_internal.cuh"
+
+namespace gdp {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float ldf(const __half* p) { return __half2float(*p); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// ------------------------------------------------------------------------------------
+// chunk tables
+// ------------------------------------------------------------------------------------
+__global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M, int BT,
+                              int64_t NE_max, int64_t NT_max, int4* seq_info, int2* exp_tab,
+                              int2* tok_tab, int* status) {
+  __shared__ int s_bad;
+  __shared__ int s_ne, s_nt;
+  if (threadIdx.x == 0) {
+    int bad = 0;
+    int64_t eoff = 0, toff = 0;
+    int prev = 0;
+    for (int i = 0; i < N_seq; ++i) {
+      int t0, len;
+      if (cu) {
+        t0 = cu[i];
+        const int t1 = cu[i + 1];
+        if (i == 0 && t0 != 0) bad = 1;
+        if (t0 < prev || t1 < t0 || t1 > (int64_t)B * T) bad = 1;
+        prev = t1;
+        len = t1 - t0;
+      } else {
+        t0 = i * T;
+        len = T;
+      }
+      if (bad) break;
+      seq_info[i] = make_int4(t0, len, (int)eoff, (int)toff);
+      eoff += cdiv((int64_t)len * M, BT);
+      toff += cdiv((int64_t)len, BT);
+    }
+    if (eoff > NE_max || toff > NT_max) bad = 1;
+    s_bad = bad;
+    s_ne = bad ? 0 : (int)eoff;
+    s_nt = bad ? 0 : (int)toff;
+    if (bad) atomicExch(status, kDevBadSeqlens);
+  }
+  __syncthreads();
+  const int ne = s_ne, nt = s_nt;
+  if (!s_bad) {
+    for (int i = 0; i < N_seq; ++i) {
+      const int4 si = seq_info[i];
+      const int nei = (int)cdiv((int64_t)si.y * M, BT), nti = (int)cdiv((int64_t)si.y, BT);
+      for (int c = threadIdx.x; c < nei; c += blockDim.x) exp_tab[si.z + c] = make_int2(i, c);
+      for (int c = threadIdx.x; c < nti; c += blockDim.x) tok_tab[si.w + c] = make_int2(i, c);
+    }
+  }
+  for (int64_t c = ne + threadIdx.x; c < NE_max; c += blockDim.x) exp_tab[c] = make_int2(-1, 0);
+  for (int64_t c = nt + threadIdx.x; c < NT_max; c += blockDim.x) tok_tab[c] = make_int2(-1, 0);
+}
+
+// ------------------------------------------------------------------------------------
+// wy: transition block, solve_tril, w and u for one expanded chunk and value head
+// ------------------------------------------------------------------------------------
+struct GenArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* g;
+  const float* h0;
+  float* o;
+  float* hT;
+  int N_seq, H, HV, K, V, M, BT, l2norm;
+  float scale;
+  const int4* seq_info;
+  const int2* exp_tab;
+  const int2* tok_tab;
+  float* A;
+  float* w;
+  float* u;
+  float* gexp;
+  float* v_new;
+  float* h;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
+  extern __shared__ float sm[];
+  const int2 tab = a.exp_tab[blockIdx.x];
+  if (tab.x < 0) return;
+  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int4 si = a.seq_info[tab.x];
+  const int BT = a.BT, K = a.K, V = a.V, M = a.M;
+  const int e_start = tab.y * BT;
+  const int n = min(BT, si.y * M - e_start);
+  const int64_t R0 = (int64_t)si.x * M + e_start;  // first global expanded row
+  const int KP = K + 1, BP = BT + 1;
+  float* ks = sm;                 // [BT][KP]
+  float* Ls = ks + BT * KP;       // [BT][BP]
+  float* As = Ls + BT * BP;       // [BT][BP]
+  float* sb = As + BT * BP;       // beta
+  float* sG = sb + BT;            // Gam (log2)
+  float* srk = sG + BT;           // 1/|k| or 1
+  const Tin* kin = static_cast<const Tin*>(a.k);
+  const Tin* vin = static_cast<const Tin*>(a.v);
+  const int tid = threadIdx.x, nth = blockDim.x;
+
+  for (int p = tid; p < BT; p += nth) {
+    float b = 0.f, gl = 0.f;
+    if (p < n) {
+      const int e = e_start + p, t = e / M, jj = e - t * M;
+      b = a.beta[(R0 + p) * a.HV + hv];
+      if (a.g && jj == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv] * kLog2e;
+    }
+    sb[p] = b;
+    sG[p] = gl;
+  }
+  for (int i = tid; i < BT * K; i += nth) {
+    const int p = i / K, c = i - p * K;
+    ks[p * KP + c] = p < n ? ldf(kin + ((R0 + p) * a.H + kh) * K + c) : 0.f;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int p = 0; p < BT; ++p) { acc += sG[p]; sG[p] = acc; }
+  }
+  {
+    const int wid = tid >> 5, lane = tid & 31, nw = nth >> 5;
+    for (int p = wid; p < BT; p += nw) {
+      float ss = 0.f;
+      for (int c = lane; c < K; c += 32) ss += ks[p * KP + c] * ks[p * KP + c];
+      ss = warp_sum(ss);
+      if (lane == 0) srk[p] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+  }
+  __syncthreads();
+  // strictly-lower transition block
+  for (int i2 = tid; i2 < BT * BT; i2 += nth) {
+    const int p = i2 / BT, i = i2 - p * BT;
+    float val = 0.f;
+    if (i < p && p < n) {
+      float d = 0.f;
+      for (int c = 0; c < K; ++c) d += ks[p * KP + c] * ks[i * KP + c];
+      val = sb[p] * exp2f(sG[p] - sG[i]) * srk[p] * srk[i] * d;
+    }
+    Ls[p * BP + i] = val;
+    As[p * BP + i] = (p == i) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  // solve_tril: rows of A = (I + L)^-1 by forward substitution
+  for (int p = 1; p < n; ++p) {
+    for (int c = tid; c < p; c += nth) {
+      float s = 0.f;
+      for (int i = c; i < p; ++i) s += Ls[p * BP + i] * As[i * BP + c];
+      As[p * BP + c] = -s;
+    }
+    __syncthreads();
+  }
+  for (int i2 = tid; i2 < n * BT; i2 += nth) {
+    const int p = i2 / BT, c = i2 - p * BT;
+    a.A[((R0 + p) * a.HV + hv) * BT + c] = As[p * BP + c];
+  }
+  // w = A (beta 2^Gam k / |k|)
+  for (int i2 = tid; i2 < n * K; i2 += nth) {
+    const int p = i2 / K, c = i2 - p * K;
+    float s = 0.f;
+    for (int i = 0; i <= p; ++i)
+      s += As[p * BP + i] * (sb[i] * exp2f(sG[i]) * srk[i]) * ks[i * KP + c];
+    a.w[((R0 + p) * a.HV + hv) * K + c] = s;
+  }
+  // u = A (beta v)
+  for (int i2 = tid; i2 < n * V; i2 += nth) {
+    const int p = i2 / V, c = i2 - p * V;
+    float s = 0.f;
+    for (int i = 0; i <= p; ++i)
+      s += As[p * BP + i] * sb[i] * ldf(vin + ((R0 + i) * a.HV + hv) * V + c);
+    a.u[((R0 + p) * a.HV + hv) * V + c] = s;
+  }
+  for (int p = tid; p < n; p += nth) a.gexp[(R0 + p) * a.HV + hv] = sG[p];
+}
+
+// ------------------------------------------------------------------------------------
+// chunk_h: sequential state recurrence over the expanded chunks of one sequence
+// ------------------------------------------------------------------------------------
+constexpr int kBVH = 32;
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) h_generic_kernel(GenArgs a) {
+  extern __shared__ float sm[];
+  const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int v0 = blockIdx.z * kBVH;
+  const int nv = min(kBVH, a.V - v0);
+  const int4 si = a.seq_info[seq];
+  const int BT = a.BT, K = a.K, V = a.V, M = a.M;
+  const int KP = K + 1;
+  float* hs = sm;                 // [K][kBVH]
+  float* ws = hs + K * kBVH;      // [BT][KP]
+  float* ks = ws + BT * KP;       // [BT][KP]
+  float* us = ks + BT * KP;       // [BT][kBVH]
+  float* vn = us + BT * kBVH;     // [BT][kBVH]
+  float* sG = vn + BT * kBVH;     // [BT]
+  float* srk = sG + BT;           // [BT]
+  const Tin* kin = static_cast<const Tin*>(a.k);
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int64_t hoff = ((int64_t)seq * a.HV + hv) * K * V;
+
+  for (int i = tid; i < K * kBVH; i += nth) {
+    const int r = i / kBVH, c = i - r * kBVH;
+    hs[i] = (a.h0 && c < nv) ? a.h0[hoff + (int64_t)r * V + v0 + c] : 0.f;
+  }
+  const int ne = (int)cdiv((int64_t)si.y * M, BT);
+  for (int jc = 0; jc < ne; ++jc) {
+    __syncthreads();
+    if (jc % M == 0) {
+      float* hb = a.h + (((int64_t)si.w + jc / M) * a.HV + hv) * K * V;
+      for (int i = tid; i < K * nv; i += nth) {
+        const int r = i / nv, c = i - r * nv;
+        hb[(int64_t)r * V + v0 + c] = hs[r * kBVH + c];
+      }
+    }
+    const int e_start = jc * BT;
+    const int n = min(BT, si.y * M - e_start);
+    const int64_t R0 = (int64_t)si.x * M + e_start;
+    for (int i = tid; i < BT * K; i += nth) {
+      const int p = i / K, c = i - p * K;
+      const bool ok = p < n;
+      ws[p * KP + c] = ok ? a.w[((R0 + p) * a.HV + hv) * K + c] : 0.f;
+      ks[p * KP + c] = ok ? ldf(kin + ((R0 + p) * a.H + kh) * K + c) : 0.f;
+    }
+    for (int i = tid; i < BT * kBVH; i += nth) {
+      const int p = i / kBVH, c = i - p * kBVH;
+      us[i] = (p < n && c < nv) ? a.u[((R0 + p) * a.HV + hv) * V + v0 + c] : 0.f;
+    }
+    for (int p = tid; p < BT; p += nth) sG[p] = p < n ? a.gexp[(R0 + p) * a.HV + hv] : 0.f;
+    __syncthreads();
+    {
+      const int wid = tid >> 5, lane = tid & 31, nw = nth >> 5;
+      for (int p = wid; p < BT; p += nw) {
+        float ss = 0.f;
+        for (int c = lane; c < K; c += 32) ss += ks[p * KP + c] * ks[p * KP + c];
+        ss = warp_sum(ss);
+        if (lane == 0) srk[p] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+      }
+    }
+    // v_new = u - w h
+    for (int i = tid; i < BT * kBVH; i += nth) {
+      const int p = i / kBVH, c = i - p * kBVH;
+      float s = 0.f;
+      for (int r = 0; r < K; ++r) s += ws[p * KP + r] * hs[r * kBVH + c];
+      const float val = (p < n) ? us[i] - s : 0.f;
+      vn[i] = val;
+      if (p < n && c < nv) a.v_new[((R0 + p) * a.HV + hv) * V + v0 + c] = val;
+    }
+    __syncthreads();
+    const float glast = sG[n - 1];
+    // h <- 2^Gam_last h + (k 2^(Gam_last - Gam) / |k|)^T v_new
+    for (int i = tid; i < K * kBVH; i += nth) {
+      const int r = i / kBVH, c = i - r * kBVH;
+      float s = 0.f;
+      for (int p = 0; p < n; ++p) s += ks[p * KP + r] * srk[p] * exp2f(glast - sG[p]) * vn[p * kBVH + c];
+      hs[i] = exp2f(glast) * hs[i] + s;
+    }
+  }
+  __syncthreads();
+  if (a.hT) {
+    for (int i = tid; i < K * nv; i += nth) {
+      const int r = i / nv, c = i - r * nv;
+      a.hT[hoff + (int64_t)r * V + v0 + c] = hs[r * kBVH + c];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// chunk_o: output of one token chunk, one value head, one value slice
+// ------------------------------------------------------------------------------------
+constexpr int kBVO = 64, kKT = 32, kEB = 64;
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
+  extern __shared__ float sm[];
+  const int2 tab = a.tok_tab[blockIdx.x];
+  if (tab.x < 0) return;
+  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int v0 = blockIdx.z * kBVO;
+  const int nv = min(kBVO, a.V - v0);
+  const int4 si = a.seq_info[tab.x];
+  const int BT = a.BT, K = a.K, V = a.V, M = a.M;
+  const int t_start = tab.y * BT;
+  const int nt = min(BT, si.y - t_start);
+  const int ne = nt * M;
+  const int64_t T0 = (int64_t)si.x + t_start;  // first global token
+  const int64_t E0 = T0 * M;                   // first global expanded row
+  float* sGt = sm;                   // [BT]
+  float* srq = sGt + BT;             // [BT]
+  float* srk = srq + BT;             // [BT*M]
+  float* qt = srk + BT * M;          // [BT][kKT+1]
+  float* kt = qt + BT * (kKT + 1);   // [kEB][kKT+1]
+  float* Ps = kt + kEB * (kKT + 1);  // [BT][kEB+1]
+  float* ht = Ps + BT * (kEB + 1);   // [kKT][kBVO]
+  float* vt = ht + kKT * kBVO;       // [kEB][kBVO]
+  const Tin* qin = static_cast<const Tin*>(a.q);
+  const Tin* kin = static_cast<const Tin*>(a.k);
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int wid = tid >> 5, lane = tid & 31, nw = nth >> 5;
+  const float* hc = a.h + (((int64_t)si.w + tab.y) * a.HV + hv) * K * V;
+
+  for (int p = tid; p < BT; p += nth)
+    sGt[p] = (p < nt && a.g) ? a.g[(T0 + p) * a.HV + hv] * kLog2e : 0.f;
+  for (int t = wid; t < BT; t += nw) {
+    float ss = 0.f;
+    if (t < nt)
+      for (int c = lane; c < K; c += 32) {
+        const float x = ldf(qin + ((T0 + t) * a.H + kh) * K + c);
+        ss += x * x;
+      }
+    ss = warp_sum(ss);
+    if (lane == 0) srq[t] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  }
+  for (int e = wid; e < BT * M; e += nw) {
+    float ss = 0.f;
+    if (e < ne)
+      for (int c = lane; c < K; c += 32) {
+        const float x = ldf(kin + ((E0 + e) * a.H + kh) * K + c);
+        ss += x * x;
+      }
+    ss = warp_sum(ss);
+    if (lane == 0) srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int p = 0; p < BT; ++p) { acc += sGt[p]; sGt[p] = acc; }
+  }
+  // thread owns column c of rows tg, tg+4, ...
+  const int c = tid % kBVO, tg = tid / kBVO;
+  constexpr int RPT = 64 / 4;  // rows per thread for BT <= 64 with 256 threads
+  float acc[RPT];
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) acc[r] = 0.f;
+  // inter-chunk term q.h over K tiles
+  for (int k0 = 0; k0 < K; k0 += kKT) {
+    __syncthreads();
+    for (int i = tid; i < BT * kKT; i += nth) {
+      const int t = i / kKT, cc = i - t * kKT;
+      qt[t * (kKT + 1) + cc] =
+          (t < nt && k0 + cc < K) ? ldf(qin + ((T0 + t) * a.H + kh) * K + k0 + cc) : 0.f;
+    }
+    for (int i = tid; i < kKT * kBVO; i += nth) {
+      const int r = i / kBVO, cc = i - r * kBVO;
+      ht[i] = (k0 + r < K && cc < nv) ? hc[(int64_t)(k0 + r) * V + v0 + cc] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const int t = tg + 4 * r;
+      if (t < BT) {
+        float s = 0.f;
+        for (int kk = 0; kk < kKT; ++kk) s += qt[t * (kKT + 1) + kk] * ht[kk * kBVO + c];
+        acc[r] += s;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RPT; ++r) {
+    const int t = tg + 4 * r;
+    if (t < BT) acc[r] *= exp2f(sGt[t]) * srq[t];
+  }
+  // intra-chunk term, expanded positions in tiles of kEB
+  for (int e0 = 0; e0 < ne; e0 += kEB) {
+    __syncthreads();
+    for (int i = tid; i < BT * kEB; i += nth) Ps[(i / kEB) * (kEB + 1) + i % kEB] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += kKT) {
+      __syncthreads();
+      for (int i = tid; i < BT * kKT; i += nth) {
+        const int t = i / kKT, cc = i - t * kKT;
+        qt[t * (kKT + 1) + cc] =
+            (t < nt && k0 + cc < K) ? ldf(qin + ((T0 + t) * a.H + kh) * K + k0 + cc) : 0.f;
+      }
+      for (int i = tid; i < kEB * kKT; i += nth) {
+        const int e = i / kKT, cc = i - e * kKT;
+        kt[e * (kKT + 1) + cc] = (e0 + e < ne && k0 + cc < K)
+                                     ? ldf(kin + ((E0 + e0 + e) * a.H + kh) * K + k0 + cc)
+                                     : 0.f;
+      }
+      __syncthreads();
+      for (int i = tid; i < BT * kEB; i += nth) {
+        const int t = i / kEB, e = i - t * kEB;
+        float s = 0.f;
+        for (int kk = 0; kk < kKT; ++kk) s += qt[t * (kKT + 1) + kk] * kt[e * (kKT + 1) + kk];
+        Ps[t * (kEB + 1) + e] += s;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < BT * kEB; i += nth) {
+      const int t = i / kEB, e = i - t * kEB;
+      const int eg = e0 + e, s = eg / M;
+      float val = 0.f;
+      if (t < nt && eg < ne && s <= t)
+        val = Ps[t * (kEB + 1) + e] * srq[t] * srk[eg] * exp2f(sGt[t] - sGt[s]);
+      Ps[t * (kEB + 1) + e] = val;
+    }
+    for (int i = tid; i < kEB * kBVO; i += nth) {
+      const int e = i / kBVO, cc = i - e * kBVO;
+      vt[i] = (e0 + e < ne && cc < nv) ? a.v_new[((E0 + e0 + e) * a.HV + hv) * V + v0 + cc]
+                                       : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const int t = tg + 4 * r;
+      if (t < BT) {
+        float s = 0.f;
+        for (int e = 0; e < kEB; ++e) s += Ps[t * (kEB + 1) + e] * vt[e * kBVO + c];
+        acc[r] += s;
+      }
+    }
+  }
+  if (c < nv) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      const int t = tg + 4 * r;
+      if (t < nt) a.o[((T0 + t) * a.HV + hv) * V + v0 + c] = a.scale * acc[r];
+    }
+  }
+}
+
+template <typename Tin>
+cudaError_t run_generic(const ChunkProblem& p, const GenArgs& a) {
+  const int BT = p.BT, K = p.K;
+  const size_t smem_wy = sizeof(float) * ((size_t)BT * (K + 1) + 2 * (size_t)BT * (BT + 1) + 3 * BT);
+  const size_t smem_h = sizeof(float) * ((size_t)K * kBVH + 2 * (size_t)BT * (K + 1) +
+                                         2 * (size_t)BT * kBVH + 2 * BT);
+  const size_t smem_o = sizeof(float) * (2 * (size_t)BT + (size_t)BT * p.M + BT * (kKT + 1) +
+                                         kEB * (kKT + 1) + BT * (kEB + 1) + kKT * kBVO +
+                                         kEB * kBVO);
+  cudaError_t e;
+  e = cudaFuncSetAttribute(wy_generic_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_wy);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(h_generic_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_h);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(o_generic_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_o);
+  if (e != cudaSuccess) return e;
+  if (p.NE_max > 0) {
+    wy_generic_kernel<Tin><<<dim3((unsigned)p.NE_max, p.HV), 256, smem_wy, p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  record_stage(2, p.stream);
+  if (p.N_seq > 0) {
+    h_generic_kernel<Tin><<<dim3(p.N_seq, p.HV, (unsigned)cdiv(p.V, kBVH)), 256, smem_h,
+                            p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  record_stage(3, p.stream);
+  if (p.NT_max > 0) {
+    o_generic_kernel<Tin><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)cdiv(p.V, kBVO)), 256,
+                            smem_o, p.stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  record_stage(4, p.stream);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+WsLayout generic_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, int BT) {
+  (void)H;
+  WsLayout L;
+  int64_t NE, NT;
+  chunk_bounds(B, T, N_seq, M, BT, &NE, &NT);
+  const size_t Te = (size_t)B * T * M;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t at = off; off = align_up(off + bytes); return at; };
+  L.status = take(kAlign);
+  L.seq_info = take(sizeof(int4) * (size_t)(N_seq > 0 ? N_seq : 1));
+  L.exp_tab = take(sizeof(int2) * (size_t)NE);
+  L.tok_tab = take(sizeof(int2) * (size_t)NT);
+  L.A = take(sizeof(float) * Te * HV * BT);
+  L.w = take(sizeof(float) * Te * HV * K);
+  L.u = take(sizeof(float) * Te * HV * V);
+  L.gexp = take(sizeof(float) * Te * HV);
+  L.v_new = take(sizeof(float) * Te * HV * V);
+  L.h = take(sizeof(float) * (size_t)NT * HV * K * V);
+  L.total = off;
+  L.path = 0;
+  return L;
+}
+
+cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {
+  tables_kernel<<<1, 512, 0, p.stream>>>(
+      p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT, p.NE_max, p.NT_max,
+      reinterpret_cast<int4*>(ws + L.seq_info), reinterpret_cast<int2*>(ws + L.exp_tab),
+      reinterpret_cast<int2*>(ws + L.tok_tab), reinterpret_cast<int*>(ws + L.status));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {
+  GenArgs a;
+  a.q = p.q; a.k = p.k; a.v = p.v; a.beta = p.beta; a.g = p.g; a.h0 = p.h0; a.o = p.o;
+  a.hT = p.hT;
+  a.N_seq = p.N_seq; a.H = p.H; a.HV = p.HV; a.K = p.K; a.V = p.V; a.M = p.M; a.BT = p.BT;
+  a.l2norm = p.l2norm; a.scale = p.scale;
+  a.seq_info = reinterpret_cast<const int4*>(ws + L.seq_info);
+  a.exp_tab = reinterpret_cast<const int2*>(ws + L.exp_tab);
+  a.tok_tab = reinterpret_cast<const int2*>(ws + L.tok_tab);
+  a.A = reinterpret_cast<float*>(ws + L.A);
+  a.w = reinterpret_cast<float*>(ws + L.w);
+  a.u = reinterpret_cast<float*>(ws + L.u);
+  a.gexp = reinterpret_cast<float*>(ws + L.gexp);
+  a.v_new = reinterpret_cast<float*>(ws + L.v_new);
+  a.h = reinterpret_cast<float*>(ws + L.h);
+  switch (p.dt) {
+    case GDP_BF16: return run_generic<__nv_bfloat16>(p, a);
+    case GDP_F16: return run_generic<__half>(p, a);
+    default: return run_generic<float>(p, a);
+  }
+}
+
+}  // namespace gdp

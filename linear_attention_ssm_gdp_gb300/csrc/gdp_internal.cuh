@@ -1,0 +1,91 @@
+// Internal declarations shared by the CUDA translation units of libgdp.
+// Nothing here is part of the C ABI (include/gdp.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdp.h"
+
+namespace gdp {
+
+constexpr size_t kAlign = 256;
+__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Device status word codes (first int32 of a chunk_fwd workspace).
+enum DeviceStatus : int { kDevOk = 0, kDevBadSeqlens = 1, kDevTimeout = 2 };
+
+// Per-sequence descriptor built on the device from cu_seqlens (or from B, T):
+// x = first token in the flattened [B*T] token stream, y = length in tokens,
+// z = index of its first expanded chunk, w = index of its first token chunk.
+// Chunk tables map a global chunk index to (sequence, chunk-in-sequence);
+// entries past the real total hold sequence -1 and their CTAs exit.
+
+// One chunked-forward problem, as validated by the API layer.
+struct ChunkProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* g;  // may be null (ungated)
+  const float* h0; // may be null
+  const int32_t* cu_seqlens;  // may be null
+  int N_seq, B, T, H, HV, K, V, M, BT;
+  float scale;
+  int l2norm;
+  gdp_dtype dt;
+  float* o;
+  float* hT;  // may be null
+  cudaStream_t stream;
+  int64_t NE_max;  // upper bound on expanded chunks over all sequences
+  int64_t NT_max;  // upper bound on token chunks over all sequences
+};
+
+// Byte offsets inside a chunk_fwd workspace.
+struct WsLayout {
+  size_t status = 0, seq_info = 0, exp_tab = 0, tok_tab = 0;
+  size_t A = SIZE_MAX, w = SIZE_MAX, u = SIZE_MAX, gexp = SIZE_MAX, v_new = SIZE_MAX,
+         h = SIZE_MAX;
+  // tensor-core path buffers
+  size_t w_hi = SIZE_MAX, w_lo = SIZE_MAX, kn = SIZE_MAX, gam = SIZE_MAX, rk = SIZE_MAX;
+  size_t total = 0;
+  int path = 0;  // 0 generic, 1 tensor core
+};
+
+// Sizes derived from (B, T, N_seq, M, BT): upper bounds on chunk counts.
+inline void chunk_bounds(int B, int T, int N_seq, int M, int BT, int64_t* NE, int64_t* NT) {
+  const int64_t Ttot = (int64_t)B * T;
+  *NE = cdiv(Ttot * M, BT) + N_seq;
+  *NT = cdiv(Ttot, BT) + N_seq;
+}
+
+WsLayout generic_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, int BT);
+WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, int BT);
+bool tc_supported(int H, int HV, int K, int V, int M, int BT, gdp_dtype dt);
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void* ba,
+                           int64_t ba_sn, int64_t ba_st, const float* A_log,
+                           const float* dt_bias, int n, int T, int M, int H, int G, int P,
+                           int N, gdp_dtype dt, bool decode, void* q, void* k, void* v,
+                           float* beta, float* g, cudaStream_t stream);
+
+cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
+cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
+cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
+
+cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const float* beta,
+                             const float* g, float* state, int n, int L, int H, int HV, int K,
+                             int V, float scale, int l2norm, gdp_dtype dt, float* o,
+                             cudaStream_t stream);
+
+int sm_count();  // multiprocessors on the current device (cached per device)
+
+// Records stage-boundary event i (gdp_set_stage_events) on `s`; no-op when off.
+// Slots: 0 entry, 1 after the chunk tables, 2 after the WY stage (transition
+// block, solve_tril, w/u), 3 after the state recurrence, 4 after the output.
+void record_stage(int i, cudaStream_t s);
+
+}  // namespace gdp

@@ -177,9 +177,11 @@ def recurrent(q, k, v, beta, g, state, scale: float, l2norm: bool = False, nthre
     HV, V = v.shape[2], v.shape[3]
     st = _d(state).clone()
     o = torch.zeros((n, L, HV, V), dtype=torch.float64)
-    rc = _load().oracle_gdp_recurrent(_ptr(_d(q)), _ptr(_d(k)), _ptr(_d(v)), _ptr(_d(beta)),
-                                      _ptr(_d(g)), _ptr(st), n, L, H, HV, K, V, float(scale),
-                                      1 if l2norm else 0, int(nthreads), _ptr(o))
+    # keep every converted input alive for the duration of the C call
+    qd, kd, vd, bd, gd = _d(q), _d(k), _d(v), _d(beta), _d(g)
+    rc = _load().oracle_gdp_recurrent(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(bd), _ptr(gd), _ptr(st),
+                                      n, L, H, HV, K, V, float(scale), 1 if l2norm else 0,
+                                      int(nthreads), _ptr(o))
     if rc:
         raise ValueError("oracle_gdp_recurrent: bad arguments")
     return o, st

@@ -1,0 +1,31 @@
+"""Shared helpers for the parity tests (no method arithmetic beyond error metrics)."""
+from __future__ import annotations
+
+import torch
+
+import oracle
+import synth_inputs as si
+
+# Tolerances: max |x - x_ref| <= tol * RMS(x_ref), separately for o and the final
+# state; tol = 2e-3 for bf16/fp16 inputs and 1e-5 for fp32 inputs.
+TOL = {torch.bfloat16: 2e-3, torch.float16: 2e-3, torch.float32: 1e-5}
+
+
+def rel_err(got, want) -> float:
+    want = want.detach().cpu().to(torch.float64)
+    got = got.detach().cpu().to(torch.float64)
+    rms = want.pow(2).mean().sqrt().item()
+    if want.numel() == 0:
+        return 0.0
+    return (got - want).abs().max().item() / max(rms, 1e-300)
+
+
+def chunk_case(B, T, H, HV, K, V, M, seed=0, dtype=torch.bfloat16, gated=True):
+    """Seeded raw inputs plus oracle-computed gates (identical bits for both sides)."""
+    d = si.chunk_inputs(B, T, H, HV, K, V, M, seed=seed, dtype=dtype)
+    beta, g = oracle.gate_map(d["b"], d["a"], d["A_log"], d["dt_bias"])
+    return d["q"], d["k"], d["v"], beta, (g if gated else None)
+
+
+def to(dev, *ts):
+    return [None if t is None else t.to(dev) for t in ts]

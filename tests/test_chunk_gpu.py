@@ -1,0 +1,236 @@
+"""Parity of gdp_chunk_fwd (wy_fast page: recompute_w_u_fwd; chunk_o page:
+chunk_gated_delta_product_fwd_o) against the CPU oracle's fp64 token walk,
+element by element, plus stage-by-stage checks against the oracle's chunked
+WY restatement.
+
+Tolerance: max |x - x_ref| <= tol * RMS(x_ref) for o and for the final state,
+tol = 2e-3 for bf16/fp16 inputs and 1e-5 for fp32 inputs. The oracle reads
+the same quantised inputs (and the same fp32 gates) as the GPU.
+"""
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from _util import TOL, chunk_case, rel_err, to
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run(gdp, q, k, v, beta, g, M, BT, l2, h0=None, cu=None):
+    qd, kd, vd, bd, gd, hd, cd = to(DEV, q, k, v, beta, g, h0, cu)
+    o, fs = gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, cu_seqlens=cd, chunk_size=BT,
+                              num_householder=M, initial_state=hd, use_qk_l2norm=l2)
+    torch.cuda.synchronize()
+    return o.cpu(), fs.cpu()
+
+
+CASES = [
+    # B, T, H, HV, K, V, M, BT, dtype, l2norm, gated, h0
+    (1, 128, 2, 2, 32, 32, 2, 64, torch.float32, True, True, False),   # tiny fp32 workload
+    (2, 200, 2, 2, 64, 64, 2, 64, torch.bfloat16, True, True, False),
+    (1, 150, 2, 2, 32, 48, 3, 64, torch.bfloat16, True, True, True),   # chunks split tokens
+    (1, 77, 1, 1, 64, 32, 1, 32, torch.float32, False, True, True),
+    (2, 90, 2, 6, 32, 48, 2, 64, torch.bfloat16, True, True, False),   # GVA
+    (1, 70, 2, 2, 32, 32, 2, 16, torch.float32, True, False, True),    # ungated
+    (1, 100, 2, 2, 64, 64, 4, 64, torch.float16, True, True, False),
+    (1, 300, 2, 2, 128, 128, 2, 64, torch.bfloat16, True, True, True),
+    (1, 260, 2, 4, 128, 256, 2, 64, torch.bfloat16, True, True, False),
+    (1, 131, 2, 2, 128, 128, 3, 64, torch.bfloat16, False, True, False),
+    (1, 65, 1, 1, 256, 64, 1, 64, torch.float32, True, True, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_chunk_fwd_matches_walk(gdp, case):
+    B, T, H, HV, K, V, M, BT, dtype, l2, gated, with_h0 = case
+    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=T + K, dtype=dtype, gated=gated)
+    h0 = torch.randn(B, HV, K, V, generator=torch.Generator().manual_seed(3)) if with_h0 else None
+    o, fs = _run(gdp, q, k, v, beta, g, M, BT, l2, h0=h0)
+    ro, rfs = oracle.walk(q, k, v, beta, g, M, K ** -0.5, h0=h0, l2norm=l2)
+    tol = TOL[dtype]
+    assert rel_err(o, ro) <= tol, rel_err(o, ro)
+    assert rel_err(fs, rfs) <= tol, rel_err(fs, rfs)
+
+
+@pytest.mark.parametrize("K,V,M", [(32, 32, 2), (128, 128, 2), (128, 128, 3)])
+def test_varlen_with_ragged_and_empty_sequences(gdp, K, V, M):
+    lens = [1, 63, 64, 65, 130, 0, 7, 200]
+    cu = si.cu_seqlens_of(lens)
+    T = int(cu[-1]) + 5  # padding tokens after the last sequence are untouched
+    q, k, v, beta, g = chunk_case(1, T, 2, 2, K, V, M, seed=11)
+    h0 = torch.randn(len(lens), 2, K, V, generator=torch.Generator().manual_seed(4))
+    o, fs = _run(gdp, q, k, v, beta, g, M, 64, True, h0=h0, cu=cu)
+    ro, rfs = oracle.walk(q, k, v, beta, g, M, K ** -0.5, cu_seqlens=cu, h0=h0, l2norm=True)
+    n = int(cu[-1])
+    assert rel_err(o[:, :n], ro[:, :n]) <= 2e-3
+    assert rel_err(fs, rfs) <= 2e-3
+    # empty sequence: final state is its initial state
+    assert torch.equal(fs[5], h0[5])
+
+
+def test_varlen_equals_separate_calls(gdp):
+    lens = [70, 129, 5]
+    cu = si.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    q, k, v, beta, g = chunk_case(1, T, 2, 2, 64, 64, 2, seed=5)
+    o, fs = _run(gdp, q, k, v, beta, g, 2, 64, True, cu=cu)
+    for i in range(len(lens)):
+        t0, t1 = int(cu[i]), int(cu[i + 1])
+        oi, fi = _run(gdp, q[:, t0:t1], k[:, 2 * t0:2 * t1], v[:, 2 * t0:2 * t1],
+                      beta[:, 2 * t0:2 * t1], g[:, t0:t1], 2, 64, True)
+        assert rel_err(o[:, t0:t1], oi) <= 1e-5
+        assert rel_err(fs[i:i + 1], fi) <= 1e-5
+
+
+def test_gva_equals_repeated_heads(gdp):
+    q, k, v, beta, g = chunk_case(1, 140, 2, 8, 64, 64, 2, seed=6)
+    o, fs = _run(gdp, q, k, v, beta, g, 2, 64, True)
+    o2, fs2 = _run(gdp, q.repeat_interleave(4, 2), k.repeat_interleave(4, 2), v, beta, g, 2, 64,
+                   True)
+    assert rel_err(o, o2) <= 1e-5 and rel_err(fs, fs2) <= 1e-5
+
+
+def test_deterministic_and_causal(gdp):
+    q, k, v, beta, g = chunk_case(1, 160, 2, 2, 128, 128, 2, seed=8)
+    o1, f1 = _run(gdp, q, k, v, beta, g, 2, 64, True)
+    o2, f2 = _run(gdp, q, k, v, beta, g, 2, 64, True)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    t = 100  # perturb token t and everything after; outputs before t must not move
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    q2[:, t:] = -q2[:, t:]
+    k2[:, 2 * t:] = k2[:, 2 * t:].flip(-1)
+    v2[:, 2 * t:] *= 3
+    o3, _ = _run(gdp, q2, k2, v2, beta, g, 2, 64, True)
+    assert rel_err(o3[:, :t], o1[:, :t]) <= 1e-6
+    assert rel_err(o3[:, t:], o1[:, t:]) > 1e-2
+
+
+def test_continuation_through_initial_state(gdp):
+    q, k, v, beta, g = chunk_case(1, 200, 2, 2, 64, 64, 2, seed=9)
+    o, fs = _run(gdp, q, k, v, beta, g, 2, 64, True)
+    oa, fa = _run(gdp, q[:, :77], k[:, :154], v[:, :154], beta[:, :154], g[:, :77], 2, 64, True)
+    ob, fb = _run(gdp, q[:, 77:], k[:, 154:], v[:, 154:], beta[:, 154:], g[:, 77:], 2, 64, True,
+                  h0=fa)
+    assert rel_err(torch.cat([oa, ob], 1), o) <= 2e-3
+    assert rel_err(fb, fs) <= 2e-3
+
+
+def test_empty_inputs(gdp):
+    q, k, v, beta, g = chunk_case(1, 0, 2, 2, 32, 32, 2, seed=1, dtype=torch.float32)
+    o, fs = _run(gdp, q, k, v, beta, g, 2, 64, False)
+    assert o.numel() == 0 and torch.count_nonzero(fs) == 0
+    cu = torch.zeros(1, dtype=torch.int32)  # no sequences at all
+    q, k, v, beta, g = chunk_case(1, 4, 2, 2, 32, 32, 2, seed=1, dtype=torch.float32)
+    qd, kd, vd, bd, gd, cd = to(DEV, q, k, v, beta, g, cu)
+    o, fs = gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, cu_seqlens=cd, num_householder=2)
+    assert fs.numel() == 0
+
+
+def test_bad_seqlens_reported_on_device(gdp):
+    q, k, v, beta, g = chunk_case(1, 10, 2, 2, 32, 32, 2, seed=1, dtype=torch.float32)
+    cu = torch.tensor([0, 6, 4], dtype=torch.int32)  # decreasing
+    qd, kd, vd, bd, gd, cd = to(DEV, q, k, v, beta, g, cu)
+    need = gdp.gdp_chunk_fwd_workspace_size(1, 10, 2, 2, 2, 32, 32, 2, 64, torch.float32)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, cu_seqlens=cd, num_householder=2, workspace=ws)
+    assert gdp.gdp_read_status(ws) == 1
+
+
+# ---------------------------------------------------------------------------------
+# stage-by-stage parity against the chunked WY restatement
+# ---------------------------------------------------------------------------------
+@pytest.mark.parametrize("K,V,M,dtype", [(32, 48, 3, torch.float32), (128, 128, 2, torch.bfloat16)])
+def test_stages_match_chunked_restatement(gdp, K, V, M, dtype):
+    B, T, H, HV, BT = 1, 150, 2, 2, 64
+    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=21, dtype=dtype)
+    qd, kd, vd, bd, gd = to(DEV, q, k, v, beta, g)
+    need = gdp.gdp_chunk_fwd_workspace_size(B, T, B, H, HV, K, V, M, BT, dtype)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, chunk_size=BT, num_householder=M, use_qk_l2norm=True,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    off = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, HV, K, V, M, BT, dtype)
+    Te = B * T * M
+    NONE = (1 << 64) - 1
+
+    def view(i, shape):
+        return ws[off[i]:off[i] + 4 * int(torch.tensor(shape).prod())].view(torch.float32).view(
+            *shape).cpu().double()
+
+    for hv in range(HV):
+        ref = oracle.chunked_stream(q[0, :, hv].numpy(), k[0, :, hv].numpy(),
+                                    v[0, :, hv].numpy(), beta[0, :, hv].numpy(),
+                                    g[0, :, hv].numpy(), M, BT, K ** -0.5, l2norm=True)
+        if off[0] != NONE:
+            A = view(0, (Te, HV, BT))[:, hv]
+            for c, Ac in enumerate(ref["A"]):
+                n = Ac.shape[0]
+                assert rel_err(A[c * BT:c * BT + n, :n], torch.from_numpy(Ac)) <= 1e-5
+        for name, idx, width in (("w", 1, K), ("u", 2, V), ("v_new", 3, V)):
+            if off[idx] != NONE:
+                got = view(idx, (Te, HV, width))[:, hv]
+                assert rel_err(got, torch.from_numpy(ref[name])) <= 1e-4, name
+        if off[4] != NONE:
+            hs = view(4, (-(-T // BT), HV, K, V))[:, hv]
+            for c in range(hs.shape[0]):
+                want = torch.from_numpy(ref["h_chunks"][c * M])
+                if want.abs().max() > 0:
+                    assert rel_err(hs[c], want) <= 1e-4
+
+
+# ---------------------------------------------------------------------------------
+# full-size workloads, launched as the benchmark launches them, checked on
+# sampled (sequence, head) units that the oracle walks one by one
+# ---------------------------------------------------------------------------------
+def _sample_check(o, fs, q, k, v, beta, g, M, units, l2=True, cu=None):
+    """units: list of (batch-or-seq, hv); compares o rows and final states."""
+    H, HV, K = q.shape[2], v.shape[2], q.shape[3]
+    for s, hv in units:
+        kh = hv // (HV // H)
+        if cu is None:
+            b, t0, t1 = s, 0, q.shape[1]
+        else:
+            b, t0, t1 = 0, int(cu[s]), int(cu[s + 1])
+        sl = lambda x, h, m=1: x[b:b + 1, t0 * m:t1 * m, h:h + 1]
+        ro, rfs = oracle.walk(sl(q, kh), sl(k, kh, M), sl(v, hv, M), sl(beta, hv, M),
+                              sl(g, hv), M, K ** -0.5, l2norm=l2)
+        assert rel_err(o[b:b + 1, t0:t1, hv:hv + 1], ro) <= 2e-3, (s, hv)
+        assert rel_err(fs[s:s + 1, hv:hv + 1], rfs) <= 2e-3, (s, hv)
+
+
+def test_prefill_bf16_workload(gdp):
+    w = si.WORKLOADS["prefill_bf16"].dims
+    q, k, v, beta, g = chunk_case(w["B"], w["T"], w["H"], w["HV"], w["K"], w["V"], w["M"], seed=0)
+    o, fs = _run(gdp, q, k, v, beta, g, w["M"], w["BT"], True)
+    assert torch.isfinite(o).all()
+    _sample_check(o, fs, q, k, v, beta, g, w["M"], [(0, 0), (1, 15), (1, 6)])
+
+
+def test_gva_bf16_workload(gdp):
+    w = si.WORKLOADS["gva_bf16"].dims
+    q, k, v, beta, g = chunk_case(w["B"], w["T"], w["H"], w["HV"], w["K"], w["V"], w["M"], seed=0)
+    o, fs = _run(gdp, q, k, v, beta, g, w["M"], w["BT"], True)
+    assert torch.isfinite(o).all()
+    _sample_check(o, fs, q, k, v, beta, g, w["M"], [(0, 0), (3, 31), (2, 13)])
+
+
+def test_varlen_workload_from_prepare(gdp):
+    w = si.WORKLOADS["varlen_bf16"].dims
+    lens = si.varlen_lengths(w["n_seq"], seed=0)
+    cu = si.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    M, H, G, P, N = w["M"], w["H"], w["G"], w["P"], w["N"]
+    d = si.prepare_inputs(1, T, M, H, G, P, N, seed=0)
+    q, k, v, beta, g = gdp.gdp_prefill_prepare(d["x"].to(DEV), d["ba"].to(DEV),
+                                               d["A_log"].to(DEV), d["dt_bias"].to(DEV), M, H,
+                                               G, P, N)
+    o, fs = gdp.gdp_chunk_fwd(q, k, v, beta, g, cu_seqlens=cu.to(DEV), chunk_size=w["BT"],
+                              num_householder=M, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    # the oracle walks its own prepare of the same raw inputs
+    rq, rk, rv, rb, rg = oracle.prepare(d["x"], d["ba"], d["A_log"], d["dt_bias"], M, H, G, P, N,
+                                        decode=False)
+    _sample_check(o.cpu(), fs.cpu(), rq, rk, rv, rb, rg, M, [(0, 0), (7, 31), (15, 9)], cu=cu)

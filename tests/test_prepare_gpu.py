@@ -1,0 +1,131 @@
+"""Parity of the fused prepare kernel (prepare page: gdp_prefill_prepare,
+gdp_decode_prepare) against the CPU oracle's fp32 map and the eager PyTorch
+composition of the same fp32 operations.
+
+q/k/v and the +0 placements are bit moves: bit-exact against the oracle.
+beta and g are bit-exact against the eager GPU composition (the pages'
+contract, asserted with torch.equal) and within 4 ulp of the oracle, whose host
+libm expf/log1pf are not CUDA's.
+"""
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth_inputs as si
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _ulp(a, b):
+    ai = a.contiguous().view(torch.int32).to(torch.int64)
+    bi = b.contiguous().view(torch.int32).to(torch.int64)
+    ai = torch.where(ai < 0, -(ai & 0x7FFFFFFF), ai)
+    bi = torch.where(bi < 0, -(bi & 0x7FFFFFFF), bi)
+    return (ai - bi).abs()
+
+
+def _eager_gates(ba, A_log, dt_bias, M, H, decode):
+    n, T = ba.shape[:2]
+    b = ba[..., :M * H].float().reshape(n, T * M, H)
+    a = ba[..., M * H:].float()
+    beta = torch.sigmoid(b)
+    gt = -torch.exp(A_log.float()) * F.softplus(a + dt_bias.float())
+    if decode:
+        g = torch.zeros(n, T, M, H, dtype=torch.float32, device=ba.device)
+        g[:, :, 0] = gt
+        gt = g.reshape(n, T * M, H)
+    return beta, gt
+
+
+def _check(gdp, x, ba, A_log, dt_bias, M, H, G, P, N, decode):
+    fn = gdp.gdp_decode_prepare if decode else gdp.gdp_prefill_prepare
+    out = fn(x.to(DEV) if not x.is_cuda else x, ba.to(DEV) if not ba.is_cuda else ba,
+             A_log.to(DEV), dt_bias.to(DEV), M, H, G, P, N)
+    torch.cuda.synchronize()
+    ref = oracle.prepare(x.cpu(), ba.cpu(), A_log, dt_bias, M, H, G, P, N, decode=decode)
+    names = ("q", "k", "v", "beta", "g")
+    for nm, a, b in zip(names[:3], out[:3], ref[:3]):
+        assert a.dtype == b.dtype and tuple(a.shape) == tuple(b.shape), nm
+        assert torch.equal(a.cpu(), b), f"{nm} differs from the oracle's bit copy"
+    eb, eg = _eager_gates(ba.to(DEV), A_log.to(DEV), dt_bias.to(DEV), M, H, decode)
+    assert torch.equal(out[3], eb), "beta differs from the eager composition"
+    assert torch.equal(out[4], eg), "g differs from the eager composition"
+    for nm, a, b in zip(names[3:], out[3:], ref[3:]):
+        d = _ulp(a.cpu(), b)
+        assert int(d.max()) <= 4, f"{nm}: {int(d.max())} ulp from the oracle"
+    if decode:
+        n, T = x.shape[:2]
+        assert torch.count_nonzero(out[0].view(n, T, M, H, N)[:, :, :M - 1]) == 0
+        assert torch.count_nonzero(out[4].view(n, T, M, H)[:, :, 1:]) == 0
+
+
+def test_prefill_prepare_varlen_packed_workload(gdp):
+    w = si.WORKLOADS["varlen_bf16"].dims
+    T = int(si.varlen_lengths(w["n_seq"], seed=0).sum())
+    d = si.prepare_inputs(1, T, w["M"], w["H"], w["G"], w["P"], w["N"], seed=0)
+    _check(gdp, d["x"], d["ba"], d["A_log"], d["dt_bias"], w["M"], w["H"], w["G"], w["P"],
+           w["N"], decode=False)
+
+
+def test_decode_prepare_workload(gdp):
+    w = si.WORKLOADS["decode"].dims
+    d = si.prepare_inputs(w["n"], w["S"], w["M"], w["H"], w["G"], w["P"], w["N"], seed=1)
+    _check(gdp, d["x"], d["ba"], d["A_log"], d["dt_bias"], w["M"], w["H"], w["G"], w["P"],
+           w["N"], decode=True)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+@pytest.mark.parametrize("M,H,G,P,N,dtype", [
+    (3, 6, 3, 24, 16, torch.bfloat16),   # 16-byte vector path
+    (2, 4, 2, 3, 5, torch.bfloat16),     # odd head sizes: element path
+    (1, 2, 1, 8, 8, torch.float32),
+    (2, 4, 4, 5, 4, torch.float32),
+    (4, 8, 2, 16, 8, torch.float16),
+])
+def test_prepare_small_strided(gdp, decode, M, H, G, P, N, dtype):
+    n, T = 3, 5
+    d = si.prepare_inputs(n, T, M, H, G, P, N, seed=7, dtype=dtype)
+    D = d["x"].shape[-1]
+    # rows strided inside a wider buffer (a view of a conv output), ba non-contiguous
+    big = torch.zeros(n, T + 1, D + 24, dtype=dtype)
+    big[:, :T, 8:8 + D] = d["x"]
+    x = big.to(DEV)[:, :T, 8:8 + D]
+    bbig = torch.zeros(n, T, M * H + H + 5, dtype=dtype)
+    bbig[..., 2:2 + M * H + H] = d["ba"]
+    ba = bbig.to(DEV)[..., 2:2 + M * H + H]
+    assert not x.is_contiguous() and not ba.is_contiguous()
+    _check(gdp, x, ba, d["A_log"], d["dt_bias"], M, H, G, P, N, decode)
+
+
+def test_gate_extremes(gdp):
+    """Saturation of softplus above 20 and sigmoid tails, through the kernel."""
+    M, H, G, P, N = 1, 8, 1, 8, 8
+    vals = torch.tensor([-100., -30., -20., -1e-3, 0., 1e-3, 19.99, 20., 20.01, 25., 88., 1e4])
+    T = vals.numel()
+    d = si.prepare_inputs(1, T, M, H, G, P, N, seed=2, dtype=torch.float32)
+    ba = d["ba"].clone()
+    ba[0, :, :M * H] = vals.view(T, 1)
+    ba[0, :, M * H:] = vals.view(T, 1)
+    _check(gdp, d["x"], ba, d["A_log"], torch.zeros(H), M, H, G, P, N, decode=False)
+
+
+def test_empty_prefill_is_a_no_op(gdp):
+    M, H, G, P, N = 2, 4, 2, 8, 8
+    x = torch.empty(1, 0, M * H * P + M * G * N + G * N, dtype=torch.bfloat16, device=DEV)
+    ba = torch.empty(1, 0, M * H + H, dtype=torch.bfloat16, device=DEV)
+    q, k, v, beta, g = gdp.gdp_prefill_prepare(x, ba, torch.zeros(H, device=DEV),
+                                               torch.zeros(H, device=DEV), M, H, G, P, N)
+    assert q.numel() == 0 and k.numel() == 0 and beta.numel() == 0
+
+
+def test_deterministic(gdp):
+    M, H, G, P, N = 2, 8, 4, 64, 64
+    d = si.prepare_inputs(2, 33, M, H, G, P, N, seed=5)
+    args = (d["x"].to(DEV), d["ba"].to(DEV), d["A_log"].to(DEV), d["dt_bias"].to(DEV), M, H, G,
+            P, N)
+    a = gdp.gdp_prefill_prepare(*args)
+    b = gdp.gdp_prefill_prepare(*args)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

@@ -1,0 +1,103 @@
+"""Parity of gdp_recurrent_update (decode: the copies walked as a sequence,
+prepare page decode bullet) against the oracle's fp64 per-step walk."""
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from _util import TOL, chunk_case, rel_err, to
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_decode_workload_prepare_then_update(gdp):
+    w = si.WORKLOADS["decode"].dims
+    n, S, M, H, G, P, N = w["n"], w["S"], w["M"], w["H"], w["G"], w["P"], w["N"]
+    d = si.prepare_inputs(n, S, M, H, G, P, N, seed=1)
+    q, k, v, beta, g = gdp.gdp_decode_prepare(d["x"].to(DEV), d["ba"].to(DEV),
+                                              d["A_log"].to(DEV), d["dt_bias"].to(DEV), M, H, G,
+                                              P, N)
+    state = si.decode_state(n, H, N, P).to(DEV)
+    s0 = state.cpu()
+    o = gdp.gdp_recurrent_update(q, k, v, beta, g, state, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    rq, rk, rv, rb, rg = oracle.prepare(d["x"], d["ba"], d["A_log"], d["dt_bias"], M, H, G, P, N,
+                                        decode=True)
+    ro, rs = oracle.recurrent(rq, rk, rv, rb, rg, s0, N ** -0.5, l2norm=True)
+    assert rel_err(o, ro) <= 2e-3
+    assert rel_err(state, rs) <= 2e-3
+
+
+@pytest.mark.parametrize("n,L,H,HV,K,V,dtype,l2", [
+    (3, 5, 2, 2, 32, 16, torch.float32, True),
+    (2, 8, 1, 4, 64, 128, torch.float32, False),     # GVA
+    (4, 3, 2, 2, 256, 136, torch.bfloat16, True),    # several CTAs along V, ragged slice
+    (2, 4, 2, 2, 128, 128, torch.float16, True),
+])
+def test_recurrent_small(gdp, n, L, H, HV, K, V, dtype, l2):
+    gen = torch.Generator().manual_seed(n * L + K)
+    q = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    k = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    v = torch.randn(n, L, HV, V, generator=gen).to(dtype)
+    beta = torch.rand(n, L, HV, generator=gen)
+    g = -torch.rand(n, L, HV, generator=gen)
+    state = torch.randn(n, HV, K, V, generator=gen) * 0.1
+    ro, rs = oracle.recurrent(q, k, v, beta, g, state, K ** -0.5, l2norm=l2)
+    sd = state.to(DEV)
+    o = gdp.gdp_recurrent_update(*to(DEV, q, k, v, beta, g), sd, use_qk_l2norm=l2)
+    torch.cuda.synchronize()
+    assert rel_err(o, ro) <= TOL[dtype]
+    assert rel_err(sd, rs) <= TOL[dtype]
+
+
+def test_recurrent_matches_chunked_prefill(gdp):
+    """Walking a prefill's copies one step at a time (q on the last copy, g on the
+    first) gives the chunked forward's outputs and final state."""
+    B, T, H, HV, K, V, M = 2, 40, 2, 2, 64, 64, 3
+    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=2)
+    qd, kd, vd, bd, gd = to(DEV, q, k, v, beta, g)
+    o, fs = gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, chunk_size=64, num_householder=M,
+                              use_qk_l2norm=True)
+    qp = torch.zeros(B, T * M, H, K, dtype=q.dtype, device=DEV)
+    qp.view(B, T, M, H, K)[:, :, M - 1] = qd
+    gp = torch.zeros(B, T * M, HV, device=DEV)
+    gp.view(B, T, M, HV)[:, :, 0] = gd
+    state = torch.zeros(B, HV, K, V, device=DEV)
+    od = gdp.gdp_recurrent_update(qp, kd, vd, bd, gp, state, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert rel_err(od.view(B, T, M, HV, V)[:, :, M - 1], o) <= 1e-4
+    assert rel_err(state, fs) <= 1e-4
+
+
+def test_graph_capture_replay(gdp):
+    """Static shapes, no host sync: the decode step captures into a CUDA graph."""
+    w = si.WORKLOADS["decode"].dims
+    n, S, M, H, G, P, N = 16, w["S"], w["M"], w["H"], w["G"], w["P"], w["N"]
+    d = si.prepare_inputs(n, S, M, H, G, P, N, seed=3)
+    x, ba = d["x"].to(DEV), d["ba"].to(DEV)
+    A_log, dt_bias = d["A_log"].to(DEV), d["dt_bias"].to(DEV)
+    s_init = si.decode_state(n, H, N, P).to(DEV)
+    outs = gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N)
+    state = s_init.clone()
+    o = torch.empty(n, S * M, H, P, device=DEV)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # warm up
+        gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
+        gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True, out=o)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
+        gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True, out=o)
+    state.copy_(s_init)
+    graph.replay()
+    torch.cuda.synchronize()
+    o_graph, s_graph = o.clone(), state.clone()
+    state.copy_(s_init)
+    gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
+    o2 = gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_graph, o2) and torch.equal(s_graph, state)
