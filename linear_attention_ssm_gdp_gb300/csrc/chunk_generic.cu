@@ -8,15 +8,16 @@
 // delta rule over the Householder-expanded stream, copy j of token t at t*M+j):
 //   tables   device-built chunk descriptors from cu_seqlens (no host sync)
 //   wy       per expanded chunk of BT positions: Gam = inclusive cumsum of the
-//            per-position decay in log2 units (g_t on a token's first copy),
-//            L[p,i] = beta_p 2^(Gam_p-Gam_i) k_p.k_i (i<p), A = (I+L)^-1
-//            (solve_tril, forward substitution), w = A(beta 2^Gam k),
+//            per-position log decay (g_t on a token's first copy, 0 on the
+//            others), kept as a compensated two-float sum,
+//            L[p,i] = beta_p e^(Gam_p-Gam_i) k_p.k_i (i<p), A = (I+L)^-1
+//            (solve_tril, forward substitution), w = A(beta e^Gam k),
 //            u = A(beta v)  (recompute_w_u)
 //   chunk_h  per (sequence, value head, value slice), sequential over chunks:
-//            v_new = u - w h ; h <- 2^Gam_last h + (k 2^(Gam_last-Gam))^T v_new;
+//            v_new = u - w h ; h <- e^Gam_last h + (k e^(Gam_last-Gam))^T v_new;
 //            the state at each token-chunk start is stored for chunk_o
-//   chunk_o  per token chunk of BT tokens: o_t = scale (2^Gt_t q_t.h_c +
-//            sum_{s<=t} sum_j 2^(Gt_t-Gt_s) (q_t.k_{s,j}) v_new_{s,j}), the
+//   chunk_o  per token chunk of BT tokens: o_t = scale (e^Gt_t q_t.h_c +
+//            sum_{s<=t} sum_j e^(Gt_t-Gt_s) (q_t.k_{s,j}) v_new_{s,j}), the
 //            token chunk c starting at expanded chunk c*M.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -26,7 +27,24 @@
 namespace gdp {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+// Inclusive prefix sum of the per-position log decays, compensated (Neumaier):
+// hi[p] + lo[p] carries the sum to about twice fp32 precision, so that the
+// difference of two prefixes, (hi[p]-hi[i]) + (lo[p]-lo[i]), stays accurate
+// even when the prefixes themselves are large (strong decay over a chunk).
+__device__ __forceinline__ void comp_prefix(float* hi, float* lo, int n) {
+  float s = 0.f, c = 0.f;
+  for (int p = 0; p < n; ++p) {
+    const float x = hi[p];
+    const float t = s + x;
+    c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+    s = t;
+    hi[p] = s;
+    lo[p] = c;
+  }
+}
+__device__ __forceinline__ float gam_diff(const float* hi, const float* lo, int p, int i) {
+  return (hi[p] - hi[i]) + (lo[p] - lo[i]);
+}
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -129,8 +147,9 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
   float* Ls = ks + BT * KP;       // [BT][BP]
   float* As = Ls + BT * BP;       // [BT][BP]
   float* sb = As + BT * BP;       // beta
-  float* sG = sb + BT;            // Gam (log2)
-  float* srk = sG + BT;           // 1/|k| or 1
+  float* sG = sb + BT;            // Gam, compensated prefix: high part
+  float* sGl = sG + BT;           //                            low part
+  float* srk = sGl + BT;          // 1/|k| or 1
   const Tin* kin = static_cast<const Tin*>(a.k);
   const Tin* vin = static_cast<const Tin*>(a.v);
   const int tid = threadIdx.x, nth = blockDim.x;
@@ -140,7 +159,7 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
     if (p < n) {
       const int e = e_start + p, t = e / M, jj = e - t * M;
       b = a.beta[(R0 + p) * a.HV + hv];
-      if (a.g && jj == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv] * kLog2e;
+      if (a.g && jj == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv];
     }
     sb[p] = b;
     sG[p] = gl;
@@ -150,10 +169,7 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
     ks[p * KP + c] = p < n ? ldf(kin + ((R0 + p) * a.H + kh) * K + c) : 0.f;
   }
   __syncthreads();
-  if (tid == 0) {
-    float acc = 0.f;
-    for (int p = 0; p < BT; ++p) { acc += sG[p]; sG[p] = acc; }
-  }
+  if (tid == 0) comp_prefix(sG, sGl, BT);
   {
     const int wid = tid >> 5, lane = tid & 31, nw = nth >> 5;
     for (int p = wid; p < BT; p += nw) {
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
     if (i < p && p < n) {
       float d = 0.f;
       for (int c = 0; c < K; ++c) d += ks[p * KP + c] * ks[i * KP + c];
-      val = sb[p] * exp2f(sG[p] - sG[i]) * srk[p] * srk[i] * d;
+      val = sb[p] * expf(gam_diff(sG, sGl, p, i)) * srk[p] * srk[i] * d;
     }
     Ls[p * BP + i] = val;
     As[p * BP + i] = (p == i) ? 1.f : 0.f;
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
     const int p = i2 / K, c = i2 - p * K;
     float s = 0.f;
     for (int i = 0; i <= p; ++i)
-      s += As[p * BP + i] * (sb[i] * exp2f(sG[i]) * srk[i]) * ks[i * KP + c];
+      s += As[p * BP + i] * (sb[i] * expf(sG[i] + sGl[i]) * srk[i]) * ks[i * KP + c];
     a.w[((R0 + p) * a.HV + hv) * K + c] = s;
   }
   // u = A (beta v)
@@ -206,7 +222,10 @@ __global__ void __launch_bounds__(256) wy_generic_kernel(GenArgs a) {
       s += As[p * BP + i] * sb[i] * ldf(vin + ((R0 + i) * a.HV + hv) * V + c);
     a.u[((R0 + p) * a.HV + hv) * V + c] = s;
   }
-  for (int p = tid; p < n; p += nth) a.gexp[(R0 + p) * a.HV + hv] = sG[p];
+  for (int p = tid; p < n; p += nth) {
+    a.gexp[2 * ((R0 + p) * a.HV + hv)] = sG[p];
+    a.gexp[2 * ((R0 + p) * a.HV + hv) + 1] = sGl[p];
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -228,8 +247,9 @@ __global__ void __launch_bounds__(256) h_generic_kernel(GenArgs a) {
   float* ks = ws + BT * KP;       // [BT][KP]
   float* us = ks + BT * KP;       // [BT][kBVH]
   float* vn = us + BT * kBVH;     // [BT][kBVH]
-  float* sG = vn + BT * kBVH;     // [BT]
-  float* srk = sG + BT;           // [BT]
+  float* sG = vn + BT * kBVH;     // [BT] Gam high part
+  float* sGl = sG + BT;           // [BT] Gam low part
+  float* srk = sGl + BT;          // [BT]
   const Tin* kin = static_cast<const Tin*>(a.k);
   const int tid = threadIdx.x, nth = blockDim.x;
   const int64_t hoff = ((int64_t)seq * a.HV + hv) * K * V;
@@ -261,7 +281,10 @@ __global__ void __launch_bounds__(256) h_generic_kernel(GenArgs a) {
       const int p = i / kBVH, c = i - p * kBVH;
       us[i] = (p < n && c < nv) ? a.u[((R0 + p) * a.HV + hv) * V + v0 + c] : 0.f;
     }
-    for (int p = tid; p < BT; p += nth) sG[p] = p < n ? a.gexp[(R0 + p) * a.HV + hv] : 0.f;
+    for (int p = tid; p < BT; p += nth) {
+      sG[p] = p < n ? a.gexp[2 * ((R0 + p) * a.HV + hv)] : 0.f;
+      sGl[p] = p < n ? a.gexp[2 * ((R0 + p) * a.HV + hv) + 1] : 0.f;
+    }
     __syncthreads();
     {
       const int wid = tid >> 5, lane = tid & 31, nw = nth >> 5;
@@ -282,13 +305,14 @@ __global__ void __launch_bounds__(256) h_generic_kernel(GenArgs a) {
       if (p < n && c < nv) a.v_new[((R0 + p) * a.HV + hv) * V + v0 + c] = val;
     }
     __syncthreads();
-    const float glast = sG[n - 1];
-    // h <- 2^Gam_last h + (k 2^(Gam_last - Gam) / |k|)^T v_new
+    const float dlast = expf(sG[n - 1] + sGl[n - 1]);
+    // h <- e^Gam_last h + (k e^(Gam_last - Gam) / |k|)^T v_new
     for (int i = tid; i < K * kBVH; i += nth) {
       const int r = i / kBVH, c = i - r * kBVH;
       float s = 0.f;
-      for (int p = 0; p < n; ++p) s += ks[p * KP + r] * srk[p] * exp2f(glast - sG[p]) * vn[p * kBVH + c];
-      hs[i] = exp2f(glast) * hs[i] + s;
+      for (int p = 0; p < n; ++p)
+        s += ks[p * KP + r] * srk[p] * expf(gam_diff(sG, sGl, n - 1, p)) * vn[p * kBVH + c];
+      hs[i] = dlast * hs[i] + s;
     }
   }
   __syncthreads();
@@ -320,8 +344,9 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
   const int ne = nt * M;
   const int64_t T0 = (int64_t)si.x + t_start;  // first global token
   const int64_t E0 = T0 * M;                   // first global expanded row
-  float* sGt = sm;                   // [BT]
-  float* srq = sGt + BT;             // [BT]
+  float* sGt = sm;                   // [BT] token-chunk Gam, high part
+  float* sGtl = sGt + BT;            // [BT] low part
+  float* srq = sGtl + BT;            // [BT]
   float* srk = srq + BT;             // [BT*M]
   float* qt = srk + BT * M;          // [BT][kKT+1]
   float* kt = qt + BT * (kKT + 1);   // [kEB][kKT+1]
@@ -335,7 +360,7 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
   const float* hc = a.h + (((int64_t)si.w + tab.y) * a.HV + hv) * K * V;
 
   for (int p = tid; p < BT; p += nth)
-    sGt[p] = (p < nt && a.g) ? a.g[(T0 + p) * a.HV + hv] * kLog2e : 0.f;
+    sGt[p] = (p < nt && a.g) ? a.g[(T0 + p) * a.HV + hv] : 0.f;
   for (int t = wid; t < BT; t += nw) {
     float ss = 0.f;
     if (t < nt)
@@ -357,10 +382,7 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
     if (lane == 0) srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
   __syncthreads();
-  if (tid == 0) {
-    float acc = 0.f;
-    for (int p = 0; p < BT; ++p) { acc += sGt[p]; sGt[p] = acc; }
-  }
+  if (tid == 0) comp_prefix(sGt, sGtl, BT);
   // thread owns column c of rows tg, tg+4, ...
   const int c = tid % kBVO, tg = tid / kBVO;
   constexpr int RPT = 64 / 4;  // rows per thread for BT <= 64 with 256 threads
@@ -393,7 +415,7 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
 #pragma unroll
   for (int r = 0; r < RPT; ++r) {
     const int t = tg + 4 * r;
-    if (t < BT) acc[r] *= exp2f(sGt[t]) * srq[t];
+    if (t < BT) acc[r] *= expf(sGt[t] + sGtl[t]) * srq[t];
   }
   // intra-chunk term, expanded positions in tiles of kEB
   for (int e0 = 0; e0 < ne; e0 += kEB) {
@@ -426,7 +448,7 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
       const int eg = e0 + e, s = eg / M;
       float val = 0.f;
       if (t < nt && eg < ne && s <= t)
-        val = Ps[t * (kEB + 1) + e] * srq[t] * srk[eg] * exp2f(sGt[t] - sGt[s]);
+        val = Ps[t * (kEB + 1) + e] * srq[t] * srk[eg] * expf(gam_diff(sGt, sGtl, t, s));
       Ps[t * (kEB + 1) + e] = val;
     }
     for (int i = tid; i < kEB * kBVO; i += nth) {
@@ -457,10 +479,10 @@ __global__ void __launch_bounds__(256) o_generic_kernel(GenArgs a) {
 template <typename Tin>
 cudaError_t run_generic(const ChunkProblem& p, const GenArgs& a) {
   const int BT = p.BT, K = p.K;
-  const size_t smem_wy = sizeof(float) * ((size_t)BT * (K + 1) + 2 * (size_t)BT * (BT + 1) + 3 * BT);
+  const size_t smem_wy = sizeof(float) * ((size_t)BT * (K + 1) + 2 * (size_t)BT * (BT + 1) + 4 * BT);
   const size_t smem_h = sizeof(float) * ((size_t)K * kBVH + 2 * (size_t)BT * (K + 1) +
-                                         2 * (size_t)BT * kBVH + 2 * BT);
-  const size_t smem_o = sizeof(float) * (2 * (size_t)BT + (size_t)BT * p.M + BT * (kKT + 1) +
+                                         2 * (size_t)BT * kBVH + 3 * BT);
+  const size_t smem_o = sizeof(float) * (3 * (size_t)BT + (size_t)BT * p.M + BT * (kKT + 1) +
                                          kEB * (kKT + 1) + BT * (kEB + 1) + kKT * kBVO +
                                          kEB * kBVO);
   cudaError_t e;
@@ -510,7 +532,7 @@ WsLayout generic_layout(int B, int T, int N_seq, int H, int HV, int K, int V, in
   L.A = take(sizeof(float) * Te * HV * BT);
   L.w = take(sizeof(float) * Te * HV * K);
   L.u = take(sizeof(float) * Te * HV * V);
-  L.gexp = take(sizeof(float) * Te * HV);
+  L.gexp = take(sizeof(float) * Te * HV * 2);
   L.v_new = take(sizeof(float) * Te * HV * V);
   L.h = take(sizeof(float) * (size_t)NT * HV * K * V);
   L.total = off;

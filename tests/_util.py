@@ -20,11 +20,20 @@ def rel_err(got, want) -> float:
     return (got - want).abs().max().item() / max(rms, 1e-300)
 
 
-def chunk_case(B, T, H, HV, K, V, M, seed=0, dtype=torch.bfloat16, gated=True):
-    """Seeded raw inputs plus oracle-computed gates (identical bits for both sides)."""
+def chunk_case(B, T, H, HV, K, V, M, seed=0, dtype=torch.bfloat16, gated=True, shrink=False):
+    """Seeded raw inputs plus oracle-computed gates (identical bits for both sides).
+
+    shrink=True scales q and k by K**-0.5 (then re-rounds to ``dtype``) so that
+    runs without the in-kernel L2 norm keep beta*|k|^2 near 1; with raw N(0,1)
+    keys the delta rule's transition has eigenvalues far below -1 and the
+    recurrence diverges, which no finite-precision path can follow."""
     d = si.chunk_inputs(B, T, H, HV, K, V, M, seed=seed, dtype=dtype)
+    q, k = d["q"], d["k"]
+    if shrink:
+        q = (q.float() * K ** -0.5).to(dtype)
+        k = (k.float() * K ** -0.5).to(dtype)
     beta, g = oracle.gate_map(d["b"], d["a"], d["A_log"], d["dt_bias"])
-    return d["q"], d["k"], d["v"], beta, (g if gated else None)
+    return q, k, d["v"], beta, (g if gated else None)
 
 
 def to(dev, *ts):

@@ -45,7 +45,8 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
 def test_chunk_fwd_matches_walk(gdp, case):
     B, T, H, HV, K, V, M, BT, dtype, l2, gated, with_h0 = case
-    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=T + K, dtype=dtype, gated=gated)
+    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=T + K, dtype=dtype, gated=gated,
+                                  shrink=not l2)
     h0 = torch.randn(B, HV, K, V, generator=torch.Generator().manual_seed(3)) if with_h0 else None
     o, fs = _run(gdp, q, k, v, beta, g, M, BT, l2, h0=h0)
     ro, rfs = oracle.walk(q, k, v, beta, g, M, K ** -0.5, h0=h0, l2norm=l2)
@@ -160,9 +161,10 @@ def test_stages_match_chunked_restatement(gdp, K, V, M, dtype):
             *shape).cpu().double()
 
     for hv in range(HV):
-        ref = oracle.chunked_stream(q[0, :, hv].numpy(), k[0, :, hv].numpy(),
-                                    v[0, :, hv].numpy(), beta[0, :, hv].numpy(),
-                                    g[0, :, hv].numpy(), M, BT, K ** -0.5, l2norm=True)
+        f = lambda x: x.double().numpy()
+        ref = oracle.chunked_stream(f(q[0, :, hv]), f(k[0, :, hv]), f(v[0, :, hv]),
+                                    f(beta[0, :, hv]), f(g[0, :, hv]), M, BT, K ** -0.5,
+                                    l2norm=True)
         if off[0] != NONE:
             A = view(0, (Te, HV, BT))[:, hv]
             for c, Ac in enumerate(ref["A"]):
