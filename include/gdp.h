@@ -192,6 +192,31 @@ gdp_status gdp_read_status(const void* workspace, cudaStream_t stream);
 gdp_status gdp_chunk_fwd_stage_offsets(int B, int T, int N_seq, int H, int HV, int K, int V,
                                        int M, int chunk_size, gdp_dtype dt, size_t* out);
 
+/*
+ * gdp_chunk_fwd_noalloc - gdp_chunk_fwd for callers that cannot allocate
+ * device memory. The pages have no counterpart to this call; it exists for
+ * callers that run under a memory budget fixed in advance, from inside
+ * another allocator's callbacks, or in loops that must never reach
+ * cudaMalloc/cudaFree (which can synchronise the device), and so cannot
+ * provide a workspace.
+ * Arguments and outputs are those of gdp_chunk_fwd without the workspace.
+ * Scratch: a 32 MiB array in device memory that the library holds on every
+ * GPU that loads it, until the process exits. Problems whose workspace
+ * (gdp_chunk_fwd_workspace_size) exceeds 32 MiB are rejected with
+ * GDP_ERR_WORKSPACE before anything is launched. The call allocates nothing.
+ * All calls share the array and it keeps the previous call's contents; each
+ * call clears what must start at zero. Calls that overlap on the GPU (other
+ * streams or host threads) race on the array: serialise them.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.
+ */
+gdp_status gdp_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* beta,
+                                 const float* g, const float* initial_state,
+                                 const int32_t* cu_seqlens, int N_seq, int B, int T, int H,
+                                 int HV, int K, int V, int M, int chunk_size, float scale,
+                                 int use_qk_l2norm, gdp_dtype dt, float* o, float* final_state,
+                                 cudaStream_t stream);
+
 /* Number of stage-boundary events gdp_set_stage_events takes. */
 #define GDP_STAGE_EVENTS 5
 

@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "load", "GDPError", "gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
     "gdp_chunk_fwd_workspace_size", "gdp_chunk_fwd_stage_offsets", "gdp_recurrent_update",
-    "gdp_read_status", "gdp_version", "gdp_set_stage_events", "LIB_PATH",
+    "gdp_read_status", "gdp_version", "gdp_set_stage_events", "gdp_chunk_fwd_noalloc",
+    "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdp.so")
@@ -56,6 +57,8 @@ def load() -> ctypes.CDLL:
             lib.gdp_chunk_fwd_stage_offsets.argtypes = [I] * 9 + [I, P]
             lib.gdp_chunk_fwd.argtypes = ([P] * 7 + [I] * 9 + [F, I, I] + [P, P, P, SZ, P])
             lib.gdp_recurrent_update.argtypes = [P] * 6 + [I] * 6 + [F, I, I, P, P]
+            lib.gdp_chunk_fwd_noalloc.argtypes = [P] * 7 + [I] * 9 + [F, I, I] + [P, P, P]
+            lib.gdp_chunk_fwd_noalloc.restype = I
             lib.gdp_read_status.argtypes = [P, P]
             lib.gdp_set_stage_events.argtypes = [P, I]
             lib.gdp_set_stage_events.restype = I
@@ -228,6 +231,37 @@ def gdp_set_stage_events(events):
         e.record()  # forces the lazy creation of the CUDA event
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("gdp_set_stage_events", lib.gdp_set_stage_events(arr, len(events)))
+
+
+def gdp_chunk_fwd_noalloc(q, k, v, beta, g=None, cu_seqlens=None, chunk_size: int = 64,
+                          num_householder: int = 1, scale: float | None = None,
+                          initial_state=None, use_qk_l2norm: bool = False,
+                          output_final_state: bool = True, out=None):
+    """gdp_chunk_fwd without a caller workspace: the library's fixed 32 MiB device
+    scratch array is used instead, for callers that cannot allocate device memory
+    (fixed memory budgets, allocator callbacks, loops that must not reach
+    cudaMalloc). Outputs are still allocated here unless ``out`` is given; pass
+    ``out`` to allocate nothing. Larger problems raise GDPError (workspace).
+    Calls sharing the array must not overlap on the GPU."""
+    _need_cuda(q, k, v, beta, g, cu_seqlens, initial_state)
+    M = int(num_householder)
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    if out is None:
+        o = torch.empty((B, T, HV, V), dtype=torch.float32, device=q.device)
+        fs = (torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+              if output_final_state else None)
+    else:
+        o, fs = out
+    st = load().gdp_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(beta), _p(g), _p(initial_state),
+                                      _p(cu_seqlens), N, B, T, H, HV, K, V, M, int(chunk_size),
+                                      float(scale), 1 if use_qk_l2norm else 0, _DTYPE[q.dtype],
+                                      _p(o), _p(fs), _stream(q.device))
+    _check("gdp_chunk_fwd_noalloc", st)
+    return o, fs
 
 
 def gdp_read_status(workspace) -> int:

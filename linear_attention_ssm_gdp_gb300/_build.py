@@ -30,6 +30,7 @@ UNITS = {
     "chunk_generic.cu": [],
     "chunk_tc.cu": [],
     "recurrent.cu": [],
+    "noalloc.cu": [],
 }
 
 
