@@ -1,17 +1,942 @@
-// Tensor-core (tcgen05) chunked forward: not built yet; every problem goes
-// through the generic path.
+// Tensor-core chunked Gated Delta Product forward for GB300 (sm_103a):
+// bf16 inputs, K = 128, chunk 64, V in {64, 128, 256}, M <= 3.
+//
+// Same stages and algebra as the generic path (Megatron-core API pages
+// "core.ssm.ops.gdp.wy_fast" and "core.ssm.ops.gdp.chunk_o"; the WY form of
+// the gated delta rule over the Householder-expanded stream), with every
+// dense contraction on the 5th-generation tensor core: operands staged in
+// shared memory by TMA (128-byte swizzle), tcgen05.mma issued by one thread,
+// fp32 accumulators in TMEM read back with tcgen05.ld.
+//
+// Precision. Raw q, k, v are bf16 and enter the MMAs exactly; the L2 norms,
+// gates and decays are applied as fp32 row/column scales outside the MMAs.
+// Every operand computed on chip (A, h, v_new, the score matrix P) is split
+// into bf16 hi + lo (x = hi + lo to ~2^-16 relative) and a product of two
+// such operands takes three MMAs (hi*hi + hi*lo + lo*hi), a product with an
+// exact operand two. One bf16 rounding of any of them would by itself cost
+// about 2^-9 of the output RMS per element.
+//
+// Kernels (one launch each):
+//   wy  grid (expanded chunk, HV): Gram matrix k k^T (MMA), transition block
+//       L and its inverse A = (I+L)^-1 (blocked forward substitution in fp32
+//       on CUDA cores), then w = (A diag(beta e^Gam/|k|)) k and
+//       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32.
+//   h   grid (sequence, HV, 32-column slice of V): the sequential chunk-state
+//       recurrence, fp32 state in registers (thread = state row), per chunk
+//       v_new = u - w h (3 MMA passes) and h <- e^Gam_last h + k^T (e^(Gam_last
+//       - Gam)/|k| v_new) (2 passes); inputs double-buffered by TMA; writes
+//       v_new (hi/lo) and the state at every token-chunk start (hi/lo).
+//   o   grid (token chunk, HV, 64-column slice): scores q k^T (MMA), q h
+//       (2 passes), P = masked decayed scores (fp32 -> hi/lo), P v_new
+//       (3 passes), o = scale (e^Gt |q|^-1 q h + P v_new).
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "gdp_internal.cuh"
+#include "ptx.cuh"
 
 namespace gdp {
+namespace {
 
-bool tc_supported(int, int, int, int, int, int, gdp_dtype) { return false; }
+using bf16 = __nv_bfloat16;
+using namespace ptx;
 
-WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, int BT) {
-  return generic_layout(B, T, N_seq, H, HV, K, V, M, BT);
+constexpr int kBT = 64;    // chunk length (positions for wy/h, tokens for o)
+constexpr int kK = 128;    // key/query head dimension
+constexpr int kHBV = 32;   // value columns per chunk_h CTA
+constexpr int kOBV = 64;   // value columns per chunk_o CTA
+
+// ------------------------------------------------------------------ helpers
+__device__ __forceinline__ float gam_diff4(const float* hi, const float* lo, int p, int i) {
+  return (hi[p] - hi[i]) + (lo[p] - lo[i]);
 }
 
-cudaError_t launch_chunk_tc(const ChunkProblem&, const WsLayout&, uint8_t*) {
-  return cudaErrorNotSupported;
+// Neumaier-compensated inclusive prefix sum, serial (n <= 64).
+__device__ __forceinline__ void comp_prefix(float* hi, float* lo, int n) {
+  float s = 0.f, c = 0.f;
+  for (int p = 0; p < n; ++p) {
+    const float x = hi[p];
+    const float t = s + x;
+    c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+    s = t;
+    hi[p] = s;
+    lo[p] = c;
+  }
+}
+
+__device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
+  hi = __float2bfloat16_rn(x);
+  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// Sum of squares of one 128-byte row of bf16 (any chunk order).
+__device__ __forceinline__ float row_sumsq(const uint8_t* row) {
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 u = reinterpret_cast<const uint4*>(row)[j];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float a = __uint_as_float(w[t] << 16), b = __uint_as_float(w[t] & 0xffff0000u);
+      s += a * a + b * b;
+    }
+  }
+  return s;
+}
+
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const bf16* src) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    reinterpret_cast<uint4*>(dst)[j] = reinterpret_cast<const uint4*>(src)[j];
+}
+
+// Ends the CTA's tensor-core use: make every thread's TMEM traffic complete,
+// then free the columns (warp 0).
+__device__ __forceinline__ void tmem_release(uint32_t tmem, uint32_t ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, ncols);
+}
+
+// ============================================================================ wy
+struct WyArgs {
+  int H, HV, V, M, l2norm;
+  int64_t Te;
+  const float* beta;
+  const float* g;
+  const int4* seq_info;
+  const int2* exp_tab;
+  bf16* w_hi;
+  bf16* w_lo;
+  float* u;
+  float4* gk;  // [HV][Te]: (Gam hi, Gam lo, 1/|k|, 0)
+  int* status;
+};
+
+// Shared memory (offsets from a 1024-aligned base). Operand tiles hold 64
+// rows of 128 bytes (one 128B-swizzle row each); MMA views with M = 128 read
+// 128 rows, i.e. 8 KB past a tile, which always lands on other live data and
+// only feeds accumulator rows 64..127 that are never read.
+constexpr int WY_K = 0;                     // k: 2 K-halves at stride 8 KB (+8 KB view)
+constexpr int WY_V = 24576;                 // v: V/64 column chunks of 8 KB
+constexpr int wy_a_off(int V) { return WY_V + (V / 64) * 8192; }   // A'hi A'lo A''hi A''lo
+constexpr int wy_l_off(int V) { return wy_a_off(V) + 4 * 8192; }   // L fp32 [64][65]
+constexpr int wy_i_off(int V) { return wy_l_off(V) + 64 * 65 * 4; }  // A fp32 [64][65]
+constexpr int wy_s_off(int V) { return wy_i_off(V) + 64 * 65 * 4; }  // small arrays
+constexpr int wy_smem(int V) { return wy_s_off(V) + 6 * 64 * 4 + 64 + 1024; }
+
+// Blocked inversion of the unit lower-triangular 64x64 matrix I + L (L strictly
+// lower, row stride 65) into A (row stride 65): 16x16 diagonal blocks by
+// column-parallel forward substitution, then two merge levels
+// A10 = -A11 (L10 A00). X is a 32x33 scratch. 256 threads.
+__device__ void solve_tril64(const float* Ls, float* As, float* X) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 64 * 65; i += 256) As[i] = 0.f;
+  __syncthreads();
+  if (tid < 64) {  // level 0: block b, column c
+    const int b = tid >> 4, c = tid;  // absolute column
+    const int r_end = (b + 1) * 16;
+    float col[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) col[i] = 0.f;
+    col[c - b * 16] = 1.f;
+    for (int r = c + 1; r < r_end; ++r) {
+      float s = 0.f;
+      for (int i = c; i < r; ++i) s += Ls[r * 65 + i] * col[i - b * 16];
+      col[r - b * 16] = -s;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) As[(b * 16 + i) * 65 + c] = col[i];
+  }
+  __syncthreads();
+  // level 1: two pairs of 16-blocks; level 2: one pair of 32-blocks
+#pragma unroll 1
+  for (int lvl = 0; lvl < 2; ++lvl) {
+    const int sz = lvl == 0 ? 16 : 32;      // size of the blocks being merged
+    const int npairs = lvl == 0 ? 2 : 1;
+    // X = L10 A00  (X stored per pair at X + pair * sz * 33)
+    for (int idx = tid; idx < npairs * sz * sz; idx += 256) {
+      const int pair = idx / (sz * sz), rc = idx - pair * sz * sz;
+      const int r = rc / sz, c = rc - r * sz;
+      const int base = pair * 2 * sz;
+      float s = 0.f;
+      for (int i = c; i < sz; ++i) s += Ls[(base + sz + r) * 65 + base + i] * As[(base + i) * 65 + base + c];
+      X[pair * sz * 33 + r * 33 + c] = s;
+    }
+    __syncthreads();
+    // A10 = -A11 X
+    for (int idx = tid; idx < npairs * sz * sz; idx += 256) {
+      const int pair = idx / (sz * sz), rc = idx - pair * sz * sz;
+      const int r = rc / sz, c = rc - r * sz;
+      const int base = pair * 2 * sz;
+      float s = 0.f;
+      for (int i = 0; i <= r; ++i) s += As[(base + sz + r) * 65 + base + sz + i] * X[pair * sz * 33 + i * 33 + c];
+      As[(base + sz + r) * 65 + base + c] = -s;
+    }
+    __syncthreads();
+  }
+}
+
+template <int V>
+__global__ void __launch_bounds__(256, 1) wy_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+                                                       const __grid_constant__ CUtensorMap map_v,
+                                                       WyArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int2 tab = a.exp_tab[blockIdx.x];
+  if (tab.x < 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int4 si = a.seq_info[tab.x];
+  const int M = a.M;
+  const int e_start = tab.y * kBT;
+  const int n = min(kBT, si.y * M - e_start);
+  const int64_t R0 = (int64_t)si.x * M + e_start;
+
+  uint8_t* kbuf = sm + WY_K;
+  uint8_t* vbuf = sm + WY_V;
+  uint8_t* atile = sm + wy_a_off(V);
+  float* Ls = reinterpret_cast<float*>(sm + wy_l_off(V));
+  float* As = reinterpret_cast<float*>(sm + wy_i_off(V));
+  float* X = reinterpret_cast<float*>(atile);  // solve scratch, dead before the A tiles
+  float* sb = reinterpret_cast<float*>(sm + wy_s_off(V));
+  float* sgh = sb + 64;
+  float* sgl = sgh + 64;
+  float* srk = sgl + 64;
+  float* sco = srk + 64;   // beta e^Gam / |k|
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 64);  // [0] tma, [1] mma
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2);
+  constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
+
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (tid < kBT) {
+    float b = 0.f, gl = 0.f;
+    if (tid < n) {
+      const int e = e_start + tid, t = e / M;
+      b = a.beta[(R0 + tid) * a.HV + hv];
+      if (a.g && e - t * M == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv];
+    }
+    sb[tid] = b;
+    sgh[tid] = gl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  if (tid == 0) {
+    mbar_expect_tx(&bars[0], 2 * 8192 + (V / 64) * 8192);
+    tma_load_3d(kbuf, &map_k, 0, kh, (int)R0, &bars[0]);
+    tma_load_3d(kbuf + 8192, &map_k, 64, kh, (int)R0, &bars[0]);
+#pragma unroll
+    for (int c = 0; c < V / 64; ++c) tma_load_3d(vbuf + c * 8192, &map_v, 64 * c, hv, (int)R0, &bars[0]);
+    comp_prefix(sgh, sgl, kBT);
+  }
+  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  if (tid == 0) {  // Gram matrix k k^T: M = 128 (rows 64.. unused), N = 64, K = 128
+    const uint32_t kb = smem_u32(kbuf);
+    const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+      mma_bf16(tmem, d, d, id, kk > 0);
+    }
+    mma_commit(&bars[1]);
+  }
+  if (tid < kBT) {
+    const float ss = row_sumsq(kbuf + tid * 128) + row_sumsq(kbuf + 8192 + tid * 128);
+    const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    srk[tid] = r;
+    sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
+  }
+  ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
+  tc_fence_after();
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  // transition block L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|), i < p
+  if ((warp & 3) < 2) {
+    const int p = (warp & 3) * 32 + lane, c0 = (warp >> 2) * 32;
+    uint32_t r[32];
+    GDP_TMEM_LD32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0, r);
+    tmem_wait_ld();
+    const float bp = sb[p] * srk[p];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int i = c0 + j;
+      Ls[p * 65 + i] = (i < p) ? bp * expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
+    }
+  }
+  __syncthreads();
+  solve_tril64(Ls, As, X);
+  // A' = A diag(beta e^Gam / |k|), A'' = A diag(beta), split into bf16 hi + lo,
+  // written as K-major operand tiles (row p, column i) with the 128B swizzle
+  for (int idx = tid; idx < 64 * 64; idx += 256) {
+    const int p = idx >> 6, i = idx & 63;
+    const float av = As[p * 65 + i];
+    bf16 h1, l1, h2, l2;
+    split_bf16(av * sco[i], h1, l1);
+    split_bf16(av * sb[i], h2, l2);
+    const uint32_t off = sw128_offset(p, i * 2);
+    *reinterpret_cast<bf16*>(atile + 0 * 8192 + off) = h1;
+    *reinterpret_cast<bf16*>(atile + 1 * 8192 + off) = l1;
+    *reinterpret_cast<bf16*>(atile + 2 * 8192 + off) = h2;
+    *reinterpret_cast<bf16*>(atile + 3 * 8192 + off) = l2;
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t ab = smem_u32(atile), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
+    const uint32_t idw = idesc_bf16(128, 128, false, true);
+    const uint32_t idu = idesc_bf16(128, V, false, true);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // K = 64 positions
+        const uint64_t ad = sdesc_sw128(ab + pass * 8192 + kk * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(kb + kk * 2048, 8192, 1024);
+        mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
+      }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = sdesc_sw128(ab + (2 + pass) * 8192 + kk * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(vb + kk * 2048, 8192, 1024);
+        mma_bf16(tmem + 128, ad, bd, idu, (pass | kk) != 0);
+      }
+    mma_commit(&bars[1]);
+  }
+  ok = mbar_wait(&bars[1], 1, a.status, kDevTimeout);
+  tc_fence_after();
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  if ((warp & 3) < 2) {
+    const int p = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    if (warp < 4) {  // w: 128 columns -> bf16 hi/lo
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t r[32];
+        GDP_TMEM_LD32(lane_addr + c0, r);
+        tmem_wait_ld();
+        if (p < n) {
+          bf16 hi[32], lo[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
+          const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
+          store_bf16x32(a.w_hi + row, hi);
+          store_bf16x32(a.w_lo + row, lo);
+        }
+      }
+      if (p < n) a.gk[(int64_t)hv * a.Te + R0 + p] = make_float4(sgh[p], sgl[p], srk[p], 0.f);
+    } else {  // u: V columns fp32
+      for (int c0 = 0; c0 < V; c0 += 32) {
+        uint32_t r[32];
+        GDP_TMEM_LD32(lane_addr + 128 + c0, r);
+        tmem_wait_ld();
+        if (p < n) {
+          float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+    }
+  }
+  tmem_release(tmem, kCols);
+}
+
+// ============================================================================ chunk_h
+struct HArgs {
+  int HV, V, M;
+  int64_t Te;
+  const int4* seq_info;
+  const float* u;
+  const float4* gk;
+  const float* h0;
+  float* hT;
+  bf16* vn_hi;
+  bf16* vn_lo;
+  bf16* h_hi;   // [n_tok_chunks][HV][V][K]
+  bf16* h_lo;
+  int* status;
+};
+
+// Per stage: w_hi (16 KB) | w_lo (16 KB) | k (16 KB) | u fp32 64x32 (8 KB) | gk 64x16 B (1 KB)
+constexpr int H_STAGE = 16384 * 3 + 8192 + 1024;          // 58 KB
+constexpr int H_HT = 2 * H_STAGE;                         // h^T hi (8 KB) | lo (8 KB)
+constexpr int H_VP = H_HT + 16384;                        // v'^T hi (4 KB) | lo (4 KB)
+constexpr int H_BAR = H_VP + 8192;
+constexpr int H_SMEM = H_BAR + 64 + 1024;
+
+__device__ __forceinline__ void h_issue_loads(uint8_t* st, const CUtensorMap* mw_hi,
+                                              const CUtensorMap* mw_lo, const CUtensorMap* mk,
+                                              const CUtensorMap* mu, const CUtensorMap* mgk, int kh,
+                                              int hv, int v0, int64_t R, int64_t gk_row,
+                                              uint64_t* bar) {
+  mbar_expect_tx(bar, 6 * 8192 + 8192 + 1024);
+  tma_load_3d(st, mw_hi, 0, hv, (int)R, bar);
+  tma_load_3d(st + 8192, mw_hi, 64, hv, (int)R, bar);
+  tma_load_3d(st + 16384, mw_lo, 0, hv, (int)R, bar);
+  tma_load_3d(st + 24576, mw_lo, 64, hv, (int)R, bar);
+  tma_load_3d(st + 32768, mk, 0, kh, (int)R, bar);
+  tma_load_3d(st + 40960, mk, 64, kh, (int)R, bar);
+  tma_load_3d(st + 49152, mu, v0, hv, (int)R, bar);
+  tma_load_2d(st + 57344, mgk, 0, (int)gk_row, bar);
+}
+
+__global__ void __launch_bounds__(128, 1) h_tc_kernel(
+    const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
+    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
+    const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
+  const int v0 = blockIdx.z * kHBV;
+  const int V = a.V, M = a.M;
+  const int4 si = a.seq_info[seq];
+  const int ne = (int)cdiv((int64_t)si.y * M, kBT);
+  uint8_t* ht = sm + H_HT;
+  uint8_t* vp = sm + H_VP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + H_BAR);  // [0,1] stage full, [2] p1, [3] p2
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+  const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
+
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 64);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  // state row kf = tid, 32 columns, fp32 in registers
+  float h[kHBV];
+  {
+    const float* src = a.h0 ? a.h0 + hoff + (int64_t)tid * V + v0 : nullptr;
+#pragma unroll
+    for (int c = 0; c < kHBV; ++c) h[c] = src ? src[c] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int64_t Rseq = (int64_t)si.x * M;
+  if (tid == 0 && ne > 0) {
+    h_issue_loads(sm, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0, Rseq,
+                  (int64_t)hv * a.Te + Rseq, &bars[0]);
+    if (ne > 1)
+      h_issue_loads(sm + H_STAGE, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0,
+                    Rseq + kBT, (int64_t)hv * a.Te + Rseq + kBT, &bars[1]);
+  }
+  const uint32_t id1 = idesc_bf16(128, kHBV, false, false);
+  const uint32_t id2 = idesc_bf16(128, kHBV, true, false);
+  for (int j = 0; j <= ne; ++j) {
+    // publish the state at the start of chunk j (operand h^T, and for chunk_o at token-chunk starts)
+    {
+      bf16 hi[kHBV], lo[kHBV];
+#pragma unroll
+      for (int c = 0; c < kHBV; ++c) split_bf16(h[c], hi[c], lo[c]);
+      const uint32_t half = (tid >> 6) * 4096, b = (tid & 63) * 2;
+#pragma unroll
+      for (int c = 0; c < kHBV; ++c) {
+        const uint32_t off = half + sw128_offset(c, b);
+        *reinterpret_cast<bf16*>(ht + off) = hi[c];
+        *reinterpret_cast<bf16*>(ht + 8192 + off) = lo[c];
+      }
+      if (j < ne && j % M == 0) {
+        const int64_t base = (((int64_t)si.w + j / M) * a.HV + hv) * V + v0;
+#pragma unroll
+        for (int c = 0; c < kHBV; ++c) {
+          a.h_hi[(base + c) * kK + tid] = hi[c];
+          a.h_lo[(base + c) * kK + tid] = lo[c];
+        }
+      }
+    }
+    if (j == ne) break;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int s = j & 1;
+    uint8_t* st = sm + s * H_STAGE;
+    const int n = min(kBT, si.y * M - j * kBT);
+    const int64_t R = Rseq + (int64_t)j * kBT;
+    bool ok = mbar_wait(&bars[s], (j >> 1) & 1, a.status, kDevTimeout);
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {  // product 1: D1 = w h  (rows = positions)
+      const uint32_t whi = smem_u32(st), wlo = smem_u32(st + 16384), hb = smem_u32(ht);
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t A = pass == 2 ? wlo : whi;
+        const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(Bm + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
+          mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
+        }
+      }
+      mma_commit(&bars[2]);
+    }
+    const float4* gk = reinterpret_cast<const float4*>(st + 57344);
+    const float4 glast = gk[n - 1];
+    if (warp < 2) {  // positions p = tid
+      const int p = tid;
+      ok = mbar_wait(&bars[2], j & 1, a.status, kDevTimeout);
+      tc_fence_after();
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16), r);
+      tmem_wait_ld();
+      const float* us = reinterpret_cast<const float*>(st + 49152) + p * kHBV;
+      const float4 gp = gk[p];
+      const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
+      bf16 vh[kHBV], vl[kHBV], ph[kHBV], pl[kHBV];
+#pragma unroll
+      for (int c = 0; c < kHBV; ++c) {
+        const float vn = us[c] - __uint_as_float(r[c]);
+        split_bf16(vn, vh[c], vl[c]);
+        split_bf16(p < n ? vn * sc : 0.f, ph[c], pl[c]);
+      }
+      if (p < n) {
+        const int64_t row = (R + p) * a.HV * V + (int64_t)hv * V + v0;
+        store_bf16x32(a.vn_hi + row, vh);
+        store_bf16x32(a.vn_lo + row, vl);
+      }
+#pragma unroll
+      for (int c = 0; c < kHBV; ++c) {
+        const uint32_t off = sw128_offset(c, p * 2);
+        *reinterpret_cast<bf16*>(vp + off) = ph[c];
+        *reinterpret_cast<bf16*>(vp + 4096 + off) = pl[c];
+      }
+      fence_async_smem();
+      tc_fence_before();
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    tc_fence_after();
+    if (tid == 0) {  // product 2: D2 = k^T v'  (rows = state rows kf)
+      const uint32_t kb = smem_u32(st + 32768), vb = smem_u32(vp);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sdesc_sw128(kb + kk * 2048, 8192, 1024);
+          const uint64_t bd = sdesc_sw128(vb + pass * 4096 + kk * 32, 16, 1024);
+          mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
+        }
+      mma_commit(&bars[3]);
+    }
+    ok = mbar_wait(&bars[3], j & 1, a.status, kDevTimeout);
+    tc_fence_after();
+    {
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16) + 32, r);
+      tmem_wait_ld();
+      const float dl = expf(glast.x + glast.y);
+#pragma unroll
+      for (int c = 0; c < kHBV; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+    }
+    tc_fence_before();
+    if (!__syncthreads_and(ok)) break;
+    // stage s is free again: prefetch chunk j + 2
+    if (tid == 0 && j + 2 < ne)
+      h_issue_loads(st, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0, R + 2 * kBT,
+                    (int64_t)hv * a.Te + R + 2 * kBT, &bars[s]);
+  }
+  if (a.hT) {
+    float* dst = a.hT + hoff + (int64_t)tid * V + v0;
+#pragma unroll
+    for (int c = 0; c < kHBV; c += 4)
+      *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
+  }
+  tmem_release(tmem, 64);
+}
+
+// ============================================================================ chunk_o
+struct OArgs {
+  int H, HV, V, M, l2norm;
+  float scale;
+  const float* g;
+  const int4* seq_info;
+  const int2* tok_tab;
+  float* o;
+  int* status;
+};
+
+// q (24 KB incl. view) | k (2 halves of 64M rows, 16M KB) | h hi, lo (16 KB each) |
+// v_new hi, lo (8M KB each) | P hi, lo (M K-blocks each, 8 KB per block, +8 KB view) | small
+constexpr int o_k_off() { return 24576; }
+constexpr int o_h_off(int M) { return o_k_off() + 16384 * M; }
+constexpr int o_v_off(int M) { return o_h_off(M) + 32768; }
+constexpr int o_p_off(int M) { return o_v_off(M) + 16384 * M; }
+constexpr int o_s_off(int M) { return o_p_off(M) + (2 * M + 1) * 8192; }
+constexpr int o_smem(int M) { return o_s_off(M) + (3 * 64 + 64 * M) * 4 + 64 + 1024; }
+
+template <int M>
+__global__ void __launch_bounds__(128, 1) o_tc_kernel(
+    const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+    const __grid_constant__ CUtensorMap map_hhi, const __grid_constant__ CUtensorMap map_hlo,
+    const __grid_constant__ CUtensorMap map_vhi, const __grid_constant__ CUtensorMap map_vlo,
+    OArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int2 tab = a.tok_tab[blockIdx.x];
+  if (tab.x < 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int v0 = blockIdx.z * kOBV;
+  const int4 si = a.seq_info[tab.x];
+  const int t_start = tab.y * kBT;
+  const int nt = min(kBT, si.y - t_start);
+  const int ne = nt * M;
+  const int64_t T0 = (int64_t)si.x + t_start, E0 = T0 * M;
+  const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * a.V + v0;
+  constexpr int NE = 64 * M;  // expanded positions in a full token chunk
+  uint8_t* qb = sm;
+  uint8_t* kb = sm + o_k_off();
+  uint8_t* hb = sm + o_h_off(M);
+  uint8_t* vb = sm + o_v_off(M);
+  uint8_t* pb = sm + o_p_off(M);
+  float* sgh = reinterpret_cast<float*>(sm + o_s_off(M));
+  float* sgl = sgh + 64;
+  float* srq = sgl + 64;
+  float* srk = srq + 64;     // [64 M]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);  // [0] tma [1] mma1 [2] mma2
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
+  constexpr uint32_t kCols = (NE + 64) <= 128 ? 128 : 256;
+
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (tid < kBT) sgh[tid] = (tid < nt && a.g) ? a.g[(T0 + tid) * a.HV + hv] : 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  if (tid == 0) {
+    mbar_expect_tx(&bars[0], 2 * 8192 + 2 * NE * 128 + 4 * 8192 + 2 * NE * 128);
+    tma_load_3d(qb, &map_q, 0, kh, (int)T0, &bars[0]);
+    tma_load_3d(qb + 8192, &map_q, 64, kh, (int)T0, &bars[0]);
+    tma_load_3d(kb, &map_k, 0, kh, (int)E0, &bars[0]);
+    tma_load_3d(kb + NE * 128, &map_k, 64, kh, (int)E0, &bars[0]);
+    tma_load_2d(hb, &map_hhi, 0, (int)hrow, &bars[0]);
+    tma_load_2d(hb + 8192, &map_hhi, 64, (int)hrow, &bars[0]);
+    tma_load_2d(hb + 16384, &map_hlo, 0, (int)hrow, &bars[0]);
+    tma_load_2d(hb + 24576, &map_hlo, 64, (int)hrow, &bars[0]);
+    tma_load_3d(vb, &map_vhi, v0, hv, (int)E0, &bars[0]);
+    tma_load_3d(vb + NE * 128, &map_vlo, v0, hv, (int)E0, &bars[0]);
+    comp_prefix(sgh, sgl, kBT);
+  }
+  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  if (tid == 0) {
+    const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
+    const uint32_t ids = idesc_bf16(128, NE, false, false);
+    const uint32_t idh = idesc_bf16(128, kOBV, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {  // scores S = q k^T: N = 64 M positions
+      const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+      const uint64_t bd = sdesc_sw128(k0 + (kk >> 2) * (NE * 128) + (kk & 3) * 32, 16, 1024);
+      mma_bf16(tmem, ad, bd, ids, kk > 0);
+    }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass)  // q h (h hi then lo), N = 64 columns
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(h0 + pass * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        mma_bf16(tmem + NE, ad, bd, idh, (pass | kk) != 0);
+      }
+    mma_commit(&bars[1]);
+  }
+  // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
+  if (tid < kBT) {
+    const float ss = row_sumsq(qb + tid * 128) + row_sumsq(qb + 8192 + tid * 128);
+    srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  }
+  for (int e = tid; e < NE; e += 128) {
+    const float ss = row_sumsq(kb + e * 128) + row_sumsq(kb + NE * 128 + e * 128);
+    srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+  }
+  // value rows past the chunk's end may hold anything: zero them (their P is 0)
+  for (int idx = tid; idx < 2 * NE * 8; idx += 128) {
+    const int row = idx >> 3, ch = idx & 7;
+    const int e = row % NE;
+    if (e >= ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (warp < 2) {  // P rows t = tid
+    const int t = tid;
+    ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
+    tc_fence_after();
+    const float rt = srq[t];
+#pragma unroll 1
+    for (int c0 = 0; c0 < NE; c0 += 32) {
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = c0 + j, s = e / M;
+        float pv = 0.f;
+        if (e < ne && s <= t && t < nt)
+          pv = __uint_as_float(r[j]) * rt * srk[e] * expf(gam_diff4(sgh, sgl, t, s));
+        bf16 ph, pl;
+        split_bf16(pv, ph, pl);
+        const uint32_t off = (e >> 6) * 8192 + sw128_offset(t, (e & 63) * 2);
+        *reinterpret_cast<bf16*>(pb + off) = ph;
+        *reinterpret_cast<bf16*>(pb + M * 8192 + off) = pl;
+      }
+    }
+    fence_async_smem();
+  }
+  tc_fence_before();
+  ok = __syncthreads_and(ok);
+  tc_fence_after();
+  if (!ok) { tmem_release(tmem, kCols); return; }
+  if (tid == 0) {  // O = P v_new (3 passes), into the score columns (consumed)
+    const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
+    const uint32_t ido = idesc_bf16(128, kOBV, false, true);
+#pragma unroll
+    for (int pass = 0; pass < 3; ++pass) {
+      const uint32_t A = p0 + (pass == 2 ? M * 8192 : 0);
+      const uint32_t Bm = vv + (pass == 1 ? NE * 128 : 0);
+#pragma unroll
+      for (int kk = 0; kk < 4 * M; ++kk) {
+        const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(Bm + kk * 2048, NE * 128, 1024);
+        mma_bf16(tmem, ad, bd, ido, (pass | kk) != 0);
+      }
+    }
+    mma_commit(&bars[2]);
+  }
+  if (warp < 2) {
+    const int t = tid;
+    ok = mbar_wait(&bars[2], 0, a.status, kDevTimeout);
+    tc_fence_after();
+    const float qs = expf(sgh[t] + sgl[t]) * srq[t];
+    const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kOBV; c0 += 32) {
+      uint32_t ro[32], rh[32];
+      GDP_TMEM_LD32(la + c0, ro);
+      GDP_TMEM_LD32(la + NE + c0, rh);
+      tmem_wait_ld();
+      if (t < nt && ok) {
+        float4* dst = reinterpret_cast<float4*>(a.o + ((T0 + t) * a.HV + hv) * a.V + v0 + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float x[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            x[q] = a.scale * (qs * __uint_as_float(rh[4 * j + q]) + __uint_as_float(ro[4 * j + q]));
+          dst[j] = make_float4(x[0], x[1], x[2], x[3]);
+        }
+      }
+    }
+  }
+  tmem_release(tmem, kCols);
+}
+
+// ============================================================================ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows][heads][width] tensor; box = box_w elements x 1 head x box_rows rows.
+bool map3(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esz, uint64_t width,
+          uint64_t heads, uint64_t rows, uint32_t box_w, uint32_t box_rows, bool swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {width, heads, rows};
+  const cuuint64_t strides[2] = {width * esz, heads * width * esz};
+  const cuuint32_t box[3] = {box_w, 1, box_rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major [rows][width]; box = box_w x box_rows.
+bool map2(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esz, uint64_t width,
+          uint64_t rows, uint32_t box_w, uint32_t box_rows, bool swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {width, rows};
+  const cuuint64_t strides[1] = {width * esz};
+  const cuuint32_t box[2] = {box_w, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+
+template <int V>
+cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
+  const int64_t Te = (int64_t)p.B * p.T * p.M;
+  CUtensorMap mk, mv;
+  if (!map3(&mk, p.k, BF, 2, kK, p.H, Te, 64, 64, true)) return cudaErrorInvalidValue;
+  if (!map3(&mv, p.v, BF, 2, V, p.HV, Te, 64, 64, true)) return cudaErrorInvalidValue;
+  const int smem = wy_smem(V);
+  cudaError_t e = cudaFuncSetAttribute(wy_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  wy_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 256, smem, p.stream>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
+template <int M>
+cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi,
+                  const CUtensorMap& mhlo, const CUtensorMap& mvhi, const CUtensorMap& mvlo) {
+  const int64_t Tt = (int64_t)p.B * p.T, Te = Tt * M;
+  CUtensorMap mq, mk;
+  if (!map3(&mq, p.q, BF, 2, kK, p.H, Tt, 64, 64, true)) return cudaErrorInvalidValue;
+  if (!map3(&mk, p.k, BF, 2, kK, p.H, Te, 64, 64 * M, true)) return cudaErrorInvalidValue;
+  const int smem = o_smem(M);
+  cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 128, smem, p.stream>>>(
+      mq, mk, mhhi, mhlo, mvhi, mvlo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int H, int HV, int K, int V, int M, int BT, gdp_dtype dt) {
+  (void)H;
+  (void)HV;
+  return dt == GDP_BF16 && K == kK && BT == kBT && (V == 64 || V == 128 || V == 256) && M >= 1 &&
+         M <= 3;
+}
+
+WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, int BT) {
+  (void)H;
+  WsLayout L;
+  int64_t NE, NT;
+  chunk_bounds(B, T, N_seq, M, BT, &NE, &NT);
+  const size_t Te = (size_t)B * T * M;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t at = off; off = align_up(off + bytes); return at; };
+  L.status = take(kAlign);
+  L.seq_info = take(sizeof(int4) * (size_t)(N_seq > 0 ? N_seq : 1));
+  L.exp_tab = take(sizeof(int2) * (size_t)NE);
+  L.tok_tab = take(sizeof(int2) * (size_t)NT);
+  L.w_hi = take(2 * Te * HV * K);
+  L.w_lo = take(2 * Te * HV * K);
+  L.u = take(4 * Te * HV * V);
+  L.gam = take(16 * Te * HV);
+  L.vn_hi = take(2 * Te * HV * V);
+  L.vn_lo = take(2 * Te * HV * V);
+  L.h_hi = take(2 * (size_t)NT * HV * V * K);
+  L.h_lo = take(2 * (size_t)NT * HV * V * K);
+  L.total = off;
+  L.path = 1;
+  return L;
+}
+
+cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {
+  const int64_t Te = (int64_t)p.B * p.T * p.M;
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  const int4* seq_info = reinterpret_cast<const int4*>(ws + L.seq_info);
+  bf16* w_hi = reinterpret_cast<bf16*>(ws + L.w_hi);
+  bf16* w_lo = reinterpret_cast<bf16*>(ws + L.w_lo);
+  float* u = reinterpret_cast<float*>(ws + L.u);
+  float4* gk = reinterpret_cast<float4*>(ws + L.gam);
+  bf16* vn_hi = reinterpret_cast<bf16*>(ws + L.vn_hi);
+  bf16* vn_lo = reinterpret_cast<bf16*>(ws + L.vn_lo);
+  bf16* h_hi = reinterpret_cast<bf16*>(ws + L.h_hi);
+  bf16* h_lo = reinterpret_cast<bf16*>(ws + L.h_lo);
+  cudaError_t e;
+  // WY stage
+  if (p.NE_max > 0 && Te > 0) {
+    WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
+             reinterpret_cast<const int2*>(ws + L.exp_tab), w_hi, w_lo, u, gk, status};
+    switch (p.V) {
+      case 64: e = run_wy<64>(p, a); break;
+      case 128: e = run_wy<128>(p, a); break;
+      default: e = run_wy<256>(p, a); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  record_stage(2, p.stream);
+  // state recurrence
+  {
+    CUtensorMap mwh, mwl, mk, mu, mg;
+    const int64_t Tr = Te > 0 ? Te : 1;
+    if (!map3(&mwh, w_hi, BF, 2, kK, p.HV, Tr, 64, 64, true) ||
+        !map3(&mwl, w_lo, BF, 2, kK, p.HV, Tr, 64, 64, true) ||
+        !map3(&mk, p.k ? p.k : w_hi, BF, 2, kK, p.H, Tr, 64, 64, true) ||
+        !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, 64, false) ||
+        !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, 64, false))
+      return cudaErrorInvalidValue;
+    HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
+    e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
+    if (e != cudaSuccess) return e;
+    h_tc_kernel<<<dim3(p.N_seq, p.HV, (unsigned)(p.V / kHBV)), 128, H_SMEM, p.stream>>>(
+        mwh, mwl, mk, mu, mg, a, p.H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  record_stage(3, p.stream);
+  // output
+  if (p.NT_max > 0 && Te > 0) {
+    CUtensorMap mhh, mhl, mvh, mvl;
+    const uint64_t hrows = (uint64_t)p.NT_max * p.HV * p.V;
+    if (!map2(&mhh, h_hi, BF, 2, kK, hrows, 64, kOBV, true) ||
+        !map2(&mhl, h_lo, BF, 2, kK, hrows, 64, kOBV, true) ||
+        !map3(&mvh, vn_hi, BF, 2, p.V, p.HV, Te, 64, 64 * p.M, true) ||
+        !map3(&mvl, vn_lo, BF, 2, p.V, p.HV, Te, 64, 64 * p.M, true))
+      return cudaErrorInvalidValue;
+    OArgs a{p.H, p.HV, p.V, p.M, p.l2norm, p.scale, p.g, seq_info,
+            reinterpret_cast<const int2*>(ws + L.tok_tab), p.o, status};
+    switch (p.M) {
+      case 1: e = run_o<1>(p, a, mhh, mhl, mvh, mvl); break;
+      case 2: e = run_o<2>(p, a, mhh, mhl, mvh, mvl); break;
+      default: e = run_o<3>(p, a, mhh, mhl, mvh, mvl); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  record_stage(4, p.stream);
+  return cudaSuccess;
 }
 
 }  // namespace gdp

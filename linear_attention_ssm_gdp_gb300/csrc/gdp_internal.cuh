@@ -48,8 +48,10 @@ struct WsLayout {
   size_t status = 0, seq_info = 0, exp_tab = 0, tok_tab = 0;
   size_t A = SIZE_MAX, w = SIZE_MAX, u = SIZE_MAX, gexp = SIZE_MAX, v_new = SIZE_MAX,
          h = SIZE_MAX;
-  // tensor-core path buffers
-  size_t w_hi = SIZE_MAX, w_lo = SIZE_MAX, kn = SIZE_MAX, gam = SIZE_MAX, rk = SIZE_MAX;
+  // tensor-core path buffers: w and v_new as bf16 hi/lo pairs, per-position
+  // (Gam hi, Gam lo, 1/|k|) records, chunk-start states as bf16 hi/lo [.., V, K]
+  size_t w_hi = SIZE_MAX, w_lo = SIZE_MAX, gam = SIZE_MAX, vn_hi = SIZE_MAX, vn_lo = SIZE_MAX,
+         h_hi = SIZE_MAX, h_lo = SIZE_MAX;
   size_t total = 0;
   int path = 0;  // 0 generic, 1 tensor core
 };
