@@ -272,8 +272,9 @@ def run_ours(args, rank, world, dev):
                 "peak_source": pk_src + " (sustained bf16)"}
     roof["traffic"] = args.traffic
 
-    e2e = run_e2e(args, gdp, d, dev, pf)
-    decode = run_decode(args, gdp, dev, pk)
+    full = args.only == "all"
+    e2e = run_e2e(args, gdp, d, dev, pf) if full else None
+    decode = run_decode(args, gdp, dev, pk) if full else None
     clocks = sampler.summary()
     w = WORKLOAD
     line = {
@@ -300,7 +301,7 @@ def run_ours(args, rank, world, dev):
         "clocks": clocks,
         "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tc, "source": pk_src},
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and full and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, max_seconds=args.cpu_seconds)
     return line
 
@@ -468,6 +469,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="profiling runs: time only the prefill step (no e2e, decode or CPU "
+                         "baseline) or only the decode step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -483,7 +487,12 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    line = run_ours(args, rank, world, dev)
+    if args.only == "decode":
+        import linear_attention_ssm_gdp_gb300 as gdp
+        gdp.load()
+        line = {"decode": run_decode(args, gdp, dev, peaks()[0])}
+    else:
+        line = run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

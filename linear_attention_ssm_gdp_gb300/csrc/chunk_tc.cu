@@ -135,17 +135,18 @@ __device__ void solve_tril64(const float* Ls, float* As, float* X) {
   const int tid = threadIdx.x;
   for (int i = tid; i < 64 * 65; i += 256) As[i] = 0.f;
   __syncthreads();
-  if (tid < 64) {  // level 0: block b, column c
-    const int b = tid >> 4, c = tid;  // absolute column
-    const int r_end = (b + 1) * 16;
+  if (tid < 64) {  // level 0: block b, column c = 16 b + cl; fully unrolled, column in registers
+    const int b = tid >> 4, cl = tid & 15, c = tid;
+    const float* Lb = Ls + (b * 16) * 65 + b * 16;
     float col[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) col[i] = 0.f;
-    col[c - b * 16] = 1.f;
-    for (int r = c + 1; r < r_end; ++r) {
+    for (int i = 0; i < 16; ++i) col[i] = (i == cl) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
       float s = 0.f;
-      for (int i = c; i < r; ++i) s += Ls[r * 65 + i] * col[i - b * 16];
-      col[r - b * 16] = -s;
+#pragma unroll
+      for (int i = 0; i < r; ++i) s += Lb[r * 65 + i] * col[i];  // col[i] = 0 for i < cl
+      if (r > cl) col[r] = -s;
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) As[(b * 16 + i) * 65 + c] = col[i];
@@ -180,7 +181,7 @@ __device__ void solve_tril64(const float* Ls, float* As, float* X) {
 }
 
 template <int V>
-__global__ void __launch_bounds__(256, 1) wy_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                        const __grid_constant__ CUtensorMap map_v,
                                                        WyArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(256, 1) wy_tc_kernel(const __grid_constant__ C
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int i = c0 + j;
-      Ls[p * 65 + i] = (i < p) ? bp * expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
+      Ls[p * 65 + i] = (i < p) ? bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
     }
   }
   __syncthreads();
@@ -396,14 +397,25 @@ __device__ __forceinline__ void h_issue_loads(uint8_t* st, const CUtensorMap* mw
   tma_load_2d(st + 57344, mgk, 0, (int)gk_row, bar);
 }
 
-__global__ void __launch_bounds__(128, 1) h_tc_kernel(
+// 256 threads: thread (warp w, lane l) owns state row kf = 32 (w % 4) + l (the
+// TMEM lane quarter its warp may access) and the 16 value columns
+// [16 (w / 4), 16 (w / 4) + 16) of the CTA's 32; in the value phase the warps
+// of lane quarters 0 and 1 own position p = 32 (w % 4) + l and the same 16
+// columns. Splitting the columns over two warps per lane quarter halves the
+// per-thread work on the sequential critical path.
+constexpr int kHCols = kHBV / 2;
+
+__global__ void __launch_bounds__(256, 1) h_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, chalf = warp >> 2;
+  const int row = quarter * 32 + lane;          // state row kf / position p
+  const int cb = chalf * kHCols;                // first of this thread's 16 columns
   const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
   const int v0 = blockIdx.z * kHBV;
   const int V = a.V, M = a.M;
@@ -414,6 +426,7 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + H_BAR);  // [0,1] stage full, [2] p1, [3] p2
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
   const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
   if (warp == 0) {
     tmem_alloc(s_tmem, 64);
@@ -423,12 +436,23 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
     for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  // state row kf = tid, 32 columns, fp32 in registers
-  float h[kHBV];
+  // swizzled byte offsets of (row c, 2-byte column b) for this thread's columns:
+  // the pattern repeats every 8 rows, so 8 offsets per operand suffice
+  uint32_t off_h[8], off_v[8];
   {
-    const float* src = a.h0 ? a.h0 + hoff + (int64_t)tid * V + v0 : nullptr;
+    const uint32_t bh = (row & 63) * 2, bv = (row & 63) * 2;
 #pragma unroll
-    for (int c = 0; c < kHBV; ++c) h[c] = src ? src[c] : 0.f;
+    for (int c = 0; c < 8; ++c) {
+      off_h[c] = sw128_offset(c, bh);
+      off_v[c] = sw128_offset(c, bv);
+    }
+  }
+  const uint32_t ht_half = (row >> 6) * 4096;
+  float h[kHCols];
+  {
+    const float* src = a.h0 ? a.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
+#pragma unroll
+    for (int c = 0; c < kHCols; ++c) h[c] = src ? src[c] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -447,22 +471,22 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
   for (int j = 0; j <= ne; ++j) {
     // publish the state at the start of chunk j (operand h^T, and for chunk_o at token-chunk starts)
     {
-      bf16 hi[kHBV], lo[kHBV];
+      bf16 hi[kHCols], lo[kHCols];
 #pragma unroll
-      for (int c = 0; c < kHBV; ++c) split_bf16(h[c], hi[c], lo[c]);
-      const uint32_t half = (tid >> 6) * 4096, b = (tid & 63) * 2;
+      for (int c = 0; c < kHCols; ++c) split_bf16(h[c], hi[c], lo[c]);
 #pragma unroll
-      for (int c = 0; c < kHBV; ++c) {
-        const uint32_t off = half + sw128_offset(c, b);
+      for (int c = 0; c < kHCols; ++c) {
+        const int cc = cb + c;  // row of h^T
+        const uint32_t off = ht_half + (cc & ~7) * 128 + off_h[cc & 7];
         *reinterpret_cast<bf16*>(ht + off) = hi[c];
         *reinterpret_cast<bf16*>(ht + 8192 + off) = lo[c];
       }
       if (j < ne && j % M == 0) {
-        const int64_t base = (((int64_t)si.w + j / M) * a.HV + hv) * V + v0;
+        const int64_t base = (((int64_t)si.w + j / M) * a.HV + hv) * V + v0 + cb;
 #pragma unroll
-        for (int c = 0; c < kHBV; ++c) {
-          a.h_hi[(base + c) * kK + tid] = hi[c];
-          a.h_lo[(base + c) * kK + tid] = lo[c];
+        for (int c = 0; c < kHCols; ++c) {
+          a.h_hi[(base + c) * kK + row] = hi[c];
+          a.h_lo[(base + c) * kK + row] = lo[c];
         }
       }
     }
@@ -494,31 +518,36 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
     }
     const float4* gk = reinterpret_cast<const float4*>(st + 57344);
     const float4 glast = gk[n - 1];
-    if (warp < 2) {  // positions p = tid
-      const int p = tid;
+    if (quarter < 2) {  // positions p = row, columns cb .. cb + 15
+      const int p = row;
       ok = mbar_wait(&bars[2], j & 1, a.status, kDevTimeout);
       tc_fence_after();
-      uint32_t r[32];
-      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16), r);
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + lane_base + cb, r);
       tmem_wait_ld();
-      const float* us = reinterpret_cast<const float*>(st + 49152) + p * kHBV;
+      const float* us = reinterpret_cast<const float*>(st + 49152) + p * kHBV + cb;
       const float4 gp = gk[p];
       const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
-      bf16 vh[kHBV], vl[kHBV], ph[kHBV], pl[kHBV];
+      bf16 vh[kHCols], vl[kHCols], ph[kHCols], pl[kHCols];
 #pragma unroll
-      for (int c = 0; c < kHBV; ++c) {
+      for (int c = 0; c < kHCols; ++c) {
         const float vn = us[c] - __uint_as_float(r[c]);
         split_bf16(vn, vh[c], vl[c]);
         split_bf16(p < n ? vn * sc : 0.f, ph[c], pl[c]);
       }
       if (p < n) {
-        const int64_t row = (R + p) * a.HV * V + (int64_t)hv * V + v0;
-        store_bf16x32(a.vn_hi + row, vh);
-        store_bf16x32(a.vn_lo + row, vl);
+        const int64_t rowg = (R + p) * a.HV * V + (int64_t)hv * V + v0 + cb;
+        uint4* dh = reinterpret_cast<uint4*>(a.vn_hi + rowg);
+        uint4* dl = reinterpret_cast<uint4*>(a.vn_lo + rowg);
+        dh[0] = reinterpret_cast<const uint4*>(vh)[0];
+        dh[1] = reinterpret_cast<const uint4*>(vh)[1];
+        dl[0] = reinterpret_cast<const uint4*>(vl)[0];
+        dl[1] = reinterpret_cast<const uint4*>(vl)[1];
       }
 #pragma unroll
-      for (int c = 0; c < kHBV; ++c) {
-        const uint32_t off = sw128_offset(c, p * 2);
+      for (int c = 0; c < kHCols; ++c) {
+        const int cc = cb + c;
+        const uint32_t off = (cc & ~7) * 128 + off_v[cc & 7];
         *reinterpret_cast<bf16*>(vp + off) = ph[c];
         *reinterpret_cast<bf16*>(vp + 4096 + off) = pl[c];
       }
@@ -543,12 +572,12 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
     ok = mbar_wait(&bars[3], j & 1, a.status, kDevTimeout);
     tc_fence_after();
     {
-      uint32_t r[32];
-      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16) + 32, r);
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
       tmem_wait_ld();
       const float dl = expf(glast.x + glast.y);
 #pragma unroll
-      for (int c = 0; c < kHBV; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+      for (int c = 0; c < kHCols; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
     }
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
@@ -558,9 +587,9 @@ __global__ void __launch_bounds__(128, 1) h_tc_kernel(
                     (int64_t)hv * a.Te + R + 2 * kBT, &bars[s]);
   }
   if (a.hT) {
-    float* dst = a.hT + hoff + (int64_t)tid * V + v0;
+    float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
 #pragma unroll
-    for (int c = 0; c < kHBV; c += 4)
+    for (int c = 0; c < kHCols; c += 4)
       *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
   }
   tmem_release(tmem, 64);
@@ -587,7 +616,7 @@ constexpr int o_s_off(int M) { return o_p_off(M) + (2 * M + 1) * 8192; }
 constexpr int o_smem(int M) { return o_s_off(M) + (3 * 64 + 64 * M) * 4 + 64 + 1024; }
 
 template <int M>
-__global__ void __launch_bounds__(128, 1) o_tc_kernel(
+__global__ void __launch_bounds__(256, 1) o_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
     const __grid_constant__ CUtensorMap map_hhi, const __grid_constant__ CUtensorMap map_hlo,
     const __grid_constant__ CUtensorMap map_vhi, const __grid_constant__ CUtensorMap map_vlo,
@@ -597,7 +626,8 @@ __global__ void __launch_bounds__(128, 1) o_tc_kernel(
                                            ~uintptr_t(1023));
   const int2 tab = a.tok_tab[blockIdx.x];
   if (tab.x < 0) return;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, chalf = warp >> 2;  // TMEM lane quarter, column half
   const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
   const int v0 = blockIdx.z * kOBV;
   const int4 si = a.seq_info[tab.x];
@@ -674,34 +704,34 @@ __global__ void __launch_bounds__(128, 1) o_tc_kernel(
     const float ss = row_sumsq(qb + tid * 128) + row_sumsq(qb + 8192 + tid * 128);
     srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
-  for (int e = tid; e < NE; e += 128) {
+  for (int e = tid; e < NE; e += 256) {
     const float ss = row_sumsq(kb + e * 128) + row_sumsq(kb + NE * 128 + e * 128);
     srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
   // value rows past the chunk's end may hold anything: zero them (their P is 0)
-  for (int idx = tid; idx < 2 * NE * 8; idx += 128) {
+  for (int idx = tid; idx < 2 * NE * 8; idx += 256) {
     const int row = idx >> 3, ch = idx & 7;
     const int e = row % NE;
     if (e >= ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
   }
   fence_async_smem();
   __syncthreads();
-  if (warp < 2) {  // P rows t = tid
-    const int t = tid;
+  if (quarter < 2) {  // P rows t, this warp's half of the N = 64 M columns
+    const int t = quarter * 32 + lane;
     ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
     tc_fence_after();
     const float rt = srq[t];
 #pragma unroll 1
-    for (int c0 = 0; c0 < NE; c0 += 32) {
+    for (int c0 = chalf * (NE / 2); c0 < (chalf + 1) * (NE / 2); c0 += 32) {
       uint32_t r[32];
-      GDP_TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16) + c0, r);
+      GDP_TMEM_LD32(tmem + ((uint32_t)(quarter * 32) << 16) + c0, r);
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int e = c0 + j, s = e / M;
         float pv = 0.f;
         if (e < ne && s <= t && t < nt)
-          pv = __uint_as_float(r[j]) * rt * srk[e] * expf(gam_diff4(sgh, sgl, t, s));
+          pv = __uint_as_float(r[j]) * rt * srk[e] * __expf(gam_diff4(sgh, sgl, t, s));
         bf16 ph, pl;
         split_bf16(pv, ph, pl);
         const uint32_t off = (e >> 6) * 8192 + sw128_offset(t, (e & 63) * 2);
@@ -731,14 +761,14 @@ __global__ void __launch_bounds__(128, 1) o_tc_kernel(
     }
     mma_commit(&bars[2]);
   }
-  if (warp < 2) {
-    const int t = tid;
+  if (quarter < 2) {
+    const int t = quarter * 32 + lane;
     ok = mbar_wait(&bars[2], 0, a.status, kDevTimeout);
     tc_fence_after();
     const float qs = expf(sgh[t] + sgl[t]) * srq[t];
-    const uint32_t la = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kOBV; c0 += 32) {
+    const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
+    {
+      const int c0 = chalf * 32;
       uint32_t ro[32], rh[32];
       GDP_TMEM_LD32(la + c0, ro);
       GDP_TMEM_LD32(la + NE + c0, rh);
@@ -835,7 +865,7 @@ cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi
   const int smem = o_smem(M);
   cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 128, smem, p.stream>>>(
+  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 256, smem, p.stream>>>(
       mq, mk, mhhi, mhlo, mvhi, mvlo, a);
   return cudaGetLastError();
 }
@@ -912,7 +942,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
     HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
     e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
     if (e != cudaSuccess) return e;
-    h_tc_kernel<<<dim3(p.N_seq, p.HV, (unsigned)(p.V / kHBV)), 128, H_SMEM, p.stream>>>(
+    h_tc_kernel<<<dim3(p.N_seq, p.HV, (unsigned)(p.V / kHBV)), 256, H_SMEM, p.stream>>>(
         mwh, mwl, mk, mu, mg, a, p.H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

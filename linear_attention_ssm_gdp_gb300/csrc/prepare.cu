@@ -61,7 +61,7 @@ template <int VB, bool DECODE>
 __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
   using VT = typename std::conditional<VB == 16, uint4,
              typename std::conditional<VB == 4, uint32_t, uint16_t>::type>::type;
-  constexpr int U = 4;  // vectors in flight per thread
+  constexpr int U = 8;  // vectors in flight per thread
   const int64_t rows = (int64_t)a.n * a.T;
   const int hpg = a.H / a.G;
   const int64_t vrow_b = (int64_t)a.M * a.H * a.P * a.es;   // value bytes per token
@@ -73,76 +73,46 @@ __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
   const int nv = (int)(vrow_b / VB), nk = (int)(krow_b / VB), nq = (int)(qrow_b / VB);
   const int head_v = (int)(head_kb / VB);  // vectors per head row
 
+  const int ntot = nv + nk + nq;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const int64_t in = r / a.T, t = r - in * a.T;
     const uint8_t* xr = a.x + in * a.x_sn_b + t * a.x_st_b;
-    // value: contiguous copy of the row's value block
-    {
-      const VT* src = reinterpret_cast<const VT*>(xr);
-      VT* dst = reinterpret_cast<VT*>(a.v + r * vrow_b);
-      for (int c0 = threadIdx.x; c0 < nv; c0 += blockDim.x * U) {
-        VT buf[U];
+    VT* vdst = reinterpret_cast<VT*>(a.v + r * vrow_b);
+    VT* kdst = reinterpret_cast<VT*>(a.k + r * krow_b);
+    VT* qdst = reinterpret_cast<VT*>(a.q + r * qrow_b);
+    // one index space over the row's value, key and query outputs, so that a
+    // thread has all of its loads for the row in flight before it stores
+    for (int c0 = threadIdx.x; c0 < ntot; c0 += blockDim.x * U) {
+      VT buf[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nv) buf[u] = __ldcs(src + c);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nv) __stcs(dst + c, buf[u]);
-        }
-      }
-    }
-    // key: output head (j, h) reads group (j, h / hpg)
-    {
-      VT* dst = reinterpret_cast<VT*>(a.k + r * krow_b);
-      for (int c0 = threadIdx.x; c0 < nk; c0 += blockDim.x * U) {
-        VT buf[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nk) {
-            const int jh = c / head_v, w = c - jh * head_v;
-            const int j = jh / a.H, h = jh - j * a.H;
-            const VT* src = reinterpret_cast<const VT*>(
-                xr + kbase_b + ((int64_t)j * a.G + h / hpg) * head_kb);
-            buf[u] = __ldcs(src + w);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nk) __stcs(dst + c, buf[u]);
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * blockDim.x;
+        if (c < nv) {  // value: contiguous copy of the row's value block
+          buf[u] = __ldcs(reinterpret_cast<const VT*>(xr) + c);
+        } else if (c < nv + nk) {  // key: output head (j, h) reads group (j, h / hpg)
+          const int ck = c - nv;
+          const int jh = ck / head_v, w = ck - jh * head_v;
+          const int j = jh / a.H, h = jh - j * a.H;
+          buf[u] = __ldcs(reinterpret_cast<const VT*>(
+                              xr + kbase_b + ((int64_t)j * a.G + h / hpg) * head_kb) + w);
+        } else if (c < ntot) {  // query: prefill one row per token; decode the last copy
+          const int cq = c - nv - nk;
+          const int jh = cq / head_v, w = cq - jh * head_v;
+          const int j = DECODE ? jh / a.H : a.M - 1;
+          const int h = DECODE ? jh - j * a.H : jh;
+          if (j == a.M - 1)
+            buf[u] = __ldcs(reinterpret_cast<const VT*>(xr + qbase_b +
+                                                        (int64_t)(h / hpg) * head_kb) + w);
+          else
+            buf[u] = VT{};  // +0.0 in every dtype
         }
       }
-    }
-    // query: prefill one row per token; decode the last copy holds it
-    {
-      VT* dst = reinterpret_cast<VT*>(a.q + r * qrow_b);
-      for (int c0 = threadIdx.x; c0 < nq; c0 += blockDim.x * U) {
-        VT buf[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nq) {
-            const int jh = c / head_v, w = c - jh * head_v;
-            const int j = DECODE ? jh / a.H : a.M - 1;
-            const int h = DECODE ? jh - j * a.H : jh;
-            if (j == a.M - 1) {
-              const VT* src =
-                  reinterpret_cast<const VT*>(xr + qbase_b + (int64_t)(h / hpg) * head_kb);
-              buf[u] = __ldcs(src + w);
-            } else {
-              buf[u] = VT{};  // +0.0 in every dtype
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + u * blockDim.x;
-          if (c < nq) __stcs(dst + c, buf[u]);
-        }
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * blockDim.x;
+        if (c < nv) __stcs(vdst + c, buf[u]);
+        else if (c < nv + nk) __stcs(kdst + (c - nv), buf[u]);
+        else if (c < ntot) __stcs(qdst + (c - nv - nk), buf[u]);
       }
     }
     // gates

@@ -10,10 +10,14 @@
 //
 // GB300 design: the work is the fp32 state read + write (8 bytes per state
 // element per call), so the kernel is an HBM stream: one CTA per (request,
-// value head, 128-column slice), 16 warps, each warp owning 8 columns and
-// every lane K/32 rows, so a lane holds its K/32 x 8 state block in registers
-// for all L steps. The column reductions h^T k and h^T q are warp shuffles;
-// each state element is read once and written once.
+// value head, 32-column slice) with K/32 warps; warp w holds state rows
+// [32w, 32w + 32) of all 32 columns (lane = column), so every warp reads and
+// writes whole 128-byte rows, each element once (streaming cache hints). A
+// step's inputs (k, q, v, beta, e^g) are staged in shared memory for up to 16
+// steps with one batched load and k, q are normalised there once per step;
+// in the step loop the key/query rows are warp-broadcast 16-byte loads and the
+// column sums over K combine per-thread partials across the K/32 warps through
+// shared memory (two barriers per step).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,103 +36,150 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-constexpr int kCols = 8;      // columns per warp
-constexpr int kWarps = 16;    // warps per CTA -> 128 columns per CTA
+constexpr int kCtaCols = 32;  // value columns per CTA (one per lane)
+constexpr int kLC = 16;       // steps staged in shared memory at a time
 
-template <typename Tin, int KR>
-__global__ void __launch_bounds__(kWarps * 32)
+// Shared memory per CTA: normalised k and q rows [kLC][K] fp32, the CTA's value
+// columns [kLC][32], beta and e^g per step, and two double-buffered
+// [K/32][32] tables of per-warp partial column sums.
+template <int K>
+constexpr int rec_smem() {
+  return (2 * kLC * K + kLC * kCtaCols + 2 * kLC + 4 * (K / 32) * 32) * 4;
+}
+
+// Thread layout: K/32 warps; warp w owns state rows [32 w, 32 w + 32), lane l
+// owns value column cbase + l, so a warp touches full 128-byte rows of the
+// state. Column sums over K are in-thread over 32 rows, then across the K/32
+// warps through shared memory.
+template <typename Tin, int KW>
+__global__ void __launch_bounds__(KW * 32)
 recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                  const float* __restrict__ beta, const float* __restrict__ g,
                  float* __restrict__ state, int L, int H, int HV, int V, float scale,
                  int l2norm, float* __restrict__ o) {
-  constexpr int K = KR * 32;
+  constexpr int K = KW * 32;
+  extern __shared__ __align__(16) float smr[];
+  float* kn = smr;                      // [kLC][K]
+  float* qn = kn + kLC * K;             // [kLC][K]
+  float* vs = qn + kLC * K;             // [kLC][32]
+  float* bt = vs + kLC * kCtaCols;      // [kLC]
+  float* eg = bt + kLC;                 // [kLC]
+  float* part = eg + kLC;               // [2][KW][32]  h^T k partials
+  float* parto = part + 2 * KW * 32;    // [2][KW][32]  h^T q partials
   const int rh = blockIdx.x;  // request * HV + hv
   const int r = rh / HV, hv = rh - r * HV, kh = hv / (HV / H);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = blockIdx.y * (kWarps * kCols) + warp * kCols;
-  if (c0 >= V) return;  // V % 8 == 0: a warp is either fully in or fully out
-  float* st = state + (int64_t)rh * K * V;
-  float h[KR][kCols];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cbase = blockIdx.y * kCtaCols;
+  const int c = cbase + lane;
+  const bool active = c < V;
+  const int nth = KW * 32;
+  float* st = state + (int64_t)rh * K * V + (int64_t)(warp * 32) * V + c;
+  float h[32];
 #pragma unroll
-  for (int i = 0; i < KR; ++i) {
-    const float4* p = reinterpret_cast<const float4*>(st + (int64_t)(lane + 32 * i) * V + c0);
-    const float4 a = p[0], b = p[1];
-    h[i][0] = a.x; h[i][1] = a.y; h[i][2] = a.z; h[i][3] = a.w;
-    h[i][4] = b.x; h[i][5] = b.y; h[i][6] = b.z; h[i][7] = b.w;
-  }
-  for (int e = 0; e < L; ++e) {
-    const int64_t re = (int64_t)r * L + e;
-    float kv[KR], qv[KR];
-    float skk = 0.f, sqq = 0.f;
-#pragma unroll
-    for (int i = 0; i < KR; ++i) {
-      kv[i] = ldf(k + (re * H + kh) * K + lane + 32 * i);
-      qv[i] = ldf(q + (re * H + kh) * K + lane + 32 * i);
-      skk += kv[i] * kv[i];
-      sqq += qv[i] * qv[i];
+  for (int i = 0; i < 32; ++i) h[i] = active ? __ldcs(st + (int64_t)i * V) : 0.f;
+  int buf = 0;
+  for (int e0 = 0; e0 < L; e0 += kLC) {
+    const int lc = min(kLC, L - e0);
+    const int64_t re0 = (int64_t)r * L + e0;
+    __syncthreads();  // the previous batch has been consumed
+    for (int idx = tid; idx < lc * K; idx += nth) {
+      const int e = idx / K, cc = idx - e * K;
+      kn[idx] = ldf(k + ((re0 + e) * H + kh) * K + cc);
+      qn[idx] = ldf(q + ((re0 + e) * H + kh) * K + cc);
     }
-    if (l2norm) {
-      const float rk = 1.0f / sqrtf(warp_sum(skk) + 1e-6f);
-      const float rq = 1.0f / sqrtf(warp_sum(sqq) + 1e-6f);
-#pragma unroll
-      for (int i = 0; i < KR; ++i) { kv[i] *= rk; qv[i] *= rq; }
+    for (int idx = tid; idx < lc * kCtaCols; idx += nth) {
+      const int e = idx / kCtaCols, cc = idx - e * kCtaCols;
+      vs[idx] = (cbase + cc < V) ? ldf(v + ((re0 + e) * HV + hv) * V + cbase + cc) : 0.f;
     }
-    float vv[kCols];
-    {
-      const Tin* vp = v + (re * HV + hv) * V + c0;
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) vv[c] = ldf(vp + c);
+    if (tid < lc) {
+      bt[tid] = beta[(re0 + tid) * HV + hv];
+      eg[tid] = expf(g[(re0 + tid) * HV + hv]);
     }
-    const float bt = beta[re * HV + hv];
-    const float eg = expf(g[re * HV + hv]);
-    float out[kCols];
+    __syncthreads();
+    if (l2norm) {  // one warp per row, each row normalised once for the whole CTA
+      for (int rr = warp; rr < 2 * lc; rr += KW) {
+        float* x = rr < lc ? kn + rr * K : qn + (rr - lc) * K;
+        float ss = 0.f;
 #pragma unroll
-    for (int c = 0; c < kCols; ++c) {
-      float part = 0.f;
+        for (int i = 0; i < KW; ++i) ss += x[lane + 32 * i] * x[lane + 32 * i];
+        const float rn = 1.0f / sqrtf(warp_sum(ss) + 1e-6f);
 #pragma unroll
-      for (int i = 0; i < KR; ++i) {
-        h[i][c] *= eg;
-        part += h[i][c] * kv[i];
+        for (int i = 0; i < KW; ++i) x[lane + 32 * i] *= rn;
       }
-      const float delta = bt * (vv[c] - warp_sum(part));
+      __syncthreads();
+    }
+    for (int e = 0; e < lc; ++e) {
+      const float4* kr = reinterpret_cast<const float4*>(kn + e * K + warp * 32);
+      const float4* qr = reinterpret_cast<const float4*>(qn + e * K + warp * 32);
+      const float d = eg[e];
+      float p = 0.f;
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {  // broadcast 16-byte loads of this warp's 32 key rows
+        const float4 kk = kr[i4];
+        h[4 * i4 + 0] *= d; p += h[4 * i4 + 0] * kk.x;
+        h[4 * i4 + 1] *= d; p += h[4 * i4 + 1] * kk.y;
+        h[4 * i4 + 2] *= d; p += h[4 * i4 + 2] * kk.z;
+        h[4 * i4 + 3] *= d; p += h[4 * i4 + 3] * kk.w;
+      }
+      float* pb = part + buf * KW * 32;
+      pb[warp * 32 + lane] = p;
+      __syncthreads();
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < KW; ++w) s += pb[w * 32 + lane];
+      const float delta = bt[e] * (vs[e * kCtaCols + lane] - s);
       float po = 0.f;
 #pragma unroll
-      for (int i = 0; i < KR; ++i) {
-        h[i][c] += kv[i] * delta;
-        po += h[i][c] * qv[i];
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 kk = kr[i4], qq = qr[i4];
+        h[4 * i4 + 0] += kk.x * delta; po += h[4 * i4 + 0] * qq.x;
+        h[4 * i4 + 1] += kk.y * delta; po += h[4 * i4 + 1] * qq.y;
+        h[4 * i4 + 2] += kk.z * delta; po += h[4 * i4 + 2] * qq.z;
+        h[4 * i4 + 3] += kk.w * delta; po += h[4 * i4 + 3] * qq.w;
       }
-      out[c] = scale * warp_sum(po);
-    }
-    if (lane == 0) {
-      float4* op = reinterpret_cast<float4*>(o + (re * HV + hv) * V + c0);
-      op[0] = make_float4(out[0], out[1], out[2], out[3]);
-      op[1] = make_float4(out[4], out[5], out[6], out[7]);
-    }
-  }
+      float* ob = parto + buf * KW * 32;
+      ob[warp * 32 + lane] = po;
+      __syncthreads();
+      if (warp == 0 && active) {
+        float so = 0.f;
 #pragma unroll
-  for (int i = 0; i < KR; ++i) {
-    float4* p = reinterpret_cast<float4*>(st + (int64_t)(lane + 32 * i) * V + c0);
-    p[0] = make_float4(h[i][0], h[i][1], h[i][2], h[i][3]);
-    p[1] = make_float4(h[i][4], h[i][5], h[i][6], h[i][7]);
+        for (int w = 0; w < KW; ++w) so += ob[w * 32 + lane];
+        o[((re0 + e) * HV + hv) * V + c] = scale * so;
+      }
+      buf ^= 1;  // the next step writes the other buffers; reuse is two barriers away
+    }
   }
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) __stcs(st + (int64_t)i * V, h[i]);
+  }
+}
+
+template <typename Tin, int KW>
+cudaError_t launch_k(const dim3& grid, const void* q, const void* k, const void* v,
+                     const float* beta, const float* g, float* state, int L, int H, int HV,
+                     int V, float scale, int l2norm, float* o, cudaStream_t s) {
+  constexpr int smem = rec_smem<KW * 32>();
+  cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<Tin, KW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  recurrent_kernel<Tin, KW><<<grid, KW * 32, smem, s>>>(
+      static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), beta,
+      g, state, L, H, HV, V, scale, l2norm, o);
+  return cudaGetLastError();
 }
 
 template <typename Tin>
 cudaError_t run(const void* q, const void* k, const void* v, const float* beta, const float* g,
                 float* state, int n, int L, int H, int HV, int K, int V, float scale, int l2norm,
                 float* o, cudaStream_t s) {
-  const dim3 grid((unsigned)((int64_t)n * HV), (unsigned)cdiv(V, kWarps * kCols));
-  const dim3 block(kWarps * 32);
-  auto qq = static_cast<const Tin*>(q);
-  auto kk = static_cast<const Tin*>(k);
-  auto vv = static_cast<const Tin*>(v);
+  const dim3 grid((unsigned)((int64_t)n * HV), (unsigned)cdiv(V, kCtaCols));
   switch (K) {
-    case 32: recurrent_kernel<Tin, 1><<<grid, block, 0, s>>>(qq, kk, vv, beta, g, state, L, H, HV, V, scale, l2norm, o); break;
-    case 64: recurrent_kernel<Tin, 2><<<grid, block, 0, s>>>(qq, kk, vv, beta, g, state, L, H, HV, V, scale, l2norm, o); break;
-    case 128: recurrent_kernel<Tin, 4><<<grid, block, 0, s>>>(qq, kk, vv, beta, g, state, L, H, HV, V, scale, l2norm, o); break;
-    default: recurrent_kernel<Tin, 8><<<grid, block, 0, s>>>(qq, kk, vv, beta, g, state, L, H, HV, V, scale, l2norm, o); break;
+    case 32: return launch_k<Tin, 1>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
+    case 64: return launch_k<Tin, 2>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
+    case 128: return launch_k<Tin, 4>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
+    default: return launch_k<Tin, 8>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -37,8 +37,10 @@ def test_decode_workload_prepare_then_update(gdp):
 ])
 def test_recurrent_small(gdp, n, L, H, HV, K, V, dtype, l2):
     gen = torch.Generator().manual_seed(n * L + K)
-    q = torch.randn(n, L, H, K, generator=gen).to(dtype)
-    k = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    # without the L2 norm, raw N(0,1) keys make the delta rule diverge; scale them
+    sc = 1.0 if l2 else K ** -0.5
+    q = (torch.randn(n, L, H, K, generator=gen) * sc).to(dtype)
+    k = (torch.randn(n, L, H, K, generator=gen) * sc).to(dtype)
     v = torch.randn(n, L, HV, V, generator=gen).to(dtype)
     beta = torch.rand(n, L, HV, generator=gen)
     g = -torch.rand(n, L, HV, generator=gen)
