@@ -127,10 +127,72 @@ constexpr int wy_i_off(int V) { return wy_l_off(V) + 64 * 65 * 4; }  // A fp32 [
 constexpr int wy_s_off(int V) { return wy_i_off(V) + 64 * 65 * 4; }  // small arrays
 constexpr int wy_smem(int V) { return wy_s_off(V) + 6 * 64 * 4 + 64 + 1024; }
 
+// One merge level of the blocked triangular inverse, for NP independent pairs
+// of SZ x SZ blocks along the diagonal of the in-place matrix LA (row stride
+// lda): X = L10 A00, then A10 = -A11 X written over L10. Dense products (the
+// zeros above the diagonals are stored), register-tiled: each of the 256
+// threads owns a TR x TC tile of outputs with independent accumulators.
+template <int SZ, int NP>
+__device__ __forceinline__ void merge_level(float* LA, int lda, float* X) {
+  constexpr int E = NP * SZ * SZ / 256;
+  constexpr int TC = E >= 4 ? 4 : E;
+  constexpr int TR = E / TC;
+  constexpr int NCB = SZ / TC, NRB = SZ / TR;
+  constexpr int XS = SZ + 4;
+  const int t = threadIdx.x;
+  const int pair = t / (NRB * NCB), rem = t - pair * (NRB * NCB);
+  const int r0 = (rem / NCB) * TR, c0 = (rem % NCB) * TC;
+  const int base = pair * 2 * SZ;
+  float* Xp = X + pair * SZ * XS;
+  float acc[TR][TC];
+#pragma unroll
+  for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < SZ; ++i) {
+    float av[TR], bv[TC];
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + i];
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) bv[cc] = LA[(base + i) * lda + base + c0 + cc];
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+  }
+#pragma unroll
+  for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) Xp[(r0 + rr) * XS + c0 + cc] = acc[rr][cc];
+  __syncthreads();
+#pragma unroll
+  for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < SZ; ++i) {
+    float av[TR], bv[TC];
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + SZ + i];
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) bv[cc] = Xp[i * XS + c0 + cc];
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+  }
+#pragma unroll
+  for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+    for (int cc = 0; cc < TC; ++cc) LA[(base + SZ + r0 + rr) * lda + base + c0 + cc] = -acc[rr][cc];
+  __syncthreads();
+}
+
 // Blocked inversion of the unit lower-triangular 64x64 matrix I + L (L strictly
 // lower, row stride 65) into A (row stride 65): 16x16 diagonal blocks by
 // column-parallel forward substitution, then two merge levels
-// A10 = -A11 (L10 A00). X is a 32x33 scratch. 256 threads.
+// A10 = -A11 (L10 A00). X is a scratch of at least 32 x 36 floats. 256 threads.
 __device__ void solve_tril64(const float* Ls, float* As, float* X) {
   const int tid = threadIdx.x;
   for (int i = tid; i < 64 * 65; i += 256) As[i] = 0.f;
@@ -152,32 +214,14 @@ __device__ void solve_tril64(const float* Ls, float* As, float* X) {
     for (int i = 0; i < 16; ++i) As[(b * 16 + i) * 65 + c] = col[i];
   }
   __syncthreads();
-  // level 1: two pairs of 16-blocks; level 2: one pair of 32-blocks
-#pragma unroll 1
-  for (int lvl = 0; lvl < 2; ++lvl) {
-    const int sz = lvl == 0 ? 16 : 32;      // size of the blocks being merged
-    const int npairs = lvl == 0 ? 2 : 1;
-    // X = L10 A00  (X stored per pair at X + pair * sz * 33)
-    for (int idx = tid; idx < npairs * sz * sz; idx += 256) {
-      const int pair = idx / (sz * sz), rc = idx - pair * sz * sz;
-      const int r = rc / sz, c = rc - r * sz;
-      const int base = pair * 2 * sz;
-      float s = 0.f;
-      for (int i = c; i < sz; ++i) s += Ls[(base + sz + r) * 65 + base + i] * As[(base + i) * 65 + base + c];
-      X[pair * sz * 33 + r * 33 + c] = s;
-    }
-    __syncthreads();
-    // A10 = -A11 X
-    for (int idx = tid; idx < npairs * sz * sz; idx += 256) {
-      const int pair = idx / (sz * sz), rc = idx - pair * sz * sz;
-      const int r = rc / sz, c = rc - r * sz;
-      const int base = pair * 2 * sz;
-      float s = 0.f;
-      for (int i = 0; i <= r; ++i) s += As[(base + sz + r) * 65 + base + sz + i] * X[pair * sz * 33 + i * 33 + c];
-      As[(base + sz + r) * 65 + base + c] = -s;
-    }
-    __syncthreads();
+  // below the diagonal blocks, As takes L (the merges read L10 there and overwrite it)
+  for (int i = tid; i < 64 * 64; i += 256) {
+    const int r = i >> 6, c = i & 63;
+    if ((r >> 4) > (c >> 4)) As[r * 65 + c] = Ls[r * 65 + c];
   }
+  __syncthreads();
+  merge_level<16, 2>(As, 65, X);
+  merge_level<32, 1>(As, 65, X);
 }
 
 template <int V>
@@ -369,7 +413,7 @@ struct HArgs {
   float* hT;
   bf16* vn_hi;
   bf16* vn_lo;
-  bf16* h_hi;   // [n_tok_chunks][HV][V][K]
+  bf16* h_hi;   // [n_tok_chunks][HV][K][V]
   bf16* h_lo;
   int* status;
 };
@@ -436,18 +480,10 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  // swizzled byte offsets of (row c, 2-byte column b) for this thread's columns:
-  // the pattern repeats every 8 rows, so 8 offsets per operand suffice
-  uint32_t off_h[8], off_v[8];
-  {
-    const uint32_t bh = (row & 63) * 2, bv = (row & 63) * 2;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      off_h[c] = sw128_offset(c, bh);
-      off_v[c] = sw128_offset(c, bv);
-    }
-  }
-  const uint32_t ht_half = (row >> 6) * 4096;
+  // The B operands h (rows kf) and v' (rows p) are MN-major tiles with 64-byte
+  // rows (32 value columns, 64-byte swizzle): a thread stores its 16 columns
+  // of its own row as two 16-byte chunks.
+  const uint32_t off_r0 = sw64_chunk(row, 2 * chalf), off_r1 = sw64_chunk(row, 2 * chalf + 1);
   float h[kHCols];
   {
     const float* src = a.h0 ? a.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
@@ -466,28 +502,29 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
       h_issue_loads(sm + H_STAGE, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0,
                     Rseq + kBT, (int64_t)hv * a.Te + Rseq + kBT, &bars[1]);
   }
-  const uint32_t id1 = idesc_bf16(128, kHBV, false, false);
-  const uint32_t id2 = idesc_bf16(128, kHBV, true, false);
+  const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
+  const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
   for (int j = 0; j <= ne; ++j) {
     // publish the state at the start of chunk j (operand h^T, and for chunk_o at token-chunk starts)
     {
-      bf16 hi[kHCols], lo[kHCols];
+      __align__(16) bf16 hi[kHCols];
+      __align__(16) bf16 lo[kHCols];
 #pragma unroll
       for (int c = 0; c < kHCols; ++c) split_bf16(h[c], hi[c], lo[c]);
-#pragma unroll
-      for (int c = 0; c < kHCols; ++c) {
-        const int cc = cb + c;  // row of h^T
-        const uint32_t off = ht_half + (cc & ~7) * 128 + off_h[cc & 7];
-        *reinterpret_cast<bf16*>(ht + off) = hi[c];
-        *reinterpret_cast<bf16*>(ht + 8192 + off) = lo[c];
-      }
-      if (j < ne && j % M == 0) {
-        const int64_t base = (((int64_t)si.w + j / M) * a.HV + hv) * V + v0 + cb;
-#pragma unroll
-        for (int c = 0; c < kHCols; ++c) {
-          a.h_hi[(base + c) * kK + row] = hi[c];
-          a.h_lo[(base + c) * kK + row] = lo[c];
-        }
+      const uint4* h4 = reinterpret_cast<const uint4*>(hi);
+      const uint4* l4 = reinterpret_cast<const uint4*>(lo);
+      *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
+      *reinterpret_cast<uint4*>(ht + off_r1) = h4[1];
+      *reinterpret_cast<uint4*>(ht + 8192 + off_r0) = l4[0];
+      *reinterpret_cast<uint4*>(ht + 8192 + off_r1) = l4[1];
+      if (j < ne && j % M == 0) {  // state at a token-chunk start, [chunk][HV][K][V]
+        const int64_t base = ((((int64_t)si.w + j / M) * a.HV + hv) * kK + row) * V + v0 + cb;
+        uint4* dh = reinterpret_cast<uint4*>(a.h_hi + base);
+        uint4* dl = reinterpret_cast<uint4*>(a.h_lo + base);
+        dh[0] = h4[0];
+        dh[1] = h4[1];
+        dl[0] = l4[0];
+        dl[1] = l4[1];
       }
     }
     if (j == ne) break;
@@ -510,7 +547,7 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(Bm + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
           mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
         }
       }
@@ -528,7 +565,10 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
       const float* us = reinterpret_cast<const float*>(st + 49152) + p * kHBV + cb;
       const float4 gp = gk[p];
       const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
-      bf16 vh[kHCols], vl[kHCols], ph[kHCols], pl[kHCols];
+      __align__(16) bf16 vh[kHCols];
+      __align__(16) bf16 vl[kHCols];
+      __align__(16) bf16 ph[kHCols];
+      __align__(16) bf16 pl[kHCols];
 #pragma unroll
       for (int c = 0; c < kHCols; ++c) {
         const float vn = us[c] - __uint_as_float(r[c]);
@@ -544,13 +584,10 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
         dl[0] = reinterpret_cast<const uint4*>(vl)[0];
         dl[1] = reinterpret_cast<const uint4*>(vl)[1];
       }
-#pragma unroll
-      for (int c = 0; c < kHCols; ++c) {
-        const int cc = cb + c;
-        const uint32_t off = (cc & ~7) * 128 + off_v[cc & 7];
-        *reinterpret_cast<bf16*>(vp + off) = ph[c];
-        *reinterpret_cast<bf16*>(vp + 4096 + off) = pl[c];
-      }
+      *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(ph)[0];
+      *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(ph)[1];
+      *reinterpret_cast<uint4*>(vp + 4096 + off_r0) = reinterpret_cast<const uint4*>(pl)[0];
+      *reinterpret_cast<uint4*>(vp + 4096 + off_r1) = reinterpret_cast<const uint4*>(pl)[1];
       fence_async_smem();
       tc_fence_before();
     }
@@ -564,7 +601,7 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t ad = sdesc_sw128(kb + kk * 2048, 8192, 1024);
-          const uint64_t bd = sdesc_sw128(vb + pass * 4096 + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw64(vb + pass * 4096 + kk * 1024, 4096, 512);
           mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
         }
       mma_commit(&bars[3]);
@@ -585,6 +622,491 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     if (tid == 0 && j + 2 < ne)
       h_issue_loads(st, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0, R + 2 * kBT,
                     (int64_t)hv * a.Te + R + 2 * kBT, &bars[s]);
+  }
+  if (a.hT) {
+    float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
+#pragma unroll
+    for (int c = 0; c < kHCols; c += 4)
+      *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
+  }
+  tmem_release(tmem, 64);
+}
+
+// ============================================================================ wy, 128-position blocks
+// For even M the WY factors are built for blocks of 128 expanded positions (two
+// of the pages' 64-position chunks): the 128x128 inverse
+// A = (I + L)^-1 = [[A0, 0], [-A1 (L10 A0), A1]] is formed in place in fp32,
+// so the state recurrence can advance 128 positions per step. v_new does not
+// depend on where the blocks fall, so the results are those of the 64-chunk
+// algebra up to rounding.
+//
+// Shared memory: k (2 K-halves of 128 rows, 32 KB) | v (two 64-column chunks of
+// 128 rows, 32 KB; V = 256 loads it in two rounds) | operand tiles (2 x 32 KB;
+// the solve scratch lives here before the tiles are built) | L/A fp32 [128][129]
+// | small arrays
+constexpr int W8_K = 0;
+constexpr int W8_V = 32768;
+constexpr int W8_T = 65536;
+constexpr int W8_LA = W8_T + 65536;
+constexpr int W8_S = W8_LA + 128 * 129 * 4;
+constexpr int W8_SMEM = W8_S + 5 * 128 * 4 + 64 + 1024;
+
+// In-place inverse of the unit lower-triangular 128x128 matrix I + L held
+// strictly lower in LA (row stride 129, zeros on and above the diagonal):
+// 16x16 diagonal blocks by forward substitution (results staged in scratch,
+// then copied back), then merges A10 = -A11 (L10 A00) at sizes 16, 32, 64.
+// scratch >= 64 * 68 floats. 256 threads.
+__device__ void solve_tril128(float* LA, float* scratch) {
+  const int tid = threadIdx.x;
+  if (tid < 128) {
+    const int b = tid >> 4, cl = tid & 15;
+    const float* Lb = LA + (b * 16) * 129 + b * 16;
+    float col[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) col[i] = (i == cl) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) s += Lb[r * 129 + i] * col[i];  // col[i] = 0 for i < cl
+      if (r > cl) col[r] = -s;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) scratch[(b * 16 + i) * 16 + cl] = col[i];
+  }
+  __syncthreads();
+  for (int idx = tid; idx < 128 * 16; idx += 256) {
+    const int row = idx >> 4, cl = idx & 15;
+    LA[row * 129 + (row & ~15) + cl] = scratch[idx];
+  }
+  __syncthreads();
+  merge_level<16, 4>(LA, 129, scratch);
+  merge_level<32, 2>(LA, 129, scratch);
+  merge_level<64, 1>(LA, 129, scratch);
+}
+
+template <int V>
+__global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+                                                          const __grid_constant__ CUtensorMap map_v,
+                                                          WyArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int2 tab = a.exp_tab[blockIdx.x];
+  if (tab.x < 0 || (tab.y & 1)) return;  // one CTA per pair of 64-position chunks
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, chalf = warp >> 2;
+  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
+  const int4 si = a.seq_info[tab.x];
+  const int M = a.M;
+  const int b_start = tab.y * kBT;
+  const int n = min(128, si.y * M - b_start);
+  const int64_t R0 = (int64_t)si.x * M + b_start;
+  constexpr int VR = V < 128 ? V : 128;          // value columns per round
+  constexpr int NR = V / VR;                     // rounds
+  uint8_t* kbuf = sm + W8_K;
+  uint8_t* vbuf = sm + W8_V;
+  uint8_t* tiles = sm + W8_T;
+  float* LA = reinterpret_cast<float*>(sm + W8_LA);
+  float* scratch = reinterpret_cast<float*>(tiles);
+  float* sb = reinterpret_cast<float*>(sm + W8_S);
+  float* sgh = sb + 128;
+  float* sgl = sgh + 128;
+  float* srk = sgl + 128;
+  float* sco = srk + 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 128);  // [0] k + v, [1] mma, [2] v round
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
+  constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (tid < 128) {
+    float b = 0.f, gl = 0.f;
+    if (tid < n) {
+      const int e = b_start + tid, t = e / M;
+      b = a.beta[(R0 + tid) * a.HV + hv];
+      if (a.g && e - t * M == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv];
+    }
+    sb[tid] = b;
+    sgh[tid] = gl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  if (tid == 0) {
+    mbar_expect_tx(&bars[0], 32768 + (VR / 64) * 16384);
+    tma_load_3d(kbuf, &map_k, 0, kh, (int)R0, &bars[0]);
+    tma_load_3d(kbuf + 16384, &map_k, 64, kh, (int)R0, &bars[0]);
+#pragma unroll
+    for (int c = 0; c < VR / 64; ++c) tma_load_3d(vbuf + c * 16384, &map_v, 64 * c, hv, (int)R0, &bars[0]);
+    comp_prefix(sgh, sgl, 128);
+  }
+  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  uint32_t mma_phase = 0;
+  if (tid == 0) {  // Gram matrix k k^T, 128 x 128
+    const uint32_t kb = smem_u32(kbuf);
+    const uint32_t id = idesc_bf16(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+      mma_bf16(tmem, d, d, id, kk > 0);
+    }
+    mma_commit(&bars[1]);
+  }
+  if (tid < 128) {
+    const float ss = row_sumsq(kbuf + tid * 128) + row_sumsq(kbuf + 16384 + tid * 128);
+    const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    srk[tid] = r;
+    sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
+  }
+  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+  mma_phase ^= 1;
+  tc_fence_after();
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  {  // L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|) for i < p
+    const int p = quarter * 32 + lane;
+    const float bp = sb[p] * srk[p];
+#pragma unroll 1
+    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + lane_base + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int i = c0 + j;
+        LA[p * 129 + i] =
+            (i < p) ? bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  solve_tril128(LA, scratch);
+  // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u)
+  auto build_tiles = [&](int which) {
+    const float* sc = which == 0 ? sco : sb;
+    for (int idx = tid; idx < 128 * 64; idx += 256) {
+      const int prow = idx >> 6, i = (idx & 63) * 2;  // pairs of adjacent columns
+      const float a0 = LA[prow * 129 + i] * sc[i], a1 = LA[prow * 129 + i + 1] * sc[i + 1];
+      bf16 h0, l0, h1, l1;
+      split_bf16(a0, h0, l0);
+      split_bf16(a1, h1, l1);
+      const uint32_t off = (i >> 6) * 16384 + sw128_offset(prow, (i & 63) * 2);
+      __nv_bfloat162 hh, ll;
+      hh.x = h0; hh.y = h1;
+      ll.x = l0; ll.y = l1;
+      *reinterpret_cast<__nv_bfloat162*>(tiles + off) = hh;
+      *reinterpret_cast<__nv_bfloat162*>(tiles + 32768 + off) = ll;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  build_tiles(0);
+  if (tid == 0) {  // w = A' k: M = 128 positions, N = 128, K = 128 positions
+    const uint32_t tb = smem_u32(tiles), kb = smem_u32(kbuf);
+    const uint32_t idw = idesc_bf16(128, 128, false, true);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(kb + kk * 2048, 16384, 1024);
+        mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
+      }
+    mma_commit(&bars[1]);
+  }
+  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+  mma_phase ^= 1;
+  tc_fence_after();
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  build_tiles(1);
+  auto issue_u = [&](int round) {
+    const uint32_t tb = smem_u32(tiles), vb = smem_u32(vbuf);
+    const uint32_t idu = idesc_bf16(128, VR, false, true);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+        mma_bf16(tmem + 128 + round * VR, ad, bd, idu, (pass | kk) != 0);
+      }
+    mma_commit(&bars[1]);
+  };
+  if (tid == 0) issue_u(0);
+  // w epilogue (overlaps the u MMAs): row p, 64 of the 128 columns per thread
+  {
+    const int p = quarter * 32 + lane;
+#pragma unroll 1
+    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + lane_base + c0, r);
+      tmem_wait_ld();
+      if (p < n) {
+        __align__(16) bf16 hi[32];
+        __align__(16) bf16 lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
+        const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
+        store_bf16x32(a.w_hi + row, hi);
+        store_bf16x32(a.w_lo + row, lo);
+      }
+    }
+  }
+#pragma unroll 1
+  for (int round = 1; round < NR; ++round) {  // V = 256: second half of the value columns
+    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+    mma_phase ^= 1;
+    if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+    if (tid == 0) {
+      mbar_expect_tx(&bars[2], (VR / 64) * 16384);
+#pragma unroll
+      for (int c = 0; c < VR / 64; ++c)
+        tma_load_3d(vbuf + c * 16384, &map_v, round * VR + 64 * c, hv, (int)R0, &bars[2]);
+    }
+    ok = mbar_wait(&bars[2], (round - 1) & 1, a.status, kDevTimeout);
+    if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+    if (tid == 0) issue_u(round);
+  }
+  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+  tc_fence_after();
+  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  {  // u epilogue: row p, V / 2 columns per thread
+    const int p = quarter * 32 + lane;
+#pragma unroll 1
+    for (int c0 = chalf * (V / 2); c0 < (chalf + 1) * (V / 2); c0 += 32) {
+      uint32_t r[32];
+      GDP_TMEM_LD32(tmem + lane_base + 128 + c0, r);
+      tmem_wait_ld();
+      if (p < n) {
+        float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+    }
+    if (tid < n) a.gk[(int64_t)hv * a.Te + R0 + tid] = make_float4(sgh[tid], sgl[tid], srk[tid], 0.f);
+  }
+  tmem_release(tmem, kCols);
+}
+
+// ============================================================================ chunk_h, 128-position steps
+// Same recurrence as h_tc_kernel, one 128-position block per step (WY factors
+// from wy128_tc_kernel), every accumulator row in use. Operand buffers are
+// single: each group is refilled for the next block as soon as its last
+// consumer of this block is done (w after product 1, u and the per-position
+// records after the value phase, k after product 2).
+constexpr int S8_WHI = 0;                   // w hi: 2 K-halves x 128 rows x 128 B
+constexpr int S8_WLO = 32768;               // w lo
+constexpr int S8_K = 65536;                 // k: 2 K-halves x 128 rows x 128 B
+constexpr int S8_U = 98304;                 // u fp32 128 x 32
+constexpr int S8_G = 114688;                // (Gam hi, Gam lo, 1/|k|, 0) x 128
+constexpr int S8_HT = 116736;               // h operand hi | lo: 128 rows x 64 B each
+constexpr int S8_VP = S8_HT + 16384;        // v' operand hi | lo: 128 rows x 64 B each
+constexpr int S8_BAR = S8_VP + 16384;
+constexpr int S8_SMEM = S8_BAR + 64 + 1024;
+
+__global__ void __launch_bounds__(256, 1) h128_tc_kernel(
+    const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
+    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
+    const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, chalf = warp >> 2;
+  const int row = quarter * 32 + lane;          // state row kf / position p
+  const int cb = chalf * kHCols;
+  const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
+  const int v0 = blockIdx.z * kHBV;
+  const int V = a.V, M = a.M;
+  const int4 si = a.seq_info[seq];
+  const int nb = (int)cdiv((int64_t)si.y * M, 128);
+  const int tok_blocks = M / 2;                 // 128-blocks per token chunk (M even)
+  uint8_t* ht = sm + S8_HT;
+  uint8_t* vp = sm + S8_VP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S8_BAR);  // [0] w [1] u+gk [2] k [3] p1 [4] p2
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
+  const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const int64_t Rseq = (int64_t)si.x * M;
+  const int64_t gk_base = (int64_t)hv * a.Te + Rseq;
+
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 64);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  const uint32_t off_r0 = sw64_chunk(row, 2 * chalf), off_r1 = sw64_chunk(row, 2 * chalf + 1);
+  float h[kHCols];
+  {
+    const float* src = a.h0 ? a.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
+#pragma unroll
+    for (int c = 0; c < kHCols; ++c) h[c] = src ? src[c] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  auto load_w = [&](int64_t R) {
+    mbar_expect_tx(&bars[0], 65536);
+    tma_load_3d(sm + S8_WHI, &map_whi, 0, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + S8_WHI + 16384, &map_whi, 64, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + S8_WLO, &map_wlo, 0, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + S8_WLO + 16384, &map_wlo, 64, hv, (int)R, &bars[0]);
+  };
+  auto load_ug = [&](int64_t R, int64_t G) {
+    mbar_expect_tx(&bars[1], 16384 + 2048);
+    tma_load_3d(sm + S8_U, &map_u, v0, hv, (int)R, &bars[1]);
+    tma_load_2d(sm + S8_G, &map_gk, 0, (int)G, &bars[1]);
+  };
+  auto load_k = [&](int64_t R) {
+    mbar_expect_tx(&bars[2], 32768);
+    tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[2]);
+    tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[2]);
+  };
+  if (tid == 0 && nb > 0) {
+    load_w(Rseq);
+    load_ug(Rseq, gk_base);
+    load_k(Rseq);
+  }
+  const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
+  const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+  for (int j = 0; j <= nb; ++j) {
+    {  // publish the state at the start of block j
+      __align__(16) bf16 hi[kHCols];
+      __align__(16) bf16 lo[kHCols];
+#pragma unroll
+      for (int c = 0; c < kHCols; ++c) split_bf16(h[c], hi[c], lo[c]);
+      const uint4* h4 = reinterpret_cast<const uint4*>(hi);
+      const uint4* l4 = reinterpret_cast<const uint4*>(lo);
+      *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
+      *reinterpret_cast<uint4*>(ht + off_r1) = h4[1];
+      *reinterpret_cast<uint4*>(ht + 8192 + off_r0) = l4[0];
+      *reinterpret_cast<uint4*>(ht + 8192 + off_r1) = l4[1];
+      if (j < nb && j % tok_blocks == 0) {
+        const int64_t base =
+            ((((int64_t)si.w + j / tok_blocks) * a.HV + hv) * kK + row) * V + v0 + cb;
+        uint4* dh = reinterpret_cast<uint4*>(a.h_hi + base);
+        uint4* dl = reinterpret_cast<uint4*>(a.h_lo + base);
+        dh[0] = h4[0];
+        dh[1] = h4[1];
+        dl[0] = l4[0];
+        dl[1] = l4[1];
+      }
+    }
+    if (j == nb) break;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int n = min(128, si.y * M - j * 128);
+    const int64_t R = Rseq + (int64_t)j * 128;
+    const uint32_t ph = j & 1;
+    bool ok = mbar_wait(&bars[0], ph, a.status, kDevTimeout);
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {  // product 1: D1 = w h (rows = 128 positions)
+      const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO), hb = smem_u32(ht);
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t A = pass == 2 ? wlo : whi;
+        const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
+          mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
+        }
+      }
+      mma_commit(&bars[3]);
+    }
+    ok = mbar_wait(&bars[1], ph, a.status, kDevTimeout);
+    const float4* gk = reinterpret_cast<const float4*>(sm + S8_G);
+    const float4 glast = gk[n - 1];
+    {  // value phase: position p = row, columns cb .. cb + 15
+      const int p = row;
+      ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout) && ok;
+      tc_fence_after();
+      if (tid == 0 && j + 1 < nb) load_w(R + 128);  // w buffers are free once product 1 is done
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + lane_base + cb, r);
+      tmem_wait_ld();
+      const float* us = reinterpret_cast<const float*>(sm + S8_U) + p * kHBV + cb;
+      const float4 gp = gk[p];
+      const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
+      __align__(16) bf16 vh[kHCols];
+      __align__(16) bf16 vl[kHCols];
+      __align__(16) bf16 pvh[kHCols];
+      __align__(16) bf16 pvl[kHCols];
+#pragma unroll
+      for (int c = 0; c < kHCols; ++c) {
+        const float vn = us[c] - __uint_as_float(r[c]);
+        split_bf16(vn, vh[c], vl[c]);
+        split_bf16(p < n ? vn * sc : 0.f, pvh[c], pvl[c]);
+      }
+      if (p < n) {
+        const int64_t rowg = (R + p) * a.HV * V + (int64_t)hv * V + v0 + cb;
+        uint4* dh = reinterpret_cast<uint4*>(a.vn_hi + rowg);
+        uint4* dl = reinterpret_cast<uint4*>(a.vn_lo + rowg);
+        dh[0] = reinterpret_cast<const uint4*>(vh)[0];
+        dh[1] = reinterpret_cast<const uint4*>(vh)[1];
+        dl[0] = reinterpret_cast<const uint4*>(vl)[0];
+        dl[1] = reinterpret_cast<const uint4*>(vl)[1];
+      }
+      *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(pvh)[0];
+      *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(pvh)[1];
+      *reinterpret_cast<uint4*>(vp + 8192 + off_r0) = reinterpret_cast<const uint4*>(pvl)[0];
+      *reinterpret_cast<uint4*>(vp + 8192 + off_r1) = reinterpret_cast<const uint4*>(pvl)[1];
+      fence_async_smem();
+      tc_fence_before();
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    tc_fence_after();
+    if (tid == 0) {
+      if (j + 1 < nb) load_ug(R + 128, gk_base + (int64_t)(j + 1) * 128);  // u, records consumed
+      ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout);
+      if (ok) {  // product 2: D2 = k^T v' (rows = state rows kf), K = 128 positions
+        const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
+            const uint64_t bd = sdesc_sw64(vb + pass * 8192 + kk * 1024, 8192, 512);
+            mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
+          }
+        mma_commit(&bars[4]);
+      }
+    }
+    if (!__syncthreads_and(ok)) break;
+    ok = mbar_wait(&bars[4], ph, a.status, kDevTimeout);
+    tc_fence_after();
+    if (tid == 0 && ok && j + 1 < nb) load_k(R + 128);  // k consumed by product 2
+    {
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
+      tmem_wait_ld();
+      const float dl = expf(glast.x + glast.y);
+#pragma unroll
+      for (int c = 0; c < kHCols; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+    }
+    tc_fence_before();
+    if (!__syncthreads_and(ok)) break;
   }
   if (a.hT) {
     float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
@@ -635,7 +1157,7 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
   const int nt = min(kBT, si.y - t_start);
   const int ne = nt * M;
   const int64_t T0 = (int64_t)si.x + t_start, E0 = T0 * M;
-  const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * a.V + v0;
+  const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * kK;  // first of K rows
   constexpr int NE = 64 * M;  // expanded positions in a full token chunk
   uint8_t* qb = sm;
   uint8_t* kb = sm + o_k_off();
@@ -669,10 +1191,8 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
     tma_load_3d(qb + 8192, &map_q, 64, kh, (int)T0, &bars[0]);
     tma_load_3d(kb, &map_k, 0, kh, (int)E0, &bars[0]);
     tma_load_3d(kb + NE * 128, &map_k, 64, kh, (int)E0, &bars[0]);
-    tma_load_2d(hb, &map_hhi, 0, (int)hrow, &bars[0]);
-    tma_load_2d(hb + 8192, &map_hhi, 64, (int)hrow, &bars[0]);
-    tma_load_2d(hb + 16384, &map_hlo, 0, (int)hrow, &bars[0]);
-    tma_load_2d(hb + 24576, &map_hlo, 64, (int)hrow, &bars[0]);
+    tma_load_2d(hb, &map_hhi, v0, (int)hrow, &bars[0]);
+    tma_load_2d(hb + 16384, &map_hlo, v0, (int)hrow, &bars[0]);
     tma_load_3d(vb, &map_vhi, v0, hv, (int)E0, &bars[0]);
     tma_load_3d(vb + NE * 128, &map_vlo, v0, hv, (int)E0, &bars[0]);
     comp_prefix(sgh, sgl, kBT);
@@ -682,7 +1202,7 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
   if (tid == 0) {
     const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
     const uint32_t ids = idesc_bf16(128, NE, false, false);
-    const uint32_t idh = idesc_bf16(128, kOBV, false, false);
+    const uint32_t idh = idesc_bf16(128, kOBV, false, true);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {  // scores S = q k^T: N = 64 M positions
       const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
@@ -694,7 +1214,7 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(h0 + pass * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(h0 + pass * 16384 + kk * 2048, 16384, 1024);
         mma_bf16(tmem + NE, ad, bd, idh, (pass | kk) != 0);
       }
     mma_commit(&bars[1]);
@@ -855,6 +1375,19 @@ cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
   return cudaGetLastError();
 }
 
+template <int V>
+cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
+  const int64_t Te = (int64_t)p.B * p.T * p.M;
+  CUtensorMap mk, mv;
+  if (!map3(&mk, p.k, BF, 2, kK, p.H, Te, 64, 128, true)) return cudaErrorInvalidValue;
+  if (!map3(&mv, p.v, BF, 2, V, p.HV, Te, 64, 128, true)) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
+  if (e != cudaSuccess) return e;
+  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 256, W8_SMEM, p.stream>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
 template <int M>
 cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi,
                   const CUtensorMap& mhlo, const CUtensorMap& mvhi, const CUtensorMap& mvlo) {
@@ -921,38 +1454,47 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
   if (p.NE_max > 0 && Te > 0) {
     WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
              reinterpret_cast<const int2*>(ws + L.exp_tab), w_hi, w_lo, u, gk, status};
+    const bool blk128 = (p.M % 2) == 0;
     switch (p.V) {
-      case 64: e = run_wy<64>(p, a); break;
-      case 128: e = run_wy<128>(p, a); break;
-      default: e = run_wy<256>(p, a); break;
+      case 64: e = blk128 ? run_wy128<64>(p, a) : run_wy<64>(p, a); break;
+      case 128: e = blk128 ? run_wy128<128>(p, a) : run_wy<128>(p, a); break;
+      default: e = blk128 ? run_wy128<256>(p, a) : run_wy<256>(p, a); break;
     }
     if (e != cudaSuccess) return e;
   }
   record_stage(2, p.stream);
-  // state recurrence
+  // state recurrence: 128-position steps for even M, 64-position steps otherwise
   {
+    const bool blk128 = (p.M % 2) == 0;
+    const uint32_t rows = blk128 ? 128 : 64;
     CUtensorMap mwh, mwl, mk, mu, mg;
     const int64_t Tr = Te > 0 ? Te : 1;
-    if (!map3(&mwh, w_hi, BF, 2, kK, p.HV, Tr, 64, 64, true) ||
-        !map3(&mwl, w_lo, BF, 2, kK, p.HV, Tr, 64, 64, true) ||
-        !map3(&mk, p.k ? p.k : w_hi, BF, 2, kK, p.H, Tr, 64, 64, true) ||
-        !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, 64, false) ||
-        !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, 64, false))
+    if (!map3(&mwh, w_hi, BF, 2, kK, p.HV, Tr, 64, rows, true) ||
+        !map3(&mwl, w_lo, BF, 2, kK, p.HV, Tr, 64, rows, true) ||
+        !map3(&mk, p.k ? p.k : w_hi, BF, 2, kK, p.H, Tr, 64, rows, true) ||
+        !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, rows, false) ||
+        !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, rows, false))
       return cudaErrorInvalidValue;
     HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
-    e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
-    if (e != cudaSuccess) return e;
-    h_tc_kernel<<<dim3(p.N_seq, p.HV, (unsigned)(p.V / kHBV)), 256, H_SMEM, p.stream>>>(
-        mwh, mwl, mk, mu, mg, a, p.H);
+    const dim3 grid(p.N_seq, p.HV, (unsigned)(p.V / kHBV));
+    if (blk128) {
+      e = cudaFuncSetAttribute(h128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S8_SMEM);
+      if (e != cudaSuccess) return e;
+      h128_tc_kernel<<<grid, 256, S8_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, a, p.H);
+    } else {
+      e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
+      if (e != cudaSuccess) return e;
+      h_tc_kernel<<<grid, 256, H_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, a, p.H);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   record_stage(3, p.stream);
   // output
   if (p.NT_max > 0 && Te > 0) {
     CUtensorMap mhh, mhl, mvh, mvl;
-    const uint64_t hrows = (uint64_t)p.NT_max * p.HV * p.V;
-    if (!map2(&mhh, h_hi, BF, 2, kK, hrows, 64, kOBV, true) ||
-        !map2(&mhl, h_lo, BF, 2, kK, hrows, 64, kOBV, true) ||
+    const uint64_t hrows = (uint64_t)p.NT_max * p.HV * kK;
+    if (!map2(&mhh, h_hi, BF, 2, p.V, hrows, kOBV, kK, true) ||
+        !map2(&mhl, h_lo, BF, 2, p.V, hrows, kOBV, kK, true) ||
         !map3(&mvh, vn_hi, BF, 2, p.V, p.HV, Te, 64, 64 * p.M, true) ||
         !map3(&mvl, vn_lo, BF, 2, p.V, p.HV, Te, 64, 64 * p.M, true))
       return cudaErrorInvalidValue;

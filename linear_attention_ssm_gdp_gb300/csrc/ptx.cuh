@@ -153,6 +153,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle: 64-byte rows, 8-row groups
+// of 512 bytes, 16-byte chunk j of row r stored at chunk j ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
+
+// Byte offset of 16-byte chunk j (0..3) of row r in a 64B-swizzled tile.
+__device__ __forceinline__ uint32_t sw64_chunk(uint32_t r, uint32_t j) {
+  return r * 64u + ((j ^ ((r >> 1) & 3u)) << 4);
+}
+
 // TMEM -> registers: the calling warp reads its 32 lanes (lane base = 32 * (warp % 4),
 // encoded in taddr bits 31:16), 16 or 32 consecutive 32-bit columns each.
 #define GDP_TMEM_LD16(taddr, r)                                                            \

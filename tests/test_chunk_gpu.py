@@ -155,6 +155,7 @@ def test_stages_match_chunked_restatement(gdp, K, V, M, dtype):
     off = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, HV, K, V, M, BT, dtype)
     Te = B * T * M
     NONE = (1 << 64) - 1
+    WY = off[6]  # WY block length of the selected path (A, w, u live on these blocks)
 
     def view(i, shape):
         return ws[off[i]:off[i] + 4 * int(torch.tensor(shape).prod())].view(torch.float32).view(
@@ -165,15 +166,19 @@ def test_stages_match_chunked_restatement(gdp, K, V, M, dtype):
         ref = oracle.chunked_stream(f(q[0, :, hv]), f(k[0, :, hv]), f(v[0, :, hv]),
                                     f(beta[0, :, hv]), f(g[0, :, hv]), M, BT, K ** -0.5,
                                     l2norm=True)
+        wyref = ref if WY == BT else oracle.chunked_stream(
+            f(q[0, :, hv]), f(k[0, :, hv]), f(v[0, :, hv]), f(beta[0, :, hv]), f(g[0, :, hv]),
+            M, WY, K ** -0.5, l2norm=True)
         if off[0] != NONE:
-            A = view(0, (Te, HV, BT))[:, hv]
-            for c, Ac in enumerate(ref["A"]):
+            A = view(0, (Te, HV, WY))[:, hv]
+            for c, Ac in enumerate(wyref["A"]):
                 n = Ac.shape[0]
-                assert rel_err(A[c * BT:c * BT + n, :n], torch.from_numpy(Ac)) <= 1e-5
+                assert rel_err(A[c * WY:c * WY + n, :n], torch.from_numpy(Ac)) <= 1e-5
         for name, idx, width in (("w", 1, K), ("u", 2, V), ("v_new", 3, V)):
             if off[idx] != NONE:
                 got = view(idx, (Te, HV, width))[:, hv]
-                assert rel_err(got, torch.from_numpy(ref[name])) <= 1e-4, name
+                want = (wyref if name != "v_new" else ref)[name]
+                assert rel_err(got, torch.from_numpy(want)) <= 1e-4, name
         if off[4] != NONE:
             hs = view(4, (-(-T // BT), HV, K, V))[:, hv]
             for c in range(hs.shape[0]):
