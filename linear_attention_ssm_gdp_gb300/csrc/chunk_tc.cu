@@ -129,63 +129,71 @@ constexpr int wy_smem(int V) { return wy_s_off(V) + 6 * 64 * 4 + 64 + 1024; }
 
 // One merge level of the blocked triangular inverse, for NP independent pairs
 // of SZ x SZ blocks along the diagonal of the in-place matrix LA (row stride
-// lda): X = L10 A00, then A10 = -A11 X written over L10. Dense products (the
-// zeros above the diagonals are stored), register-tiled: each of the 256
-// threads owns a TR x TC tile of outputs with independent accumulators.
-template <int SZ, int NP>
+// lda): X = L10 A00, then A10 = -A11 X written over L10. Register-tiled: each
+// of the NT threads owns a TR x TC tile of outputs with independent
+// accumulators. Both products skip the zero triangles of A00 / A11; the
+// thread-to-tile maps put threads sharing a loop bound in the same warp (a
+// column block for X = L10 A00, where i runs from the tile's first column; a
+// row block for A10 = -A11 X, where i runs up to the tile's last row).
+template <int SZ, int NP, int NT>
 __device__ __forceinline__ void merge_level(float* LA, int lda, float* X) {
-  constexpr int E = NP * SZ * SZ / 256;
+  constexpr int E = NP * SZ * SZ / NT;
   constexpr int TC = E >= 4 ? 4 : E;
   constexpr int TR = E / TC;
   constexpr int NCB = SZ / TC, NRB = SZ / TR;
   constexpr int XS = SZ + 4;
   const int t = threadIdx.x;
   const int pair = t / (NRB * NCB), rem = t - pair * (NRB * NCB);
-  const int r0 = (rem / NCB) * TR, c0 = (rem % NCB) * TC;
   const int base = pair * 2 * SZ;
   float* Xp = X + pair * SZ * XS;
   float acc[TR][TC];
-#pragma unroll
-  for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < SZ; ++i) {
-    float av[TR], bv[TC];
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + i];
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) bv[cc] = LA[(base + i) * lda + base + c0 + cc];
+  {  // X = L10 A00, A00 lower triangular: i >= c0
+    const int r0 = (rem % NRB) * TR, c0 = (rem / NRB) * TC;
 #pragma unroll
     for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
-      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
+#pragma unroll 4
+    for (int i = c0; i < SZ; ++i) {
+      float av[TR], bv[TC];
+#pragma unroll
+      for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + i];
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) bv[cc] = LA[(base + i) * lda + base + c0 + cc];
+#pragma unroll
+      for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+    }
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) Xp[(r0 + rr) * XS + c0 + cc] = acc[rr][cc];
   }
-#pragma unroll
-  for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) Xp[(r0 + rr) * XS + c0 + cc] = acc[rr][cc];
   __syncthreads();
-#pragma unroll
-  for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < SZ; ++i) {
-    float av[TR], bv[TC];
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + SZ + i];
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) bv[cc] = Xp[i * XS + c0 + cc];
+  {  // A10 = -A11 X, A11 lower triangular: i <= r0 + TR - 1
+    const int r0 = (rem / NCB) * TR, c0 = (rem % NCB) * TC;
 #pragma unroll
     for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
-      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < r0 + TR; ++i) {
+      float av[TR], bv[TC];
+#pragma unroll
+      for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + SZ + i];
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) bv[cc] = Xp[i * XS + c0 + cc];
+#pragma unroll
+      for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
+    }
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) LA[(base + SZ + r0 + rr) * lda + base + c0 + cc] = -acc[rr][cc];
   }
-#pragma unroll
-  for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-    for (int cc = 0; cc < TC; ++cc) LA[(base + SZ + r0 + rr) * lda + base + c0 + cc] = -acc[rr][cc];
   __syncthreads();
 }
 
@@ -220,8 +228,8 @@ __device__ void solve_tril64(const float* Ls, float* As, float* X) {
     if ((r >> 4) > (c >> 4)) As[r * 65 + c] = Ls[r * 65 + c];
   }
   __syncthreads();
-  merge_level<16, 2>(As, 65, X);
-  merge_level<32, 1>(As, 65, X);
+  merge_level<16, 2, 256>(As, 65, X);
+  merge_level<32, 1, 256>(As, 65, X);
 }
 
 template <int V>
@@ -562,7 +570,13 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
       uint32_t r[16];
       GDP_TMEM_LD16(tmem + lane_base + cb, r);
       tmem_wait_ld();
-      const float* us = reinterpret_cast<const float*>(st + 49152) + p * kHBV + cb;
+      const uint8_t* urow = st + 49152 + p * 128;  // u row p, 128B-swizzled 16-byte chunks
+      float us[kHCols];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v4 = *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + j) ^ (p & 7)) << 4));
+        us[4 * j] = v4.x; us[4 * j + 1] = v4.y; us[4 * j + 2] = v4.z; us[4 * j + 3] = v4.w;
+      }
       const float4 gp = gk[p];
       const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
       __align__(16) bf16 vh[kHCols];
@@ -655,7 +669,7 @@ constexpr int W8_SMEM = W8_S + 5 * 128 * 4 + 64 + 1024;
 // strictly lower in LA (row stride 129, zeros on and above the diagonal):
 // 16x16 diagonal blocks by forward substitution (results staged in scratch,
 // then copied back), then merges A10 = -A11 (L10 A00) at sizes 16, 32, 64.
-// scratch >= 64 * 68 floats. 256 threads.
+// scratch >= 64 * 68 floats. 512 threads.
 __device__ void solve_tril128(float* LA, float* scratch) {
   const int tid = threadIdx.x;
   if (tid < 128) {
@@ -675,18 +689,18 @@ __device__ void solve_tril128(float* LA, float* scratch) {
     for (int i = 0; i < 16; ++i) scratch[(b * 16 + i) * 16 + cl] = col[i];
   }
   __syncthreads();
-  for (int idx = tid; idx < 128 * 16; idx += 256) {
+  for (int idx = tid; idx < 128 * 16; idx += 512) {
     const int row = idx >> 4, cl = idx & 15;
     LA[row * 129 + (row & ~15) + cl] = scratch[idx];
   }
   __syncthreads();
-  merge_level<16, 4>(LA, 129, scratch);
-  merge_level<32, 2>(LA, 129, scratch);
-  merge_level<64, 1>(LA, 129, scratch);
+  merge_level<16, 4, 512>(LA, 129, scratch);
+  merge_level<32, 2, 512>(LA, 129, scratch);
+  merge_level<64, 1, 512>(LA, 129, scratch);
 }
 
 template <int V>
-__global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                           const __grid_constant__ CUtensorMap map_v,
                                                           WyArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -695,7 +709,7 @@ __global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant_
   const int2 tab = a.exp_tab[blockIdx.x];
   if (tab.x < 0 || (tab.y & 1)) return;  // one CTA per pair of 64-position chunks
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, chalf = warp >> 2;
+  const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
   const int4 si = a.seq_info[tab.x];
   const int M = a.M;
@@ -774,8 +788,11 @@ __global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant_
   {  // L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|) for i < p
     const int p = quarter * 32 + lane;
     const float bp = sb[p] * srk[p];
-#pragma unroll 1
-    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+    const int c0 = cq * 32;
+    if (cq > quarter) {  // block entirely on or above the diagonal: zeros
+#pragma unroll
+      for (int j = 0; j < 32; ++j) LA[p * 129 + c0 + j] = 0.f;
+    } else {
       uint32_t r[32];
       GDP_TMEM_LD32(tmem + lane_base + c0, r);
       tmem_wait_ld();
@@ -791,18 +808,26 @@ __global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant_
   __syncthreads();
   solve_tril128(LA, scratch);
   // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u)
+  // (A is lower triangular: the first build writes the zero upper triangle, the
+  // second leaves it in place since the w MMAs only read the tiles)
   auto build_tiles = [&](int which) {
     const float* sc = which == 0 ? sco : sb;
-    for (int idx = tid; idx < 128 * 64; idx += 256) {
+    for (int idx = tid; idx < 128 * 64; idx += 512) {
       const int prow = idx >> 6, i = (idx & 63) * 2;  // pairs of adjacent columns
-      const float a0 = LA[prow * 129 + i] * sc[i], a1 = LA[prow * 129 + i + 1] * sc[i + 1];
-      bf16 h0, l0, h1, l1;
-      split_bf16(a0, h0, l0);
-      split_bf16(a1, h1, l1);
+      if (i > prow && which == 1) continue;
       const uint32_t off = (i >> 6) * 16384 + sw128_offset(prow, (i & 63) * 2);
       __nv_bfloat162 hh, ll;
-      hh.x = h0; hh.y = h1;
-      ll.x = l0; ll.y = l1;
+      if (i > prow) {
+        hh = __floats2bfloat162_rn(0.f, 0.f);
+        ll = hh;
+      } else {
+        const float a0 = LA[prow * 129 + i] * sc[i], a1 = LA[prow * 129 + i + 1] * sc[i + 1];
+        bf16 h0, l0, h1, l1;
+        split_bf16(a0, h0, l0);
+        split_bf16(a1, h1, l1);
+        hh.x = h0; hh.y = h1;
+        ll.x = l0; ll.y = l1;
+      }
       *reinterpret_cast<__nv_bfloat162*>(tiles + off) = hh;
       *reinterpret_cast<__nv_bfloat162*>(tiles + 32768 + off) = ll;
     }
@@ -844,11 +869,11 @@ __global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant_
     mma_commit(&bars[1]);
   };
   if (tid == 0) issue_u(0);
-  // w epilogue (overlaps the u MMAs): row p, 64 of the 128 columns per thread
+  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread
   {
     const int p = quarter * 32 + lane;
-#pragma unroll 1
-    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+    {
+      const int c0 = cq * 32;
       uint32_t r[32];
       GDP_TMEM_LD32(tmem + lane_base + c0, r);
       tmem_wait_ld();
@@ -881,17 +906,17 @@ __global__ void __launch_bounds__(256, 1) wy128_tc_kernel(const __grid_constant_
   ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
   tc_fence_after();
   if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  {  // u epilogue: row p, V / 2 columns per thread
+  {  // u epilogue: row p, V / 4 columns per thread
     const int p = quarter * 32 + lane;
 #pragma unroll 1
-    for (int c0 = chalf * (V / 2); c0 < (chalf + 1) * (V / 2); c0 += 32) {
-      uint32_t r[32];
-      GDP_TMEM_LD32(tmem + lane_base + 128 + c0, r);
+    for (int c0 = cq * (V / 4); c0 < (cq + 1) * (V / 4); c0 += 16) {
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + lane_base + 128 + c0, r);
       tmem_wait_ld();
       if (p < n) {
         float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 4; ++j)
           dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
@@ -925,9 +950,10 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, chalf = warp >> 2;
+  const int quarter = warp & 3, cgrp = warp >> 2;
   const int row = quarter * 32 + lane;          // state row kf / position p
-  const int cb = chalf * kHCols;
+  constexpr int NC = 16;                        // value columns per thread
+  const int cb = cgrp * NC;
   const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
   const int v0 = blockIdx.z * kHBV;
   const int V = a.V, M = a.M;
@@ -951,12 +977,13 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
     for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  const uint32_t off_r0 = sw64_chunk(row, 2 * chalf), off_r1 = sw64_chunk(row, 2 * chalf + 1);
-  float h[kHCols];
+  // this thread's two 16-byte chunks of an operand row
+  const uint32_t off_r0 = sw64_chunk(row, 2 * cgrp), off_r1 = sw64_chunk(row, 2 * cgrp + 1);
+  float h[NC];
   {
     const float* src = a.h0 ? a.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
 #pragma unroll
-    for (int c = 0; c < kHCols; ++c) h[c] = src ? src[c] : 0.f;
+    for (int c = 0; c < NC; ++c) h[c] = src ? src[c] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -988,10 +1015,10 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
   for (int j = 0; j <= nb; ++j) {
     {  // publish the state at the start of block j
-      __align__(16) bf16 hi[kHCols];
-      __align__(16) bf16 lo[kHCols];
+      __align__(16) bf16 hi[NC];
+      __align__(16) bf16 lo[NC];
 #pragma unroll
-      for (int c = 0; c < kHCols; ++c) split_bf16(h[c], hi[c], lo[c]);
+      for (int c = 0; c < NC; ++c) split_bf16(h[c], hi[c], lo[c]);
       const uint4* h4 = reinterpret_cast<const uint4*>(hi);
       const uint4* l4 = reinterpret_cast<const uint4*>(lo);
       *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
@@ -1042,18 +1069,24 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
       ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout) && ok;
       tc_fence_after();
       if (tid == 0 && j + 1 < nb) load_w(R + 128);  // w buffers are free once product 1 is done
-      uint32_t r[16];
+      uint32_t r[NC];
       GDP_TMEM_LD16(tmem + lane_base + cb, r);
       tmem_wait_ld();
-      const float* us = reinterpret_cast<const float*>(sm + S8_U) + p * kHBV + cb;
+      const uint8_t* urow = sm + S8_U + p * 128;  // u row p, 128B-swizzled 16-byte chunks
+      float us[NC];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v4 = *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + j) ^ (p & 7)) << 4));
+        us[4 * j] = v4.x; us[4 * j + 1] = v4.y; us[4 * j + 2] = v4.z; us[4 * j + 3] = v4.w;
+      }
       const float4 gp = gk[p];
       const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
-      __align__(16) bf16 vh[kHCols];
-      __align__(16) bf16 vl[kHCols];
-      __align__(16) bf16 pvh[kHCols];
-      __align__(16) bf16 pvl[kHCols];
+      __align__(16) bf16 vh[NC];
+      __align__(16) bf16 vl[NC];
+      __align__(16) bf16 pvh[NC];
+      __align__(16) bf16 pvl[NC];
 #pragma unroll
-      for (int c = 0; c < kHCols; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const float vn = us[c] - __uint_as_float(r[c]);
         split_bf16(vn, vh[c], vl[c]);
         split_bf16(p < n ? vn * sc : 0.f, pvh[c], pvl[c]);
@@ -1098,12 +1131,12 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
     tc_fence_after();
     if (tid == 0 && ok && j + 1 < nb) load_k(R + 128);  // k consumed by product 2
     {
-      uint32_t r[16];
+      uint32_t r[NC];
       GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
       tmem_wait_ld();
       const float dl = expf(glast.x + glast.y);
 #pragma unroll
-      for (int c = 0; c < kHCols; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+      for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
     }
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
@@ -1111,7 +1144,7 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   if (a.hT) {
     float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
 #pragma unroll
-    for (int c = 0; c < kHCols; c += 4)
+    for (int c = 0; c < NC; c += 4)
       *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
   }
   tmem_release(tmem, 64);
@@ -1129,16 +1162,16 @@ struct OArgs {
 };
 
 // q (24 KB incl. view) | k (2 halves of 64M rows, 16M KB) | h hi, lo (16 KB each) |
-// v_new hi, lo (8M KB each) | P hi, lo (M K-blocks each, 8 KB per block, +8 KB view) | small
+// v_new hi, lo (8M KB each) | P hi, lo (MN-major: 64M rows e x 64 tokens t, 8M KB each) | small
 constexpr int o_k_off() { return 24576; }
 constexpr int o_h_off(int M) { return o_k_off() + 16384 * M; }
 constexpr int o_v_off(int M) { return o_h_off(M) + 32768; }
 constexpr int o_p_off(int M) { return o_v_off(M) + 16384 * M; }
-constexpr int o_s_off(int M) { return o_p_off(M) + (2 * M + 1) * 8192; }
+constexpr int o_s_off(int M) { return o_p_off(M) + 2 * M * 8192; }
 constexpr int o_smem(int M) { return o_s_off(M) + (3 * 64 + 64 * M) * 4 + 64 + 1024; }
 
 template <int M>
-__global__ void __launch_bounds__(256, 1) o_tc_kernel(
+__global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
     const __grid_constant__ CUtensorMap map_hhi, const __grid_constant__ CUtensorMap map_hlo,
     const __grid_constant__ CUtensorMap map_vhi, const __grid_constant__ CUtensorMap map_vlo,
@@ -1149,7 +1182,7 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
   const int2 tab = a.tok_tab[blockIdx.x];
   if (tab.x < 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, chalf = warp >> 2;  // TMEM lane quarter, column half
+  const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
   const int v0 = blockIdx.z * kOBV;
   const int4 si = a.seq_info[tab.x];
@@ -1224,37 +1257,38 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
     const float ss = row_sumsq(qb + tid * 128) + row_sumsq(qb + 8192 + tid * 128);
     srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
-  for (int e = tid; e < NE; e += 256) {
+  for (int e = tid; e < NE; e += 512) {
     const float ss = row_sumsq(kb + e * 128) + row_sumsq(kb + NE * 128 + e * 128);
     srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
   // value rows past the chunk's end may hold anything: zero them (their P is 0)
-  for (int idx = tid; idx < 2 * NE * 8; idx += 256) {
+  for (int idx = tid; idx < 2 * NE * 8; idx += 512) {
     const int row = idx >> 3, ch = idx & 7;
     const int e = row % NE;
     if (e >= ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
   }
   fence_async_smem();
   __syncthreads();
-  if (quarter < 2) {  // P rows t, this warp's half of the N = 64 M columns
+  if (quarter < 2) {  // P rows t, this warp's quarter of the N = 64 M columns
     const int t = quarter * 32 + lane;
     ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
     tc_fence_after();
     const float rt = srq[t];
 #pragma unroll 1
-    for (int c0 = chalf * (NE / 2); c0 < (chalf + 1) * (NE / 2); c0 += 32) {
-      uint32_t r[32];
-      GDP_TMEM_LD32(tmem + ((uint32_t)(quarter * 32) << 16) + c0, r);
+    for (int c0 = cq * (NE / 4); c0 < (cq + 1) * (NE / 4); c0 += 16) {
+      uint32_t r[16];
+      GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int e = c0 + j, s = e / M;
         float pv = 0.f;
         if (e < ne && s <= t && t < nt)
           pv = __uint_as_float(r[j]) * rt * srk[e] * __expf(gam_diff4(sgh, sgl, t, s));
         bf16 ph, pl;
         split_bf16(pv, ph, pl);
-        const uint32_t off = (e >> 6) * 8192 + sw128_offset(t, (e & 63) * 2);
+        // MN-major operand: row e (K), column t (M); a warp writes 64 contiguous bytes of a row
+        const uint32_t off = sw128_offset(e, t * 2);
         *reinterpret_cast<bf16*>(pb + off) = ph;
         *reinterpret_cast<bf16*>(pb + M * 8192 + off) = pl;
       }
@@ -1267,14 +1301,16 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
   if (!ok) { tmem_release(tmem, kCols); return; }
   if (tid == 0) {  // O = P v_new (3 passes), into the score columns (consumed)
     const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
-    const uint32_t ido = idesc_bf16(128, kOBV, false, true);
+    // A = P, MN-major with M = 128: the second 64-token atom is never written and
+    // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
+    const uint32_t ido = idesc_bf16(128, kOBV, true, true);
 #pragma unroll
     for (int pass = 0; pass < 3; ++pass) {
       const uint32_t A = p0 + (pass == 2 ? M * 8192 : 0);
       const uint32_t Bm = vv + (pass == 1 ? NE * 128 : 0);
 #pragma unroll
       for (int kk = 0; kk < 4 * M; ++kk) {
-        const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        const uint64_t ad = sdesc_sw128(A + kk * 2048, 0, 1024);
         const uint64_t bd = sdesc_sw128(Bm + kk * 2048, NE * 128, 1024);
         mma_bf16(tmem, ad, bd, ido, (pass | kk) != 0);
       }
@@ -1288,15 +1324,15 @@ __global__ void __launch_bounds__(256, 1) o_tc_kernel(
     const float qs = expf(sgh[t] + sgl[t]) * srq[t];
     const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
     {
-      const int c0 = chalf * 32;
-      uint32_t ro[32], rh[32];
-      GDP_TMEM_LD32(la + c0, ro);
-      GDP_TMEM_LD32(la + NE + c0, rh);
+      const int c0 = cq * 16;
+      uint32_t ro[16], rh[16];
+      GDP_TMEM_LD16(la + c0, ro);
+      GDP_TMEM_LD16(la + NE + c0, rh);
       tmem_wait_ld();
       if (t < nt && ok) {
         float4* dst = reinterpret_cast<float4*>(a.o + ((T0 + t) * a.HV + hv) * a.V + v0 + c0);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           float x[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -1384,7 +1420,7 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   cudaError_t e =
       cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
-  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 256, W8_SMEM, p.stream>>>(mk, mv, a);
+  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -1398,7 +1434,7 @@ cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi
   const int smem = o_smem(M);
   cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 256, smem, p.stream>>>(
+  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 512, smem, p.stream>>>(
       mq, mk, mhhi, mhlo, mvhi, mvlo, a);
   return cudaGetLastError();
 }
@@ -1472,7 +1508,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
     if (!map3(&mwh, w_hi, BF, 2, kK, p.HV, Tr, 64, rows, true) ||
         !map3(&mwl, w_lo, BF, 2, kK, p.HV, Tr, 64, rows, true) ||
         !map3(&mk, p.k ? p.k : w_hi, BF, 2, kK, p.H, Tr, 64, rows, true) ||
-        !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, rows, false) ||
+        !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, rows, true) ||
         !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, rows, false))
       return cudaErrorInvalidValue;
     HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};

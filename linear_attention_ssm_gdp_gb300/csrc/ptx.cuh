@@ -167,6 +167,12 @@ __device__ __forceinline__ uint32_t sw64_chunk(uint32_t r, uint32_t j) {
 
 // TMEM -> registers: the calling warp reads its 32 lanes (lane base = 32 * (warp % 4),
 // encoded in taddr bits 31:16), 16 or 32 consecutive 32-bit columns each.
+#define GDP_TMEM_LD8(taddr, r)                                                             \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"   \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),  \
+                 "=r"(r[6]), "=r"(r[7])                                                   \
+               : "r"(taddr))
+
 #define GDP_TMEM_LD16(taddr, r)                                                            \
   asm volatile(                                                                           \
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                           \
