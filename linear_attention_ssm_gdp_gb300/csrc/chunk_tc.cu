@@ -1150,6 +1150,407 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   tmem_release(tmem, 64);
 }
 
+// ============================================================================ chunk_h + chunk_o, M = 2
+// For M = 2 a 128-position block is exactly one 64-token output chunk, so the
+// output of a block can be formed from what the scan CTA already holds on
+// chip: the state at the start of the block (product 1's h tile), the block's
+// keys (product 2's k tile) and v_new. Neither states nor v_new go to HBM.
+//
+// Warp roles (512 threads):
+//  * warps 0-7, the chain: the state recurrence of h128_tc_kernel. Thread
+//    (warp w, lane l) owns state row / position 32 (w % 4) + l and value
+//    columns [16 (w / 4), +16) of the CTA's 32. Besides the v' operand it
+//    writes v_new itself as an operand tile.
+//  * warps 8-15, the output: per block, S^T = k q^T (positions x tokens) and
+//    Qh = q h (tokens x columns, 2 passes), then the masked decayed scores
+//      P^T[e][t] = S^T[e][t] |q_t|^-1 |k_e|^-1 e^(Gam_t - Gam_e),  e <= 2t + 1,
+//    as hi/lo operand tiles (thread = position e, 32 tokens), then
+//    O = P v_new (3 passes) and o_t = scale (e^Gam_t |q_t|^-1 Qh_t + O_t),
+//    Gam_t being the cumulative log decay at the token's last copy.
+// The output of block j runs beside the chain's block j + 1; the groups meet
+// only at mbarriers: the output needs the h tile (H) and v_new (VN), the chain
+// re-fills k and re-writes h after S and Qh are done (SQ) and re-writes v_new
+// after O is done (O). Each group syncs internally with its own named barrier.
+struct HOArgs {
+  HArgs h;
+  int H, l2norm;
+  float scale;
+  float* o;
+};
+
+constexpr int F_OG = 116736;                // output group's records: 2 buffers x 128 x 16 B
+constexpr int F_HT = F_OG + 4096;           // h operand hi | lo
+constexpr int F_VP = F_HT + 16384;          // v' operand hi | lo
+constexpr int F_Q = F_VP + 16384;           // q: 2 K-halves x 64 rows x 128 B
+constexpr int F_VN = F_Q + 16384;           // v_new operand hi | lo: 128 rows x 64 B each
+constexpr int F_P = F_VN + 16384;           // P^T operand hi | lo: 128 rows (e) x 128 B (64 t)
+constexpr int F_SM = F_P + 32768;           // 1/|q_t|, barriers, TMEM address
+constexpr int F_SMEM = F_SM + 256 + 16 * 8 + 16 + 1024;
+enum { FB_W, FB_UG, FB_K, FB_Q, FB_OG0, FB_OG1, FB_P1, FB_P2, FB_SQ, FB_O, FB_H, FB_VN, FB_N };
+
+// AND of pred over the count threads of named barrier id (warp-uniform use)
+__device__ __forceinline__ bool group_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
+    const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
+    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
+    const __grid_constant__ CUtensorMap map_gk, const __grid_constant__ CUtensorMap map_q,
+    HOArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, cgrp = (warp >> 2) & 1;
+  const int row = quarter * 32 + lane;
+  constexpr int NC = 16;
+  const int cb = cgrp * NC;
+  const int seq = blockIdx.x, hv = blockIdx.y;
+  const int HVn = f.h.HV, V = f.h.V;
+  const int kh = hv / (HVn / f.H);
+  const int v0 = blockIdx.z * kHBV;
+  const int4 si = f.h.seq_info[seq];
+  const int nb = (int)cdiv((int64_t)si.y * 2, 128);
+  int* status = f.h.status;
+  uint8_t* ht = sm + F_HT;
+  uint8_t* vp = sm + F_VP;
+  uint8_t* vnt = sm + F_VN;
+  uint8_t* pt = sm + F_P;
+  float* srq = reinterpret_cast<float*>(sm + F_SM);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 256);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const int64_t Rseq = (int64_t)si.x * 2;
+  const int64_t gk_base = (int64_t)hv * f.h.Te + Rseq;
+  // TMEM columns: D1 [0,32) D2 [32,64) S^T [64,128) Qh [128,160) O [160,192)
+  constexpr uint32_t TS = 64, TQH = 128, TO = 160;
+
+  if (warp == 0) {
+    tmem_alloc(s_tmem, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < FB_N; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t off_r0 = sw64_chunk(row, 2 * cgrp), off_r1 = sw64_chunk(row, 2 * cgrp + 1);
+
+  if (warp < 8) {  // ------------------------------------------------ chain
+    const int64_t hoff = ((int64_t)seq * HVn + hv) * kK * V;
+    float h[NC];
+    {
+      const float* src = f.h.h0 ? f.h.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) h[c] = src ? src[c] : 0.f;
+    }
+    auto load_w = [&](int64_t R) {
+      mbar_expect_tx(&bars[FB_W], 65536);
+      tma_load_3d(sm + S8_WHI, &map_whi, 0, hv, (int)R, &bars[FB_W]);
+      tma_load_3d(sm + S8_WHI + 16384, &map_whi, 64, hv, (int)R, &bars[FB_W]);
+      tma_load_3d(sm + S8_WLO, &map_wlo, 0, hv, (int)R, &bars[FB_W]);
+      tma_load_3d(sm + S8_WLO + 16384, &map_wlo, 64, hv, (int)R, &bars[FB_W]);
+    };
+    auto load_ug = [&](int64_t R, int64_t G) {
+      mbar_expect_tx(&bars[FB_UG], 16384 + 2048);
+      tma_load_3d(sm + S8_U, &map_u, v0, hv, (int)R, &bars[FB_UG]);
+      tma_load_2d(sm + S8_G, &map_gk, 0, (int)G, &bars[FB_UG]);
+    };
+    auto load_k = [&](int64_t R) {
+      mbar_expect_tx(&bars[FB_K], 32768);
+      tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[FB_K]);
+      tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[FB_K]);
+    };
+    if (tid == 0 && nb > 0) {
+      load_w(Rseq);
+      load_ug(Rseq, gk_base);
+      load_k(Rseq);
+    }
+    const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
+    const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+    bool ok = true;
+    for (int j = 0; j <= nb; ++j) {
+      // the h tile is re-written once Qh of the previous block has read it
+      if (j > 0) ok = mbar_wait(&bars[FB_SQ], (j - 1) & 1, status, kDevTimeout) && ok;
+      {
+        __align__(16) bf16 hi[NC];
+        __align__(16) bf16 lo[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) split_bf16(h[c], hi[c], lo[c]);
+        const uint4* h4 = reinterpret_cast<const uint4*>(hi);
+        const uint4* l4 = reinterpret_cast<const uint4*>(lo);
+        *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
+        *reinterpret_cast<uint4*>(ht + off_r1) = h4[1];
+        *reinterpret_cast<uint4*>(ht + 8192 + off_r0) = l4[0];
+        *reinterpret_cast<uint4*>(ht + 8192 + off_r1) = l4[1];
+      }
+      if (j == nb) break;
+      fence_async_smem();
+      tc_fence_before();
+      ok = group_and(1, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int n = min(128, si.y * 2 - j * 128);
+      const int64_t R = Rseq + (int64_t)j * 128;
+      const uint32_t ph = j & 1;
+      if (tid == 0) {
+        mbar_arrive(&bars[FB_H]);
+        ok = mbar_wait(&bars[FB_W], ph, status, kDevTimeout);
+        if (ok) {  // product 1: D1 = w h
+          const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO);
+          const uint32_t hb = smem_u32(ht);
+#pragma unroll
+          for (int pass = 0; pass < 3; ++pass) {
+            const uint32_t A = pass == 2 ? wlo : whi;
+            const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
+              mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
+            }
+          }
+          mma_commit(&bars[FB_P1]);
+        }
+      }
+      ok = mbar_wait(&bars[FB_UG], ph, status, kDevTimeout) && ok;
+      const float4* gk = reinterpret_cast<const float4*>(sm + S8_G);
+      const float4 glast = gk[n - 1];
+      {  // value phase: position p = row, columns cb .. cb + 15
+        const int p = row;
+        const float4 gp = gk[p];
+        const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
+        ok = mbar_wait(&bars[FB_P1], ph, status, kDevTimeout) && ok;
+        tc_fence_after();
+        if (tid == 0 && ok && j + 1 < nb) load_w(R + 128);
+        uint32_t r[NC];
+        GDP_TMEM_LD16(tmem + lane_base + cb, r);
+        tmem_wait_ld();
+        const uint8_t* urow = sm + S8_U + p * 128;
+        __align__(16) bf16 vh[NC];
+        __align__(16) bf16 vl[NC];
+        __align__(16) bf16 pvh[NC];
+        __align__(16) bf16 pvl[NC];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float4 u4 =
+              *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + jj) ^ (p & 7)) << 4));
+          const float us[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 4 * jj + q;
+            const float vn = (p < n) ? us[q] - __uint_as_float(r[c]) : 0.f;
+            split_bf16(vn, vh[c], vl[c]);
+            split_bf16(vn * sc, pvh[c], pvl[c]);
+          }
+        }
+        *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(pvh)[0];
+        *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(pvh)[1];
+        *reinterpret_cast<uint4*>(vp + 8192 + off_r0) = reinterpret_cast<const uint4*>(pvl)[0];
+        *reinterpret_cast<uint4*>(vp + 8192 + off_r1) = reinterpret_cast<const uint4*>(pvl)[1];
+        // the v_new tile is re-written once O of the previous block has read it
+        if (j > 0) ok = mbar_wait(&bars[FB_O], (j - 1) & 1, status, kDevTimeout) && ok;
+        *reinterpret_cast<uint4*>(vnt + off_r0) = reinterpret_cast<const uint4*>(vh)[0];
+        *reinterpret_cast<uint4*>(vnt + off_r1) = reinterpret_cast<const uint4*>(vh)[1];
+        *reinterpret_cast<uint4*>(vnt + 8192 + off_r0) = reinterpret_cast<const uint4*>(vl)[0];
+        *reinterpret_cast<uint4*>(vnt + 8192 + off_r1) = reinterpret_cast<const uint4*>(vl)[1];
+        fence_async_smem();
+        tc_fence_before();
+      }
+      ok = group_and(1, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (tid == 0) {
+        mbar_arrive(&bars[FB_VN]);
+        if (j + 1 < nb) load_ug(R + 128, gk_base + (int64_t)(j + 1) * 128);
+        ok = mbar_wait(&bars[FB_K], ph, status, kDevTimeout);
+        if (ok) {  // product 2: D2 = k^T v', K = 128 positions
+          const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
+              const uint64_t bd = sdesc_sw64(vb + pass * 8192 + kk * 1024, 8192, 512);
+              mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
+            }
+          mma_commit(&bars[FB_P2]);
+        }
+      }
+      ok = mbar_wait(&bars[FB_P2], ph, status, kDevTimeout) && ok;
+      tc_fence_after();
+      if (tid == 0 && ok && j + 1 < nb) {  // k is free once product 2 and S are done
+        ok = mbar_wait(&bars[FB_SQ], ph, status, kDevTimeout);
+        if (ok) load_k(R + 128);
+      }
+      {
+        uint32_t r[NC];
+        GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
+        tmem_wait_ld();
+        const float dl = expf(glast.x + glast.y);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+      }
+      tc_fence_before();
+    }
+    if (f.h.hT) {
+      float* dst = f.h.hT + hoff + (int64_t)row * V + v0 + cb;
+#pragma unroll
+      for (int c = 0; c < NC; c += 4)
+        *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
+    }
+  } else {  // ------------------------------------------------------ output
+    const int otid = tid - 256;
+    auto load_q = [&](int64_t T0) {
+      mbar_expect_tx(&bars[FB_Q], 16384);
+      tma_load_3d(sm + F_Q, &map_q, 0, kh, (int)T0, &bars[FB_Q]);
+      tma_load_3d(sm + F_Q + 8192, &map_q, 64, kh, (int)T0, &bars[FB_Q]);
+    };
+    auto load_og = [&](int b, int64_t G) {
+      mbar_expect_tx(&bars[FB_OG0 + b], 2048);
+      tma_load_2d(sm + F_OG + b * 2048, &map_gk, 0, (int)G, &bars[FB_OG0 + b]);
+    };
+    if (otid == 0 && nb > 0) {
+      load_q(si.x);
+      load_og(0, gk_base);
+      if (nb > 1) load_og(1, gk_base + 128);
+    }
+    const uint32_t ids = idesc_bf16(128, 64, false, false);
+    const uint32_t idq = idesc_bf16(128, kHBV, false, true);
+    const uint32_t ido = idesc_bf16(128, kHBV, true, true);
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int n = min(128, si.y * 2 - j * 128);
+      const int nt = n >> 1;
+      const int64_t T0 = (int64_t)si.x + (int64_t)j * 64;
+      const uint32_t ph = j & 1;
+      const float4* og = reinterpret_cast<const float4*>(sm + F_OG + (j & 1) * 2048);
+      ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
+      ok = mbar_wait(&bars[FB_OG0 + (j & 1)], (j >> 1) & 1, status, kDevTimeout) && ok;
+      if (otid < 64) {  // query norms from the staged tile
+        const uint8_t* qt = sm + F_Q;
+        const float ss = row_sumsq(qt + otid * 128) + row_sumsq(qt + 8192 + otid * 128);
+        srq[otid] = f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+      }
+      if (otid == 0 && ok) {
+        const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
+        ok = mbar_wait(&bars[FB_K], ph, status, kDevTimeout);
+        if (ok) {  // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TS, ad, bd, ids, kk > 0);
+          }
+        }
+        ok = mbar_wait(&bars[FB_H], ph, status, kDevTimeout) && ok;
+        if (ok) {  // Qh = q h: rows = tokens (64.. unused), h hi then lo
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw64(hb + pass * 8192 + kk * 1024, 8192, 512);
+              mma_bf16(tmem + TQH, ad, bd, idq, (pass | kk) != 0);
+            }
+          mma_commit(&bars[FB_SQ]);
+        }
+      }
+      ok = group_and(2, 256, ok);
+      if (!ok) break;
+      ok = mbar_wait(&bars[FB_SQ], ph, status, kDevTimeout);
+      tc_fence_after();
+      {  // P^T row e = row, tokens [32 cgrp, 32 cgrp + 32)
+        const int e = row, s = e >> 1;
+        const float4 re = og[e];
+        uint32_t r[32];
+        GDP_TMEM_LD32(tmem + lane_base + TS + 32 * cgrp, r);
+        tmem_wait_ld();
+        __align__(16) bf16 ph_[32];
+        __align__(16) bf16 pl_[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = 32 * cgrp + i;
+          float pv = 0.f;
+          if (e < n && s <= t && t < nt) {
+            const float4 rt = og[2 * t + 1];
+            pv = __uint_as_float(r[i]) * srq[t] * re.z * expf((rt.x - re.x) + (rt.y - re.y));
+          }
+          split_bf16(pv, ph_[i], pl_[i]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t off = e * 128 + ((((uint32_t)(4 * cgrp + q)) ^ (e & 7)) << 4);
+          *reinterpret_cast<uint4*>(pt + off) = reinterpret_cast<const uint4*>(ph_)[q];
+          *reinterpret_cast<uint4*>(pt + 16384 + off) = reinterpret_cast<const uint4*>(pl_)[q];
+        }
+        fence_async_smem();
+        tc_fence_before();
+      }
+      ok = group_and(2, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (otid == 0) {
+        if (j + 1 < nb) load_q(T0 + 64);  // q consumed by S, Qh and the norms
+        ok = mbar_wait(&bars[FB_VN], ph, status, kDevTimeout);
+        if (ok) {  // O = P v_new; A = P^T MN-major, second atom re-read (LBO = 0)
+          const uint32_t pb = smem_u32(pt), vv = smem_u32(vnt);
+#pragma unroll
+          for (int pass = 0; pass < 3; ++pass) {
+            const uint32_t A = pb + (pass == 2 ? 16384 : 0);
+            const uint32_t Bm = vv + (pass == 1 ? 8192 : 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(A + kk * 2048, 0, 1024);
+              const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
+              mma_bf16(tmem + TO, ad, bd, ido, (pass | kk) != 0);
+            }
+          }
+          mma_commit(&bars[FB_O]);
+        }
+      }
+      if (quarter < 2) {  // output rows t = row, columns cb .. cb + 15
+        const int t = row;
+        ok = mbar_wait(&bars[FB_O], ph, status, kDevTimeout) && ok;
+        tc_fence_after();
+        uint32_t ro[16], rq[16];
+        GDP_TMEM_LD16(tmem + lane_base + TO + cb, ro);
+        GDP_TMEM_LD16(tmem + lane_base + TQH + cb, rq);
+        tmem_wait_ld();
+        if (t < nt && ok) {
+          const float4 rt = og[2 * t + 1];
+          const float qs = expf(rt.x + rt.y) * srq[t];
+          float4* dst = reinterpret_cast<float4*>(f.o + ((T0 + t) * HVn + hv) * V + v0 + cb);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float x[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              x[q] = f.scale *
+                     (qs * __uint_as_float(rq[4 * jj + q]) + __uint_as_float(ro[4 * jj + q]));
+            dst[jj] = make_float4(x[0], x[1], x[2], x[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      ok = group_and(2, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (otid == 0 && j + 2 < nb) load_og(j & 1, gk_base + (int64_t)(j + 2) * 128);
+    }
+  }
+  tmem_release(tmem, 256);
+}
+
 // ============================================================================ chunk_o
 struct OArgs {
   int H, HV, V, M, l2norm;
@@ -1464,10 +1865,13 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
   L.gam = take(16 * Te * HV);
-  L.vn_hi = take(2 * Te * HV * V);
-  L.vn_lo = take(2 * Te * HV * V);
-  L.h_hi = take(2 * (size_t)NT * HV * V * K);
-  L.h_lo = take(2 * (size_t)NT * HV * V * K);
+  // v_new and the chunk states go through HBM only when the output is a
+  // separate kernel (M != 2)
+  const size_t keep = M == 2 ? 0 : 1;
+  L.vn_hi = take(keep * 2 * Te * HV * V);
+  L.vn_lo = take(keep * 2 * Te * HV * V);
+  L.h_hi = take(keep * 2 * (size_t)NT * HV * V * K);
+  L.h_lo = take(keep * 2 * (size_t)NT * HV * V * K);
   L.total = off;
   L.path = 1;
   return L;
@@ -1513,6 +1917,20 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       return cudaErrorInvalidValue;
     HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
     const dim3 grid(p.N_seq, p.HV, (unsigned)(p.V / kHBV));
+    if (p.M == 2) {  // state recurrence and output fused
+      CUtensorMap mq;
+      const int64_t Tt = (int64_t)p.B * p.T;
+      if (!map3(&mq, p.q ? p.q : w_hi, BF, 2, kK, p.H, Tt > 0 ? Tt : 1, 64, 64, true))
+        return cudaErrorInvalidValue;
+      HOArgs fa{a, p.H, p.l2norm, p.scale, p.o};
+      e = cudaFuncSetAttribute(ho128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+      if (e != cudaSuccess) return e;
+      ho128_tc_kernel<<<grid, 512, F_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, mq, fa);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      record_stage(3, p.stream);
+      record_stage(4, p.stream);
+      return cudaSuccess;
+    }
     if (blk128) {
       e = cudaFuncSetAttribute(h128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S8_SMEM);
       if (e != cudaSuccess) return e;
