@@ -39,7 +39,18 @@ import torch  # noqa: E402
 METRIC = "GDP prefill tokens/sec (T·M) and % of bf16 TC peak; prepare GB/s vs HBM"
 WORKLOAD = dict(B=2, T=4096, H=16, HV=16, G=16, K=128, V=128, M=2, BT=64)
 DECODE = dict(n=256, S=4, M=2, H=32, G=8, P=128, N=128)
+# Device-side pause (~1 ms) between the L2 flush and the start event of a timed
+# step, so that the launches of the step are all queued before it starts: the
+# kernel-timed value then holds no host (Python/ctypes) launch latency. The e2e
+# figure keeps every host cost.
+HOST_LEAD_CYCLES = 2_000_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# DRAM bytes (read + write) per launch of each kernel at the bench workload, from
+# one ncu capture of the committed profiling command (profiles/ncu_prefill_b2t4096_kernels.md).
+# A kernel's entry is removed whenever the kernel changes after the capture.
+TRAFFIC = {"wy": 358.3e6, "scan_out": 431.0e6, "prepare": 288.5e6}
 
 
 def peaks():
@@ -56,23 +67,46 @@ def peaks():
 # ----------------------------------------------------------------------------------
 
 def algorithmic(w=WORKLOAD):
+    """Algorithmic work per step. Flops follow the chunked method at chunk BT (one
+    multiply-add = 2 flops); bytes are each kernel's own inputs and outputs at their
+    stored widths (bf16 q/k/v, fp32 gates, w as a bf16 hi/lo pair = 4 B, fp32 u,
+    16-byte per-position decay records, fp32 o and state)."""
     B, T, H, HV, G, K, V, M, BT = (w[k] for k in ("B", "T", "H", "HV", "G", "K", "V", "M", "BT"))
-    E = B * T * M  # expanded tokens
+    E = B * T * M          # expanded positions
+    Tt = B * T             # tokens
     D = M * H * V + M * G * K + G * K
-    prep_bytes = (B * T * D * 2 + B * T * (M * H + H) * 2          # x, ba read
-                  + B * T * H * K * 2 + E * H * K * 2 + E * H * V * 2  # q, k, v written
-                  + E * H * 4 + B * T * H * 4)                       # beta, g written
-    # chunked forward, fused floor: read q, k, v (bf16), beta, g; write o, final state (fp32)
-    chunk_bytes = (B * T * H * K * 2 + E * H * K * 2 + E * HV * V * 2 + E * HV * 4
-                   + B * T * HV * 4 + B * T * HV * V * 4 + B * HV * K * V * 4)
-    per_tok = (2 * BT * (2 * K + V) + 4 * K * V + 2 * BT * (K + V) + 2 * K * V / M)
-    flops = {
-        "wy": E * HV * 2 * BT * (2 * K + V),
-        "h": E * HV * 4 * K * V,
-        "o": E * HV * (2 * BT * (K + V) + 2 * K * V / M),
-    }
-    flops["chunk"] = E * HV * per_tok
-    return {"E": E, "prepare_bytes": prep_bytes, "chunk_bytes": chunk_bytes, "flops": flops}
+    prep_bytes = (Tt * D * 2 + Tt * (M * H + H) * 2                # x, ba read
+                  + Tt * H * K * 2 + E * H * K * 2 + E * H * V * 2  # q, k, v written
+                  + E * H * 4 + Tt * H * 4)                         # beta, g written
+    # whole chunked forward, fused floor: q, k, v, beta, g in; o, final state out
+    chunk_bytes = (Tt * H * K * 2 + E * H * K * 2 + E * HV * V * 2 + E * HV * 4
+                   + Tt * HV * 4 + Tt * HV * V * 4 + B * HV * K * V * 4)
+    f_wy = E * HV * 2 * BT * (2 * K + V)
+    f_h = E * HV * 4 * K * V
+    f_o = E * HV * (2 * BT * (K + V) + 2 * K * V / M)
+    b_wy = (E * H * K * 2 + E * HV * V * 2 + E * HV * 4 + Tt * HV * 4
+            + E * HV * K * 4 + E * HV * V * 4 + E * HV * 16)
+    b_scan_in = E * HV * K * 4 + E * HV * V * 4 + E * H * K * 2 + E * HV * 16
+    b_state = B * HV * K * V * 4
+    NTc = -(-T // BT) * B
+    b_h = b_scan_in + b_state + E * HV * V * 4 + NTc * HV * K * V * 4   # + v_new, h out
+    b_o = Tt * H * K * 2 + E * H * K * 2 + E * HV * V * 4 + NTc * HV * K * V * 4 + Tt * HV * V * 4
+    b_ho = b_scan_in + b_state + Tt * H * K * 2 + Tt * HV * V * 4
+    return {"E": E, "prepare_bytes": prep_bytes, "chunk_bytes": chunk_bytes,
+            "flops": {"wy": f_wy, "h": f_h, "o": f_o, "scan_out": f_h + f_o,
+                      "chunk": f_wy + f_h + f_o},
+            "bytes": {"wy": b_wy, "h": b_h, "o": b_o, "scan_out": b_ho}}
+
+
+def roof_entry(ms, flops, nbytes, tc, hbm):
+    """Achieved rates of one kernel and its binding roofline (the larger of the
+    tensor-core time and the HBM time at the measured peaks)."""
+    sec = ms * 1e-3
+    tf = flops / sec / 1e12
+    gbs = nbytes / sec / 1e9
+    bound = "tensor" if flops / (tc * 1e12) >= nbytes / (hbm * 1e9) else "hbm"
+    return {"ms": ms, "TFLOPs": tf, "tc_frac": tf / tc, "GBps": gbs, "hbm_frac": gbs / hbm,
+            "bound": bound, "frac": tf / tc if bound == "tensor" else gbs / hbm}
 
 
 # ----------------------------------------------------------------------------------
@@ -168,7 +202,8 @@ class Prefill:
         self.fs = torch.empty(B, H, K, V, dtype=torch.float32, device=dev)
         need = gdp.gdp_chunk_fwd_workspace_size(B, T, B, H, H, K, V, M, w["BT"], bf)
         self.ws = torch.empty(need, dtype=torch.uint8, device=dev)
-        self.path = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, H, K, V, M, w["BT"], bf)[5]
+        off = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, H, K, V, M, w["BT"], bf)
+        self.path, self.fused = off[5], off[7] == 1
 
     def step(self, ev_prep=None):
         w = WORKLOAD
@@ -183,9 +218,14 @@ class Prefill:
                                use_qk_l2norm=True, workspace=self.ws, out=(self.o, self.fs))
 
 
-def launches_per_step(path: int) -> int:
-    # prepare + tables + chunk kernels (generic: wy, h, o; tensor-core path: see the design doc)
-    return 1 + 1 + (3 if path == 0 else 3)
+def launches_per_step(fused: bool) -> int:
+    # prepare, chunk tables, WY, then the scan with the output fused into it
+    # (one launch) or the scan and the output kernel (two)
+    return 1 + 1 + 1 + (1 if fused else 2)
+
+
+def kernel_names(pf) -> tuple:
+    return ("wy", "scan_out") if pf.fused else ("wy", "h", "o")
 
 
 def run_ours(args, rank, world, dev):
@@ -215,6 +255,7 @@ def run_ours(args, rank, world, dev):
     torch.cuda.synchronize()
     for _ in range(args.steps):
         flush.fill_(1.0)
+        torch.cuda._sleep(HOST_LEAD_CYCLES)  # the host queues the whole step meanwhile
         step_ev[0].record()
         pf.step(prep_ev)
         step_ev[1].record()
@@ -236,11 +277,7 @@ def run_ours(args, rank, world, dev):
     sampler.stop()
     gdp.gdp_set_stage_events(None)
 
-    ms = statistics.mean(times["step"])
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times["step"]), world, dev)
     units = alg["E"] * world
     value = units / (ms * 1e-3)
 
@@ -249,28 +286,28 @@ def run_ours(args, rank, world, dev):
     hbm = pk["hbm_gbs"]
     tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     prep_ms = statistics.mean(times["prepare"])
-    kern["prepare"] = {"ms": prep_ms, "bound": "hbm",
-                       "GBps": alg["prepare_bytes"] / (prep_ms * 1e-3) / 1e9}
-    kern["prepare"]["frac"] = kern["prepare"]["GBps"] / hbm
-    for name in ("wy", "h", "o"):
-        kms = statistics.mean(times[name])
-        tf = alg["flops"][name] / (kms * 1e-3) / 1e12
-        kern[name] = {"ms": kms, "bound": "tensor", "TFLOPs": tf, "frac": tf / tc}
+    kern["prepare"] = roof_entry(prep_ms, 0, alg["prepare_bytes"], tc, hbm)
+    stage_ms = {"wy": statistics.mean(times["wy"]), "h": statistics.mean(times["h"]),
+                "o": statistics.mean(times["o"])}
+    if pf.fused:  # stage events 3 and 4 are recorded back to back
+        stage_ms = {"wy": stage_ms["wy"], "scan_out": stage_ms["h"] + stage_ms["o"]}
+    for name in kernel_names(pf):
+        kern[name] = roof_entry(stage_ms[name], alg["flops"][name], alg["bytes"][name], tc, hbm)
     kern["tables"] = {"ms": statistics.mean(times["tables"])}
-    chunk_ms = sum(kern[n]["ms"] for n in ("tables", "wy", "h", "o"))
+    chunk_ms = kern["tables"]["ms"] + sum(kern[n]["ms"] for n in kernel_names(pf))
     chunk_tf = alg["flops"]["chunk"] / (chunk_ms * 1e-3) / 1e12
     chunk_gbs = alg["chunk_bytes"] / (chunk_ms * 1e-3) / 1e9
-    dominant = max(("prepare", "wy", "h", "o"), key=lambda n: kern[n]["ms"])
+    dominant = max(("prepare",) + kernel_names(pf), key=lambda n: kern[n]["ms"])
     dk = kern[dominant]
     if dk["bound"] == "hbm":
         roof = {"kernel": dominant, "bound": "hbm", "achieved": dk["GBps"], "peak": hbm,
-                "unit": "GB/s", "frac": dk["frac"],
-                "traffic": None, "peak_source": pk_src}
+                "unit": "GB/s", "frac": dk["hbm_frac"], "traffic": None,
+                "peak_source": pk_src + " (hbm_gbs)"}
     else:
         roof = {"kernel": dominant, "bound": "tensor", "achieved": dk["TFLOPs"], "peak": tc,
-                "unit": "TFLOP/s", "frac": dk["frac"], "traffic": None,
-                "peak_source": pk_src + " (sustained bf16)"}
-    roof["traffic"] = args.traffic
+                "unit": "TFLOP/s", "frac": dk["tc_frac"], "traffic": None,
+                "peak_source": pk_src + " (bf16_tflops_sustained)"}
+    roof["traffic"] = TRAFFIC.get(dominant) if args.traffic is None else args.traffic
 
     full = args.only == "all"
     e2e = run_e2e(args, gdp, d, dev, pf) if full else None
@@ -288,7 +325,8 @@ def run_ours(args, rank, world, dev):
                    "K": w["K"], "V": w["V"], "M": w["M"], "chunk_size": w["BT"],
                    "parallelism": f"replicas x{world} (no collective)",
                    "l2": "flushed before every timed step (256 MiB write)",
-                   "chunk_path": "tensor-core" if pf.path == 1 else "generic"},
+                   "chunk_path": ("tensor-core" if pf.path == 1 else "generic")
+                   + (", scan and output fused" if pf.fused else "")},
         "roofline": roof,
         "chunk": {"ms": chunk_ms, "TFLOPs": chunk_tf, "tc_frac": chunk_tf / tc,
                   "GBps_fused_floor": chunk_gbs, "hbm_frac": chunk_gbs / hbm},
@@ -297,12 +335,13 @@ def run_ours(args, rank, world, dev):
         "kernels": kern,
         "decode": decode,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(pf.path) * args.steps,
+        "gpu_launches": launches_per_step(pf.fused) * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tc, "source": pk_src},
     }
     if rank == 0 and full and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(d, max_seconds=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(d, min_seconds=args.cpu_seconds,
+                                            max_seconds=max(30.0, args.cpu_seconds))
     return line
 
 
@@ -362,6 +401,7 @@ def run_decode(args, gdp, dev, pk):
     tp, tr = [], []
     for _ in range(max(5, min(args.steps, 50))):
         flush.fill_(1.0)
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         ev[0].record()
         gdp.gdp_decode_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=outs)
         ev[1].record()
@@ -390,62 +430,79 @@ def run_decode(args, gdp, dev, pk):
 # CPU oracle (baseline / reference arm)
 # ----------------------------------------------------------------------------------
 
-def _oracle_sample(d, heads, t_len):
-    """Oracle prepare + fp64 walk over batch row 0, `heads` value heads, first t_len tokens."""
+def _oracle_sample(d, rows, heads, t_len):
+    """Oracle prepare + fp64 walk over batch rows [0, rows), value heads [0, heads) and
+    the first t_len tokens of the prefill workload; returns expanded token-heads done."""
     import oracle
     w = WORKLOAD
-    x = d["x"][:1, :t_len]
-    ba = d["ba"][:1, :t_len]
+    x = d["x"][:rows, :t_len]
+    ba = d["ba"][:rows, :t_len]
     q, k, v, beta, g = oracle.prepare(x, ba, d["A_log"], d["dt_bias"], w["M"], w["H"], w["G"],
                                       w["V"], w["K"], decode=False)
     hs = slice(0, heads)
     oracle.walk(q[:, :, hs], k[:, :, hs], v[:, :, hs], beta[:, :, hs], g[:, :, hs], w["M"],
                 w["K"] ** -0.5, l2norm=True)
-    return t_len * w["M"] * heads  # expanded token-heads
+    return rows * t_len * w["M"] * heads
 
 
-def cpu_baseline(d, max_seconds=20.0):
+def _oracle_rate(d):
+    """Calibration: expanded token-heads per second of the oracle on a small sample."""
+    w = WORKLOAD
+    t0 = time.perf_counter()
+    done = _oracle_sample(d, 1, w["HV"], 128)
+    return done / max(time.perf_counter() - t0, 1e-9)
+
+
+def cpu_baseline(d, min_seconds=10.0, max_seconds=30.0):
+    """The oracle as it stands on the host cores: the whole prefill workload (both batch
+    rows, all heads, all tokens), repeated until about min_seconds of CPU work; if one
+    pass would exceed max_seconds, a prefix of the tokens instead."""
     import oracle
     oracle.build()
     w = WORKLOAD
-    heads, t_len = w["HV"], w["T"]
-    t0 = time.perf_counter()
-    done = _oracle_sample(d, 2, 256)  # calibration
+    full = w["B"] * w["T"] * w["M"] * w["HV"]
+    est = full / _oracle_rate(d)
+    if est <= max_seconds:
+        rows, t_len = w["B"], w["T"]
+        reps = max(1, min(math.ceil(min_seconds / max(est, 1e-9)), int(max_seconds / max(est, 1e-9))))
+    else:
+        rows, reps = 1, 1
+        t_len = max(64, int(w["T"] * (0.5 * max_seconds) / (est / w["B"])))
+    done, t0 = 0, time.perf_counter()
+    for _ in range(reps):
+        done += _oracle_sample(d, rows, w["HV"], t_len)
     dt = time.perf_counter() - t0
-    rate = done / max(dt, 1e-9)
-    target = rate * max_seconds * 0.5
-    t_len = int(min(w["T"], max(64, target / (w["M"] * heads))))
-    t0 = time.perf_counter()
-    done = _oracle_sample(d, heads, t_len)
-    dt = time.perf_counter() - t0
-    per_head_tokens_per_s = done / dt  # expanded token-heads per second
-    value = per_head_tokens_per_s / w["HV"]  # expanded tokens (all heads) per second
+    value = done / w["HV"] / dt  # expanded tokens (all heads) per second
     return {"value": value, "unit": "expanded tokens/s (B*T*M)", "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": f"batch row 0, {heads} heads, first {t_len} tokens (x{w['M']} copies): "
-                      f"oracle prepare + fp64 walk, {dt:.1f} s"}
+            "sample": f"{reps} x (batch rows 0..{rows - 1}, all {w['HV']} heads, first {t_len} "
+                      f"tokens x {w['M']} copies): oracle prepare + fp64 walk, {dt:.1f} s"}
 
 
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, budget_seconds=150.0):
+    """Reference arm: the CPU oracle, rank 0 only. Each step is batch row 0, all heads,
+    a token prefix sized so that warm-up + timed steps take about budget_seconds."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
     d = make_inputs(torch.device("cpu"))
     w = WORKLOAD
-    heads, t_len = w["HV"], 256
+    heads = w["HV"]
+    rate = _oracle_rate(d)
+    per_step = budget_seconds / max(1, args.steps + args.warmup)
+    t_len = int(min(w["T"], max(64, rate * per_step / (w["M"] * heads))))
     for _ in range(args.warmup):
-        _oracle_sample(d, heads, t_len)
+        _oracle_sample(d, 1, heads, t_len)
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_sample(d, heads, t_len)
+        _oracle_sample(d, 1, heads, t_len)
         ts.append(time.perf_counter() - t0)
     per_step = statistics.mean(ts)
-    # each step is a bounded sample: scale its throughput to whole-workload tokens/s
-    value = (t_len * w["M"] * heads / w["HV"]) / per_step
-    sample = (f"per step: batch row 0, {heads} of {w['HV']} heads, first {t_len} tokens: "
-              f"oracle prepare + fp64 walk")
+    value = (t_len * w["M"]) / per_step  # expanded tokens (all heads) per second
+    sample = (f"per step: batch row 0, all {heads} heads, first {t_len} of {w['T']} tokens "
+              f"x {w['M']} copies: oracle prepare + fp64 walk")
     cores = oracle.max_threads()
     return {"metric": METRIC, "value": value, "unit": "expanded tokens/s (B*T*M)",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -459,13 +516,23 @@ def run_reference(args, rank, world):
                     "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """Slowest rank's step time (every rank calls this; world 1 returns ms)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")

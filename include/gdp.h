@@ -188,7 +188,9 @@ gdp_status gdp_read_status(const void* workspace, cudaStream_t stream);
  *   [5] path   not an offset: 0 = generic fp32 path, 1 = tensor-core path
  *   [6] wy_len not an offset: positions per WY block (the A/w/u stages); the
  *              tensor-core path uses 128-position blocks (two chunks) for even M
- *   [7]        reserved (SIZE_MAX)
+ *   [7] fused  not an offset: 1 when the chunk output is computed inside the
+ *              state-scan kernel (the tensor-core path for M = 2: no separate
+ *              output launch, v_new and h are not stored), else 0
  * Returns GDP_ERR_INVALID_ARG on invalid sizes.
  */
 gdp_status gdp_chunk_fwd_stage_offsets(int B, int T, int N_seq, int H, int HV, int K, int V,

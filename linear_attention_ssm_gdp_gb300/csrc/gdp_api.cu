@@ -149,7 +149,7 @@ gdp_status gdp_chunk_fwd_stage_offsets(int B, int T, int N_seq, int H, int HV, i
   out[4] = L.h;
   out[5] = (size_t)L.path;
   out[6] = (size_t)((L.path == 1 && M % 2 == 0) ? 128 : chunk_size);
-  out[7] = SIZE_MAX;
+  out[7] = (L.path == 1 && M == 2) ? 1 : 0;
   return GDP_OK;
 }
 
