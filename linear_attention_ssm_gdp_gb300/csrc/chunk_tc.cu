@@ -1167,10 +1167,15 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
 //    as hi/lo operand tiles (thread = position e, 32 tokens), then
 //    O = P v_new (3 passes) and o_t = scale (e^Gam_t |q_t|^-1 Qh_t + O_t),
 //    Gam_t being the cumulative log decay at the token's last copy.
-// The output of block j runs beside the chain's block j + 1; the groups meet
-// only at mbarriers: the output needs the h tile (H) and v_new (VN), the chain
-// re-fills k and re-writes h after S and Qh are done (SQ) and re-writes v_new
-// after O is done (O). Each group syncs internally with its own named barrier.
+// The chain's MMA thread issues Qh and S right behind its own product 2, so
+// the k and q tiles are released early and the state tile can be re-written
+// at the next block; the output group (P, O, epilogue) then runs beside the
+// chain's next block. S and Qh go to one of two TMEM column sets by block
+// parity, so the chain can run a block ahead of the output. The groups meet
+// only at mbarriers (QH[b]: Qh done, the h tile may be re-written; S[b]: S
+// done, k and q may be re-loaded; VN: v_new written; O: O done, v_new may be
+// re-written; E[b]: the output of a block is finished, its column set may be
+// re-used). Each group syncs internally with its own named barrier.
 struct HOArgs {
   HArgs h;
   int H, l2norm;
@@ -1184,9 +1189,10 @@ constexpr int F_VP = F_HT + 16384;          // v' operand hi | lo
 constexpr int F_Q = F_VP + 16384;           // q: 2 K-halves x 64 rows x 128 B
 constexpr int F_VN = F_Q + 16384;           // v_new operand hi | lo: 128 rows x 64 B each
 constexpr int F_P = F_VN + 16384;           // P^T operand hi | lo: 128 rows (e) x 128 B (64 t)
-constexpr int F_SM = F_P + 32768;           // 1/|q_t|, barriers, TMEM address
-constexpr int F_SMEM = F_SM + 256 + 16 * 8 + 16 + 1024;
-enum { FB_W, FB_UG, FB_K, FB_Q, FB_OG0, FB_OG1, FB_P1, FB_P2, FB_SQ, FB_O, FB_H, FB_VN, FB_N };
+constexpr int F_SM = F_P + 32768;           // token records, barriers, TMEM address
+constexpr int F_SMEM = F_SM + 1024 + 16 * 8 + 16 + 1024;
+enum { FB_W, FB_UG, FB_K, FB_Q, FB_OG0, FB_OG1, FB_P1, FB_P2, FB_QH0, FB_QH1, FB_S0, FB_S1,
+       FB_O, FB_E0, FB_E1, FB_VN, FB_N };
 
 // AND of pred over the count threads of named barrier id (warp-uniform use)
 __device__ __forceinline__ bool group_and(uint32_t id, uint32_t count, bool pred) {
@@ -1222,17 +1228,17 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   uint8_t* vp = sm + F_VP;
   uint8_t* vnt = sm + F_VN;
   uint8_t* pt = sm + F_P;
-  float* srq = reinterpret_cast<float*>(sm + F_SM);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 256);
+  float4* stok = reinterpret_cast<float4*>(sm + F_SM);  // per token: Gam hi, Gam lo, 1/|q|
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 1024);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   const int64_t Rseq = (int64_t)si.x * 2;
   const int64_t gk_base = (int64_t)hv * f.h.Te + Rseq;
-  // TMEM columns: D1 [0,32) D2 [32,64) S^T [64,128) Qh [128,160) O [160,192)
-  constexpr uint32_t TS = 64, TQH = 128, TO = 160;
+  // TMEM columns: D1 [0,32) D2 [32,64) O [64,96) S^T[b] [128 + 64b, +64) Qh[b] [256 + 32b, +32)
+  constexpr uint32_t TD1 = 0, TD2 = 32, TO = 64, TS = 128, TQH = 256;
 
   if (warp == 0) {
-    tmem_alloc(s_tmem, 256);
+    tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -1265,22 +1271,19 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       tma_load_3d(sm + S8_U, &map_u, v0, hv, (int)R, &bars[FB_UG]);
       tma_load_2d(sm + S8_G, &map_gk, 0, (int)G, &bars[FB_UG]);
     };
-    auto load_k = [&](int64_t R) {
-      mbar_expect_tx(&bars[FB_K], 32768);
-      tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[FB_K]);
-      tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[FB_K]);
-    };
     if (tid == 0 && nb > 0) {
       load_w(Rseq);
       load_ug(Rseq, gk_base);
-      load_k(Rseq);
     }
     const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
     const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+    const uint32_t ids = idesc_bf16(128, 64, false, false);
+    const uint32_t idq = idesc_bf16(128, kHBV, false, true);
     bool ok = true;
     for (int j = 0; j <= nb; ++j) {
       // the h tile is re-written once Qh of the previous block has read it
-      if (j > 0) ok = mbar_wait(&bars[FB_SQ], (j - 1) & 1, status, kDevTimeout) && ok;
+      if (j > 0)
+        ok = mbar_wait(&bars[FB_QH0 + ((j - 1) & 1)], ((j - 1) >> 1) & 1, status, kDevTimeout) && ok;
       {
         __align__(16) bf16 hi[NC];
         __align__(16) bf16 lo[NC];
@@ -1303,7 +1306,6 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const int64_t R = Rseq + (int64_t)j * 128;
       const uint32_t ph = j & 1;
       if (tid == 0) {
-        mbar_arrive(&bars[FB_H]);
         ok = mbar_wait(&bars[FB_W], ph, status, kDevTimeout);
         if (ok) {  // product 1: D1 = w h
           const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO);
@@ -1316,7 +1318,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
-              mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
+              mma_bf16(tmem + TD1, ad, bd, id1, (pass | kk) != 0);
             }
           }
           mma_commit(&bars[FB_P1]);
@@ -1333,7 +1335,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         tc_fence_after();
         if (tid == 0 && ok && j + 1 < nb) load_w(R + 128);
         uint32_t r[NC];
-        GDP_TMEM_LD16(tmem + lane_base + cb, r);
+        GDP_TMEM_LD16(tmem + lane_base + TD1 + cb, r);
         tmem_wait_ld();
         const uint8_t* urow = sm + S8_U + p * 128;
         __align__(16) bf16 vh[NC];
@@ -1381,20 +1383,41 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
               const uint64_t bd = sdesc_sw64(vb + pass * 8192 + kk * 1024, 8192, 512);
-              mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
+              mma_bf16(tmem + TD2, ad, bd, id2, (pass | kk) != 0);
             }
           mma_commit(&bars[FB_P2]);
+        }
+        // column set cs is re-used once the output has finished block j - 2
+        const int cs = j & 1;
+        if (j > 1) ok = mbar_wait(&bars[FB_E0 + cs], ((j - 2) >> 1) & 1, status, kDevTimeout) && ok;
+        ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
+        if (ok) {
+          const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
+          // Qh = q h: rows = tokens (64.. unused), h hi then lo
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw64(hb + pass * 8192 + kk * 1024, 8192, 512);
+              mma_bf16(tmem + TQH + 32 * cs, ad, bd, idq, (pass | kk) != 0);
+            }
+          mma_commit(&bars[FB_QH0 + cs]);
+          // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TS + 64 * cs, ad, bd, ids, kk > 0);
+          }
+          mma_commit(&bars[FB_S0 + cs]);
         }
       }
       ok = mbar_wait(&bars[FB_P2], ph, status, kDevTimeout) && ok;
       tc_fence_after();
-      if (tid == 0 && ok && j + 1 < nb) {  // k is free once product 2 and S are done
-        ok = mbar_wait(&bars[FB_SQ], ph, status, kDevTimeout);
-        if (ok) load_k(R + 128);
-      }
       {
         uint32_t r[NC];
-        GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
+        GDP_TMEM_LD16(tmem + lane_base + TD2 + cb, r);
         tmem_wait_ld();
         const float dl = expf(glast.x + glast.y);
 #pragma unroll
@@ -1415,17 +1438,21 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       tma_load_3d(sm + F_Q, &map_q, 0, kh, (int)T0, &bars[FB_Q]);
       tma_load_3d(sm + F_Q + 8192, &map_q, 64, kh, (int)T0, &bars[FB_Q]);
     };
+    auto load_k = [&](int64_t R) {
+      mbar_expect_tx(&bars[FB_K], 32768);
+      tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[FB_K]);
+      tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[FB_K]);
+    };
     auto load_og = [&](int b, int64_t G) {
       mbar_expect_tx(&bars[FB_OG0 + b], 2048);
       tma_load_2d(sm + F_OG + b * 2048, &map_gk, 0, (int)G, &bars[FB_OG0 + b]);
     };
     if (otid == 0 && nb > 0) {
+      load_k(Rseq);
       load_q(si.x);
       load_og(0, gk_base);
       if (nb > 1) load_og(1, gk_base + 128);
     }
-    const uint32_t ids = idesc_bf16(128, 64, false, false);
-    const uint32_t idq = idesc_bf16(128, kHBV, false, true);
     const uint32_t ido = idesc_bf16(128, kHBV, true, true);
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -1436,44 +1463,27 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const float4* og = reinterpret_cast<const float4*>(sm + F_OG + (j & 1) * 2048);
       ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
       ok = mbar_wait(&bars[FB_OG0 + (j & 1)], (j >> 1) & 1, status, kDevTimeout) && ok;
-      if (otid < 64) {  // query norms from the staged tile
+      if (otid < 64) {  // token records: Gam at the last copy, query norm from the staged tile
         const uint8_t* qt = sm + F_Q;
         const float ss = row_sumsq(qt + otid * 128) + row_sumsq(qt + 8192 + otid * 128);
-        srq[otid] = f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-      }
-      if (otid == 0 && ok) {
-        const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
-        ok = mbar_wait(&bars[FB_K], ph, status, kDevTimeout);
-        if (ok) {  // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TS, ad, bd, ids, kk > 0);
-          }
-        }
-        ok = mbar_wait(&bars[FB_H], ph, status, kDevTimeout) && ok;
-        if (ok) {  // Qh = q h: rows = tokens (64.. unused), h hi then lo
-#pragma unroll
-          for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw64(hb + pass * 8192 + kk * 1024, 8192, 512);
-              mma_bf16(tmem + TQH, ad, bd, idq, (pass | kk) != 0);
-            }
-          mma_commit(&bars[FB_SQ]);
-        }
+        const float4 rt = og[2 * otid + 1];
+        stok[otid] = make_float4(rt.x, rt.y, f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f, 0.f);
       }
       ok = group_and(2, 256, ok);
       if (!ok) break;
-      ok = mbar_wait(&bars[FB_SQ], ph, status, kDevTimeout);
+      // S done (so Qh and product 2 too): k and q are free for the next block
+      const int cs = j & 1;
+      ok = mbar_wait(&bars[FB_S0 + cs], (j >> 1) & 1, status, kDevTimeout);
       tc_fence_after();
+      if (otid == 0 && ok && j + 1 < nb) {
+        load_k(Rseq + (int64_t)(j + 1) * 128);
+        load_q(T0 + 64);
+      }
       {  // P^T row e = row, tokens [32 cgrp, 32 cgrp + 32)
         const int e = row, s = e >> 1;
         const float4 re = og[e];
         uint32_t r[32];
-        GDP_TMEM_LD32(tmem + lane_base + TS + 32 * cgrp, r);
+        GDP_TMEM_LD32(tmem + lane_base + TS + 64 * cs + 32 * cgrp, r);
         tmem_wait_ld();
         __align__(16) bf16 ph_[32];
         __align__(16) bf16 pl_[32];
@@ -1482,8 +1492,8 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
           const int t = 32 * cgrp + i;
           float pv = 0.f;
           if (e < n && s <= t && t < nt) {
-            const float4 rt = og[2 * t + 1];
-            pv = __uint_as_float(r[i]) * srq[t] * re.z * expf((rt.x - re.x) + (rt.y - re.y));
+            const float4 tk = stok[t];
+            pv = __uint_as_float(r[i]) * tk.z * re.z * __expf((tk.x - re.x) + (tk.y - re.y));
           }
           split_bf16(pv, ph_[i], pl_[i]);
         }
@@ -1500,7 +1510,6 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       if (!ok) break;
       tc_fence_after();
       if (otid == 0) {
-        if (j + 1 < nb) load_q(T0 + 64);  // q consumed by S, Qh and the norms
         ok = mbar_wait(&bars[FB_VN], ph, status, kDevTimeout);
         if (ok) {  // O = P v_new; A = P^T MN-major, second atom re-read (LBO = 0)
           const uint32_t pb = smem_u32(pt), vv = smem_u32(vnt);
@@ -1524,11 +1533,11 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         tc_fence_after();
         uint32_t ro[16], rq[16];
         GDP_TMEM_LD16(tmem + lane_base + TO + cb, ro);
-        GDP_TMEM_LD16(tmem + lane_base + TQH + cb, rq);
+        GDP_TMEM_LD16(tmem + lane_base + TQH + 32 * cs + cb, rq);
         tmem_wait_ld();
         if (t < nt && ok) {
-          const float4 rt = og[2 * t + 1];
-          const float qs = expf(rt.x + rt.y) * srq[t];
+          const float4 tk = stok[t];
+          const float qs = expf(tk.x + tk.y) * tk.z;
           float4* dst = reinterpret_cast<float4*>(f.o + ((T0 + t) * HVn + hv) * V + v0 + cb);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -1545,10 +1554,13 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       ok = group_and(2, 256, ok);
       if (!ok) break;
       tc_fence_after();
-      if (otid == 0 && j + 2 < nb) load_og(j & 1, gk_base + (int64_t)(j + 2) * 128);
+      if (otid == 0) {
+        mbar_arrive(&bars[FB_E0 + cs]);
+        if (j + 2 < nb) load_og(j & 1, gk_base + (int64_t)(j + 2) * 128);
+      }
     }
   }
-  tmem_release(tmem, 256);
+  tmem_release(tmem, 512);
 }
 
 // ============================================================================ chunk_o
