@@ -1234,8 +1234,13 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   const int64_t Rseq = (int64_t)si.x * 2;
   const int64_t gk_base = (int64_t)hv * f.h.Te + Rseq;
-  // TMEM columns: D1 [0,32) D2 [32,64) O [64,96) S^T[b] [128 + 64b, +64) Qh[b] [256 + 32b, +32)
-  constexpr uint32_t TD1 = 0, TD2 = 32, TO = 64, TS = 128, TQH = 256;
+  // TMEM columns: D1 [0,64) D2 [64,128) O [128,192) S^T[b] [192 + 64b, +64)
+  // Qh[b] [320 + 64b, +64). The hi and lo halves of an operand tile sit 8 KB
+  // apart, the leading-byte offset of a 64-column MN-major operand, so
+  // x_hi [y_hi | y_lo] is one N = 64 MMA per k-step (columns [0,32) take
+  // x_hi y_hi, [32,64) x_hi y_lo) and the lo-hi term accumulates into [0,32):
+  // a product is the sum of its two 32-column halves.
+  constexpr uint32_t TD1 = 0, TD2 = 64, TO = 128, TS = 192, TQH = 320;
 
   if (warp == 0) {
     tmem_alloc(s_tmem, 512);
@@ -1275,10 +1280,10 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       load_w(Rseq);
       load_ug(Rseq, gk_base);
     }
+    const uint32_t id1w = idesc_bf16(128, 2 * kHBV, false, true);
     const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
-    const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+    const uint32_t id2w = idesc_bf16(128, 2 * kHBV, true, true);
     const uint32_t ids = idesc_bf16(128, 64, false, false);
-    const uint32_t idq = idesc_bf16(128, kHBV, false, true);
     bool ok = true;
     for (int j = 0; j <= nb; ++j) {
       // the h tile is re-written once Qh of the previous block has read it
@@ -1311,15 +1316,14 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
           const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO);
           const uint32_t hb = smem_u32(ht);
 #pragma unroll
-          for (int pass = 0; pass < 3; ++pass) {
-            const uint32_t A = pass == 2 ? wlo : whi;
-            const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
+          for (int kk = 0; kk < 8; ++kk) {  // w_hi [h_hi | h_lo]
+            const uint64_t ad = sdesc_sw128(whi + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
+          }
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
-              mma_bf16(tmem + TD1, ad, bd, id1, (pass | kk) != 0);
-            }
+          for (int kk = 0; kk < 8; ++kk) {  // + w_lo h_hi
+            const uint64_t ad = sdesc_sw128(wlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1, true);
           }
           mma_commit(&bars[FB_P1]);
         }
@@ -1334,9 +1338,15 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         ok = mbar_wait(&bars[FB_P1], ph, status, kDevTimeout) && ok;
         tc_fence_after();
         if (tid == 0 && ok && j + 1 < nb) load_w(R + 128);
-        uint32_t r[NC];
-        GDP_TMEM_LD16(tmem + lane_base + TD1 + cb, r);
-        tmem_wait_ld();
+        float d1[NC];
+        {
+          uint32_t r0[NC], r1[NC];
+          GDP_TMEM_LD16(tmem + lane_base + TD1 + cb, r0);
+          GDP_TMEM_LD16(tmem + lane_base + TD1 + 32 + cb, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < NC; ++c) d1[c] = __uint_as_float(r0[c]) + __uint_as_float(r1[c]);
+        }
         const uint8_t* urow = sm + S8_U + p * 128;
         __align__(16) bf16 vh[NC];
         __align__(16) bf16 vl[NC];
@@ -1350,7 +1360,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = 4 * jj + q;
-            const float vn = (p < n) ? us[q] - __uint_as_float(r[c]) : 0.f;
+            const float vn = (p < n) ? us[q] - d1[c] : 0.f;
             split_bf16(vn, vh[c], vl[c]);
             split_bf16(vn * sc, pvh[c], pvl[c]);
           }
@@ -1378,13 +1388,10 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         if (ok) {  // product 2: D2 = k^T v', K = 128 positions
           const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
 #pragma unroll
-          for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
-              const uint64_t bd = sdesc_sw64(vb + pass * 8192 + kk * 1024, 8192, 512);
-              mma_bf16(tmem + TD2, ad, bd, id2, (pass | kk) != 0);
-            }
+          for (int kk = 0; kk < 8; ++kk) {  // k^T [v'_hi | v'_lo]
+            const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
+            mma_bf16(tmem + TD2, ad, sdesc_sw64(vb + kk * 1024, 8192, 512), id2w, kk > 0);
+          }
           mma_commit(&bars[FB_P2]);
         }
         // column set cs is re-used once the output has finished block j - 2
@@ -1393,15 +1400,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
         if (ok) {
           const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
-          // Qh = q h: rows = tokens (64.. unused), h hi then lo
+          // Qh = q [h_hi | h_lo]: rows = tokens (64.. unused)
 #pragma unroll
-          for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw64(hb + pass * 8192 + kk * 1024, 8192, 512);
-              mma_bf16(tmem + TQH + 32 * cs, ad, bd, idq, (pass | kk) != 0);
-            }
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TQH + 64 * cs, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
+          }
           mma_commit(&bars[FB_QH0 + cs]);
           // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
 #pragma unroll
@@ -1416,12 +1420,13 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       ok = mbar_wait(&bars[FB_P2], ph, status, kDevTimeout) && ok;
       tc_fence_after();
       {
-        uint32_t r[NC];
-        GDP_TMEM_LD16(tmem + lane_base + TD2 + cb, r);
+        uint32_t r0[NC], r1[NC];
+        GDP_TMEM_LD16(tmem + lane_base + TD2 + cb, r0);
+        GDP_TMEM_LD16(tmem + lane_base + TD2 + 32 + cb, r1);
         tmem_wait_ld();
         const float dl = expf(glast.x + glast.y);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+        for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + (__uint_as_float(r0[c]) + __uint_as_float(r1[c]));
       }
       tc_fence_before();
     }
@@ -1453,6 +1458,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       load_og(0, gk_base);
       if (nb > 1) load_og(1, gk_base + 128);
     }
+    const uint32_t idow = idesc_bf16(128, 2 * kHBV, true, true);
     const uint32_t ido = idesc_bf16(128, kHBV, true, true);
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -1514,16 +1520,13 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         if (ok) {  // O = P v_new; A = P^T MN-major, second atom re-read (LBO = 0)
           const uint32_t pb = smem_u32(pt), vv = smem_u32(vnt);
 #pragma unroll
-          for (int pass = 0; pass < 3; ++pass) {
-            const uint32_t A = pb + (pass == 2 ? 16384 : 0);
-            const uint32_t Bm = vv + (pass == 1 ? 8192 : 0);
+          for (int kk = 0; kk < 8; ++kk)  // P_hi [vn_hi | vn_lo]
+            mma_bf16(tmem + TO, sdesc_sw128(pb + kk * 2048, 0, 1024),
+                     sdesc_sw64(vv + kk * 1024, 8192, 512), idow, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(A + kk * 2048, 0, 1024);
-              const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
-              mma_bf16(tmem + TO, ad, bd, ido, (pass | kk) != 0);
-            }
-          }
+          for (int kk = 0; kk < 8; ++kk)  // + P_lo vn_hi
+            mma_bf16(tmem + TO, sdesc_sw128(pb + 16384 + kk * 2048, 0, 1024),
+                     sdesc_sw64(vv + kk * 1024, 8192, 512), ido, true);
           mma_commit(&bars[FB_O]);
         }
       }
@@ -1531,9 +1534,11 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         const int t = row;
         ok = mbar_wait(&bars[FB_O], ph, status, kDevTimeout) && ok;
         tc_fence_after();
-        uint32_t ro[16], rq[16];
+        uint32_t ro[16], ro2[16], rq[16], rq2[16];
         GDP_TMEM_LD16(tmem + lane_base + TO + cb, ro);
-        GDP_TMEM_LD16(tmem + lane_base + TQH + 32 * cs + cb, rq);
+        GDP_TMEM_LD16(tmem + lane_base + TO + 32 + cb, ro2);
+        GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + cb, rq);
+        GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + 32 + cb, rq2);
         tmem_wait_ld();
         if (t < nt && ok) {
           const float4 tk = stok[t];
@@ -1545,7 +1550,8 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               x[q] = f.scale *
-                     (qs * __uint_as_float(rq[4 * jj + q]) + __uint_as_float(ro[4 * jj + q]));
+                     (qs * (__uint_as_float(rq[4 * jj + q]) + __uint_as_float(rq2[4 * jj + q])) +
+                      (__uint_as_float(ro[4 * jj + q]) + __uint_as_float(ro2[4 * jj + q])));
             dst[jj] = make_float4(x[0], x[1], x[2], x[3]);
           }
         }
