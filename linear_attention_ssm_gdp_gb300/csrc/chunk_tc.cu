@@ -700,9 +700,10 @@ __device__ void solve_tril128(float* LA, float* scratch) {
 }
 
 template <int V>
-__global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant__ CUtensorMap map_k,
-                                                          const __grid_constant__ CUtensorMap map_v,
-                                                          WyArgs a) {
+__global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
+    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+    const __grid_constant__ CUtensorMap map_whs, const __grid_constant__ CUtensorMap map_wls,
+    const __grid_constant__ CUtensorMap map_us, WyArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -869,23 +870,48 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant_
     mma_commit(&bars[1]);
   };
   if (tid == 0) issue_u(0);
-  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread
+  // Epilogues. A whole block is staged in shared memory that its last reader
+  // has released and written with bulk tensor stores; a sequence's last,
+  // partial block is written row by row, so that no store reaches the rows of
+  // the next sequence.
+  const bool full = n == 128;
+  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread;
+  // staged as two 64-column boxes per array, w_hi in the k buffer, w_lo in LA
   {
     const int p = quarter * 32 + lane;
-    {
-      const int c0 = cq * 32;
-      uint32_t r[32];
-      GDP_TMEM_LD32(tmem + lane_base + c0, r);
-      tmem_wait_ld();
-      if (p < n) {
-        __align__(16) bf16 hi[32];
-        __align__(16) bf16 lo[32];
+    const int c0 = cq * 32;
+    uint32_t r[32];
+    GDP_TMEM_LD32(tmem + lane_base + c0, r);
+    tmem_wait_ld();
+    __align__(16) bf16 hi[32];
+    __align__(16) bf16 lo[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
-        const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
-        store_bf16x32(a.w_hi + row, hi);
-        store_bf16x32(a.w_lo + row, lo);
+    for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
+    if (full) {
+      const uint32_t base = (c0 >> 6) * 16384 + p * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = base + (((((c0 & 63) >> 3) + i) ^ (p & 7)) << 4);
+        *reinterpret_cast<uint4*>(kbuf + off) = reinterpret_cast<const uint4*>(hi)[i];
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(LA) + off) =
+            reinterpret_cast<const uint4*>(lo)[i];
       }
+    } else if (p < n) {
+      const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
+      store_bf16x32(a.w_hi + row, hi);
+      store_bf16x32(a.w_lo + row, lo);
+    }
+  }
+  if (full) {
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tma_store_3d(&map_whs, kbuf + h * 16384, 64 * h, hv, (int)R0);
+        tma_store_3d(&map_wls, reinterpret_cast<uint8_t*>(LA) + h * 16384, 64 * h, hv, (int)R0);
+      }
+      tma_store_commit();
     }
   }
 #pragma unroll 1
@@ -906,6 +932,13 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant_
   ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
   tc_fence_after();
   if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
+  // u staging: 32-column boxes, 0-3 in the operand tiles, 4-5 in the upper
+  // half of LA, 6-7 in the v buffer (all released by the u MMAs)
+  auto ustage = [&](int c) -> uint8_t* {
+    return c < 4 ? tiles + c * 16384
+                 : c < 6 ? reinterpret_cast<uint8_t*>(LA) + 32768 + (c - 4) * 16384
+                         : vbuf + (c - 6) * 16384;
+  };
   {  // u epilogue: row p, V / 4 columns per thread
     const int p = quarter * 32 + lane;
 #pragma unroll 1
@@ -913,7 +946,15 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant_
       uint32_t r[16];
       GDP_TMEM_LD16(tmem + lane_base + 128 + c0, r);
       tmem_wait_ld();
-      if (p < n) {
+      if (full) {
+        uint8_t* st = ustage(c0 >> 5) + p * 128;
+        const int u0 = (c0 & 31) >> 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<float4*>(st + (((u0 + j) ^ (p & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      } else if (p < n) {
         float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -922,6 +963,16 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(const __grid_constant_
       }
     }
     if (tid < n) a.gk[(int64_t)hv * a.Te + R0 + tid] = make_float4(sgh[tid], sgl[tid], srk[tid], 0.f);
+  }
+  if (full) {
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+      for (int c = 0; c < V / 32; ++c) tma_store_3d(&map_us, ustage(c), 32 * c, hv, (int)R0);
+      tma_store_commit();
+      tma_store_wait_all();  // shared memory stays allocated until the stores have read it
+    }
   }
   tmem_release(tmem, kCols);
 }
@@ -1833,13 +1884,18 @@ cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
 template <int V>
 cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   const int64_t Te = (int64_t)p.B * p.T * p.M;
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mwh, mwl, mu;
   if (!map3(&mk, p.k, BF, 2, kK, p.H, Te, 64, 128, true)) return cudaErrorInvalidValue;
   if (!map3(&mv, p.v, BF, 2, V, p.HV, Te, 64, 128, true)) return cudaErrorInvalidValue;
+  if (!map3(&mwh, a.w_hi, BF, 2, kK, p.HV, Te, 64, 128, true) ||
+      !map3(&mwl, a.w_lo, BF, 2, kK, p.HV, Te, 64, 128, true) ||
+      !map3(&mu, a.u, F32, 4, V, p.HV, Te, 32, 128, true))
+    return cudaErrorInvalidValue;
   cudaError_t e =
       cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
-  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, a);
+  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl,
+                                                                                  mu, a);
   return cudaGetLastError();
 }
 
