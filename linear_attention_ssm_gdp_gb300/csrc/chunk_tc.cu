@@ -70,20 +70,23 @@ __device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
-// Sum of squares of one 128-byte row of bf16 (any chunk order).
-__device__ __forceinline__ float row_sumsq(const uint8_t* row) {
-  float s = 0.f;
+// Sum of squares of row p (128 bytes of bf16) of a tile stored with the
+// 128-byte swizzle. The chunks are visited in the order j ^ (p & 7), which is
+// the physical order 0..7, so the lanes of a warp (consecutive rows) read
+// distinct banks; four partial sums keep the additions independent.
+__device__ __forceinline__ float row_sumsq(const uint8_t* row, int p) {
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint4 u = reinterpret_cast<const uint4*>(row)[j];
+    const uint4 u = reinterpret_cast<const uint4*>(row)[j ^ (p & 7)];
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float a = __uint_as_float(w[t] << 16), b = __uint_as_float(w[t] & 0xffff0000u);
-      s += a * a + b * b;
+      s[t] = fmaf(a, a, fmaf(b, b, s[t]));
     }
   }
-  return s;
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 __device__ __forceinline__ void store_bf16x32(bf16* dst, const bf16* src) {
@@ -108,6 +111,7 @@ struct WyArgs {
   const float* g;
   const int4* seq_info;
   const int2* exp_tab;
+  const int2* blk_tab;  // 128-position blocks (wy128 only)
   bf16* w_hi;
   bf16* w_lo;
   float* u;
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ C
     mma_commit(&bars[1]);
   }
   if (tid < kBT) {
-    const float ss = row_sumsq(kbuf + tid * 128) + row_sumsq(kbuf + 8192 + tid * 128);
+    const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 8192 + tid * 128, tid);
     const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     srk[tid] = r;
     sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
@@ -707,8 +711,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int2 tab = a.exp_tab[blockIdx.x];
-  if (tab.x < 0 || (tab.y & 1)) return;  // one CTA per pair of 64-position chunks
+  const int2 tab = a.blk_tab[blockIdx.x];  // (sequence, first of the block's two 64-chunks)
+  if (tab.x < 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
@@ -777,7 +781,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     mma_commit(&bars[1]);
   }
   if (tid < 128) {
-    const float ss = row_sumsq(kbuf + tid * 128) + row_sumsq(kbuf + 16384 + tid * 128);
+    const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 16384 + tid * 128, tid);
     const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     srk[tid] = r;
     sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
@@ -971,7 +975,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
 #pragma unroll
       for (int c = 0; c < V / 32; ++c) tma_store_3d(&map_us, ustage(c), 32 * c, hv, (int)R0);
       tma_store_commit();
-      tma_store_wait_all();  // shared memory stays allocated until the stores have read it
+      tma_store_wait_read();  // shared memory stays allocated until the stores have read it
     }
   }
   tmem_release(tmem, kCols);
@@ -1522,7 +1526,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       ok = mbar_wait(&bars[FB_OG0 + (j & 1)], (j >> 1) & 1, status, kDevTimeout) && ok;
       if (otid < 64) {  // token records: Gam at the last copy, query norm from the staged tile
         const uint8_t* qt = sm + F_Q;
-        const float ss = row_sumsq(qt + otid * 128) + row_sumsq(qt + 8192 + otid * 128);
+        const float ss = row_sumsq(qt + otid * 128, otid) + row_sumsq(qt + 8192 + otid * 128, otid);
         const float4 rt = og[2 * otid + 1];
         stok[otid] = make_float4(rt.x, rt.y, f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f, 0.f);
       }
@@ -1724,11 +1728,11 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   }
   // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
   if (tid < kBT) {
-    const float ss = row_sumsq(qb + tid * 128) + row_sumsq(qb + 8192 + tid * 128);
+    const float ss = row_sumsq(qb + tid * 128, tid) + row_sumsq(qb + 8192 + tid * 128, tid);
     srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
   for (int e = tid; e < NE; e += 512) {
-    const float ss = row_sumsq(kb + e * 128) + row_sumsq(kb + NE * 128 + e * 128);
+    const float ss = row_sumsq(kb + e * 128, e) + row_sumsq(kb + NE * 128 + e * 128, e);
     srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
   }
   // value rows past the chunk's end may hold anything: zero them (their P is 0)
@@ -1894,8 +1898,8 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   cudaError_t e =
       cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
-  wy128_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl,
-                                                                                  mu, a);
+  const int64_t NB = block128_bound(p.B, p.T, p.N_seq, p.M);
+  wy128_tc_kernel<V><<<dim3((unsigned)NB, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a);
   return cudaGetLastError();
 }
 
@@ -1935,6 +1939,7 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.seq_info = take(sizeof(int4) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.exp_tab = take(sizeof(int2) * (size_t)NE);
   L.tok_tab = take(sizeof(int2) * (size_t)NT);
+  if (M % 2 == 0) L.blk_tab = take(sizeof(int2) * (size_t)block128_bound(B, T, N_seq, M));
   L.w_hi = take(2 * Te * HV * K);
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
@@ -1967,7 +1972,9 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
   // WY stage
   if (p.NE_max > 0 && Te > 0) {
     WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
-             reinterpret_cast<const int2*>(ws + L.exp_tab), w_hi, w_lo, u, gk, status};
+             reinterpret_cast<const int2*>(ws + L.exp_tab),
+             L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<const int2*>(ws + L.blk_tab),
+             w_hi, w_lo, u, gk, status};
     const bool blk128 = (p.M % 2) == 0;
     switch (p.V) {
       case 64: e = blk128 ? run_wy128<64>(p, a) : run_wy<64>(p, a); break;

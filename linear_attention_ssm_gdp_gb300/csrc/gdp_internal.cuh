@@ -46,6 +46,8 @@ struct ChunkProblem {
 // Byte offsets inside a chunk_fwd workspace.
 struct WsLayout {
   size_t status = 0, seq_info = 0, exp_tab = 0, tok_tab = 0;
+  // tensor-core path, even M: list of 128-position blocks (sequence, first 64-chunk)
+  size_t blk_tab = SIZE_MAX;
   size_t A = SIZE_MAX, w = SIZE_MAX, u = SIZE_MAX, gexp = SIZE_MAX, v_new = SIZE_MAX,
          h = SIZE_MAX;
   // tensor-core path buffers: w and v_new as bf16 hi/lo pairs, per-position
@@ -55,6 +57,11 @@ struct WsLayout {
   size_t total = 0;
   int path = 0;  // 0 generic, 1 tensor core
 };
+
+// Upper bound on 128-position blocks over all sequences.
+inline int64_t block128_bound(int B, int T, int N_seq, int M) {
+  return ((int64_t)B * T * M + 127) / 128 + N_seq;
+}
 
 // Sizes derived from (B, T, N_seq, M, BT): upper bounds on chunk counts.
 inline void chunk_bounds(int B, int T, int N_seq, int M, int BT, int64_t* NE, int64_t* NT) {
