@@ -70,6 +70,18 @@ __device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// split_bf16 of n (even) values, two per conversion instruction (same rounding).
+template <int n>
+__device__ __forceinline__ void split_bf16_n(const float* x, bf16* hi, bf16* lo) {
+#pragma unroll
+  for (int i = 0; i < n; i += 2) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x[i], x[i + 1]);
+    const float2 hf = __bfloat1622float2(h);
+    *reinterpret_cast<__nv_bfloat162*>(hi + i) = h;
+    *reinterpret_cast<__nv_bfloat162*>(lo + i) = __floats2bfloat162_rn(x[i] - hf.x, x[i + 1] - hf.y);
+  }
+}
+
 // Sum of squares of row p (128 bytes of bf16) of a tile stored with the
 // 128-byte swizzle. The chunks are visited in the order j ^ (p & 7), which is
 // the physical order 0..7, so the lanes of a warp (consecutive rows) read
@@ -328,9 +340,10 @@ __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ C
     tmem_wait_ld();
     const float bp = sb[p] * srk[p];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
       const int i = c0 + j;
-      Ls[p * 65 + i] = (i < p) ? bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
+      const float x = bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]);
+      Ls[p * 65 + i] = (i < p) ? x : 0.f;
     }
   }
   __syncthreads();
@@ -801,40 +814,50 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       uint32_t r[32];
       GDP_TMEM_LD32(tmem + lane_base + c0, r);
       tmem_wait_ld();
+      const float gph = sgh[p], gpl = sgl[p];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
         const int i = c0 + j;
-        LA[p * 129 + i] =
-            (i < p) ? bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]) : 0.f;
+        const float x = bp * __expf((gph - sgh[i]) + (gpl - sgl[i])) * srk[i] * __uint_as_float(r[j]);
+        LA[p * 129 + i] = (i < p) ? x : 0.f;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   solve_tril128(LA, scratch);
-  // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u)
-  // (A is lower triangular: the first build writes the zero upper triangle, the
-  // second leaves it in place since the w MMAs only read the tiles)
+  // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
+  // Thread (quarter, cq) builds row p = 32 quarter + lane, columns [32 cq, 32 cq + 32):
+  // LA rows (stride 129) are read without bank conflicts, the column scales
+  // are broadcasts, and each 8-column group is one 16-byte swizzled store per
+  // half. A is lower triangular: the first build writes the zero chunks above
+  // the diagonal, the second leaves them in place (the w MMAs only read them).
   auto build_tiles = [&](int which) {
     const float* sc = which == 0 ? sco : sb;
-    for (int idx = tid; idx < 128 * 64; idx += 512) {
-      const int prow = idx >> 6, i = (idx & 63) * 2;  // pairs of adjacent columns
-      if (i > prow && which == 1) continue;
-      const uint32_t off = (i >> 6) * 16384 + sw128_offset(prow, (i & 63) * 2);
-      __nv_bfloat162 hh, ll;
-      if (i > prow) {
-        hh = __floats2bfloat162_rn(0.f, 0.f);
-        ll = hh;
-      } else {
-        const float a0 = LA[prow * 129 + i] * sc[i], a1 = LA[prow * 129 + i + 1] * sc[i + 1];
-        bf16 h0, l0, h1, l1;
-        split_bf16(a0, h0, l0);
-        split_bf16(a1, h1, l1);
-        hh.x = h0; hh.y = h1;
-        ll.x = l0; ll.y = l1;
+    const int p = quarter * 32 + lane, c0 = cq * 32;
+    uint8_t* trow = tiles + (c0 >> 6) * 16384 + p * 128;
+    const int ch0 = (c0 & 63) >> 3;
+    if (cq <= quarter) {  // warp-uniform: the chunk holds entries on or below the diagonal
+      const float* lrow = LA + p * 129 + c0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __align__(16) bf16 hi[8];
+        __align__(16) bf16 lo[8];
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = lrow[8 * q + e] * sc[c0 + 8 * q + e];
+        split_bf16_n<8>(x, hi, lo);
+        const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
+        *reinterpret_cast<uint4*>(trow + off) = *reinterpret_cast<const uint4*>(hi);
+        *reinterpret_cast<uint4*>(trow + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
       }
-      *reinterpret_cast<__nv_bfloat162*>(tiles + off) = hh;
-      *reinterpret_cast<__nv_bfloat162*>(tiles + 32768 + off) = ll;
+    } else if (which == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
+        *reinterpret_cast<uint4*>(trow + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(trow + 32768 + off) = make_uint4(0, 0, 0, 0);
+      }
     }
     fence_async_smem();
     tc_fence_before();
@@ -889,8 +912,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     tmem_wait_ld();
     __align__(16) bf16 hi[32];
     __align__(16) bf16 lo[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
+    split_bf16_n<32>(reinterpret_cast<const float*>(r), hi, lo);
     if (full) {
       const uint32_t base = (c0 >> 6) * 16384 + p * 128;
 #pragma unroll
@@ -1347,8 +1369,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       {
         __align__(16) bf16 hi[NC];
         __align__(16) bf16 lo[NC];
-#pragma unroll
-        for (int c = 0; c < NC; ++c) split_bf16(h[c], hi[c], lo[c]);
+        split_bf16_n<NC>(h, hi, lo);
         const uint4* h4 = reinterpret_cast<const uint4*>(hi);
         const uint4* l4 = reinterpret_cast<const uint4*>(lo);
         *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
@@ -1407,6 +1428,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         __align__(16) bf16 vl[NC];
         __align__(16) bf16 pvh[NC];
         __align__(16) bf16 pvl[NC];
+        float vn[NC], pv[NC];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const float4 u4 =
@@ -1415,11 +1437,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = 4 * jj + q;
-            const float vn = (p < n) ? us[q] - d1[c] : 0.f;
-            split_bf16(vn, vh[c], vl[c]);
-            split_bf16(vn * sc, pvh[c], pvl[c]);
+            vn[c] = (p < n) ? us[q] - d1[c] : 0.f;
+            pv[c] = vn[c] * sc;
           }
         }
+        split_bf16_n<NC>(vn, vh, vl);
+        split_bf16_n<NC>(pv, pvh, pvl);
         *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(pvh)[0];
         *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(pvh)[1];
         *reinterpret_cast<uint4*>(vp + 8192 + off_r0) = reinterpret_cast<const uint4*>(pvl)[0];
@@ -1549,15 +1572,13 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         __align__(16) bf16 ph_[32];
         __align__(16) bf16 pl_[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 32; ++i) {  // branch-free, so that the iterations interleave
           const int t = 32 * cgrp + i;
-          float pv = 0.f;
-          if (e < n && s <= t && t < nt) {
-            const float4 tk = stok[t];
-            pv = __uint_as_float(r[i]) * tk.z * re.z * __expf((tk.x - re.x) + (tk.y - re.y));
-          }
-          split_bf16(pv, ph_[i], pl_[i]);
+          const float4 tk = stok[t];
+          const float x = __uint_as_float(r[i]) * tk.z * re.z * __expf((tk.x - re.x) + (tk.y - re.y));
+          r[i] = __float_as_uint((e < n && s <= t && t < nt) ? x : 0.f);
         }
+        split_bf16_n<32>(reinterpret_cast<const float*>(r), ph_, pl_);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t off = e * 128 + ((((uint32_t)(4 * cgrp + q)) ^ (e & 7)) << 4);
@@ -1754,13 +1775,11 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
       GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < 16; ++j) {  // branch-free, so that the iterations interleave
         const int e = c0 + j, s = e / M;
-        float pv = 0.f;
-        if (e < ne && s <= t && t < nt)
-          pv = __uint_as_float(r[j]) * rt * srk[e] * __expf(gam_diff4(sgh, sgl, t, s));
+        const float x = __uint_as_float(r[j]) * rt * srk[e] * __expf(gam_diff4(sgh, sgl, t, s));
         bf16 ph, pl;
-        split_bf16(pv, ph, pl);
+        split_bf16((e < ne && s <= t && t < nt) ? x : 0.f, ph, pl);
         // MN-major operand: row e (K), column t (M); a warp writes 64 contiguous bytes of a row
         const uint32_t off = sw128_offset(e, t * 2);
         *reinterpret_cast<bf16*>(pb + off) = ph;
