@@ -1266,8 +1266,8 @@ constexpr int F_VP = F_HT + 16384;          // v' operand hi | lo
 constexpr int F_Q = F_VP + 16384;           // q: 2 K-halves x 64 rows x 128 B
 constexpr int F_VN = F_Q + 16384;           // v_new operand hi | lo: 128 rows x 64 B each
 constexpr int F_P = F_VN + 16384;           // P^T operand hi | lo: 128 rows (e) x 128 B (64 t)
-constexpr int F_SM = F_P + 32768;           // token records, barriers, TMEM address
-constexpr int F_SMEM = F_SM + 1024 + 16 * 8 + 16 + 1024;
+constexpr int F_SM = F_P + 32768;           // token records x 2, barriers, TMEM address
+constexpr int F_SMEM = F_SM + 2048 + 16 * 8 + 16 + 1024;
 enum { FB_W, FB_UG, FB_K, FB_Q, FB_OG0, FB_OG1, FB_P1, FB_P2, FB_QH0, FB_QH1, FB_S0, FB_S1,
        FB_O, FB_E0, FB_E1, FB_VN, FB_N };
 
@@ -1305,8 +1305,9 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   uint8_t* vp = sm + F_VP;
   uint8_t* vnt = sm + F_VN;
   uint8_t* pt = sm + F_P;
-  float4* stok = reinterpret_cast<float4*>(sm + F_SM);  // per token: Gam hi, Gam lo, 1/|q|
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 1024);
+  // per token, by block parity: (Gam hi, Gam lo, 1/|q|, 0)
+  float4* stok2 = reinterpret_cast<float4*>(sm + F_SM);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 2048);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   const int64_t Rseq = (int64_t)si.x * 2;
@@ -1536,6 +1537,17 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       load_og(0, gk_base);
       if (nb > 1) load_og(1, gk_base + 128);
     }
+    // token t of block jb: Gam at its last copy, query norm from the staged q
+    // tile (waits for that block's q tile and records)
+    auto tok_records = [&](int jb, int t, float4* dst) -> bool {
+      bool okr = mbar_wait(&bars[FB_Q], jb & 1, status, kDevTimeout);
+      okr = mbar_wait(&bars[FB_OG0 + (jb & 1)], (jb >> 1) & 1, status, kDevTimeout) && okr;
+      const uint8_t* qt = sm + F_Q;
+      const float ss = row_sumsq(qt + t * 128, t) + row_sumsq(qt + 8192 + t * 128, t);
+      const float4 rt = reinterpret_cast<const float4*>(sm + F_OG + (jb & 1) * 2048)[2 * t + 1];
+      dst[t] = make_float4(rt.x, rt.y, f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f, 0.f);
+      return okr;
+    };
     const uint32_t idow = idesc_bf16(128, 2 * kHBV, true, true);
     const uint32_t ido = idesc_bf16(128, kHBV, true, true);
     bool ok = true;
@@ -1545,14 +1557,9 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const int64_t T0 = (int64_t)si.x + (int64_t)j * 64;
       const uint32_t ph = j & 1;
       const float4* og = reinterpret_cast<const float4*>(sm + F_OG + (j & 1) * 2048);
-      ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
+      float4* stok = stok2 + 64 * (j & 1);
       ok = mbar_wait(&bars[FB_OG0 + (j & 1)], (j >> 1) & 1, status, kDevTimeout) && ok;
-      if (otid < 64) {  // token records: Gam at the last copy, query norm from the staged tile
-        const uint8_t* qt = sm + F_Q;
-        const float ss = row_sumsq(qt + otid * 128, otid) + row_sumsq(qt + 8192 + otid * 128, otid);
-        const float4 rt = og[2 * otid + 1];
-        stok[otid] = make_float4(rt.x, rt.y, f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f, 0.f);
-      }
+      if (j == 0 && otid < 64) ok = tok_records(0, otid, stok) && ok;  // later blocks: see the end
       ok = group_and(2, 256, ok);
       if (!ok) break;
       // S done (so Qh and product 2 too): k and q are free for the next block
@@ -1632,6 +1639,8 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
           }
         }
       }
+      if (quarter >= 2 && cgrp == 0 && j + 1 < nb)  // idle in the epilogue: next block's records
+        ok = tok_records(j + 1, otid - 64, stok2 + 64 * ((j + 1) & 1)) && ok;
       tc_fence_before();
       ok = group_and(2, 256, ok);
       if (!ok) break;
