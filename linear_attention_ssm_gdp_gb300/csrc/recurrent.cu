@@ -15,9 +15,11 @@
 // writes whole 128-byte rows, each element once (streaming cache hints). A
 // step's inputs (k, q, v, beta, e^g) are staged in shared memory for up to 16
 // steps with one batched load and k, q are normalised there once per step;
-// in the step loop the key/query rows are warp-broadcast 16-byte loads and the
-// column sums over K combine per-thread partials across the K/32 warps through
-// shared memory (two barriers per step).
+// in the step loop the key/query rows are warp-broadcast 16-byte loads, the
+// per-element arithmetic runs on packed pairs of rows (f32x2 multiply and
+// fused multiply-add: half the instructions, the same per-element rounding),
+// and the column sums over K combine per-thread partials across the K/32 warps
+// through shared memory (two barriers per step).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,6 +31,30 @@ namespace {
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float ldf(const __half* p) { return __half2float(*p); }
+
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: each lane of the pair is
+// rounded exactly like the scalar fp32 operation).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(f2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -52,7 +78,7 @@ constexpr int rec_smem() {
 // state. Column sums over K are in-thread over 32 rows, then across the K/32
 // warps through shared memory.
 template <typename Tin, int KW>
-__global__ void __launch_bounds__(KW * 32)
+__global__ void __launch_bounds__(KW * 32, KW >= 4 ? 24 / KW : 8)
 recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                  const float* __restrict__ beta, const float* __restrict__ g,
                  float* __restrict__ state, int L, int H, int HV, int V, float scale,
@@ -74,9 +100,11 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
   const bool active = c < V;
   const int nth = KW * 32;
   float* st = state + (int64_t)rh * K * V + (int64_t)(warp * 32) * V + c;
-  float h[32];
+  f2 h[16];  // rows (2i, 2i + 1) of this thread's 32, packed
 #pragma unroll
-  for (int i = 0; i < 32; ++i) h[i] = active ? __ldcs(st + (int64_t)i * V) : 0.f;
+  for (int i = 0; i < 16; ++i)
+    h[i] = active ? pk2(__ldcs(st + (int64_t)(2 * i) * V), __ldcs(st + (int64_t)(2 * i + 1) * V))
+                  : pk2(0.f, 0.f);
   int buf = 0;
   for (int e0 = 0; e0 < L; e0 += kLC) {
     const int lc = min(kLC, L - e0);
@@ -109,18 +137,20 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
       __syncthreads();
     }
     for (int e = 0; e < lc; ++e) {
-      const float4* kr = reinterpret_cast<const float4*>(kn + e * K + warp * 32);
-      const float4* qr = reinterpret_cast<const float4*>(qn + e * K + warp * 32);
-      const float d = eg[e];
-      float p = 0.f;
+      const ulonglong2* kr = reinterpret_cast<const ulonglong2*>(kn + e * K + warp * 32);
+      const ulonglong2* qr = reinterpret_cast<const ulonglong2*>(qn + e * K + warp * 32);
+      const f2 d2 = pk2(eg[e], eg[e]);
+      f2 pa = pk2(0.f, 0.f), pb2 = pa;
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {  // broadcast 16-byte loads of this warp's 32 key rows
-        const float4 kk = kr[i4];
-        h[4 * i4 + 0] *= d; p += h[4 * i4 + 0] * kk.x;
-        h[4 * i4 + 1] *= d; p += h[4 * i4 + 1] * kk.y;
-        h[4 * i4 + 2] *= d; p += h[4 * i4 + 2] * kk.z;
-        h[4 * i4 + 3] *= d; p += h[4 * i4 + 3] * kk.w;
+        const ulonglong2 kk = kr[i4];
+        h[2 * i4] = mul2(h[2 * i4], d2);
+        h[2 * i4 + 1] = mul2(h[2 * i4 + 1], d2);
+        pa = fma2(h[2 * i4], kk.x, pa);
+        pb2 = fma2(h[2 * i4 + 1], kk.y, pb2);
       }
+      const float2 pav = upk2(pa), pbv = upk2(pb2);
+      const float p = (pav.x + pav.y) + (pbv.x + pbv.y);
       float* pb = part + buf * KW * 32;
       pb[warp * 32 + lane] = p;
       __syncthreads();
@@ -128,15 +158,18 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
 #pragma unroll
       for (int w = 0; w < KW; ++w) s += pb[w * 32 + lane];
       const float delta = bt[e] * (vs[e * kCtaCols + lane] - s);
-      float po = 0.f;
+      const f2 dl2 = pk2(delta, delta);
+      f2 oa = pk2(0.f, 0.f), ob2 = oa;
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 kk = kr[i4], qq = qr[i4];
-        h[4 * i4 + 0] += kk.x * delta; po += h[4 * i4 + 0] * qq.x;
-        h[4 * i4 + 1] += kk.y * delta; po += h[4 * i4 + 1] * qq.y;
-        h[4 * i4 + 2] += kk.z * delta; po += h[4 * i4 + 2] * qq.z;
-        h[4 * i4 + 3] += kk.w * delta; po += h[4 * i4 + 3] * qq.w;
+        const ulonglong2 kk = kr[i4], qq = qr[i4];
+        h[2 * i4] = fma2(kk.x, dl2, h[2 * i4]);
+        h[2 * i4 + 1] = fma2(kk.y, dl2, h[2 * i4 + 1]);
+        oa = fma2(h[2 * i4], qq.x, oa);
+        ob2 = fma2(h[2 * i4 + 1], qq.y, ob2);
       }
+      const float2 oav = upk2(oa), obv = upk2(ob2);
+      const float po = (oav.x + oav.y) + (obv.x + obv.y);
       float* ob = parto + buf * KW * 32;
       ob[warp * 32 + lane] = po;
       __syncthreads();
@@ -151,7 +184,11 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
   }
   if (active) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) __stcs(st + (int64_t)i * V, h[i]);
+    for (int i = 0; i < 16; ++i) {
+      const float2 hv2 = upk2(h[i]);
+      __stcs(st + (int64_t)(2 * i) * V, hv2.x);
+      __stcs(st + (int64_t)(2 * i + 1) * V, hv2.y);
+    }
   }
 }
 
