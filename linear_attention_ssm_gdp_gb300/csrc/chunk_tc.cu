@@ -682,12 +682,108 @@ constexpr int W8_LA = W8_T + 65536;
 constexpr int W8_S = W8_LA + 128 * 129 * 4;
 constexpr int W8_SMEM = W8_S + 5 * 128 * 4 + 64 + 1024;
 
+// Top merge of the 128x128 inverse on the tensor cores: X = L10 A00, then
+// A10 = -A11 X, each as x_hi [y_hi | y_lo] (one N = 128 MMA per k-step) plus
+// x_lo y_hi (N = 64), fp32 accumulation; the two 64-column halves of an
+// accumulator are summed when read. A operands are 128 rows of LA (the upper
+// 64 rows only produce accumulator rows that are not read): rows of
+// LA[:, 0:64] for the first product, of LA[:, 64:128] (A11 below zeros) for
+// the second; K-major, 128-byte swizzle. B operands (A00, then X) are MN-major
+// 128-byte-swizzle tiles with the lo tile one 64-column atom (8 KB) after the
+// hi tile. Operand tiles live in `tiles` (48 KB used), accumulators in TMEM
+// columns [0, 256). `bar` is an unused mbarrier whose phases 0 and 1 are taken.
+// Relative error of the products ~2^-16 of sum |x||y|, the precision the
+// inverse is later used at (its hi/lo operand tiles).
+__device__ bool merge64_tc(float* LA, uint8_t* tiles, uint32_t tmem, uint64_t* bar, int* status) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, cq = warp >> 2;
+  const int p = quarter * 32 + lane;  // row of LA / TMEM lane
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  uint8_t* a_hi = tiles;              // [128 rows][64 K] bf16, swizzled
+  uint8_t* a_lo = tiles + 16384;
+  uint8_t* b_hi = tiles + 32768;      // [64 K rows][64 N] bf16, swizzled (MN-major)
+  uint8_t* b_lo = tiles + 40960;
+  // 16 consecutive values of row r into a 128-byte swizzled row at column 16 cq
+  auto put16 = [&](uint8_t* hi_base, uint8_t* lo_base, int r, const float* x) {
+    __align__(16) bf16 h[16];
+    __align__(16) bf16 l[16];
+    split_bf16_n<16>(x, h, l);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t off = r * 128 + (((2 * cq + q) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(hi_base + off) = reinterpret_cast<const uint4*>(h)[q];
+      *reinterpret_cast<uint4*>(lo_base + off) = reinterpret_cast<const uint4*>(l)[q];
+    }
+  };
+  auto issue = [&](uint32_t dcol) {  // D[dcol..] = A B over K = 64
+    const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi);
+    const uint32_t idw = idesc_bf16(128, 128, false, true), idn = idesc_bf16(128, 64, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tmem + dcol, sdesc_sw128(ah + kk * 32, 16, 1024), sdesc_sw128(bh + kk * 2048, 8192, 1024),
+               idw, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tmem + dcol, sdesc_sw128(al + kk * 32, 16, 1024), sdesc_sw128(bh + kk * 2048, 8192, 1024),
+               idn, true);
+    mma_commit(bar);
+  };
+  float x[16];
+  // operands of X = L10 A00
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = LA[p * 129 + 16 * cq + e];
+  put16(a_hi, a_lo, p, x);
+  if (p < 64) put16(b_hi, b_lo, p, x);  // A00 rows (zero above the diagonal)
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) issue(0);
+  bool ok = mbar_wait(bar, 0, status, kDevTimeout);
+  tc_fence_after();
+  // operands of A10 = -A11 X: A11 rows from LA, X from TMEM (lanes 64..127)
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = LA[p * 129 + 64 + 16 * cq + e];
+  if (quarter >= 2) {
+    uint32_t r0[16], r1[16];
+    GDP_TMEM_LD16(tmem + lane_base + 16 * cq, r0);
+    GDP_TMEM_LD16(tmem + lane_base + 64 + 16 * cq, r1);
+    tmem_wait_ld();
+    float xs[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xs[e] = __uint_as_float(r0[e]) + __uint_as_float(r1[e]);
+    put16(b_hi, b_lo, p - 64, xs);
+  }
+  __syncthreads();  // every read of the first operands is done (MMA 1 waited)
+  put16(a_hi, a_lo, p, x);
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) issue(128);
+  ok = mbar_wait(bar, 1, status, kDevTimeout) && ok;
+  tc_fence_after();
+  if (quarter >= 2) {
+    uint32_t r0[16], r1[16];
+    GDP_TMEM_LD16(tmem + lane_base + 128 + 16 * cq, r0);
+    GDP_TMEM_LD16(tmem + lane_base + 192 + 16 * cq, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      LA[p * 129 + 16 * cq + e] = -(__uint_as_float(r0[e]) + __uint_as_float(r1[e]));
+  }
+  tc_fence_before();
+  return __syncthreads_and(ok);
+}
+
 // In-place inverse of the unit lower-triangular 128x128 matrix I + L held
 // strictly lower in LA (row stride 129, zeros on and above the diagonal):
 // 16x16 diagonal blocks by forward substitution (results staged in scratch,
-// then copied back), then merges A10 = -A11 (L10 A00) at sizes 16, 32, 64.
-// scratch >= 64 * 68 floats. 512 threads.
-__device__ void solve_tril128(float* LA, float* scratch) {
+// then copied back), then merges A10 = -A11 (L10 A00) at sizes 16 and 32 on
+// the CUDA cores and 64 on the tensor cores (merge64_tc). scratch: the 64 KB
+// operand-tile region; TMEM columns [0, 256) and `bar` (phases 0, 1) are used.
+// 512 threads. Returns false if a bounded wait gave up.
+__device__ bool solve_tril128(float* LA, float* scratch, uint32_t tmem, uint64_t* bar, int* status) {
   const int tid = threadIdx.x;
   if (tid < 128) {
     const int b = tid >> 4, cl = tid & 15;
@@ -713,7 +809,7 @@ __device__ void solve_tril128(float* LA, float* scratch) {
   __syncthreads();
   merge_level<16, 4, 512>(LA, 129, scratch);
   merge_level<32, 2, 512>(LA, 129, scratch);
-  merge_level<64, 1, 512>(LA, 129, scratch);
+  return merge64_tc(LA, reinterpret_cast<uint8_t*>(scratch), tmem, bar, status);
 }
 
 template <int V>
@@ -746,15 +842,16 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   float* sgl = sgh + 128;
   float* srk = sgl + 128;
   float* sco = srk + 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 128);  // [0] k + v, [1] mma, [2] v round
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
+  // [0] k + v, [1] mma, [2] v round, [3] solve MMAs
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 128);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
   constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
   if (warp == 0) {
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   if (tid < 128) {
@@ -825,7 +922,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   }
   tc_fence_before();
   __syncthreads();
-  solve_tril128(LA, scratch);
+  ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
+  if (!ok) { tmem_release(tmem, kCols); return; }
   // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
   // Thread (quarter, cq) builds row p = 32 quarter + lane, columns [32 cq, 32 cq + 32):
   // LA rows (stride 129) are read without bank conflicts, the column scales
