@@ -1416,14 +1416,14 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   // x_hi [y_hi | y_lo] is one N = 64 MMA per k-step (columns [0,32) take
   // x_hi y_hi, [32,64) x_hi y_lo) and the lo-hi term accumulates into [0,32):
   // a product is the sum of its two 32-column halves.
-  constexpr uint32_t TD1 = 0, TD2 = 64, TO = 128, TS = 192, TQH = 320;
+  constexpr uint32_t TD1 = 0, TD2 = 64, TO = 128, TS = 192, TQH = 320, TD1B = 448, TOB = 480;
 
   if (warp == 0) {
     tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < FB_N; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < FB_N; ++i) mbar_init(&bars[i], (i == FB_P1 || i == FB_O) ? 2 : 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -1485,20 +1485,23 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const int n = min(128, si.y * 2 - j * 128);
       const int64_t R = Rseq + (int64_t)j * 128;
       const uint32_t ph = j & 1;
-      if (tid == 0) {
+      if (tid == 0 || tid == 32) {  // product 1: D1 = w h, issued from two warps
         ok = mbar_wait(&bars[FB_W], ph, status, kDevTimeout);
-        if (ok) {  // product 1: D1 = w h
+        if (ok) {
           const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO);
           const uint32_t hb = smem_u32(ht);
+          if (tid == 0) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // w_hi [h_hi | h_lo]
-            const uint64_t ad = sdesc_sw128(whi + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
-          }
+            for (int kk = 0; kk < 8; ++kk) {  // w_hi [h_hi | h_lo]
+              const uint64_t ad = sdesc_sw128(whi + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
+            }
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // + w_lo h_hi
-            const uint64_t ad = sdesc_sw128(wlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1, true);
+            for (int kk = 0; kk < 8; ++kk) {  // w_lo h_hi, its own accumulator
+              const uint64_t ad = sdesc_sw128(wlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              mma_bf16(tmem + TD1B, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1, kk > 0);
+            }
           }
           mma_commit(&bars[FB_P1]);
         }
@@ -1515,12 +1518,14 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         if (tid == 0 && ok && j + 1 < nb) load_w(R + 128);
         float d1[NC];
         {
-          uint32_t r0[NC], r1[NC];
+          uint32_t r0[NC], r1[NC], r2[NC];
           GDP_TMEM_LD16(tmem + lane_base + TD1 + cb, r0);
           GDP_TMEM_LD16(tmem + lane_base + TD1 + 32 + cb, r1);
+          GDP_TMEM_LD16(tmem + lane_base + TD1B + cb, r2);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < NC; ++c) d1[c] = __uint_as_float(r0[c]) + __uint_as_float(r1[c]);
+          for (int c = 0; c < NC; ++c)
+            d1[c] = (__uint_as_float(r0[c]) + __uint_as_float(r2[c])) + __uint_as_float(r1[c]);
         }
         const uint8_t* urow = sm + S8_U + p * 128;
         __align__(16) bf16 vh[NC];
@@ -1571,27 +1576,30 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
           }
           mma_commit(&bars[FB_P2]);
         }
+      } else if (tid == 32 || tid == 64) {  // Qh (tid 32) and S (tid 64) beside product 2
         // column set cs is re-used once the output has finished block j - 2
         const int cs = j & 1;
         if (j > 1) ok = mbar_wait(&bars[FB_E0 + cs], ((j - 2) >> 1) & 1, status, kDevTimeout) && ok;
         ok = mbar_wait(&bars[FB_Q], ph, status, kDevTimeout) && ok;
+        if (tid == 64) ok = mbar_wait(&bars[FB_K], ph, status, kDevTimeout) && ok;
         if (ok) {
           const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
-          // Qh = q [h_hi | h_lo]: rows = tokens (64.. unused)
+          if (tid == 32) {  // Qh = q [h_hi | h_lo]: rows = tokens (64.. unused)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TQH + 64 * cs, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
-          }
-          mma_commit(&bars[FB_QH0 + cs]);
-          // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+              mma_bf16(tmem + TQH + 64 * cs, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
+            }
+            mma_commit(&bars[FB_QH0 + cs]);
+          } else {  // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TS + 64 * cs, ad, bd, ids, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+              mma_bf16(tmem + TS + 64 * cs, ad, bd, ids, kk > 0);
+            }
+            mma_commit(&bars[FB_S0 + cs]);
           }
-          mma_commit(&bars[FB_S0 + cs]);
         }
       }
       ok = mbar_wait(&bars[FB_P2], ph, status, kDevTimeout) && ok;
@@ -1660,13 +1668,17 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       if (j == 0 && otid < 64) ok = tok_records(0, otid, stok) && ok;  // later blocks: see the end
       ok = group_and(2, 256, ok);
       if (!ok) break;
-      // S done (so Qh and product 2 too): k and q are free for the next block
+      // S done; k is free once product 2 is done too, q once Qh is
       const int cs = j & 1;
       ok = mbar_wait(&bars[FB_S0 + cs], (j >> 1) & 1, status, kDevTimeout);
       tc_fence_after();
       if (otid == 0 && ok && j + 1 < nb) {
-        load_k(Rseq + (int64_t)(j + 1) * 128);
-        load_q(T0 + 64);
+        ok = mbar_wait(&bars[FB_P2], ph, status, kDevTimeout);
+        ok = mbar_wait(&bars[FB_QH0 + cs], (j >> 1) & 1, status, kDevTimeout) && ok;
+        if (ok) {
+          load_k(Rseq + (int64_t)(j + 1) * 128);
+          load_q(T0 + 64);
+        }
       }
       {  // P^T row e = row, tokens [32 cgrp, 32 cgrp + 32)
         const int e = row, s = e >> 1;
@@ -1696,18 +1708,21 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       ok = group_and(2, 256, ok);
       if (!ok) break;
       tc_fence_after();
-      if (otid == 0) {
+      if (otid == 0 || otid == 32) {  // O = P v_new from two warps; A = P^T MN-major (LBO = 0)
         ok = mbar_wait(&bars[FB_VN], ph, status, kDevTimeout);
-        if (ok) {  // O = P v_new; A = P^T MN-major, second atom re-read (LBO = 0)
+        if (ok) {
           const uint32_t pb = smem_u32(pt), vv = smem_u32(vnt);
+          if (otid == 0) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // P_hi [vn_hi | vn_lo]
-            mma_bf16(tmem + TO, sdesc_sw128(pb + kk * 2048, 0, 1024),
-                     sdesc_sw64(vv + kk * 1024, 8192, 512), idow, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)  // P_hi [vn_hi | vn_lo]
+              mma_bf16(tmem + TO, sdesc_sw128(pb + kk * 2048, 0, 1024),
+                       sdesc_sw64(vv + kk * 1024, 8192, 512), idow, kk > 0);
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // + P_lo vn_hi
-            mma_bf16(tmem + TO, sdesc_sw128(pb + 16384 + kk * 2048, 0, 1024),
-                     sdesc_sw64(vv + kk * 1024, 8192, 512), ido, true);
+            for (int kk = 0; kk < 8; ++kk)  // P_lo vn_hi, its own accumulator
+              mma_bf16(tmem + TOB, sdesc_sw128(pb + 16384 + kk * 2048, 0, 1024),
+                       sdesc_sw64(vv + kk * 1024, 8192, 512), ido, kk > 0);
+          }
           mma_commit(&bars[FB_O]);
         }
       }
@@ -1715,9 +1730,11 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         const int t = row;
         ok = mbar_wait(&bars[FB_O], ph, status, kDevTimeout) && ok;
         tc_fence_after();
-        uint32_t ro[16], ro2[16], rq[16], rq2[16];
+        ok = mbar_wait(&bars[FB_QH0 + cs], (j >> 1) & 1, status, kDevTimeout) && ok;
+        uint32_t ro[16], ro2[16], ro3[16], rq[16], rq2[16];
         GDP_TMEM_LD16(tmem + lane_base + TO + cb, ro);
         GDP_TMEM_LD16(tmem + lane_base + TO + 32 + cb, ro2);
+        GDP_TMEM_LD16(tmem + lane_base + TOB + cb, ro3);
         GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + cb, rq);
         GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + 32 + cb, rq2);
         tmem_wait_ld();
@@ -1732,7 +1749,8 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
             for (int q = 0; q < 4; ++q)
               x[q] = f.scale *
                      (qs * (__uint_as_float(rq[4 * jj + q]) + __uint_as_float(rq2[4 * jj + q])) +
-                      (__uint_as_float(ro[4 * jj + q]) + __uint_as_float(ro2[4 * jj + q])));
+                      ((__uint_as_float(ro[4 * jj + q]) + __uint_as_float(ro3[4 * jj + q])) +
+                       __uint_as_float(ro2[4 * jj + q])));
             dst[jj] = make_float4(x[0], x[1], x[2], x[3]);
           }
         }
