@@ -1335,22 +1335,24 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
 //  * warps 0-7, the chain: the state recurrence of h128_tc_kernel. Thread
 //    (warp w, lane l) owns state row / position 32 (w % 4) + l and value
 //    columns [16 (w / 4), +16) of the CTA's 32. Besides the v' operand it
-//    writes v_new itself as an operand tile.
-//  * warps 8-15, the output: per block, S^T = k q^T (positions x tokens) and
-//    Qh = q h (tokens x columns, 2 passes), then the masked decayed scores
-//      P^T[e][t] = S^T[e][t] |q_t|^-1 |k_e|^-1 e^(Gam_t - Gam_e),  e <= 2t + 1,
+//    writes v_new / |k_p| as the output's operand tile.
+//  * warps 8-15, the output: per block, from S^T = k q^T (positions x tokens)
+//    and Qh = q h (tokens x columns), the masked decayed scores
+//      P^T[e][t] = S^T[e][t] e^(Gam_t - Gam_e),  e <= 2t + 1,
 //    as hi/lo operand tiles (thread = position e, 32 tokens), then
-//    O = P v_new (3 passes) and o_t = scale (e^Gam_t |q_t|^-1 Qh_t + O_t),
-//    Gam_t being the cumulative log decay at the token's last copy.
-// The chain's MMA thread issues Qh and S right behind its own product 2, so
-// the k and q tiles are released early and the state tile can be re-written
-// at the next block; the output group (P, O, epilogue) then runs beside the
-// chain's next block. S and Qh go to one of two TMEM column sets by block
-// parity, so the chain can run a block ahead of the output. The groups meet
-// only at mbarriers (QH[b]: Qh done, the h tile may be re-written; S[b]: S
-// done, k and q may be re-loaded; VN: v_new written; O: O done, v_new may be
-// re-written; E[b]: the output of a block is finished, its column set may be
-// re-used). Each group syncs internally with its own named barrier.
+//    O = P (v_new / |k|) and o_t = scale |q_t|^-1 (e^Gam_t Qh_t + O_t), Gam_t
+//    being the cumulative log decay at the token's last copy. Warps idle in
+//    the epilogue compute the next block's token records (Gam_t, 1/|q_t|).
+// A single thread issuing a whole product was a bottleneck, so products are
+// issued from several threads into their own accumulators (summed when read):
+// product 1 by chain threads 0 and 32, product 2 by thread 0 with Qh and S
+// beside it from threads 32 and 64, O by output threads 0 and 32. S and Qh go
+// to one of two TMEM column sets by block parity. The groups meet only at
+// mbarriers (P1, O: two commits each; QH[b]: Qh done, the h tile may be
+// re-written, q may be re-loaded; S[b] and P2: k may be re-loaded; VN: v_new
+// written; O: O done, v_new may be re-written; E[b]: the output of a block is
+// finished, its column set may be re-used). Each group syncs internally with
+// its own named barrier.
 struct HOArgs {
   HArgs h;
   int H, l2norm;
@@ -1541,8 +1543,9 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int c = 4 * jj + q;
-            vn[c] = (p < n) ? us[q] - d1[c] : 0.f;
-            pv[c] = vn[c] * sc;
+            const float vv = (p < n) ? us[q] - d1[c] : 0.f;
+            pv[c] = vv * sc;
+            vn[c] = vv * gp.z;  // the output's operand carries the key norm 1/|k_p|
           }
         }
         split_bf16_n<NC>(vn, vh, vl);
@@ -1692,7 +1695,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         for (int i = 0; i < 32; ++i) {  // branch-free, so that the iterations interleave
           const int t = 32 * cgrp + i;
           const float4 tk = stok[t];
-          const float x = __uint_as_float(r[i]) * tk.z * re.z * __expf((tk.x - re.x) + (tk.y - re.y));
+          const float x = __uint_as_float(r[i]) * __expf((tk.x - re.x) + (tk.y - re.y));
           r[i] = __float_as_uint((e < n && s <= t && t < nt) ? x : 0.f);
         }
         split_bf16_n<32>(reinterpret_cast<const float*>(r), ph_, pl_);
@@ -1740,14 +1743,14 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         tmem_wait_ld();
         if (t < nt && ok) {
           const float4 tk = stok[t];
-          const float qs = expf(tk.x + tk.y) * tk.z;
+          const float qs = expf(tk.x + tk.y), rqn = tk.z;  // o = scale |q|^-1 (e^Gam Qh + O)
           float4* dst = reinterpret_cast<float4*>(f.o + ((T0 + t) * HVn + hv) * V + v0 + cb);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             float x[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              x[q] = f.scale *
+              x[q] = f.scale * rqn *
                      (qs * (__uint_as_float(rq[4 * jj + q]) + __uint_as_float(rq2[4 * jj + q])) +
                       ((__uint_as_float(ro[4 * jj + q]) + __uint_as_float(ro3[4 * jj + q])) +
                        __uint_as_float(ro2[4 * jj + q])));
