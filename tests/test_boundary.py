@@ -90,6 +90,22 @@ def test_workspace_size_query(lib):
     assert off[5] in (0, 1)
 
 
+def test_path_selection_and_fused_output(lib):
+    """Which path a problem takes, and whether the chunk output is computed inside
+    the scan (the tensor-core path for two Householder copies), as the stage-offset
+    query reports it; host arithmetic only."""
+    NONE = (1 << 64) - 1
+    q = lambda *a: lib.gdp_chunk_fwd_stage_offsets(*a)
+    bf, f32 = torch.bfloat16, torch.float32
+    tc2 = q(2, 4096, 2, 16, 16, 128, 128, 2, 64, bf)    # bf16, K = 128, M = 2
+    assert tc2[5] == 1 and tc2[7] == 1 and tc2[6] == 128
+    assert tc2[3] == NONE and tc2[4] == NONE           # v_new and states never stored
+    tc3 = q(1, 512, 1, 4, 4, 128, 128, 3, 64, bf)      # odd M: separate output kernel
+    assert tc3[5] == 1 and tc3[7] == 0 and tc3[6] == 64
+    gen = q(1, 128, 1, 2, 2, 32, 32, 2, 64, f32)       # fp32: generic path
+    assert gen[5] == 0 and gen[7] == 0 and gen[3] != NONE and gen[4] != NONE
+
+
 def _prep(fn, **kw):
     a = dict(x=1 << 20, x_sn=0, x_st=0, ba=1 << 20, ba_sn=0, ba_st=0, A=1 << 20, dtb=1 << 20,
              n=1, T=4, M=2, H=4, G=2, P=8, N=8, dt=0, q=1 << 20, k=1 << 20, v=1 << 20,
