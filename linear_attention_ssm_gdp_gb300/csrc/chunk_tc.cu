@@ -5,8 +5,8 @@
 // "core.ssm.ops.gdp.wy_fast" and "core.ssm.ops.gdp.chunk_o"; the WY form of
 // the gated delta rule over the Householder-expanded stream), with every
 // dense contraction on the 5th-generation tensor core: operands staged in
-// shared memory by TMA (128-byte swizzle), tcgen05.mma issued by one thread,
-// fp32 accumulators in TMEM read back with tcgen05.ld.
+// shared memory by TMA (128-byte swizzle), tcgen05.mma issued from one or a
+// few threads, fp32 accumulators in TMEM read back with tcgen05.ld.
 //
 // Precision. Raw q, k, v are bf16 and enter the MMAs exactly; the L2 norms,
 // gates and decays are applied as fp32 row/column scales outside the MMAs.
@@ -17,18 +17,24 @@
 // about 2^-9 of the output RMS per element.
 //
 // Kernels (one launch each):
-//   wy  grid (expanded chunk, HV): Gram matrix k k^T (MMA), transition block
-//       L and its inverse A = (I+L)^-1 (blocked forward substitution in fp32
-//       on CUDA cores), then w = (A diag(beta e^Gam/|k|)) k and
-//       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32.
-//   h   grid (sequence, HV, 32-column slice of V): the sequential chunk-state
-//       recurrence, fp32 state in registers (thread = state row), per chunk
-//       v_new = u - w h (3 MMA passes) and h <- e^Gam_last h + k^T (e^(Gam_last
-//       - Gam)/|k| v_new) (2 passes); inputs double-buffered by TMA; writes
-//       v_new (hi/lo) and the state at every token-chunk start (hi/lo).
-//   o   grid (token chunk, HV, 64-column slice): scores q k^T (MMA), q h
-//       (2 passes), P = masked decayed scores (fp32 -> hi/lo), P v_new
-//       (3 passes), o = scale (e^Gt |q|^-1 q h + P v_new).
+//   wy / wy128  grid (64- or 128-position block, HV): Gram matrix k k^T (MMA),
+//       transition block L and its inverse A = (I+L)^-1 (blocked: forward
+//       substitution and small merges in fp32 on CUDA cores, the 128 block's
+//       top merge on the tensor cores), then w = (A diag(beta e^Gam/|k|)) k and
+//       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32 (128-position
+//       blocks leave through TMA bulk stores).
+//   ho128 (M = 2) grid (sequence, HV, 32-column slice of V): the sequential
+//       state recurrence and the chunk output in one kernel (a 128-position
+//       block is one 64-token output chunk); a chain warp group and an output
+//       warp group meeting at mbarriers; states and v_new never reach HBM.
+//   h / h128 (other M) grid (sequence, HV, 32-column slice of V): the
+//       sequential chunk-state recurrence, fp32 state in registers (thread =
+//       state row), per block v_new = u - w h and h <- e^Gam_last h +
+//       k^T (e^(Gam_last - Gam)/|k| v_new); writes v_new (hi/lo) and the state
+//       at every token-chunk start (hi/lo).
+//   o   (other M) grid (token chunk, HV, 64-column slice): scores q k^T (MMA),
+//       q h, P = masked decayed scores (fp32 -> hi/lo), P v_new,
+//       o = scale (e^Gt |q|^-1 q h + P v_new).
 #include <cuda_bf16.h>
 
 #include <mutex>

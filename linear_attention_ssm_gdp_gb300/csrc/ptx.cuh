@@ -1,5 +1,5 @@
 // Inline-PTX wrappers for sm_103a: mbarriers with bounded waits, TMA tile loads
-// (cp.async.bulk.tensor, one CTA, no multicast), and the 5th-generation tensor
+// and stores (cp.async.bulk.tensor, one CTA, no multicast), and the 5th-generation tensor
 // core (tcgen05: TMEM allocation, MMA with shared-memory descriptors, commit,
 // TMEM loads). Every wait is bounded by a wall-clock budget; a wait that runs
 // out records an error in a device status word and returns false so the
