@@ -168,9 +168,14 @@ __device__ __forceinline__ void merge_level(float* LA, int lda, float* X) {
   const int pair = t / (NRB * NCB), rem = t - pair * (NRB * NCB);
   const int base = pair * 2 * SZ;
   float* Xp = X + pair * SZ * XS;
+  // Warps of a pair take their column (row) blocks in the order 0 1 2 3 7 6 5 4
+  // 8 9 10 11 15 14 13 12 ..., so that the warps sharing an SM sub-partition
+  // (w, w + 4, ...) get a heavy and a light block of the triangular loops.
+  const int wip = rem >> 5, li = rem & 31;
+  const int mw = ((wip >> 2) & 1) ? (wip | 3) - (wip & 3) : wip;
   float acc[TR][TC];
   {  // X = L10 A00, A00 lower triangular: i >= c0
-    const int r0 = (rem % NRB) * TR, c0 = (rem / NRB) * TC;
+    const int r0 = (NRB == 32 ? li : rem % NRB) * TR, c0 = (NRB == 32 ? mw : rem / NRB) * TC;
 #pragma unroll
     for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
@@ -194,7 +199,8 @@ __device__ __forceinline__ void merge_level(float* LA, int lda, float* X) {
   }
   __syncthreads();
   {  // A10 = -A11 X, A11 lower triangular: i <= r0 + TR - 1
-    const int r0 = (rem / NCB) * TR, c0 = (rem % NCB) * TC;
+    const int r0 = (32 % NCB == 0 ? mw * (32 / NCB) + li / NCB : rem / NCB) * TR;
+    const int c0 = (rem % NCB) * TC;
 #pragma unroll
     for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
@@ -931,17 +937,24 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
   if (!ok) { tmem_release(tmem, kCols); return; }
   // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
-  // Thread (quarter, cq) builds row p = 32 quarter + lane, columns [32 cq, 32 cq + 32):
-  // LA rows (stride 129) are read without bank conflicts, the column scales
-  // are broadcasts, and each 8-column group is one 16-byte swizzled store per
-  // half. A is lower triangular: the first build writes the zero chunks above
-  // the diagonal, the second leaves them in place (the w MMAs only read them).
+  // Warp w builds one 32 x 32 chunk (row block R, column block C) of A, lane =
+  // row 32 R + lane: LA rows (stride 129) are read without bank conflicts,
+  // the column scales are broadcasts, and each 8-column group is one 16-byte
+  // swizzled store per half. Warps 0-9 take the ten chunks on or below the
+  // diagonal, ordered so that each SM sub-partition (warps s, s + 4, ...) gets
+  // two or three of them; warps 10-15 write the six zero chunks above the
+  // diagonal in the first build (the second leaves them in place: the w MMAs
+  // only read them).
   auto build_tiles = [&](int which) {
+    // (R, C) by warp, one hex digit per warp (warp 0 lowest): lower chunks
+    // (0,0) (1,0) (2,0) (3,0) (1,1) (2,1) (3,1) (2,2) (3,2) (3,3), then the
+    // zero chunks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
     const float* sc = which == 0 ? sco : sb;
-    const int p = quarter * 32 + lane, c0 = cq * 32;
+    const int R = (int)((0x2110003323213210ull >> (4 * warp)) & 15), C = (int)((0x3323213221110000ull >> (4 * warp)) & 15);
+    const int p = R * 32 + lane, c0 = C * 32;
     uint8_t* trow = tiles + (c0 >> 6) * 16384 + p * 128;
     const int ch0 = (c0 & 63) >> 3;
-    if (cq <= quarter) {  // warp-uniform: the chunk holds entries on or below the diagonal
+    if (warp < 10) {
       const float* lrow = LA + p * 129 + c0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
