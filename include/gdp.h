@@ -137,6 +137,11 @@ size_t gdp_chunk_fwd_workspace_size(int B, int T, int N_seq, int H, int HV, int 
  * gdp_read_status() reads back. Calls that share a workspace must not overlap
  * on the GPU.
  * Requires HV % H == 0, K <= 256, V <= 1024, M in 1..8.
+ * Path: bf16 inputs with K = 128, chunk_size 64, V in {64, 128, 256} and
+ * M <= 3 run on the tensor cores (bf16 hi/lo operand splits, fp32
+ * accumulation; for M = 2 the output is formed inside the state-scan kernel);
+ * every other shape runs an fp32 CUDA-core path of the same algebra.
+ * gdp_chunk_fwd_stage_offsets reports which path a shape takes.
  */
 gdp_status gdp_chunk_fwd(const void* q, const void* k, const void* v, const float* beta,
                          const float* g, const float* initial_state, const int32_t* cu_seqlens,
