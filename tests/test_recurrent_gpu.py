@@ -34,6 +34,9 @@ def test_decode_workload_prepare_then_update(gdp):
     (2, 8, 1, 4, 64, 128, torch.float32, False),     # GVA
     (4, 3, 2, 2, 256, 136, torch.bfloat16, True),    # several CTAs along V, ragged slice
     (2, 4, 2, 2, 128, 128, torch.float16, True),
+    (3, 11, 2, 4, 128, 72, torch.bfloat16, True),    # K = 128 kernel: ragged slice, two batches
+    (40, 4, 4, 8, 128, 128, torch.bfloat16, True),   # more items than resident CTAs
+    (2, 3, 1, 2, 128, 136, torch.float32, False),    # K = 128 kernel: three slices, fp32
 ])
 def test_recurrent_small(gdp, n, L, H, HV, K, V, dtype, l2):
     gen = torch.Generator().manual_seed(n * L + K)
@@ -53,10 +56,11 @@ def test_recurrent_small(gdp, n, L, H, HV, K, V, dtype, l2):
     assert rel_err(sd, rs) <= TOL[dtype]
 
 
-def test_recurrent_matches_chunked_prefill(gdp):
+@pytest.mark.parametrize("K", [64, 128])
+def test_recurrent_matches_chunked_prefill(gdp, K):
     """Walking a prefill's copies one step at a time (q on the last copy, g on the
     first) gives the chunked forward's outputs and final state."""
-    B, T, H, HV, K, V, M = 2, 40, 2, 2, 64, 64, 3
+    B, T, H, HV, V, M = 2, 40, 2, 2, 64, 3
     q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=2)
     qd, kd, vd, bd, gd = to(DEV, q, k, v, beta, g)
     o, fs = gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, chunk_size=64, num_householder=M,
