@@ -13,9 +13,12 @@
 //      per head, on the token (prefill) or on the first copy (decode).
 //
 // GB300 design: a persistent grid (a multiple of the SM count) walks token
-// rows; each CTA streams one row at a time with 16-byte vector loads/stores
-// (the row's value block maps onto the output contiguously, key/query heads
-// are 16-byte-aligned runs), so the kernel is a pure HBM stream. The gates use
+// rows with 16-byte vector loads/stores (the row's value block maps onto the
+// output contiguously, key/query heads are 16-byte-aligned runs), so the
+// kernel is a pure HBM stream. When a row fits one pass of the block
+// (prepare_rows_kernel, the prefill rows of the usual head sizes) each CTA
+// already has the next row's loads in flight while it stores the current one;
+// longer rows go through prepare_kernel, a row at a time. The gates use
 // the CUDA math library's expf/log1pf and IEEE division, one fp32 operation at
 // a time; this translation unit is compiled with --fmad=false so no
 // multiply-add is contracted, which keeps beta and g bitwise equal to the
@@ -137,6 +140,130 @@ __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
   }
 }
 
+// Rows that fit one pass of the block (at most 256 x kPU 16-byte vectors, at
+// most 256 gate columns): each CTA loads row r + gridDim.x, gate inputs
+// included, before it stores row r, so every thread keeps a row of loads in
+// flight while it stores and gates the previous one. Loaded values stay raw
+// until they are stored (a conversion on arrival would stall the warp on its
+// own prefetch). Same copies and the same fp32 gate operations as
+// prepare_kernel.
+constexpr int kPU = 5;
+
+struct RowGeo {
+  int64_t vrow_b, krow_b, head_kb, kbase_b, qbase_b, qrow_b;
+  int nv, nk, nq, head_v, hpg, MH;
+};
+
+__device__ __forceinline__ RowGeo row_geo(const PrepArgs& a, bool decode) {
+  RowGeo g;
+  g.hpg = a.H / a.G;
+  g.vrow_b = (int64_t)a.M * a.H * a.P * a.es;
+  g.krow_b = (int64_t)a.M * a.H * a.N * a.es;
+  g.head_kb = (int64_t)a.N * a.es;
+  g.kbase_b = g.vrow_b;
+  g.qbase_b = g.kbase_b + (int64_t)a.M * a.G * g.head_kb;
+  g.qrow_b = (decode ? (int64_t)a.M : 1) * a.H * g.head_kb;
+  g.nv = (int)(g.vrow_b / 16);
+  g.nk = (int)(g.krow_b / 16);
+  g.nq = (int)(g.qrow_b / 16);
+  g.head_v = (int)(g.head_kb / 16);
+  g.MH = a.M * a.H;
+  return g;
+}
+
+struct RowBuf {
+  uint4 x[kPU];
+  uint32_t b, av;  // raw gate inputs: b for column tid < M*H, a for head tid < H
+};
+
+__device__ __forceinline__ uint32_t raw_ld(const void* base, int64_t idx, int dt) {
+  return dt == GDP_F32 ? static_cast<const uint32_t*>(base)[idx]
+                       : static_cast<const unsigned short*>(base)[idx];
+}
+__device__ __forceinline__ float raw_f32(uint32_t r, int dt) {
+  if (dt == GDP_F32) return __uint_as_float(r);
+  if (dt == GDP_BF16) return __uint_as_float(r << 16);
+  return __half2float(__ushort_as_half((unsigned short)r));
+}
+
+template <bool DECODE>
+__device__ __forceinline__ void load_row(const PrepArgs& a, const RowGeo& g, int64_t r,
+                                         RowBuf& rb) {
+  const int64_t in = r / a.T, t = r - in * a.T;
+  const uint8_t* xr = a.x + in * a.x_sn_b + t * a.x_st_b;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kPU; ++u) {
+    const int c = tid + u * 256;
+    if (c < g.nv) {
+      rb.x[u] = __ldcs(reinterpret_cast<const uint4*>(xr) + c);
+    } else if (c < g.nv + g.nk) {
+      const int ck = c - g.nv;
+      const int jh = ck / g.head_v, w = ck - jh * g.head_v;
+      const int j = jh / a.H, h = jh - j * a.H;
+      rb.x[u] = __ldcs(reinterpret_cast<const uint4*>(
+                           xr + g.kbase_b + ((int64_t)j * a.G + h / g.hpg) * g.head_kb) + w);
+    } else if (c < g.nv + g.nk + g.nq) {
+      const int cq = c - g.nv - g.nk;
+      const int jh = cq / g.head_v, w = cq - jh * g.head_v;
+      const int j = DECODE ? jh / a.H : a.M - 1;
+      const int h = DECODE ? jh - j * a.H : jh;
+      rb.x[u] = make_uint4(0u, 0u, 0u, 0u);  // +0.0 in every dtype
+      if (j == a.M - 1)
+        rb.x[u] = __ldcs(reinterpret_cast<const uint4*>(xr + g.qbase_b +
+                                                        (int64_t)(h / g.hpg) * g.head_kb) + w);
+    }
+  }
+  const int64_t bar = in * a.ba_sn + t * a.ba_st;
+  if (tid < g.MH) rb.b = raw_ld(a.ba, bar + tid, a.dt);
+  if (tid < a.H) rb.av = raw_ld(a.ba, bar + g.MH + tid, a.dt);
+}
+
+template <bool DECODE>
+__device__ __forceinline__ void store_row(const PrepArgs& a, const RowGeo& g, int64_t r,
+                                          const RowBuf& rb) {
+  const int tid = threadIdx.x;
+  uint4* vdst = reinterpret_cast<uint4*>(a.v + r * g.vrow_b);
+  uint4* kdst = reinterpret_cast<uint4*>(a.k + r * g.krow_b);
+  uint4* qdst = reinterpret_cast<uint4*>(a.q + r * g.qrow_b);
+#pragma unroll
+  for (int u = 0; u < kPU; ++u) {
+    const int c = tid + u * 256;
+    if (c < g.nv) __stcs(vdst + c, rb.x[u]);
+    else if (c < g.nv + g.nk) __stcs(kdst + (c - g.nv), rb.x[u]);
+    else if (c < g.nv + g.nk + g.nq) __stcs(qdst + (c - g.nv - g.nk), rb.x[u]);
+  }
+  if (tid < g.MH) a.beta[r * g.MH + tid] = 1.0f / (1.0f + expf(-raw_f32(rb.b, a.dt)));
+  const int ng = DECODE ? g.MH : a.H;
+  if (tid < ng) {
+    const int j = DECODE ? tid / a.H : 0;
+    const int h = DECODE ? tid - j * a.H : tid;
+    float gv = 0.0f;
+    if (j == 0) {
+      const float sp = softplus_page(raw_f32(rb.av, a.dt) + a.dt_bias[h]);
+      gv = -(expf(a.A_log[h]) * sp);
+    }
+    a.g[r * ng + tid] = gv;
+  }
+}
+
+template <bool DECODE>
+__global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
+  const int64_t rows = (int64_t)a.n * a.T;
+  const RowGeo g = row_geo(a, DECODE);
+  int64_t r = blockIdx.x;
+  if (r >= rows) return;
+  RowBuf cur;
+  load_row<DECODE>(a, g, r, cur);
+  for (; r < rows; r += gridDim.x) {
+    RowBuf nxt;
+    const int64_t rn = r + gridDim.x;
+    if (rn < rows) load_row<DECODE>(a, g, rn, nxt);
+    store_row<DECODE>(a, g, r, cur);
+    cur = nxt;
+  }
+}
+
 template <int VB>
 cudaError_t launch_vb(const PrepArgs& a, bool decode, cudaStream_t s) {
   const int64_t rows = (int64_t)a.n * a.T;
@@ -177,7 +304,25 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
   const bool vec16 = al16(x) && al16(q) && al16(k) && al16(v) && (a.x_sn_b % 16 == 0) &&
                      (a.x_st_b % 16 == 0) && ((int64_t)P * a.es % 16 == 0) &&
                      ((int64_t)N * a.es % 16 == 0);
-  if (vec16) return launch_vb<16>(a, decode, stream);
+  if (vec16) {
+    const int64_t ntot = ((int64_t)M * H * P + (int64_t)(decode ? 2 * M : M + 1) * H * N) *
+                         a.es / 16;
+    if (ntot <= 256 * kPU && M * H <= 256) {
+      const int64_t rows = (int64_t)n * T;
+      int per_sm = 0;
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, decode ? prepare_rows_kernel<true> : prepare_rows_kernel<false>, 256, 0);
+      if (e != cudaSuccess) return e;
+      const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+      const int grid = (int)(rows < cap ? rows : cap);
+      if (decode)
+        prepare_rows_kernel<true><<<grid, 256, 0, stream>>>(a);
+      else
+        prepare_rows_kernel<false><<<grid, 256, 0, stream>>>(a);
+      return cudaGetLastError();
+    }
+    return launch_vb<16>(a, decode, stream);
+  }
   if (a.es == 4) return launch_vb<4>(a, decode, stream);
   return launch_vb<2>(a, decode, stream);
 }
