@@ -17,12 +17,14 @@
 // about 2^-9 of the output RMS per element.
 //
 // Kernels (one launch each):
-//   wy / wy128  grid (64- or 128-position block, HV): Gram matrix k k^T (MMA),
-//       transition block L and its inverse A = (I+L)^-1 (blocked: forward
-//       substitution and small merges in fp32 on CUDA cores, the 128 block's
-//       top merge on the tensor cores), then w = (A diag(beta e^Gam/|k|)) k and
+//   wy / wy128  grid (64-position block, HV) / persistent, one CTA per SM over
+//       (128-position block, HV) items: Gram matrix k k^T (MMA), transition
+//       block L and its inverse A = (I+L)^-1 (blocked: forward substitution and
+//       small merges in fp32 on CUDA cores, the 128 block's top merge on the
+//       tensor cores), then w = (A diag(beta e^Gam/|k|)) k and
 //       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32 (128-position
-//       blocks leave through TMA bulk stores).
+//       blocks leave through TMA bulk stores while the next item's k and v
+//       load).
 //   ho128 (M = 2) grid (sequence, HV, 32-column slice of V): the sequential
 //       state recurrence and the chunk output in one kernel (a 128-position
 //       block is one 64-token output chunk); a chain warp group and an output
@@ -37,6 +39,7 @@
 //       o = scale (e^Gt |q|^-1 q h + P v_new).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdp_internal.cuh"
@@ -686,13 +689,13 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
 // Shared memory: k (2 K-halves of 128 rows, 32 KB) | v (two 64-column chunks of
 // 128 rows, 32 KB; V = 256 loads it in two rounds) | operand tiles (2 x 32 KB;
 // the solve scratch lives here before the tiles are built) | L/A fp32 [128][129]
-// | small arrays
+// | small arrays (two sets, by item parity) | barriers
 constexpr int W8_K = 0;
 constexpr int W8_V = 32768;
 constexpr int W8_T = 65536;
 constexpr int W8_LA = W8_T + 65536;
 constexpr int W8_S = W8_LA + 128 * 129 * 4;
-constexpr int W8_SMEM = W8_S + 5 * 128 * 4 + 64 + 1024;
+constexpr int W8_SMEM = W8_S + 2 * 5 * 128 * 4 + 64 + 1024;
 
 // Top merge of the 128x128 inverse on the tensor cores: X = L10 A00, then
 // A10 = -A11 X, each as x_hi [y_hi | y_lo] (one N = 128 MMA per k-step) plus
@@ -824,299 +827,399 @@ __device__ bool solve_tril128(float* LA, float* scratch, uint32_t tmem, uint64_t
   return merge64_tc(LA, reinterpret_cast<uint8_t*>(scratch), tmem, bar, status);
 }
 
+// Persistent: one CTA per SM walks (128-position block, value head) items,
+// item = head * NB + block, skipping the block list's unused tail entries.
+// TMEM, barriers and tensor maps are set up once per CTA. For V <= 128 the
+// items are pipelined: w (hi, lo) is staged in LA and u in the operand tiles,
+// so the k and v buffers are free as soon as the W and U products have read
+// them, and the next item's k and v stream in behind this item's epilogues;
+// the bulk stores only have to have read their staging before the next item
+// writes LA. For V = 256 the u staging needs the v buffer, so each item's k
+// and v are loaded once the previous item's stores have read shared memory.
+// In both modes warp 15, idle in the second tile build, stages the next
+// item's beta and decay and takes their compensated prefix there.
 template <int V>
 __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
     const __grid_constant__ CUtensorMap map_whs, const __grid_constant__ CUtensorMap map_wls,
-    const __grid_constant__ CUtensorMap map_us, WyArgs a) {
+    const __grid_constant__ CUtensorMap map_us, WyArgs a, int NB) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int2 tab = a.blk_tab[blockIdx.x];  // (sequence, first of the block's two 64-chunks)
-  if (tab.x < 0) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
-  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
-  const int4 si = a.seq_info[tab.x];
-  const int M = a.M;
-  const int b_start = tab.y * kBT;
-  const int n = min(128, si.y * M - b_start);
-  const int64_t R0 = (int64_t)si.x * M + b_start;
+  constexpr bool kPipe = V <= 128;
   constexpr int VR = V < 128 ? V : 128;          // value columns per round
   constexpr int NR = V / VR;                     // rounds
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
+  const int M = a.M;
+  const int n_items = NB * a.HV;
+  auto valid = [&](int it) { return a.blk_tab[it % NB].x >= 0; };
+  auto next_valid = [&](int it) {
+    do it += gridDim.x; while (it < n_items && !valid(it));
+    return it;
+  };
+  int it = blockIdx.x;
+  if (it < n_items && !valid(it)) it = next_valid(it);
+  if (it >= n_items) return;
+  struct Item {
+    int hv, kh, n, b_start, t0;
+    int64_t R0;
+  };
+  auto item = [&](int i) {
+    Item x;
+    const int2 tab = a.blk_tab[i % NB];  // (sequence, first of the block's two 64-chunks)
+    const int4 si = a.seq_info[tab.x];
+    x.hv = i / NB;
+    x.kh = x.hv / (a.HV / a.H);
+    x.b_start = tab.y * kBT;
+    x.n = min(128, si.y * M - x.b_start);
+    x.t0 = si.x;
+    x.R0 = (int64_t)si.x * M + x.b_start;
+    return x;
+  };
+  // beta and the decay (on a token's first copy) of position p of item x
+  auto gates = [&](const Item& x, int p, float& b, float& gl) {
+    b = 0.f;
+    gl = 0.f;
+    if (p < x.n) {
+      const int e = x.b_start + p, t = e / M;
+      b = a.beta[(x.R0 + p) * a.HV + x.hv];
+      if (a.g && e - t * M == 0) gl = a.g[((int64_t)x.t0 + t) * a.HV + x.hv];
+    }
+  };
   uint8_t* kbuf = sm + W8_K;
   uint8_t* vbuf = sm + W8_V;
   uint8_t* tiles = sm + W8_T;
   float* LA = reinterpret_cast<float*>(sm + W8_LA);
   float* scratch = reinterpret_cast<float*>(tiles);
-  float* sb = reinterpret_cast<float*>(sm + W8_S);
-  float* sgh = sb + 128;
-  float* sgl = sgh + 128;
-  float* srk = sgl + 128;
-  float* sco = srk + 128;
-  // [0] k + v, [1] mma, [2] v round, [3] solve MMAs
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 128);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+  float* sarr = reinterpret_cast<float*>(sm + W8_S);  // [2][5][128], by item parity
+  // [0] k, [1] mma, [2] v round, [3] solve MMAs, [4] v
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sarr + 2 * 5 * 128);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
   constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
+  auto issue_k = [&](const Item& x) {
+    mbar_expect_tx(&bars[0], 32768);
+    tma_load_3d(kbuf, &map_k, 0, x.kh, (int)x.R0, &bars[0]);
+    tma_load_3d(kbuf + 16384, &map_k, 64, x.kh, (int)x.R0, &bars[0]);
+  };
+  auto issue_v = [&](const Item& x) {
+    mbar_expect_tx(&bars[4], (VR / 64) * 16384);
+#pragma unroll
+    for (int c = 0; c < VR / 64; ++c) tma_load_3d(vbuf + c * 16384, &map_v, 64 * c, x.hv, (int)x.R0, &bars[4]);
+  };
   if (warp == 0) {
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
+  Item x = item(it);
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
+    issue_k(x);
+    issue_v(x);
   }
-  if (tid < 128) {
-    float b = 0.f, gl = 0.f;
-    if (tid < n) {
-      const int e = b_start + tid, t = e / M;
-      b = a.beta[(R0 + tid) * a.HV + hv];
-      if (a.g && e - t * M == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv];
-    }
-    sb[tid] = b;
-    sgh[tid] = gl;
-  }
+  if (tid < 128) gates(x, tid, sarr[tid], sarr[128 + tid]);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) comp_prefix(sarr + 128, sarr + 256, 128);
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  if (tid == 0) {
-    mbar_expect_tx(&bars[0], 32768 + (VR / 64) * 16384);
-    tma_load_3d(kbuf, &map_k, 0, kh, (int)R0, &bars[0]);
-    tma_load_3d(kbuf + 16384, &map_k, 64, kh, (int)R0, &bars[0]);
-#pragma unroll
-    for (int c = 0; c < VR / 64; ++c) tma_load_3d(vbuf + c * 16384, &map_v, 64 * c, hv, (int)R0, &bars[0]);
-    comp_prefix(sgh, sgl, 128);
-  }
-  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
   uint32_t mma_phase = 0;
-  if (tid == 0) {  // Gram matrix k k^T, 128 x 128
-    const uint32_t kb = smem_u32(kbuf);
-    const uint32_t id = idesc_bf16(128, 128, false, false);
+  // k / v loads issued and consumed so far: load i completes phase i of bars[0] / bars[4]
+  int k_iss = 1, k_got = 0, v_iss = 1, v_got = 0;
+  bool ok = true;
+  for (int c = 0;; ++c) {
+    const int par = c & 1;
+    float* sb = sarr + par * 640;
+    float* sgh = sb + 128;
+    float* sgl = sgh + 128;
+    float* srk = sgl + 128;
+    float* sco = srk + 128;
+    float* nsb = sarr + (par ^ 1) * 640;  // the next item's beta and decay
+    const int nx = next_valid(it);
+    const bool has_next = nx < n_items;
+    const Item y = has_next ? item(nx) : x;
+    float pb[4], pg[4];  // warp 15: the next item's gate inputs, staged in the second build
+    if (warp == 15 && has_next) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-      mma_bf16(tmem, d, d, id, kk > 0);
+      for (int i = 0; i < 4; ++i) gates(y, lane + 32 * i, pb[i], pg[i]);
     }
-    mma_commit(&bars[1]);
-  }
-  if (tid < 128) {
-    const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 16384 + tid * 128, tid);
-    const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    srk[tid] = r;
-    sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
-  }
-  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
-  mma_phase ^= 1;
-  tc_fence_after();
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  {  // L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|) for i < p
-    const int p = quarter * 32 + lane;
-    const float bp = sb[p] * srk[p];
-    const int c0 = cq * 32;
-    if (cq > quarter) {  // block entirely on or above the diagonal: zeros
+    const int n = x.n, hv = x.hv;
+    const int64_t R0 = x.R0;
+    ok = mbar_wait(&bars[0], k_got & 1, a.status, kDevTimeout);
+    if (ok) ++k_got;
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {  // Gram matrix k k^T, 128 x 128
+      const uint32_t kb = smem_u32(kbuf);
+      const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) LA[p * 129 + c0 + j] = 0.f;
-    } else {
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        mma_bf16(tmem, d, d, id, kk > 0);
+      }
+      mma_commit(&bars[1]);
+    }
+    if (tid < 128) {
+      const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 16384 + tid * 128, tid);
+      const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+      srk[tid] = r;
+      sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
+    }
+    fence_async_smem();  // the k buffer's generic reads end before the next k load
+    if (kPipe && tid == 0) tma_store_wait_read();  // the previous item's stores have read LA, tiles
+    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+    mma_phase ^= 1;
+    tc_fence_after();
+    if (!__syncthreads_and(ok)) break;
+    {  // L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|) for i < p
+      const int p = quarter * 32 + lane;
+      const float bp = sb[p] * srk[p];
+      const int c0 = cq * 32;
+      if (cq > quarter) {  // block entirely on or above the diagonal: zeros
+#pragma unroll
+        for (int j = 0; j < 32; ++j) LA[p * 129 + c0 + j] = 0.f;
+      } else {
+        uint32_t r[32];
+        GDP_TMEM_LD32(tmem + lane_base + c0, r);
+        tmem_wait_ld();
+        const float gph = sgh[p], gpl = sgl[p];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
+          const int i = c0 + j;
+          const float v = bp * __expf((gph - sgh[i]) + (gpl - sgl[i])) * srk[i] * __uint_as_float(r[j]);
+          LA[p * 129 + i] = (i < p) ? v : 0.f;
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
+    if (!ok) break;
+    // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
+    // Warp w builds one 32 x 32 chunk (row block R, column block C) of A, lane =
+    // row 32 R + lane: LA rows (stride 129) are read without bank conflicts,
+    // the column scales are broadcasts, and each 8-column group is one 16-byte
+    // swizzled store per half. Warps 0-9 take the ten chunks on or below the
+    // diagonal, ordered so that each SM sub-partition (warps s, s + 4, ...) gets
+    // two or three of them; warps 10-15 write the six zero chunks above the
+    // diagonal in the first build (the second leaves them in place: the w MMAs
+    // only read them), and in the second build warp 15 stages the next item's
+    // gates and takes their prefix.
+    auto build_tiles = [&](int which) {
+      // (R, C) by warp, one hex digit per warp (warp 0 lowest): lower chunks
+      // (0,0) (1,0) (2,0) (3,0) (1,1) (2,1) (3,1) (2,2) (3,2) (3,3), then the
+      // zero chunks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+      const float* sc = which == 0 ? sco : sb;
+      const int R = (int)((0x2110003323213210ull >> (4 * warp)) & 15), C = (int)((0x3323213221110000ull >> (4 * warp)) & 15);
+      const int p = R * 32 + lane, c0 = C * 32;
+      uint8_t* trow = tiles + (c0 >> 6) * 16384 + p * 128;
+      const int ch0 = (c0 & 63) >> 3;
+      if (warp < 10) {
+        const float* lrow = LA + p * 129 + c0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          __align__(16) bf16 hi[8];
+          __align__(16) bf16 lo[8];
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = lrow[8 * q + e] * sc[c0 + 8 * q + e];
+          split_bf16_n<8>(v, hi, lo);
+          const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
+          *reinterpret_cast<uint4*>(trow + off) = *reinterpret_cast<const uint4*>(hi);
+          *reinterpret_cast<uint4*>(trow + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
+        }
+      } else if (which == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
+          *reinterpret_cast<uint4*>(trow + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(trow + 32768 + off) = make_uint4(0, 0, 0, 0);
+        }
+      } else if (warp == 15 && has_next) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          nsb[lane + 32 * i] = pb[i];
+          nsb[128 + lane + 32 * i] = pg[i];
+        }
+        __syncwarp();
+        if (lane == 0) comp_prefix(nsb + 128, nsb + 256, 128);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    };
+    build_tiles(0);
+    if (tid == 0) {  // w = A' k: M = 128 positions, N = 128, K = 128 positions
+      const uint32_t tb = smem_u32(tiles), kb = smem_u32(kbuf);
+      const uint32_t idw = idesc_bf16(128, 128, false, true);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kb + kk * 2048, 16384, 1024);
+          mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
+        }
+      mma_commit(&bars[1]);
+    }
+    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+    mma_phase ^= 1;
+    tc_fence_after();
+    if (!__syncthreads_and(ok)) break;
+    if (kPipe && has_next) {  // the W product was the k buffer's last reader
+      if (tid == 0) issue_k(y);
+      ++k_iss;
+    }
+    build_tiles(1);
+    ok = mbar_wait(&bars[4], v_got & 1, a.status, kDevTimeout);
+    if (ok) ++v_got;
+    if (!__syncthreads_and(ok)) break;
+    auto issue_u = [&](int round) {
+      const uint32_t tb = smem_u32(tiles), vb = smem_u32(vbuf);
+      const uint32_t idu = idesc_bf16(128, VR, false, true);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+          mma_bf16(tmem + 128 + round * VR, ad, bd, idu, (pass | kk) != 0);
+        }
+      mma_commit(&bars[1]);
+    };
+    if (tid == 0) issue_u(0);
+    // Epilogues. A whole block is staged in shared memory that its last reader
+    // has released and written with bulk tensor stores; a sequence's last,
+    // partial block is written row by row, so that no store reaches the rows of
+    // the next sequence.
+    const bool full = n == 128;
+    // w staging, two 64-column boxes per array: pipelined, w_hi and w_lo in
+    // LA; otherwise w_hi in the k buffer and w_lo in LA
+    uint8_t* whs = kPipe ? reinterpret_cast<uint8_t*>(LA) : kbuf;
+    uint8_t* wls = reinterpret_cast<uint8_t*>(LA) + (kPipe ? 32768 : 0);
+    {  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread
+      const int p = quarter * 32 + lane;
+      const int c0 = cq * 32;
       uint32_t r[32];
       GDP_TMEM_LD32(tmem + lane_base + c0, r);
       tmem_wait_ld();
-      const float gph = sgh[p], gpl = sgl[p];
+      __align__(16) bf16 hi[32];
+      __align__(16) bf16 lo[32];
+      split_bf16_n<32>(reinterpret_cast<const float*>(r), hi, lo);
+      if (full) {
+        const uint32_t base = (c0 >> 6) * 16384 + p * 128;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
-        const int i = c0 + j;
-        const float x = bp * __expf((gph - sgh[i]) + (gpl - sgl[i])) * srk[i] * __uint_as_float(r[j]);
-        LA[p * 129 + i] = (i < p) ? x : 0.f;
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t off = base + (((((c0 & 63) >> 3) + i) ^ (p & 7)) << 4);
+          *reinterpret_cast<uint4*>(whs + off) = reinterpret_cast<const uint4*>(hi)[i];
+          *reinterpret_cast<uint4*>(wls + off) = reinterpret_cast<const uint4*>(lo)[i];
+        }
+      } else if (p < n) {
+        const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
+        store_bf16x32(a.w_hi + row, hi);
+        store_bf16x32(a.w_lo + row, lo);
       }
     }
+    if (full) {
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_store_3d(&map_whs, whs + h * 16384, 64 * h, hv, (int)R0);
+          tma_store_3d(&map_wls, wls + h * 16384, 64 * h, hv, (int)R0);
+        }
+        tma_store_commit();
+      }
+    }
+#pragma unroll 1
+    for (int round = 1; round < NR; ++round) {  // V = 256: second half of the value columns
+      ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+      mma_phase ^= 1;
+      if (!__syncthreads_and(ok)) break;
+      if (tid == 0) {
+        mbar_expect_tx(&bars[2], (VR / 64) * 16384);
+#pragma unroll
+        for (int c2 = 0; c2 < VR / 64; ++c2)
+          tma_load_3d(vbuf + c2 * 16384, &map_v, round * VR + 64 * c2, hv, (int)R0, &bars[2]);
+      }
+      ok = mbar_wait(&bars[2], (c * (NR - 1) + round - 1) & 1, a.status, kDevTimeout);
+      if (!__syncthreads_and(ok)) break;
+      if (tid == 0) issue_u(round);
+    }
+    if (!ok) break;
+    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+    mma_phase ^= 1;
+    tc_fence_after();
+    if (!__syncthreads_and(ok)) break;
+    if (kPipe && has_next) {  // the U product was the v buffer's last reader
+      if (tid == 0) issue_v(y);
+      ++v_iss;
+    }
+    // u staging: 32-column boxes, 0-3 in the operand tiles, 4-5 in the upper
+    // half of LA, 6-7 in the v buffer (V = 256; all released by the u MMAs)
+    auto ustage = [&](int cc) -> uint8_t* {
+      return cc < 4 ? tiles + cc * 16384
+                    : cc < 6 ? reinterpret_cast<uint8_t*>(LA) + 32768 + (cc - 4) * 16384
+                             : vbuf + (cc - 6) * 16384;
+    };
+    {  // u epilogue: row p, V / 4 columns per thread
+      const int p = quarter * 32 + lane;
+#pragma unroll 1
+      for (int c0 = cq * (V / 4); c0 < (cq + 1) * (V / 4); c0 += 16) {
+        uint32_t r[16];
+        GDP_TMEM_LD16(tmem + lane_base + 128 + c0, r);
+        tmem_wait_ld();
+        if (full) {
+          uint8_t* st = ustage(c0 >> 5) + p * 128;
+          const int u0 = (c0 & 31) >> 2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(st + (((u0 + j) ^ (p & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        } else if (p < n) {
+          float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (tid < n) a.gk[(int64_t)hv * a.Te + R0 + tid] = make_float4(sgh[tid], sgl[tid], srk[tid], 0.f);
+    }
+    if (full) fence_async_smem();
+    tc_fence_before();
+    __syncthreads();  // TMEM reads and the staging are done
+    tc_fence_after();
+    if (tid == 0) {
+      if (full) {
+#pragma unroll
+        for (int cc = 0; cc < V / 32; ++cc) tma_store_3d(&map_us, ustage(cc), 32 * cc, hv, (int)R0);
+        tma_store_commit();
+      }
+      if (!kPipe && has_next) {  // the next item's loads reuse the staging buffers
+        tma_store_wait_read();
+        issue_k(y);
+        issue_v(y);
+      }
+    }
+    if (!kPipe && has_next) ++k_iss, ++v_iss;
+    if (!has_next) break;
+    it = nx;
+    x = y;
+  }
+  if (tid == 0) {  // nothing may still write or read shared memory when the CTA leaves
+    bool w = true;
+    for (; w && k_got < k_iss; ++k_got) w = mbar_wait(&bars[0], k_got & 1, nullptr, 0);
+    for (; w && v_got < v_iss; ++v_got) w = mbar_wait(&bars[4], v_got & 1, nullptr, 0);
+    tma_store_wait_read();
   }
   tc_fence_before();
   __syncthreads();
-  ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
-  if (!ok) { tmem_release(tmem, kCols); return; }
-  // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
-  // Warp w builds one 32 x 32 chunk (row block R, column block C) of A, lane =
-  // row 32 R + lane: LA rows (stride 129) are read without bank conflicts,
-  // the column scales are broadcasts, and each 8-column group is one 16-byte
-  // swizzled store per half. Warps 0-9 take the ten chunks on or below the
-  // diagonal, ordered so that each SM sub-partition (warps s, s + 4, ...) gets
-  // two or three of them; warps 10-15 write the six zero chunks above the
-  // diagonal in the first build (the second leaves them in place: the w MMAs
-  // only read them).
-  auto build_tiles = [&](int which) {
-    // (R, C) by warp, one hex digit per warp (warp 0 lowest): lower chunks
-    // (0,0) (1,0) (2,0) (3,0) (1,1) (2,1) (3,1) (2,2) (3,2) (3,3), then the
-    // zero chunks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-    const float* sc = which == 0 ? sco : sb;
-    const int R = (int)((0x2110003323213210ull >> (4 * warp)) & 15), C = (int)((0x3323213221110000ull >> (4 * warp)) & 15);
-    const int p = R * 32 + lane, c0 = C * 32;
-    uint8_t* trow = tiles + (c0 >> 6) * 16384 + p * 128;
-    const int ch0 = (c0 & 63) >> 3;
-    if (warp < 10) {
-      const float* lrow = LA + p * 129 + c0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __align__(16) bf16 hi[8];
-        __align__(16) bf16 lo[8];
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = lrow[8 * q + e] * sc[c0 + 8 * q + e];
-        split_bf16_n<8>(x, hi, lo);
-        const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
-        *reinterpret_cast<uint4*>(trow + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(trow + 32768 + off) = *reinterpret_cast<const uint4*>(lo);
-      }
-    } else if (which == 0) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t off = ((ch0 + q) ^ (p & 7)) << 4;
-        *reinterpret_cast<uint4*>(trow + off) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(trow + 32768 + off) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  };
-  build_tiles(0);
-  if (tid == 0) {  // w = A' k: M = 128 positions, N = 128, K = 128 positions
-    const uint32_t tb = smem_u32(tiles), kb = smem_u32(kbuf);
-    const uint32_t idw = idesc_bf16(128, 128, false, true);
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(kb + kk * 2048, 16384, 1024);
-        mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
-      }
-    mma_commit(&bars[1]);
-  }
-  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
-  mma_phase ^= 1;
   tc_fence_after();
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  build_tiles(1);
-  auto issue_u = [&](int round) {
-    const uint32_t tb = smem_u32(tiles), vb = smem_u32(vbuf);
-    const uint32_t idu = idesc_bf16(128, VR, false, true);
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-        mma_bf16(tmem + 128 + round * VR, ad, bd, idu, (pass | kk) != 0);
-      }
-    mma_commit(&bars[1]);
-  };
-  if (tid == 0) issue_u(0);
-  // Epilogues. A whole block is staged in shared memory that its last reader
-  // has released and written with bulk tensor stores; a sequence's last,
-  // partial block is written row by row, so that no store reaches the rows of
-  // the next sequence.
-  const bool full = n == 128;
-  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread;
-  // staged as two 64-column boxes per array, w_hi in the k buffer, w_lo in LA
-  {
-    const int p = quarter * 32 + lane;
-    const int c0 = cq * 32;
-    uint32_t r[32];
-    GDP_TMEM_LD32(tmem + lane_base + c0, r);
-    tmem_wait_ld();
-    __align__(16) bf16 hi[32];
-    __align__(16) bf16 lo[32];
-    split_bf16_n<32>(reinterpret_cast<const float*>(r), hi, lo);
-    if (full) {
-      const uint32_t base = (c0 >> 6) * 16384 + p * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t off = base + (((((c0 & 63) >> 3) + i) ^ (p & 7)) << 4);
-        *reinterpret_cast<uint4*>(kbuf + off) = reinterpret_cast<const uint4*>(hi)[i];
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(LA) + off) =
-            reinterpret_cast<const uint4*>(lo)[i];
-      }
-    } else if (p < n) {
-      const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
-      store_bf16x32(a.w_hi + row, hi);
-      store_bf16x32(a.w_lo + row, lo);
-    }
-  }
-  if (full) {
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_store_3d(&map_whs, kbuf + h * 16384, 64 * h, hv, (int)R0);
-        tma_store_3d(&map_wls, reinterpret_cast<uint8_t*>(LA) + h * 16384, 64 * h, hv, (int)R0);
-      }
-      tma_store_commit();
-    }
-  }
-#pragma unroll 1
-  for (int round = 1; round < NR; ++round) {  // V = 256: second half of the value columns
-    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
-    mma_phase ^= 1;
-    if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-    if (tid == 0) {
-      mbar_expect_tx(&bars[2], (VR / 64) * 16384);
-#pragma unroll
-      for (int c = 0; c < VR / 64; ++c)
-        tma_load_3d(vbuf + c * 16384, &map_v, round * VR + 64 * c, hv, (int)R0, &bars[2]);
-    }
-    ok = mbar_wait(&bars[2], (round - 1) & 1, a.status, kDevTimeout);
-    if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-    if (tid == 0) issue_u(round);
-  }
-  ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
-  tc_fence_after();
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  // u staging: 32-column boxes, 0-3 in the operand tiles, 4-5 in the upper
-  // half of LA, 6-7 in the v buffer (all released by the u MMAs)
-  auto ustage = [&](int c) -> uint8_t* {
-    return c < 4 ? tiles + c * 16384
-                 : c < 6 ? reinterpret_cast<uint8_t*>(LA) + 32768 + (c - 4) * 16384
-                         : vbuf + (c - 6) * 16384;
-  };
-  {  // u epilogue: row p, V / 4 columns per thread
-    const int p = quarter * 32 + lane;
-#pragma unroll 1
-    for (int c0 = cq * (V / 4); c0 < (cq + 1) * (V / 4); c0 += 16) {
-      uint32_t r[16];
-      GDP_TMEM_LD16(tmem + lane_base + 128 + c0, r);
-      tmem_wait_ld();
-      if (full) {
-        uint8_t* st = ustage(c0 >> 5) + p * 128;
-        const int u0 = (c0 & 31) >> 2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<float4*>(st + (((u0 + j) ^ (p & 7)) << 4)) =
-              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                          __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      } else if (p < n) {
-        float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      }
-    }
-    if (tid < n) a.gk[(int64_t)hv * a.Te + R0 + tid] = make_float4(sgh[tid], sgl[tid], srk[tid], 0.f);
-  }
-  if (full) {
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-      for (int c = 0; c < V / 32; ++c) tma_store_3d(&map_us, ustage(c), 32 * c, hv, (int)R0);
-      tma_store_commit();
-      tma_store_wait_read();  // shared memory stays allocated until the stores have read it
-    }
-  }
   tmem_release(tmem, kCols);
 }
 
@@ -2065,7 +2168,10 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
       cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
   const int64_t NB = block128_bound(p.B, p.T, p.N_seq, p.M);
-  wy128_tc_kernel<V><<<dim3((unsigned)NB, p.HV), 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a);
+  const int64_t items = NB * p.HV;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<int64_t>(items, sm_count());  // persistent, one CTA per SM
+  wy128_tc_kernel<V><<<grid, 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a, (int)NB);
   return cudaGetLastError();
 }
 
