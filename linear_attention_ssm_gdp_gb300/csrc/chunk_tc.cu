@@ -95,6 +95,51 @@ __device__ __forceinline__ void split_bf16_n(const float* x, bf16* hi, bf16* lo)
 // 128-byte swizzle. The chunks are visited in the order j ^ (p & 7), which is
 // the physical order 0..7, so the lanes of a warp (consecutive rows) read
 // distinct banks; four partial sums keep the additions independent.
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic, each lane rounded like the
+// scalar operation).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(f2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// 2^x by the hardware approximation (relative error ~2^-22; subnormal results
+// flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// A natural-log two-float value hi + lo in base-2 units as a two-float pair:
+// p = fl(hi log2e) and its exact product error plus lo log2e. Differences of
+// such pairs keep the cancellation of the hi parts exact, as for the natural
+// values, so 2^(difference) carries the precision of e^(difference).
+__device__ __forceinline__ float2 log2e_pair(float hi, float lo) {
+  constexpr float kLog2e = 1.44269504088896341f;
+  const float p = hi * kLog2e;
+  return make_float2(p, fmaf(lo, kLog2e, fmaf(hi, kLog2e, -p)));
+}
+
 __device__ __forceinline__ float row_sumsq(const uint8_t* row, int p) {
   float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1527,8 +1572,8 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   uint8_t* vp = sm + F_VP;
   uint8_t* vnt = sm + F_VN;
   uint8_t* pt = sm + F_P;
-  // per token, by block parity: (Gam hi, Gam lo, 1/|q|, 0)
-  float4* stok2 = reinterpret_cast<float4*>(sm + F_SM);
+  // per token, by block parity: [64] Gam hi, [64] Gam lo (base 2), [64] 1/|q|
+  float* stok2 = reinterpret_cast<float*>(sm + F_SM);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + F_SM + 2048);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -1770,13 +1815,16 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
     }
     // token t of block jb: Gam at its last copy, query norm from the staged q
     // tile (waits for that block's q tile and records)
-    auto tok_records = [&](int jb, int t, float4* dst) -> bool {
+    auto tok_records = [&](int jb, int t, float* dst) -> bool {
       bool okr = mbar_wait(&bars[FB_Q], jb & 1, status, kDevTimeout);
       okr = mbar_wait(&bars[FB_OG0 + (jb & 1)], (jb >> 1) & 1, status, kDevTimeout) && okr;
       const uint8_t* qt = sm + F_Q;
       const float ss = row_sumsq(qt + t * 128, t) + row_sumsq(qt + 8192 + t * 128, t);
       const float4 rt = reinterpret_cast<const float4*>(sm + F_OG + (jb & 1) * 2048)[2 * t + 1];
-      dst[t] = make_float4(rt.x, rt.y, f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f, 0.f);
+      const float2 g2 = log2e_pair(rt.x, rt.y);
+      dst[t] = g2.x;
+      dst[64 + t] = g2.y;
+      dst[128 + t] = f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       return okr;
     };
     const uint32_t idow = idesc_bf16(128, 2 * kHBV, true, true);
@@ -1788,7 +1836,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const int64_t T0 = (int64_t)si.x + (int64_t)j * 64;
       const uint32_t ph = j & 1;
       const float4* og = reinterpret_cast<const float4*>(sm + F_OG + (j & 1) * 2048);
-      float4* stok = stok2 + 64 * (j & 1);
+      float* stok = stok2 + 256 * (j & 1);
       ok = mbar_wait(&bars[FB_OG0 + (j & 1)], (j >> 1) & 1, status, kDevTimeout) && ok;
       if (j == 0 && otid < 64) ok = tok_records(0, otid, stok) && ok;  // later blocks: see the end
       ok = group_and(2, 256, ok);
@@ -1808,17 +1856,23 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       {  // P^T row e = row, tokens [32 cgrp, 32 cgrp + 32)
         const int e = row, s = e >> 1;
         const float4 re = og[e];
+        const float2 re2 = log2e_pair(re.x, re.y);
+        const f2 rh = pk2(re2.x, re2.x), rl = pk2(re2.y, re2.y);
         uint32_t r[32];
         GDP_TMEM_LD32(tmem + lane_base + TS + 64 * cs + 32 * cgrp, r);
         tmem_wait_ld();
         __align__(16) bf16 ph_[32];
         __align__(16) bf16 pl_[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {  // branch-free, so that the iterations interleave
+        for (int i = 0; i < 32; i += 2) {  // token pairs, branch-free so that they interleave
           const int t = 32 * cgrp + i;
-          const float4 tk = stok[t];
-          const float x = __uint_as_float(r[i]) * __expf((tk.x - re.x) + (tk.y - re.y));
-          r[i] = __float_as_uint((e < n && s <= t && t < nt) ? x : 0.f);
+          const f2 th = *reinterpret_cast<const f2*>(stok + t);
+          const f2 tl = *reinterpret_cast<const f2*>(stok + 64 + t);
+          const float2 d = upk2(add2(sub2(th, rh), sub2(tl, rl)));  // Gam_t - Gam_e, base 2
+          const float2 x = upk2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                     pk2(ex2_approx(d.x), ex2_approx(d.y))));
+          r[i] = __float_as_uint((e < n && s <= t && t < nt) ? x.x : 0.f);
+          r[i + 1] = __float_as_uint((e < n && s <= t + 1 && t + 1 < nt) ? x.y : 0.f);
         }
         split_bf16_n<32>(reinterpret_cast<const float*>(r), ph_, pl_);
 #pragma unroll
@@ -1864,8 +1918,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + 32 + cb, rq2);
         tmem_wait_ld();
         if (t < nt && ok) {
-          const float4 tk = stok[t];
-          const float qs = expf(tk.x + tk.y), rqn = tk.z;  // o = scale |q|^-1 (e^Gam Qh + O)
+          const float qs = ex2_approx(stok[t] + stok[64 + t]), rqn = stok[128 + t];  // o = scale |q|^-1 (e^Gam Qh + O)
           float4* dst = reinterpret_cast<float4*>(f.o + ((T0 + t) * HVn + hv) * V + v0 + cb);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -1881,7 +1934,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         }
       }
       if (quarter >= 2 && cgrp == 0 && j + 1 < nb)  // idle in the epilogue: next block's records
-        ok = tok_records(j + 1, otid - 64, stok2 + 64 * ((j + 1) & 1)) && ok;
+        ok = tok_records(j + 1, otid - 64, stok2 + 256 * ((j + 1) & 1)) && ok;
       tc_fence_before();
       ok = group_and(2, 256, ok);
       if (!ok) break;
