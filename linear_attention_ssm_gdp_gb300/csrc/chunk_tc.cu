@@ -740,7 +740,7 @@ constexpr int W8_V = 32768;
 constexpr int W8_T = 65536;
 constexpr int W8_LA = W8_T + 65536;
 constexpr int W8_S = W8_LA + 128 * 129 * 4;
-constexpr int W8_SMEM = W8_S + 2 * 5 * 128 * 4 + 64 + 1024;
+constexpr int W8_SMEM = W8_S + 2 * 7 * 128 * 4 + 64 + 1024;
 
 // Top merge of the 128x128 inverse on the tensor cores: X = L10 A00, then
 // A10 = -A11 X, each as x_hi [y_hi | y_lo] (one N = 128 MMA per k-step) plus
@@ -937,9 +937,11 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   uint8_t* tiles = sm + W8_T;
   float* LA = reinterpret_cast<float*>(sm + W8_LA);
   float* scratch = reinterpret_cast<float*>(tiles);
-  float* sarr = reinterpret_cast<float*>(sm + W8_S);  // [2][5][128], by item parity
+  // [2][7][128] by item parity: beta, Gam hi, Gam lo, 1/|k|, column scale,
+  // Gam hi and lo in base 2
+  float* sarr = reinterpret_cast<float*>(sm + W8_S);
   // [0] k, [1] mma, [2] v round, [3] solve MMAs, [4] v
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sarr + 2 * 5 * 128);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sarr + 2 * 7 * 128);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
   constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
   auto issue_k = [&](const Item& x) {
@@ -976,12 +978,14 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   bool ok = true;
   for (int c = 0;; ++c) {
     const int par = c & 1;
-    float* sb = sarr + par * 640;
+    float* sb = sarr + par * 896;
     float* sgh = sb + 128;
     float* sgl = sgh + 128;
     float* srk = sgl + 128;
     float* sco = srk + 128;
-    float* nsb = sarr + (par ^ 1) * 640;  // the next item's beta and decay
+    float* s2h = sco + 128;
+    float* s2l = s2h + 128;
+    float* nsb = sarr + (par ^ 1) * 896;  // the next item's beta and decay
     const int nx = next_valid(it);
     const bool has_next = nx < n_items;
     const Item y = has_next ? item(nx) : x;
@@ -1010,6 +1014,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       srk[tid] = r;
       sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
+      const float2 g2 = log2e_pair(sgh[tid], sgl[tid]);
+      s2h[tid] = g2.x;
+      s2l[tid] = g2.y;
     }
     fence_async_smem();  // the k buffer's generic reads end before the next k load
     if (kPipe && tid == 0) tma_store_wait_read();  // the previous item's stores have read LA, tiles
@@ -1028,12 +1035,18 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         uint32_t r[32];
         GDP_TMEM_LD32(tmem + lane_base + c0, r);
         tmem_wait_ld();
-        const float gph = sgh[p], gpl = sgl[p];
+        const f2 ph2 = pk2(s2h[p], s2h[p]), pl2 = pk2(s2l[p], s2l[p]), bp2 = pk2(bp, bp);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
+        for (int j = 0; j < 32; j += 2) {  // column pairs, branch-free so that they interleave
           const int i = c0 + j;
-          const float v = bp * __expf((gph - sgh[i]) + (gpl - sgl[i])) * srk[i] * __uint_as_float(r[j]);
-          LA[p * 129 + i] = (i < p) ? v : 0.f;
+          const f2 ih = *reinterpret_cast<const f2*>(s2h + i);
+          const f2 il = *reinterpret_cast<const f2*>(s2l + i);
+          const f2 rk = *reinterpret_cast<const f2*>(srk + i);
+          const float2 d = upk2(add2(sub2(ph2, ih), sub2(pl2, il)));  // Gam_p - Gam_i, base 2
+          const float2 v = upk2(mul2(mul2(bp2, pk2(ex2_approx(d.x), ex2_approx(d.y))),
+                                     mul2(rk, pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])))));
+          LA[p * 129 + i] = (i < p) ? v.x : 0.f;
+          LA[p * 129 + i + 1] = (i + 1 < p) ? v.y : 0.f;
         }
       }
     }
