@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of each kernel at the bench workload, from
 # one ncu capture of the committed profiling command (profiles/ncu_prefill_b2t4096_kernels.md).
 # A kernel's entry is removed whenever the kernel changes after the capture.
-TRAFFIC = {"prepare": 283.0e6}
+TRAFFIC = {"wy": 352.1e6, "scan_out": 430.9e6, "prepare": 283.0e6}
 
 
 def peaks():
