@@ -37,6 +37,7 @@ CASES = [
     (1, 100, 2, 2, 64, 64, 4, 64, torch.float16, True, True, False),
     (1, 300, 2, 2, 128, 128, 2, 64, torch.bfloat16, True, True, True),
     (1, 260, 2, 4, 128, 256, 2, 64, torch.bfloat16, True, True, False),
+    (2, 330, 2, 2, 128, 64, 2, 64, torch.bfloat16, True, True, True),  # tensor-core path, V = 64
     (1, 131, 2, 2, 128, 128, 3, 64, torch.bfloat16, False, True, False),
     (1, 65, 1, 1, 256, 64, 1, 64, torch.float32, True, True, False),
 ]
@@ -55,7 +56,7 @@ def test_chunk_fwd_matches_walk(gdp, case):
     assert rel_err(fs, rfs) <= tol, rel_err(fs, rfs)
 
 
-@pytest.mark.parametrize("K,V,M", [(32, 32, 2), (128, 128, 2), (128, 128, 3)])
+@pytest.mark.parametrize("K,V,M", [(32, 32, 2), (128, 128, 2), (128, 128, 3), (128, 64, 2)])
 def test_varlen_with_ragged_and_empty_sequences(gdp, K, V, M):
     lens = [1, 63, 64, 65, 130, 0, 7, 200]
     cu = si.cu_seqlens_of(lens)
