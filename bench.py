@@ -49,9 +49,10 @@ HOST_LEAD_CYCLES = 2_000_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-# DRAM bytes (read + write) per launch of each kernel at the bench workload, from
-# one ncu capture of the committed profiling command (profiles/ncu_prefill_b2t4096_kernels.md).
-# A kernel's entry is removed whenever the kernel changes after the capture.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# kernel at the bench workload, from one `ncu --set full` capture of
+# `bench.py --only prefill --steps 2 --warmup 3`. A kernel's entry is removed
+# whenever the kernel changes after the capture.
 TRAFFIC = {"wy": 352.1e6, "scan_out": 430.9e6, "prepare": 283.0e6}
 
 
@@ -65,7 +66,8 @@ def peaks():
 
 
 # ----------------------------------------------------------------------------------
-# algorithmic work (per step), stated in the design doc
+# algorithmic work (per step): each kernel's own inputs and outputs at their
+# stored widths, and the flops of the fused chunk algebra
 # ----------------------------------------------------------------------------------
 
 def algorithmic(w=WORKLOAD):
