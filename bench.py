@@ -316,6 +316,7 @@ def run_ours(args, rank, world, dev):
     full = args.only == "all"
     e2e = run_e2e(args, gdp, d, dev, pf) if full else None
     decode = run_decode(args, gdp, dev, pk) if full else None
+    prep_eager = run_prepare_eager(args, gdp, dev) if full else None
     clocks = sampler.summary()
     w = WORKLOAD
     line = {
@@ -338,6 +339,7 @@ def run_ours(args, rank, world, dev):
                     "hbm_frac": kern["prepare"]["frac"]},
         "kernels": kern,
         "decode": decode,
+        "prepare_vs_eager": prep_eager,
         "e2e": e2e,
         "gpu_launches": launches_per_step(pf.fused) * args.steps,
         "clocks": clocks,
@@ -347,6 +349,72 @@ def run_ours(args, rank, world, dev):
         line["cpu_baseline"] = cpu_baseline(d, min_seconds=args.cpu_seconds,
                                             max_seconds=max(30.0, args.cpu_seconds))
     return line
+
+
+def eager_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, decode):
+    """The prepare step as the pages' eager PyTorch composition (the comparator
+    the fused prepare kernel replaces): the value/key/query splits, the group
+    expansion and the copy folding as torch copies, the gates as fp32 torch
+    ops. Same outputs, bit for bit, as gdp_{prefill,decode}_prepare."""
+    import torch.nn.functional as F
+    n, T = x.shape[:2]
+    hpg = H // G
+    kb, qb = M * H * P, M * H * P + M * G * N
+    v = x[..., :kb].reshape(n, T, M, H, P).reshape(n, T * M, H, P)
+    k = x[..., kb:qb].reshape(n, T, M, G, N).repeat_interleave(hpg, dim=3).reshape(n, T * M, H, N)
+    qx = x[..., qb:].reshape(n, T, G, N).repeat_interleave(hpg, dim=2)
+    beta = torch.sigmoid(ba[..., :M * H].float().reshape(n, T * M, H))
+    gt = -torch.exp(A_log.float()) * F.softplus(ba[..., M * H:].float() + dt_bias.float())
+    if decode:
+        q = torch.zeros(n, T, M, H, N, dtype=x.dtype, device=x.device)
+        q[:, :, M - 1] = qx
+        g = torch.zeros(n, T, M, H, dtype=torch.float32, device=x.device)
+        g[:, :, 0] = gt
+        return q.reshape(n, T * M, H, N), k, v, beta, g.reshape(n, T * M, H)
+    return qx.contiguous(), k, v, beta, gt
+
+
+def run_prepare_eager(args, gdp, dev):
+    """The fused prepare kernel against the eager composition, both timed with
+    CUDA events after an L2 flush, on the prefill and the decode workloads."""
+    import synth_inputs as si
+    flush = L2Flush(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    out = {}
+    for name, decode in (("prefill", False), ("decode", True)):
+        if decode:
+            w = DECODE
+            n, S, M, H, G, P, N = w["n"], w["S"], w["M"], w["H"], w["G"], w["P"], w["N"]
+            d = si.prepare_inputs(n, S, M, H, G, P, N, seed=1)
+        else:
+            w = WORKLOAD
+            M, H, G, P, N = w["M"], w["H"], w["G"], w["V"], w["K"]
+            d = make_inputs(dev)
+        x, ba = d["x"].to(dev), d["ba"].to(dev)
+        A_log, dt_bias = d["A_log"].to(dev), d["dt_bias"].to(dev)
+        fused = gdp.gdp_decode_prepare if decode else gdp.gdp_prefill_prepare
+        ref = eager_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, decode)
+        got = fused(x, ba, A_log, dt_bias, M, H, G, P, N)
+        exact = all(torch.equal(a, b) for a, b in zip(got, ref))
+        times = {}
+        for label, fn in (("fused", lambda: fused(x, ba, A_log, dt_bias, M, H, G, P, N, out=got)),
+                          ("eager", lambda: eager_prepare(x, ba, A_log, dt_bias, M, H, G, P, N,
+                                                          decode))):
+            for _ in range(3):
+                fn()
+            t = []
+            for _ in range(max(5, min(args.steps, 20))):
+                flush()
+                torch.cuda._sleep(HOST_LEAD_CYCLES)
+                ev[0].record()
+                fn()
+                ev[1].record()
+                torch.cuda.synchronize()
+                t.append(ev[0].elapsed_time(ev[1]))
+            times[label] = statistics.mean(t) * 1e3
+        out[name] = {"fused_us": times["fused"], "eager_us": times["eager"],
+                     "eager_over_fused": times["eager"] / times["fused"], "bit_exact": exact}
+    return out
 
 
 def run_e2e(args, gdp, d, dev, pf):
