@@ -127,7 +127,10 @@ size_t gdp_chunk_fwd_workspace_size(int B, int T, int N_seq, int H, int HV, int 
  *   cu_seqlens [N_seq + 1] int32 token offsets on the unexpanded stream, or
  *   NULL (then N_seq must equal B). With cu_seqlens, B must be 1, offsets must
  *   be non-decreasing with cu_seqlens[0] = 0 and cu_seqlens[N_seq] <= T; they
- *   are read on the device only (no host synchronisation).
+ *   are read on the device only (no host synchronisation). A list that breaks
+ *   these rules sets the workspace status word (gdp_read_status then returns
+ *   GDP_ERR_INVALID_ARG); o is left untouched and final_state receives each
+ *   sequence's initial state (zeros without one).
  *   chunk_size: 16, 32 or 64. scale: score scale (the pages' default is
  *   K^-0.5; the caller passes it). use_qk_l2norm: 1 to L2-normalise q and k
  *   per (position, head) as x / sqrt(sum x^2 + 1e-6) before use.
@@ -217,7 +220,12 @@ gdp_status gdp_chunk_fwd_stage_offsets(int B, int T, int N_seq, int H, int HV, i
  * call clears what must start at zero. Calls that overlap on the GPU (other
  * streams or host threads) race on the array: serialise them.
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.
+ * device current and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not reset the device
+ * (cudaDeviceReset) between calls, which would leave the kept address stale.
+ * cu_seqlens is validated on the device as in gdp_chunk_fwd; a bad list
+ * leaves o untouched and passes the initial states to final_state, but this
+ * call has no workspace whose status word the caller could read.
  */
 gdp_status gdp_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* beta,
                                  const float* g, const float* initial_state,

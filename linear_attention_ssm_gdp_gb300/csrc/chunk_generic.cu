@@ -93,6 +93,11 @@ __global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M,
     if (bad) atomicExch(status, kDevBadSeqlens);
   }
   __syncthreads();
+  // A bad list leaves every sequence with a zero-length record: the state
+  // kernels, which launch one CTA row per sequence, then read no input rows,
+  // write no output rows and only pass the initial state through.
+  if (s_bad)
+    for (int i = threadIdx.x; i < N_seq; i += blockDim.x) seq_info[i] = make_int4(0, 0, 0, 0);
   const int ne = s_ne, nt = s_nt;
   if (!s_bad) {
     for (int i = 0; i < N_seq; ++i) {

@@ -15,10 +15,14 @@
 // The array lives for the lifetime of the process on every GPU that loads the
 // library (kNoallocScratchBytes of device memory each). All calls share it and
 // it keeps the previous call's contents; the status word at its start is
-// cleared by every call, and everything else the kernels read is rewritten
-// before it is read. Calls that overlap on the GPU (on different streams, or
-// from different host threads) race on the array and must be serialised by
-// the caller.
+// cleared by every call, and the chunk tables (per-sequence records included,
+// which a bad cu_seqlens list sets to zero length) are rewritten before any
+// kernel reads them, so nothing a call reads depends on an earlier call.
+// Calls that overlap on the GPU (on different streams, or from different host
+// threads) race on the array and must be serialised by the caller.
+//
+// The device address is looked up once per device and kept; a cudaDeviceReset
+// between calls would leave it stale (the header says so).
 #include <mutex>
 
 #include "gdp_internal.cuh"
