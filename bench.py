@@ -66,50 +66,70 @@ def peaks():
 
 
 # ----------------------------------------------------------------------------------
-# algorithmic work (per step): each kernel's own inputs and outputs at their
-# stored widths, and the flops of the fused chunk algebra
+# algorithmic work: the method's own tensors and flops, never the intermediates of
+# this design (w, u, decay records, v_new or chunk states that kernels hand to each
+# other)
 # ----------------------------------------------------------------------------------
 
-def algorithmic(w=WORKLOAD):
-    """Algorithmic work per step. Flops follow the chunked method at chunk BT (one
-    multiply-add = 2 flops); bytes are each kernel's own inputs and outputs at their
-    stored widths (bf16 q/k/v, fp32 gates, w as a bf16 hi/lo pair = 4 B, fp32 u,
-    16-byte per-position decay records, fp32 o and state)."""
-    B, T, H, HV, G, K, V, M, BT = (w[k] for k in ("B", "T", "H", "HV", "G", "K", "V", "M", "BT"))
-    E = B * T * M          # expanded positions
-    Tt = B * T             # tokens
-    D = M * H * V + M * G * K + G * K
-    prep_bytes = (Tt * D * 2 + Tt * (M * H + H) * 2                # x, ba read
-                  + Tt * H * K * 2 + E * H * K * 2 + E * H * V * 2  # q, k, v written
-                  + E * H * 4 + Tt * H * 4)                         # beta, g written
-    # whole chunked forward, fused floor: q, k, v, beta, g in; o, final state out
-    chunk_bytes = (Tt * H * K * 2 + E * H * K * 2 + E * HV * V * 2 + E * HV * 4
-                   + Tt * HV * 4 + Tt * HV * V * 4 + B * HV * K * V * 4)
+def method_work(Tt, N_seq, H, HV, K, V, M, BT, fused):
+    """Algorithmic flops and bytes of one chunked forward over Tt tokens (all
+    sequences) in N_seq sequences, apportioned to the kernels.
+
+    Bytes are the fused floor of the method: q, k, v (bf16), beta, g (fp32) read,
+    o (fp32) and the final state (fp32) written. A kernel is charged the method
+    tensors it reads or writes: WY reads k, v, beta, g; the state scan reads k, g
+    and writes the state; the output reads q, k, g and writes o (the fused scan +
+    output does both). Flops: the chunked algebra at chunk BT per expanded token
+    and value head, 2 BT (2K + V) for the transition block, its inverse and w, u;
+    4 K V for the state recurrence; 2 BT (K + V) + 2 K V / M for the output (one
+    multiply-add = 2 flops; the hi/lo operand passes of this design are not
+    counted)."""
+    E = Tt * M
+    b_q, b_k, b_v = Tt * H * K * 2, E * H * K * 2, E * HV * V * 2
+    b_beta, b_g = E * HV * 4, Tt * HV * 4
+    b_o, b_state = Tt * HV * V * 4, N_seq * HV * K * V * 4
     f_wy = E * HV * 2 * BT * (2 * K + V)
     f_h = E * HV * 4 * K * V
     f_o = E * HV * (2 * BT * (K + V) + 2 * K * V / M)
-    b_wy = (E * H * K * 2 + E * HV * V * 2 + E * HV * 4 + Tt * HV * 4
-            + E * HV * K * 4 + E * HV * V * 4 + E * HV * 16)
-    b_scan_in = E * HV * K * 4 + E * HV * V * 4 + E * H * K * 2 + E * HV * 16
-    b_state = B * HV * K * V * 4
-    NTc = -(-T // BT) * B
-    b_h = b_scan_in + b_state + E * HV * V * 4 + NTc * HV * K * V * 4   # + v_new, h out
-    b_o = Tt * H * K * 2 + E * H * K * 2 + E * HV * V * 4 + NTc * HV * K * V * 4 + Tt * HV * V * 4
-    b_ho = b_scan_in + b_state + Tt * H * K * 2 + Tt * HV * V * 4
-    return {"E": E, "prepare_bytes": prep_bytes, "chunk_bytes": chunk_bytes,
-            "flops": {"wy": f_wy, "h": f_h, "o": f_o, "scan_out": f_h + f_o,
-                      "chunk": f_wy + f_h + f_o},
-            "bytes": {"wy": b_wy, "h": b_h, "o": b_o, "scan_out": b_ho}}
+    out = {"E": E,
+           "chunk_bytes": b_q + b_k + b_v + b_beta + b_g + b_o + b_state,
+           "flops": {"wy": f_wy, "h": f_h, "o": f_o, "scan_out": f_h + f_o,
+                     "chunk": f_wy + f_h + f_o},
+           "bytes": {"wy": b_k + b_v + b_beta + b_g,
+                     "h": b_k + b_g + b_state,
+                     "o": b_q + b_k + b_g + b_o,
+                     "scan_out": b_q + b_k + b_g + b_o + b_state}}
+    out["kernels"] = ("wy", "scan_out") if fused else ("wy", "h", "o")
+    return out
+
+
+def prepare_bytes(n, T, M, H, G, P, N, decode):
+    """Bytes the prepare map moves: x and ba read; q, k, v, beta, g written."""
+    rows = n * T
+    D = M * H * P + M * G * N + G * N
+    L = T * M
+    qrows = L if decode else T
+    return (rows * D * 2 + rows * (M * H + H) * 2 + n * qrows * H * N * 2 + n * L * H * N * 2
+            + n * L * H * P * 2 + n * L * H * 4 + n * (L if decode else T) * H * 4)
+
+
+def algorithmic(w=WORKLOAD):
+    """Algorithmic work per step of the headline prefill workload."""
+    B, T, H, HV, G, K, V, M, BT = (w[k] for k in ("B", "T", "H", "HV", "G", "K", "V", "M", "BT"))
+    out = method_work(B * T, B, H, HV, K, V, M, BT, fused=(M == 2))
+    out["prepare_bytes"] = prepare_bytes(B, T, M, H, G, V, K, False)
+    return out
 
 
 def roof_entry(ms, flops, nbytes, tc, hbm):
-    """Achieved rates of one kernel and its binding roofline (the larger of the
-    tensor-core time and the HBM time at the measured peaks)."""
+    """Achieved rates of one kernel against its algorithmic work and its binding
+    roofline (the larger of the tensor-core time and the HBM time at the peaks)."""
     sec = ms * 1e-3
     tf = flops / sec / 1e12
     gbs = nbytes / sec / 1e9
     bound = "tensor" if flops / (tc * 1e12) >= nbytes / (hbm * 1e9) else "hbm"
     return {"ms": ms, "TFLOPs": tf, "tc_frac": tf / tc, "GBps": gbs, "hbm_frac": gbs / hbm,
+            "alg_bytes": nbytes, "alg_flops": flops,
             "bound": bound, "frac": tf / tc if bound == "tensor" else gbs / hbm}
 
 
@@ -232,6 +252,33 @@ def kernel_names(pf) -> tuple:
     return ("wy", "scan_out") if pf.fused else ("wy", "h", "o")
 
 
+def kernel_rooflines(times, alg, tc, hbm, fused):
+    """Per-kernel roof entries from the stage-event times of a chunked forward."""
+    stage_ms = {"wy": statistics.mean(times["wy"]), "h": statistics.mean(times["h"]),
+                "o": statistics.mean(times["o"])}
+    if fused:  # stage events 3 and 4 are recorded back to back
+        stage_ms = {"wy": stage_ms["wy"], "scan_out": stage_ms["h"] + stage_ms["o"]}
+    kern = {n: roof_entry(stage_ms[n], alg["flops"][n], alg["bytes"][n], tc, hbm)
+            for n in alg["kernels"]}
+    kern["tables"] = {"ms": statistics.mean(times["tables"])}
+    return kern
+
+
+def roofline_object(name, k, tc, hbm, pk_src, traffic):
+    """The bench line's roofline object for kernel `name` (entry `k`)."""
+    if k["bound"] == "hbm":
+        roof = {"kernel": name, "bound": "hbm", "achieved": k["GBps"], "peak": hbm,
+                "unit": "GB/s", "frac": k["hbm_frac"], "peak_source": pk_src + " (hbm_gbs)"}
+    else:
+        roof = {"kernel": name, "bound": "tensor", "achieved": k["TFLOPs"], "peak": tc,
+                "unit": "TFLOP/s", "frac": k["tc_frac"],
+                "peak_source": pk_src + " (bf16_tflops, burst)"}
+    roof["algorithmic_bytes"] = k["alg_bytes"]
+    roof["traffic"] = traffic
+    roof["traffic_over_algorithmic"] = None if traffic is None else traffic / k["alg_bytes"]
+    return roof
+
+
 def run_ours(args, rank, world, dev):
     import linear_attention_ssm_gdp_gb300 as gdp
     gdp.load()
@@ -285,38 +332,26 @@ def run_ours(args, rank, world, dev):
     units = alg["E"] * world
     value = units / (ms * 1e-3)
 
-    # per-kernel rooflines
-    kern = {}
+    # per-kernel rooflines against the method's algorithmic work; the step is
+    # well under a millisecond, so the tensor peak is the measured burst figure
     hbm = pk["hbm_gbs"]
-    tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    tc = pk["bf16_tflops"]
+    kern = kernel_rooflines(times, alg, tc, hbm, pf.fused)
     prep_ms = statistics.mean(times["prepare"])
     kern["prepare"] = roof_entry(prep_ms, 0, alg["prepare_bytes"], tc, hbm)
-    stage_ms = {"wy": statistics.mean(times["wy"]), "h": statistics.mean(times["h"]),
-                "o": statistics.mean(times["o"])}
-    if pf.fused:  # stage events 3 and 4 are recorded back to back
-        stage_ms = {"wy": stage_ms["wy"], "scan_out": stage_ms["h"] + stage_ms["o"]}
-    for name in kernel_names(pf):
-        kern[name] = roof_entry(stage_ms[name], alg["flops"][name], alg["bytes"][name], tc, hbm)
-    kern["tables"] = {"ms": statistics.mean(times["tables"])}
-    chunk_ms = kern["tables"]["ms"] + sum(kern[n]["ms"] for n in kernel_names(pf))
+    chunk_ms = kern["tables"]["ms"] + sum(kern[n]["ms"] for n in alg["kernels"])
     chunk_tf = alg["flops"]["chunk"] / (chunk_ms * 1e-3) / 1e12
     chunk_gbs = alg["chunk_bytes"] / (chunk_ms * 1e-3) / 1e9
-    dominant = max(("prepare",) + kernel_names(pf), key=lambda n: kern[n]["ms"])
-    dk = kern[dominant]
-    if dk["bound"] == "hbm":
-        roof = {"kernel": dominant, "bound": "hbm", "achieved": dk["GBps"], "peak": hbm,
-                "unit": "GB/s", "frac": dk["hbm_frac"], "traffic": None,
-                "peak_source": pk_src + " (hbm_gbs)"}
-    else:
-        roof = {"kernel": dominant, "bound": "tensor", "achieved": dk["TFLOPs"], "peak": tc,
-                "unit": "TFLOP/s", "frac": dk["tc_frac"], "traffic": None,
-                "peak_source": pk_src + " (bf16_tflops_sustained)"}
-    roof["traffic"] = TRAFFIC.get(dominant) if args.traffic is None else args.traffic
+    dominant = max(("prepare",) + alg["kernels"], key=lambda n: kern[n]["ms"])
+    traffic = TRAFFIC.get(dominant) if args.traffic is None else args.traffic
+    roof = roofline_object(dominant, kern[dominant], tc, hbm, pk_src, traffic)
 
     full = args.only == "all"
     e2e = run_e2e(args, gdp, d, dev, pf) if full else None
     decode = run_decode(args, gdp, dev, pk) if full else None
     prep_eager = run_prepare_eager(args, gdp, dev) if full else None
+    varlen = run_varlen(args, gdp, dev, pk, pk_src) if full else None
+    gva = run_gva(args, gdp, dev, pk, pk_src) if full else None
     clocks = sampler.summary()
     w = WORKLOAD
     line = {
@@ -340,10 +375,13 @@ def run_ours(args, rank, world, dev):
         "kernels": kern,
         "decode": decode,
         "prepare_vs_eager": prep_eager,
+        "config2_varlen": varlen,
+        "config3_gva": gva,
         "e2e": e2e,
         "gpu_launches": launches_per_step(pf.fused) * args.steps,
         "clocks": clocks,
-        "peaks": {"hbm_gbs": hbm, "bf16_tflops_sustained": tc, "source": pk_src},
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": pk_src,
+                  "note": "burst tensor peak: every timed step is under a few ms"},
     }
     if rank == 0 and full and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, min_seconds=args.cpu_seconds,
@@ -525,6 +563,146 @@ def run_decode(args, gdp, dev, pk):
 
 
 # ----------------------------------------------------------------------------------
+# the other prefill workloads: measured in the same run, reported beside the headline
+# ----------------------------------------------------------------------------------
+
+def _time_chunk_steps(gdp, step, stage, flush, steps, warmup, prep_ev=None):
+    """Times `step()` (one pass of the workload) with CUDA events after an L2 flush;
+    returns per-step, prepare and stage times (ms) as lists."""
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    times = {"step": [], "prepare": [], "tables": [], "wy": [], "h": [], "o": []}
+    for _ in range(steps):
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        step_ev[0].record()
+        step()
+        step_ev[1].record()
+        torch.cuda.synchronize()
+        times["step"].append(step_ev[0].elapsed_time(step_ev[1]))
+        if prep_ev is not None:
+            times["prepare"].append(prep_ev[0].elapsed_time(prep_ev[1]))
+        times["tables"].append(stage[0].elapsed_time(stage[1]))
+        times["wy"].append(stage[1].elapsed_time(stage[2]))
+        times["h"].append(stage[2].elapsed_time(stage[3]))
+        times["o"].append(stage[3].elapsed_time(stage[4]))
+    return times
+
+
+def _workload_summary(name, times, alg, tc, hbm, pk_src, fused, prep_bytes=None):
+    ms = statistics.mean(times["step"])
+    kern = kernel_rooflines(times, alg, tc, hbm, fused)
+    chunk_ms = kern["tables"]["ms"] + sum(kern[n]["ms"] for n in alg["kernels"])
+    out = {"workload": name, "ms_per_step": ms, "value": alg["E"] / (ms * 1e-3),
+           "unit": "expanded tokens/s", "kernels": kern,
+           "chunk": {"ms": chunk_ms,
+                     "TFLOPs": alg["flops"]["chunk"] / (chunk_ms * 1e-3) / 1e12,
+                     "GBps_fused_floor": alg["chunk_bytes"] / (chunk_ms * 1e-3) / 1e9,
+                     "hbm_frac": alg["chunk_bytes"] / (chunk_ms * 1e-3) / 1e9 / hbm,
+                     "tc_frac": alg["flops"]["chunk"] / (chunk_ms * 1e-3) / 1e12 / tc}}
+    names = alg["kernels"]
+    if prep_bytes is not None:
+        pm = statistics.mean(times["prepare"])
+        kern["prepare"] = roof_entry(pm, 0, prep_bytes, tc, hbm)
+        out["prepare"] = {"us": pm * 1e3, "bytes": prep_bytes, "GBps": kern["prepare"]["GBps"],
+                          "hbm_frac": kern["prepare"]["hbm_frac"]}
+        names = ("prepare",) + names
+    dom = max(names, key=lambda n: kern[n]["ms"])
+    out["binding"] = roofline_object(dom, kern[dom], tc, hbm, pk_src, None)
+    return out
+
+
+def run_varlen(args, gdp, dev, pk, pk_src):
+    """Packed varlen prefill from prepare: 16 requests, lengths ~U(64, 2048) (seed 0),
+    H=HV=32, G=8, P=N=128, M=3, chunk 64; a step is gdp_prefill_prepare on x
+    [1, T, M*H*P + M*G*N + G*N] followed by gdp_chunk_fwd with cu_seqlens."""
+    import synth_inputs as si
+    w = si.WORKLOADS["varlen_bf16"].dims
+    M, H, G, P, N, BT = w["M"], w["H"], w["G"], w["P"], w["N"], w["BT"]
+    lens = si.varlen_lengths(w["n_seq"], seed=0)
+    cu = si.cu_seqlens_of(lens).to(dev)
+    T = int(cu[-1])
+    d = si.prepare_inputs(1, T, M, H, G, P, N, seed=0)
+    x, ba = d["x"].to(dev), d["ba"].to(dev)
+    A_log, dt_bias = d["A_log"].to(dev), d["dt_bias"].to(dev)
+    bf = torch.bfloat16
+    pre = (torch.empty(1, T, H, N, dtype=bf, device=dev),
+           torch.empty(1, T * M, H, N, dtype=bf, device=dev),
+           torch.empty(1, T * M, H, P, dtype=bf, device=dev),
+           torch.empty(1, T * M, H, dtype=torch.float32, device=dev),
+           torch.empty(1, T, H, dtype=torch.float32, device=dev))
+    nseq = len(lens)
+    o = torch.empty(1, T, H, P, dtype=torch.float32, device=dev)
+    fs = torch.empty(nseq, H, N, P, dtype=torch.float32, device=dev)
+    ws = torch.empty(gdp.gdp_chunk_fwd_workspace_size(1, T, nseq, H, H, N, P, M, BT, bf),
+                     dtype=torch.uint8, device=dev)
+    off = gdp.gdp_chunk_fwd_stage_offsets(1, T, nseq, H, H, N, P, M, BT, bf)
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(gdp.GDP_STAGE_EVENTS)]
+    prep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def step():
+        prep_ev[0].record()
+        gdp.gdp_prefill_prepare(x, ba, A_log, dt_bias, M, H, G, P, N, out=pre)
+        prep_ev[1].record()
+        q, k, v, beta, g = pre
+        gdp.gdp_chunk_fwd(q, k, v, beta, g, cu_seqlens=cu, chunk_size=BT, num_householder=M,
+                          use_qk_l2norm=True, workspace=ws, out=(o, fs))
+
+    gdp.gdp_set_stage_events(stage)
+    times = _time_chunk_steps(gdp, step, stage, L2Flush(dev), max(3, min(args.steps, 10)), 3,
+                              prep_ev)
+    gdp.gdp_set_stage_events(None)
+    fused = off[7] == 1
+    alg = method_work(T, nseq, H, H, N, P, M, BT, fused)
+    out = _workload_summary(
+        f"varlen bf16 {nseq} requests U(64,2048) T={T} H=HV=32 G8 K=V=128 M3 BT64 "
+        "(prepare + chunk_fwd with cu_seqlens)", times, alg, pk["bf16_tflops"], pk["hbm_gbs"],
+        pk_src, fused, prepare_bytes(1, T, M, H, G, P, N, False))
+    out["tokens"] = T
+    return out
+
+
+def run_gva(args, gdp, dev, pk, pk_src):
+    """GVA prefill: B=4, T=8192, H=8, HV=32, K=128, V=256, M=2, chunk 64; a step is
+    gdp_chunk_fwd on q, k, v, beta, g already in HBM. Inputs are drawn on the device
+    (seeded): q, k, v ~ N(0,1) bf16; beta = sigmoid(N(0,1)); g = -exp(A_log)
+    softplus(N(0,1) + dt_bias) with A_log ~ U(0, ln 16), dt_bias ~ N(0, 0.5^2)."""
+    import torch.nn.functional as F
+    B, T, H, HV, K, V, M, BT = 4, 8192, 8, 32, 128, 256, 2, 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    bf = torch.bfloat16
+    q = torch.randn(B, T, H, K, device=dev, generator=gen).to(bf)
+    k = torch.randn(B, T * M, H, K, device=dev, generator=gen).to(bf)
+    v = torch.randn(B, T * M, HV, V, device=dev, generator=gen).to(bf)
+    beta = torch.sigmoid(torch.randn(B, T * M, HV, device=dev, generator=gen))
+    A_log = torch.rand(HV, device=dev, generator=gen) * math.log(16.0)
+    dt_bias = torch.randn(HV, device=dev, generator=gen) * 0.5
+    g = -torch.exp(A_log) * F.softplus(torch.randn(B, T, HV, device=dev, generator=gen) + dt_bias)
+    o = torch.empty(B, T, HV, V, dtype=torch.float32, device=dev)
+    fs = torch.empty(B, HV, K, V, dtype=torch.float32, device=dev)
+    ws = torch.empty(gdp.gdp_chunk_fwd_workspace_size(B, T, B, H, HV, K, V, M, BT, bf),
+                     dtype=torch.uint8, device=dev)
+    off = gdp.gdp_chunk_fwd_stage_offsets(B, T, B, H, HV, K, V, M, BT, bf)
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(gdp.GDP_STAGE_EVENTS)]
+
+    def step():
+        gdp.gdp_chunk_fwd(q, k, v, beta, g, chunk_size=BT, num_householder=M,
+                          use_qk_l2norm=True, workspace=ws, out=(o, fs))
+
+    gdp.gdp_set_stage_events(stage)
+    times = _time_chunk_steps(gdp, step, stage, L2Flush(dev), max(3, min(args.steps, 6)), 3)
+    gdp.gdp_set_stage_events(None)
+    fused = off[7] == 1
+    alg = method_work(B * T, B, H, HV, K, V, M, BT, fused)
+    return _workload_summary("GVA bf16 B4 T8192 H8 HV32 K128 V256 M2 BT64 (chunk_fwd)", times,
+                             alg, pk["bf16_tflops"], pk["hbm_gbs"], pk_src, fused)
+
+
+# ----------------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ----------------------------------------------------------------------------------
 
@@ -638,9 +816,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per launch of the dominant kernel, if measured")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+    ap.add_argument("--only", default="all",
+                    choices=["all", "prefill", "decode", "varlen", "gva"],
                     help="profiling runs: time only the prefill step (no e2e, decode or CPU "
-                         "baseline) or only the decode step")
+                         "baseline), only the decode step, or only the varlen / GVA workload")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -656,10 +835,16 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    if args.only == "decode":
+    if args.only in ("decode", "varlen", "gva"):
         import linear_attention_ssm_gdp_gb300 as gdp
         gdp.load()
-        line = {"decode": run_decode(args, gdp, dev, peaks()[0])}
+        pk, pk_src = peaks()
+        if args.only == "decode":
+            line = {"decode": run_decode(args, gdp, dev, pk)}
+        elif args.only == "varlen":
+            line = {"config2_varlen": run_varlen(args, gdp, dev, pk, pk_src)}
+        else:
+            line = {"config3_gva": run_gva(args, gdp, dev, pk, pk_src)}
     else:
         line = run_ours(args, rank, world, dev)
     if rank == 0:
