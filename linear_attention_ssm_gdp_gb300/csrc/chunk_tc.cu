@@ -74,6 +74,58 @@ __device__ __forceinline__ void comp_prefix(float* hi, float* lo, int n) {
   }
 }
 
+// Error-free sum (Knuth's TwoSum): a + b = s + e exactly.
+__device__ __forceinline__ float two_sum(float a, float b, float& e) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return s;
+}
+
+// Compensated inclusive prefix sum of 128 values by one warp: lane l owns
+// positions 4l .. 4l + 3 (hi[] holds the summands on entry). Each lane sums its
+// four values with running TwoSum corrections, the lane totals are scanned
+// across the warp as (sum, correction) pairs combined by TwoSum, and each
+// lane re-adds its exclusive prefix. hi[p] + lo[p] carries the prefix to about
+// twice fp32 precision, like the serial Neumaier form, in 4 + 5 + 4 steps
+// instead of 128.
+__device__ __forceinline__ void comp_prefix128_warp(float* hi, float* lo, int lane) {
+  float s[4], c[4];
+  const float4 x = *reinterpret_cast<const float4*>(hi + 4 * lane);
+  const float xs[4] = {x.x, x.y, x.z, x.w};
+  s[0] = xs[0];
+  c[0] = 0.f;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    float e;
+    s[i] = two_sum(s[i - 1], xs[i], e);
+    c[i] = __fadd_rn(c[i - 1], e);
+  }
+  float S = s[3], C = c[3];  // inclusive scan of the lane totals
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float S2 = __shfl_up_sync(0xffffffffu, S, off);
+    const float C2 = __shfl_up_sync(0xffffffffu, C, off);
+    if (lane >= off) {
+      float e;
+      const float t = two_sum(S2, S, e);
+      C = __fadd_rn(__fadd_rn(C2, C), e);
+      S = t;
+    }
+  }
+  float ES = __shfl_up_sync(0xffffffffu, S, 1), EC = __shfl_up_sync(0xffffffffu, C, 1);
+  if (lane == 0) ES = EC = 0.f;
+  float oh[4], ol[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float e;
+    oh[i] = two_sum(ES, s[i], e);
+    ol[i] = __fadd_rn(__fadd_rn(EC, c[i]), e);
+  }
+  *reinterpret_cast<float4*>(hi + 4 * lane) = make_float4(oh[0], oh[1], oh[2], oh[3]);
+  *reinterpret_cast<float4*>(lo + 4 * lane) = make_float4(ol[0], ol[1], ol[2], ol[3]);
+}
+
 __device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
@@ -969,7 +1021,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid == 0) comp_prefix(sarr + 128, sarr + 256, 128);
+  if (warp == 0) comp_prefix128_warp(sarr + 128, sarr + 256, lane);
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   uint32_t mma_phase = 0;
@@ -989,17 +1041,17 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     const int nx = next_valid(it);
     const bool has_next = nx < n_items;
     const Item y = has_next ? item(nx) : x;
-    float pb[4], pg[4];  // warp 15: the next item's gate inputs, staged in the second build
+    float pb[4], pg[4];  // warp 15: the next item's gate inputs (positions 4 lane + i)
     if (warp == 15 && has_next) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) gates(y, lane + 32 * i, pb[i], pg[i]);
+      for (int i = 0; i < 4; ++i) gates(y, 4 * lane + i, pb[i], pg[i]);
     }
     const int n = x.n, hv = x.hv;
     const int64_t R0 = x.R0;
     ok = mbar_wait(&bars[0], k_got & 1, a.status, kDevTimeout);
     if (ok) ++k_got;
     if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {  // Gram matrix k k^T, 128 x 128
+    if (tid == 128) {  // Gram matrix k k^T, 128 x 128 (issued beside the row norms of tid < 128)
       const uint32_t kb = smem_u32(kbuf);
       const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
@@ -1095,13 +1147,10 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
           *reinterpret_cast<uint4*>(trow + 32768 + off) = make_uint4(0, 0, 0, 0);
         }
       } else if (warp == 15 && has_next) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          nsb[lane + 32 * i] = pb[i];
-          nsb[128 + lane + 32 * i] = pg[i];
-        }
+        *reinterpret_cast<float4*>(nsb + 4 * lane) = make_float4(pb[0], pb[1], pb[2], pb[3]);
+        *reinterpret_cast<float4*>(nsb + 128 + 4 * lane) = make_float4(pg[0], pg[1], pg[2], pg[3]);
         __syncwarp();
-        if (lane == 0) comp_prefix(nsb + 128, nsb + 256, 128);
+        comp_prefix128_warp(nsb + 128, nsb + 256, lane);
       }
       fence_async_smem();
       tc_fence_before();
