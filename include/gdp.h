@@ -174,6 +174,32 @@ gdp_status gdp_recurrent_update(const void* q, const void* k, const void* v, con
                                 cudaStream_t stream);
 
 /*
+ * gdp_recurrent_update_slots - gdp_recurrent_update for a decode batch whose
+ * requests keep their states in a shared pool (the serving side of the
+ * prepare page's decode bullet: padding requests carry slot -1 upstream,
+ * where the conv zeroes their output, and the recurrent update must leave
+ * them out). Request r updates pool entry state_slot[r]:
+ *   state_pool [n_slots, HV, K, V] fp32, read and written in place at the
+ *              entries the slots name; other entries are not touched;
+ *   state_slot [n] int32 (device): entry of request r, or -1 for a padding
+ *              request, whose o rows are written as zeros and which reads and
+ *              writes no state;
+ *   status     (device, nullable) int32 set to 1 (GDP_ERR_INVALID_ARG) when a
+ *              slot is outside [-1, n_slots) or is named by two requests; such
+ *              requests are skipped like padding. The call never clears it.
+ * Other arguments and o as gdp_recurrent_update. Slots are read on the device
+ * only: no host synchronisation, static launch shape for fixed sizes, so the
+ * call can be captured in a CUDA graph with the slot table updated in place
+ * between replays.
+ */
+gdp_status gdp_recurrent_update_slots(const void* q, const void* k, const void* v,
+                                      const float* beta, const float* g, float* state_pool,
+                                      const int32_t* state_slot, int n_slots, int n, int L,
+                                      int H, int HV, int K, int V, float scale,
+                                      int use_qk_l2norm, gdp_dtype dt, float* o,
+                                      int32_t* status, cudaStream_t stream);
+
+/*
  * gdp_read_status - synchronise `stream` and return the device status word
  * in the first bytes of a gdp_chunk_fwd workspace: GDP_OK, or
  * GDP_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel gave up.

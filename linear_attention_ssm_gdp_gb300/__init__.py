@@ -20,6 +20,7 @@ __all__ = [
     "load", "GDPError", "gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
     "gdp_chunk_fwd_workspace_size", "gdp_chunk_fwd_stage_offsets", "gdp_recurrent_update",
     "gdp_read_status", "gdp_version", "gdp_set_stage_events", "gdp_chunk_fwd_noalloc",
+    "gdp_recurrent_update_slots",
     "LIB_PATH",
 ]
 
@@ -57,6 +58,7 @@ def load() -> ctypes.CDLL:
             lib.gdp_chunk_fwd_stage_offsets.argtypes = [I] * 9 + [I, P]
             lib.gdp_chunk_fwd.argtypes = ([P] * 7 + [I] * 9 + [F, I, I] + [P, P, P, SZ, P])
             lib.gdp_recurrent_update.argtypes = [P] * 6 + [I] * 6 + [F, I, I, P, P]
+            lib.gdp_recurrent_update_slots.argtypes = ([P] * 7 + [I] * 7 + [F, I, I, P, P, P])
             lib.gdp_chunk_fwd_noalloc.argtypes = [P] * 7 + [I] * 9 + [F, I, I] + [P, P, P]
             lib.gdp_chunk_fwd_noalloc.restype = I
             lib.gdp_read_status.argtypes = [P, P]
@@ -66,7 +68,8 @@ def load() -> ctypes.CDLL:
             lib.gdp_status_string.restype = ctypes.c_char_p
             lib.gdp_version.argtypes = []
             for f in ("gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
-                      "gdp_recurrent_update", "gdp_read_status", "gdp_chunk_fwd_stage_offsets",
+                      "gdp_recurrent_update", "gdp_recurrent_update_slots", "gdp_read_status",
+                      "gdp_chunk_fwd_stage_offsets",
                       "gdp_version"):
                 getattr(lib, f).restype = I
             _lib = lib
@@ -297,4 +300,40 @@ def gdp_recurrent_update(q, k, v, beta, g, state, scale: float | None = None,
                                      HV, K, V, float(scale), 1 if use_qk_l2norm else 0,
                                      _DTYPE[q.dtype], _p(o), _stream(q.device))
     _check("gdp_recurrent_update", st)
+    return o
+
+
+def gdp_recurrent_update_slots(q, k, v, beta, g, state_pool, state_slot, scale=None,
+                               use_qk_l2norm: bool = False, status=None, out=None):
+    """Recurrent update of a decode batch whose states live in a pool: request r
+    updates ``state_pool[state_slot[r]]`` in place (``state_slot`` int32 [n] on the
+    device; -1 marks a padding request, whose o rows are zero and which touches no
+    state). ``status`` (optional int32 device tensor, one element) is set to 1 when
+    a slot is out of range or repeated; those requests are skipped. Returns o."""
+    _need_cuda(q, k, v, beta, g, state_pool, state_slot, status)
+    n, L, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    if tuple(k.shape) != (n, L, H, K) or tuple(v.shape[:2]) != (n, L):
+        raise ValueError("q, k must be [n,L,H,K] and v [n,L,HV,V]")
+    if tuple(beta.shape) != (n, L, HV) or tuple(g.shape) != (n, L, HV):
+        raise ValueError("beta and g must be [n,L,HV]")
+    if (state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, K, V)
+            or state_pool.dtype != torch.float32):
+        raise ValueError("state_pool must be fp32 [n_slots,HV,K,V]")
+    if tuple(state_slot.shape) != (n,) or state_slot.dtype != torch.int32:
+        raise ValueError("state_slot must be int32 [n]")
+    if status is not None and (status.dtype != torch.int32 or status.numel() < 1):
+        raise ValueError("status must be an int32 device tensor")
+    for t in (q, k, v, beta, g, state_pool, state_slot):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    if scale is None:
+        scale = K ** -0.5
+    o = out if out is not None else torch.empty((n, L, HV, V), dtype=torch.float32,
+                                                device=q.device)
+    st = load().gdp_recurrent_update_slots(
+        _p(q), _p(k), _p(v), _p(beta), _p(g), _p(state_pool), _p(state_slot),
+        state_pool.shape[0], n, L, H, HV, K, V, float(scale), 1 if use_qk_l2norm else 0,
+        _DTYPE[q.dtype], _p(o), _p(status), _stream(q.device))
+    _check("gdp_recurrent_update_slots", st)
     return o

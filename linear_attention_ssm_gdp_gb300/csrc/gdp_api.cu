@@ -203,7 +203,30 @@ gdp_status gdp_recurrent_update(const void* q, const void* k, const void* v, con
   if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(o)) % 16 != 0)
     return GDP_ERR_INVALID_ARG;
   const cudaError_t e = launch_recurrent(q, k, v, beta, g, state, n, L, H, HV, K, V, scale,
-                                         use_qk_l2norm ? 1 : 0, dt, o, stream);
+                                         use_qk_l2norm ? 1 : 0, dt, o, nullptr, 0, nullptr,
+                                         stream);
+  return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
+}
+
+gdp_status gdp_recurrent_update_slots(const void* q, const void* k, const void* v,
+                                      const float* beta, const float* g, float* state_pool,
+                                      const int32_t* state_slot, int n_slots, int n, int L,
+                                      int H, int HV, int K, int V, float scale,
+                                      int use_qk_l2norm, gdp_dtype dt, float* o,
+                                      int32_t* status, cudaStream_t stream) {
+  if (!dtype_ok(dt)) return GDP_ERR_UNSUPPORTED;
+  if (n < 0 || L < 0 || n_slots < 0 || H <= 0 || HV <= 0 || K <= 0 || V <= 0 || HV % H != 0)
+    return GDP_ERR_INVALID_ARG;
+  if (!(K == 32 || K == 64 || K == 128 || K == 256) || V % 8 != 0 || V > 1024)
+    return GDP_ERR_UNSUPPORTED;
+  if ((int64_t)n * L == 0) return GDP_OK;
+  if (!q || !k || !v || !beta || !g || !state_slot || !o || (n_slots > 0 && !state_pool))
+    return GDP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(state_pool) | reinterpret_cast<uintptr_t>(o)) % 16 != 0)
+    return GDP_ERR_INVALID_ARG;
+  const cudaError_t e = launch_recurrent(q, k, v, beta, g, state_pool, n, L, H, HV, K, V, scale,
+                                         use_qk_l2norm ? 1 : 0, dt, o, state_slot, n_slots,
+                                         status, stream);
   return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
 }
 

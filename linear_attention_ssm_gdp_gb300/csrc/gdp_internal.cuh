@@ -85,9 +85,13 @@ cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws)
 cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
 cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
 
+// slot: null (request r updates state entry r) or int32 [n] entries of a pool of
+// n_slots states (-1: padding request); status (nullable) is set to 1 when a slot
+// is out of range or shared by two requests.
 cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const float* beta,
                              const float* g, float* state, int n, int L, int H, int HV, int K,
                              int V, float scale, int l2norm, gdp_dtype dt, float* o,
+                             const int32_t* slot, int n_slots, int32_t* status,
                              cudaStream_t stream);
 
 int sm_count();  // multiprocessors on the current device (cached per device)

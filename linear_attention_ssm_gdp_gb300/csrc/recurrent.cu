@@ -74,6 +74,31 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// State slots (decode serving): request r updates state row block slot[r] of a
+// state pool of n_slots entries, or nothing when slot[r] is -1 (a padding
+// request: its o rows are written as zeros). Without a slot table request r
+// uses entry r. A slot outside [-1, n_slots) or shared by two requests would
+// make the update ill-defined (two requests racing on one state), so such a
+// request is skipped like padding and *status (if given) is set to 1. Every
+// thread of the block calls this with the same r.
+__device__ __forceinline__ int resolve_slot(const int* __restrict__ slot, int n, int n_slots,
+                                            int r, int* status) {
+  if (!slot) return r;
+  const int s = slot[r];
+  if (s == -1) return -1;
+  int bad = s < -1 || s >= n_slots;
+  if (!bad) {
+    int dup = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dup |= (i != r) & (slot[i] == s);
+    bad = __syncthreads_or(dup);
+  }
+  if (bad) {
+    if (threadIdx.x == 0 && status) atomicExch(status, 1);
+    return -1;
+  }
+  return s;
+}
+
 constexpr int kCtaCols = 32;  // value columns per CTA (one per lane)
 constexpr int kLC = 16;       // steps staged in shared memory at a time
 
@@ -94,7 +119,8 @@ __global__ void __launch_bounds__(KW * 32, KW >= 4 ? 24 / KW : 8)
 recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                  const float* __restrict__ beta, const float* __restrict__ g,
                  float* __restrict__ state, int L, int H, int HV, int V, float scale,
-                 int l2norm, float* __restrict__ o) {
+                 int l2norm, float* __restrict__ o, const int* __restrict__ slot, int n,
+                 int n_slots, int* status) {
   constexpr int K = KW * 32;
   extern __shared__ __align__(16) float smr[];
   float* kn = smr;                      // [kLC][K]
@@ -109,14 +135,17 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cbase = blockIdx.y * kCtaCols;
   const int c = cbase + lane;
+  const int sl = resolve_slot(slot, n, n_slots, r, status);
   const bool active = c < V;
+  const bool live = sl >= 0;  // false: padding or rejected slot (no state, zero o rows)
   const int nth = KW * 32;
-  float* st = state + (int64_t)rh * K * V + (int64_t)(warp * 32) * V + c;
+  float* st = state + ((int64_t)(live ? sl : 0) * HV + hv) * K * V + (int64_t)(warp * 32) * V + c;
   f2 h[16];  // rows (2i, 2i + 1) of this thread's 32, packed
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    h[i] = active ? pk2(__ldcs(st + (int64_t)(2 * i) * V), __ldcs(st + (int64_t)(2 * i + 1) * V))
-                  : pk2(0.f, 0.f);
+    h[i] = (active && live)
+               ? pk2(__ldcs(st + (int64_t)(2 * i) * V), __ldcs(st + (int64_t)(2 * i + 1) * V))
+               : pk2(0.f, 0.f);
   int buf = 0;
   for (int e0 = 0; e0 < L; e0 += kLC) {
     const int lc = min(kLC, L - e0);
@@ -189,12 +218,12 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
         float so = 0.f;
 #pragma unroll
         for (int w = 0; w < KW; ++w) so += ob[w * 32 + lane];
-        o[((re0 + e) * HV + hv) * V + c] = scale * so;
+        o[((re0 + e) * HV + hv) * V + c] = live ? scale * so : 0.f;
       }
       buf ^= 1;  // the next step writes the other buffers; reuse is two barriers away
     }
   }
-  if (active) {
+  if (active && live) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float2 hv2 = upk2(h[i]);
@@ -204,17 +233,24 @@ recurrent_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin
   }
 }
 
+struct SlotArgs {
+  const int* slot;  // null: request r uses state entry r
+  int n, n_slots;
+  int* status;
+};
+
 template <typename Tin, int KW>
 cudaError_t launch_k(const dim3& grid, const void* q, const void* k, const void* v,
                      const float* beta, const float* g, float* state, int L, int H, int HV,
-                     int V, float scale, int l2norm, float* o, cudaStream_t s) {
+                     int V, float scale, int l2norm, float* o, const SlotArgs& sa,
+                     cudaStream_t s) {
   constexpr int smem = rec_smem<KW * 32>();
   cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<Tin, KW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   recurrent_kernel<Tin, KW><<<grid, KW * 32, smem, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), beta,
-      g, state, L, H, HV, V, scale, l2norm, o);
+      g, state, L, H, HV, V, scale, l2norm, o, sa.slot, sa.n, sa.n_slots, sa.status);
   return cudaGetLastError();
 }
 
@@ -295,11 +331,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // row groups a warp reads at once then fall on distinct banks. Columns past V
 // are zero-filled.
 __device__ __forceinline__ void prefetch_state(float* sst, const float* state, int it, int ncs,
-                                               int V) {
+                                               int V, int64_t srh) {
   const int rh = it / ncs, cs = it - rh * ncs;
+  (void)rh;
   const int tid = threadIdx.x, c16 = tid & 15;
-  const int valid = (cs * kSliceCols + 4 * c16 < V) ? 16 : 0;
-  const float* src = state + (int64_t)rh * 128 * V + cs * kSliceCols + (valid ? 4 * c16 : 0);
+  // srh < 0 (no state for this item): every chunk is zero-filled, nothing is read
+  const int valid = (srh >= 0 && cs * kSliceCols + 4 * c16 < V) ? 16 : 0;
+  const float* src = state + (srh >= 0 ? srh : 0) * 128 * V + cs * kSliceCols + (valid ? 4 * c16 : 0);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int row = (tid >> 4) + 16 * i;
@@ -309,11 +347,20 @@ __device__ __forceinline__ void prefetch_state(float* sst, const float* state, i
   cp_async_commit();
 }
 
-__device__ __forceinline__ float* state_ptr(float* state, int it, int ncs, int V) {
-  const int rh = it / ncs, cs = it - rh * ncs;
+__device__ __forceinline__ float* state_ptr(float* state, int it, int ncs, int V, int64_t srh) {
+  const int cs = it % ncs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  return state + (int64_t)rh * 128 * V + (int64_t)(32 * (lane >> 3)) * V + cs * kSliceCols +
+  return state + srh * 128 * V + (int64_t)(32 * (lane >> 3)) * V + cs * kSliceCols +
          8 * warp + (lane & 7);
+}
+
+// State-row block (slot * HV + hv) of item `it`, or -1 when the item's request
+// has no state (padding or a rejected slot).
+__device__ __forceinline__ int64_t item_srh(int it, int ncs, int HV, const int* slot, int n,
+                                            int n_slots, int* status) {
+  const int rh = it / ncs, r = rh / HV, hv = rh - r * HV;
+  const int sl = resolve_slot(slot, n, n_slots, r, status);
+  return sl < 0 ? -1 : (int64_t)sl * HV + hv;
 }
 
 template <typename Tin>
@@ -322,7 +369,8 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                     const Tin* __restrict__ v, const float* __restrict__ beta,
                     const float* __restrict__ g, float* __restrict__ state, int n_items, int L,
                     int H, int HV, int V, int ncs, float scale, int l2norm,
-                    float* __restrict__ o) {
+                    float* __restrict__ o, const int* __restrict__ slot, int n, int n_slots,
+                    int* status) {
   __shared__ __align__(16) float kn[kB * kRowPad];
   __shared__ __align__(16) float qn[kB * kRowPad];
   __shared__ __align__(16) float vs[kB * kSliceCols];
@@ -335,14 +383,17 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
   int it = blockIdx.x;
   if (it >= n_items) return;
   Batch<Tin> pf;
-  prefetch_state(sst, state, it, ncs, V);
+  int64_t srh = item_srh(it, ncs, HV, slot, n, n_slots, status);
+  prefetch_state(sst, state, it, ncs, V, srh);
   load_batch(pf, q, k, v, beta, g, it, 0, L, H, HV, V, ncs);
   for (; it < n_items; it += gridDim.x) {
     const int rh = it / ncs, cs = it - rh * ncs;
     const int r = rh / HV, hv = rh - r * HV;
     const int col = cs * kSliceCols + cw;
     const bool active = col < V;
+    const bool live = srh >= 0;  // false: padding or rejected slot (no state, zero o rows)
     const int nx = it + gridDim.x;
+    int64_t srh_nx = -1;
     cp_async_wait_all();
     __syncthreads();  // this item's state is in shared memory
     f2 h[16];  // rows (2i, 2i + 1) of this thread's 32, packed
@@ -387,7 +438,10 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
       __syncthreads();
       // the state buffer has been read (barrier above): the next item's state
       // streams in behind this item's steps
-      if (e0 == 0 && nx < n_items) prefetch_state(sst, state, nx, ncs, V);
+      if (e0 == 0 && nx < n_items) {
+        srh_nx = item_srh(nx, ncs, HV, slot, n, n_slots, status);
+        prefetch_state(sst, state, nx, ncs, V, srh_nx);
+      }
       if (e0 + kB < L)
         load_batch(pf, q, k, v, beta, g, it, e0 + kB, L, H, HV, V, ncs);
       else if (nx < n_items)
@@ -424,11 +478,11 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         float po = (oav.x + oav.y) + (obv.x + obv.y);
         po += __shfl_xor_sync(0xffffffffu, po, 8);
         po += __shfl_xor_sync(0xffffffffu, po, 16);
-        if (grp == 0 && active) o[((re0 + e) * HV + hv) * V + col] = scale * po;
+        if (grp == 0 && active) o[((re0 + e) * HV + hv) * V + col] = live ? scale * po : 0.f;
       }
     }
-    if (active) {
-      float* sp = state_ptr(state, it, ncs, V);
+    if (active && live) {
+      float* sp = state_ptr(state, it, ncs, V, srh);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 hv2 = upk2(h[i]);
@@ -436,13 +490,14 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         __stcs(sp + (int64_t)(2 * i + 1) * V, hv2.y);
       }
     }
+    srh = srh_nx;
   }
 }
 
 template <typename Tin>
 cudaError_t launch_k128(const void* q, const void* k, const void* v, const float* beta,
                         const float* g, float* state, int n, int L, int H, int HV, int V,
-                        float scale, int l2norm, float* o, cudaStream_t s) {
+                        float scale, int l2norm, float* o, const SlotArgs& sa, cudaStream_t s) {
   const int ncs = (int)cdiv(V, kSliceCols);
   const int64_t items = (int64_t)n * HV * ncs;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
@@ -453,21 +508,22 @@ cudaError_t launch_k128(const void* q, const void* k, const void* v, const float
   if (e != cudaSuccess) return e;
   recurrent128_kernel<Tin><<<grid, 256, smem, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), beta,
-      g, state, (int)items, L, H, HV, V, ncs, scale, l2norm, o);
+      g, state, (int)items, L, H, HV, V, ncs, scale, l2norm, o, sa.slot, sa.n, sa.n_slots,
+      sa.status);
   return cudaGetLastError();
 }
 
 template <typename Tin>
 cudaError_t run(const void* q, const void* k, const void* v, const float* beta, const float* g,
                 float* state, int n, int L, int H, int HV, int K, int V, float scale, int l2norm,
-                float* o, cudaStream_t s) {
+                float* o, const SlotArgs& sa, cudaStream_t s) {
   const dim3 grid((unsigned)((int64_t)n * HV), (unsigned)cdiv(V, kCtaCols));
   switch (K) {
-    case 32: return launch_k<Tin, 1>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
-    case 64: return launch_k<Tin, 2>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
+    case 32: return launch_k<Tin, 1>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, sa, s);
+    case 64: return launch_k<Tin, 2>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, sa, s);
     case 128:  // the entry point guarantees V % 8 == 0 and a 16-byte aligned state
-      return launch_k128<Tin>(q, k, v, beta, g, state, n, L, H, HV, V, scale, l2norm, o, s);
-    default: return launch_k<Tin, 8>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, s);
+      return launch_k128<Tin>(q, k, v, beta, g, state, n, L, H, HV, V, scale, l2norm, o, sa, s);
+    default: return launch_k<Tin, 8>(grid, q, k, v, beta, g, state, L, H, HV, V, scale, l2norm, o, sa, s);
   }
 }
 
@@ -476,15 +532,17 @@ cudaError_t run(const void* q, const void* k, const void* v, const float* beta, 
 cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const float* beta,
                              const float* g, float* state, int n, int L, int H, int HV, int K,
                              int V, float scale, int l2norm, gdp_dtype dt, float* o,
+                             const int32_t* slot, int n_slots, int32_t* status,
                              cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
+  const SlotArgs sa{slot, n, n_slots, status};
   switch (dt) {
     case GDP_BF16:
-      return run<__nv_bfloat16>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, stream);
+      return run<__nv_bfloat16>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, sa, stream);
     case GDP_F16:
-      return run<__half>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, stream);
+      return run<__half>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, sa, stream);
     default:
-      return run<float>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, stream);
+      return run<float>(q, k, v, beta, g, state, n, L, H, HV, K, V, scale, l2norm, o, sa, stream);
   }
 }
 

@@ -160,3 +160,19 @@ def test_recurrent_rejects_before_launch(lib, kw, status):
                                  P(a["state"]), a["n"], a["L"], a["H"], a["HV"], a["K"],
                                  a["V"], 1.0, 0, 0, P(1 << 20), None)
     assert st == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=48), 2), (dict(slot=None), 1), (dict(n_slots=-1), 1), (dict(pool=None), 1),
+    (dict(pool=(1 << 20) + 4), 1), (dict(H=3, HV=4), 1),
+])
+def test_recurrent_slots_rejects_before_launch(lib, kw, status):
+    a = dict(n=2, L=4, H=2, HV=2, K=32, V=32, pool=1 << 20, slot=1 << 20, n_slots=4)
+    a.update(kw)
+    P = ctypes.c_void_p
+    so = lib.load()
+    st = so.gdp_recurrent_update_slots(P(1 << 20), P(1 << 20), P(1 << 20), P(1 << 20),
+                                       P(1 << 20), P(a["pool"]), P(a["slot"]), a["n_slots"],
+                                       a["n"], a["L"], a["H"], a["HV"], a["K"], a["V"], 1.0, 0,
+                                       0, P(1 << 20), None, None)
+    assert st == status

@@ -107,3 +107,121 @@ def test_graph_capture_replay(gdp):
     o2 = gdp.gdp_recurrent_update(*outs, state, use_qk_l2norm=True)
     torch.cuda.synchronize()
     assert torch.equal(o_graph, o2) and torch.equal(s_graph, state)
+
+
+def _slot_reference(q, k, v, beta, g, pool, slots, scale, l2):
+    """The oracle's per-step walk applied to the pool entries the slots name; padding
+    requests (slot -1) produce zero rows and leave the pool alone."""
+    new_pool = pool.clone().double()
+    o = torch.zeros(q.shape[0], q.shape[1], v.shape[2], v.shape[3], dtype=torch.float64)
+    live = [r for r in range(q.shape[0]) if int(slots[r]) >= 0]
+    if live:
+        idx = torch.tensor([int(slots[r]) for r in live])
+        lr = torch.tensor(live)
+        ro, rs = oracle.recurrent(q[lr], k[lr], v[lr], beta[lr], g[lr], pool[idx], scale,
+                                  l2norm=l2)
+        o[lr] = ro
+        new_pool[idx] = rs
+    return o, new_pool
+
+
+@pytest.mark.parametrize("K,V,dtype", [(128, 128, torch.bfloat16), (64, 48, torch.float32)])
+def test_recurrent_slots_with_padding(gdp, K, V, dtype):
+    n, L, H, HV, n_slots = 24, 4, 2, 4, 40
+    gen = torch.Generator().manual_seed(K + V)
+    q = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    k = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    v = torch.randn(n, L, HV, V, generator=gen).to(dtype)
+    beta = torch.rand(n, L, HV, generator=gen)
+    g = -torch.rand(n, L, HV, generator=gen)
+    pool = torch.randn(n_slots, HV, K, V, generator=gen) * 0.1
+    perm = torch.randperm(n_slots, generator=gen)[:n].to(torch.int32)
+    perm[[2, 7, 8, 20]] = -1  # padding requests
+    ro, rpool = _slot_reference(q, k, v, beta, g, pool, perm, K ** -0.5, True)
+    pd = pool.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gdp.gdp_recurrent_update_slots(*to(DEV, q, k, v, beta, g), pd, perm.to(DEV),
+                                       use_qk_l2norm=True, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert rel_err(o, ro) <= TOL[dtype]
+    assert rel_err(pd, rpool) <= TOL[dtype]
+    untouched = sorted(set(range(n_slots)) - {int(s) for s in perm if int(s) >= 0})
+    assert torch.equal(pd.cpu()[untouched], pool[untouched])  # bitwise: never written
+    pad = perm < 0
+    assert torch.count_nonzero(o.cpu()[pad]) == 0
+
+
+def test_recurrent_slots_identity_equals_dense_call(gdp):
+    """slot[r] = r over a pool of n entries is the dense call, bit for bit."""
+    n, L, H, HV, K, V = 8, 4, 2, 2, 128, 128
+    gen = torch.Generator().manual_seed(7)
+    q, k = (torch.randn(n, L, H, K, generator=gen).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn(n, L, HV, V, generator=gen).to(torch.bfloat16)
+    beta, g = torch.rand(n, L, HV, generator=gen), -torch.rand(n, L, HV, generator=gen)
+    s0 = torch.randn(n, HV, K, V, generator=gen) * 0.1
+    a, b = s0.to(DEV), s0.to(DEV)
+    ins = to(DEV, q, k, v, beta, g)
+    o1 = gdp.gdp_recurrent_update(*ins, a, use_qk_l2norm=True)
+    o2 = gdp.gdp_recurrent_update_slots(*ins, b, torch.arange(n, dtype=torch.int32, device=DEV),
+                                        use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(a, b)
+
+
+@pytest.mark.parametrize("bad", ["repeated", "out_of_range"])
+def test_recurrent_slots_rejects_bad_slots_on_device(gdp, bad):
+    n, L, H, HV, K, V, n_slots = 6, 2, 2, 2, 128, 64, 8
+    gen = torch.Generator().manual_seed(9)
+    q, k = (torch.randn(n, L, H, K, generator=gen).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn(n, L, HV, V, generator=gen).to(torch.bfloat16)
+    beta, g = torch.rand(n, L, HV, generator=gen), -torch.rand(n, L, HV, generator=gen)
+    pool = torch.randn(n_slots, HV, K, V, generator=gen) * 0.1
+    slots = torch.tensor([0, 3, 5, 1, 6, 2], dtype=torch.int32)
+    if bad == "repeated":
+        slots[4] = 3  # requests 1 and 4 both name entry 3
+        rejected = [1, 4]
+    else:
+        slots[2] = n_slots  # past the pool
+        rejected = [2]
+    ref_slots = slots.clone()
+    ref_slots[rejected] = -1
+    ro, rpool = _slot_reference(q, k, v, beta, g, pool, ref_slots, K ** -0.5, True)
+    pd = pool.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = gdp.gdp_recurrent_update_slots(*to(DEV, q, k, v, beta, g), pd, slots.to(DEV),
+                                       use_qk_l2norm=True, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert torch.count_nonzero(o.cpu()[rejected]) == 0
+    assert rel_err(o, ro) <= 2e-3 and rel_err(pd, rpool) <= 2e-3
+
+
+def test_recurrent_slots_graph_replay_with_new_slots(gdp):
+    """Captured once, replayed after the slot table changes in place."""
+    n, L, H, HV, K, V, n_slots = 8, 4, 2, 4, 128, 128, 16
+    gen = torch.Generator().manual_seed(10)
+    q, k = (torch.randn(n, L, H, K, generator=gen).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn(n, L, HV, V, generator=gen).to(torch.bfloat16)
+    beta, g = torch.rand(n, L, HV, generator=gen), -torch.rand(n, L, HV, generator=gen)
+    pool0 = torch.randn(n_slots, HV, K, V, generator=gen) * 0.1
+    ins = to(DEV, q, k, v, beta, g)
+    pd = pool0.to(DEV)
+    slots = torch.arange(n, dtype=torch.int32, device=DEV)
+    o = torch.empty(n, L, HV, V, device=DEV)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        gdp.gdp_recurrent_update_slots(*ins, pd, slots, use_qk_l2norm=True, out=o)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdp.gdp_recurrent_update_slots(*ins, pd, slots, use_qk_l2norm=True, out=o)
+    new = torch.tensor([9, -1, 3, 15, 0, -1, 12, 4], dtype=torch.int32)
+    slots.copy_(new.to(DEV))
+    pd.copy_(pool0.to(DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    ro, rpool = _slot_reference(q, k, v, beta, g, pool0, new, K ** -0.5, True)
+    assert rel_err(o, ro) <= 2e-3 and rel_err(pd, rpool) <= 2e-3
