@@ -260,6 +260,26 @@ gdp_status gdp_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  int use_qk_l2norm, gdp_dtype dt, float* o, float* final_state,
                                  cudaStream_t stream);
 
+/*
+ * gdp_debug_wait_fault - TEST HOOK for the device-side failure path; off by
+ * default and never needed in normal use. Every mbarrier wait inside the
+ * tensor-core kernels is bounded (2 s of wall time); a wait that runs out
+ * records GDP_ERR_DEVICE_TIMEOUT in the workspace status word, and the kernel
+ * leaves cleanly (it waits, bounded, for its own copies in flight and frees
+ * its tensor memory) instead of hanging the GPU.
+ *   arm = 1: the next gdp_chunk_fwd that runs the 128-position WY kernel
+ *            (tensor-core path, even M) leaves out one tensor-core commit in
+ *            its first CTA, so that CTA's wait for it runs out; the hook then
+ *            disarms itself. arm = 0: disarm.
+ *   budget_seconds: new wait budget (0 < budget <= 10), or <= 0 for the
+ *            default 2 s. The budget applies to every later launch until
+ *            changed.
+ * Synchronous (it writes a device variable on the current device). Results of
+ * the faulted call are undefined; later calls are unaffected.
+ * Errors: GDP_ERR_INVALID_ARG (budget above 10 s), GDP_ERR_CUDA.
+ */
+gdp_status gdp_debug_wait_fault(int arm, double budget_seconds);
+
 /* Number of stage-boundary events gdp_set_stage_events takes. */
 #define GDP_STAGE_EVENTS 5
 

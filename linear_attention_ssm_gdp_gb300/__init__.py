@@ -20,7 +20,7 @@ __all__ = [
     "load", "GDPError", "gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
     "gdp_chunk_fwd_workspace_size", "gdp_chunk_fwd_stage_offsets", "gdp_recurrent_update",
     "gdp_read_status", "gdp_version", "gdp_set_stage_events", "gdp_chunk_fwd_noalloc",
-    "gdp_recurrent_update_slots",
+    "gdp_recurrent_update_slots", "gdp_debug_wait_fault",
     "LIB_PATH",
 ]
 
@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
             lib.gdp_chunk_fwd_noalloc.argtypes = [P] * 7 + [I] * 9 + [F, I, I] + [P, P, P]
             lib.gdp_chunk_fwd_noalloc.restype = I
             lib.gdp_read_status.argtypes = [P, P]
+            lib.gdp_debug_wait_fault.argtypes = [I, ctypes.c_double]
+            lib.gdp_debug_wait_fault.restype = I
             lib.gdp_set_stage_events.argtypes = [P, I]
             lib.gdp_set_stage_events.restype = I
             lib.gdp_status_string.argtypes = [I]
@@ -337,3 +339,11 @@ def gdp_recurrent_update_slots(q, k, v, beta, g, state_pool, state_slot, scale=N
         _DTYPE[q.dtype], _p(o), _p(status), _stream(q.device))
     _check("gdp_recurrent_update_slots", st)
     return o
+
+
+def gdp_debug_wait_fault(arm: bool, budget_seconds: float = 0.0):
+    """Test hook (off by default): arm a one-shot missing tensor-core commit in the
+    next 128-position WY launch so that one bounded device wait runs out, and/or set
+    the wait budget (<= 0: the default 2 s)."""
+    _check("gdp_debug_wait_fault", load().gdp_debug_wait_fault(1 if arm else 0,
+                                                                float(budget_seconds)))

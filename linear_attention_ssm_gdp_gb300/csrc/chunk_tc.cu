@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gdp_internal.cuh"
@@ -235,6 +236,7 @@ struct WyArgs {
   float* u;
   float4* gk;  // [HV][Te]: (Gam hi, Gam lo, 1/|k|, 0)
   int* status;
+  int fault;   // test hook (gdp_debug_wait_fault): CTA 0 skips its first Gram product
 };
 
 // Shared memory (offsets from a 1024-aligned base). Operand tiles hold 64
@@ -1051,7 +1053,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     ok = mbar_wait(&bars[0], k_got & 1, a.status, kDevTimeout);
     if (ok) ++k_got;
     if (!__syncthreads_and(ok)) break;
-    if (tid == 128) {  // Gram matrix k k^T, 128 x 128 (issued beside the row norms of tid < 128)
+    // (the test hook leaves CTA 0's first Gram product, and so its commit, out:
+    // every thread's bounded wait below then runs out and the CTA leaves cleanly)
+    if (tid == 128 && !(a.fault && blockIdx.x == 0 && c == 0)) {  // Gram k k^T, 128 x 128, issued beside the row norms of tid < 128
       const uint32_t kb = smem_u32(kbuf);
       const uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
@@ -2204,6 +2208,9 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
 }
 
 // ============================================================================ host
+// Test hook state (gdp_debug_wait_fault): armed for the next WY-128 launch only.
+std::atomic<int> g_wy_fault{0};
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -2361,7 +2368,8 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
     WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
              reinterpret_cast<const int2*>(ws + L.exp_tab),
              L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<const int2*>(ws + L.blk_tab),
-             w_hi, w_lo, u, gk, status};
+             w_hi, w_lo, u, gk, status, 0};
+    if ((p.M % 2) == 0) a.fault = g_wy_fault.exchange(0);  // one-shot test hook
     const bool blk128 = (p.M % 2) == 0;
     switch (p.V) {
       case 64: e = blk128 ? run_wy128<64>(p, a) : run_wy<64>(p, a); break;
@@ -2434,3 +2442,16 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
 }
 
 }  // namespace gdp
+
+extern "C" gdp_status gdp_debug_wait_fault(int arm, double budget_seconds) {
+  unsigned long long ns = gdp::ptx::kWaitBudgetNs;
+  if (budget_seconds > 0.0) {
+    if (budget_seconds > 10.0) return GDP_ERR_INVALID_ARG;
+    ns = (unsigned long long)(budget_seconds * 1e9);
+    if (ns == 0) ns = 1;
+  }
+  if (cudaMemcpyToSymbol(gdp::ptx::g_wait_budget_ns, &ns, sizeof(ns)) != cudaSuccess)
+    return GDP_ERR_CUDA;
+  gdp::g_wy_fault.store(arm ? 1 : 0);
+  return GDP_OK;
+}

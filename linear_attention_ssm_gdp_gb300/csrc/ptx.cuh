@@ -50,17 +50,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait budget for one phase of one barrier (nanoseconds of wall time).
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+// Wait budget for one phase of one barrier (nanoseconds of wall time): 2 s,
+// unless the test hook gdp_debug_wait_fault has set a shorter one.
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+static __device__ unsigned long long g_wait_budget_ns = kWaitBudgetNs;
 
 // Bounded wait for `parity`; on timeout stores `code` into *status (if not
 // null) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t budget = *const_cast<volatile unsigned long long*>(&g_wait_budget_ns);
   while (true) {
     if (mbar_test(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+    if (globaltimer_ns() - t0 > budget) {
       if (status) atomicExch(status, code);
       return false;
     }

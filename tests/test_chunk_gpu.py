@@ -273,3 +273,34 @@ def test_varlen_workload_from_prepare(gdp):
     rq, rk, rv, rb, rg = oracle.prepare(d["x"], d["ba"], d["A_log"], d["dt_bias"], M, H, G, P, N,
                                         decode=False)
     _check_all(o.cpu(), fs.cpu(), rq, rk, rv, rb, rg, M, cu=cu)
+
+
+def test_bounded_wait_runs_out_and_reports_timeout(gdp):
+    """Device-side failure path without a GPU fault: the test hook leaves one
+    tensor-core commit out of the WY kernel's first CTA and shortens the wait
+    budget to 50 ms, so that CTA's bounded wait runs out. The call must return,
+    the workspace status word must read GDP_ERR_DEVICE_TIMEOUT, and the next
+    normal call must be correct."""
+    import time
+    B, T, H, HV, K, V, M = 1, 300, 2, 2, 128, 128, 2
+    q, k, v, beta, g = chunk_case(B, T, H, HV, K, V, M, seed=14)
+    qd, kd, vd, bd, gd = to(DEV, q, k, v, beta, g)
+    need = gdp.gdp_chunk_fwd_workspace_size(B, T, B, H, HV, K, V, M, 64, torch.bfloat16)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    try:
+        gdp.gdp_debug_wait_fault(True, 0.05)
+        t0 = time.time()
+        gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, chunk_size=64, num_householder=M,
+                          use_qk_l2norm=True, workspace=ws)
+        status = gdp.gdp_read_status(ws)  # synchronises
+        elapsed = time.time() - t0
+    finally:
+        gdp.gdp_debug_wait_fault(False, 0.0)
+    assert status == 4, status  # GDP_ERR_DEVICE_TIMEOUT
+    assert elapsed < 5.0, elapsed
+    ws2 = torch.zeros_like(ws)
+    o, fs = gdp.gdp_chunk_fwd(qd, kd, vd, bd, gd, chunk_size=64, num_householder=M,
+                              use_qk_l2norm=True, workspace=ws2)
+    assert gdp.gdp_read_status(ws2) == 0
+    ro, rfs = oracle.walk(q, k, v, beta, g, M, K ** -0.5, l2norm=True)
+    assert rel_err(o, ro) <= 2e-3 and rel_err(fs, rfs) <= 2e-3
