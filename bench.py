@@ -350,6 +350,7 @@ def run_ours(args, rank, world, dev):
     e2e = run_e2e(args, gdp, d, dev, pf) if full else None
     decode = run_decode(args, gdp, dev, pk) if full else None
     prep_eager = run_prepare_eager(args, gdp, dev) if full else None
+    ungated = run_ungated(args, gdp, dev, pk, pk_src, pf) if full else None
     varlen = run_varlen(args, gdp, dev, pk, pk_src) if full else None
     gva = run_gva(args, gdp, dev, pk, pk_src) if full else None
     clocks = sampler.summary()
@@ -375,6 +376,7 @@ def run_ours(args, rank, world, dev):
         "kernels": kern,
         "decode": decode,
         "prepare_vs_eager": prep_eager,
+        "ungated": ungated,
         "config2_varlen": varlen,
         "config3_gva": gva,
         "e2e": e2e,
@@ -663,6 +665,30 @@ def run_varlen(args, gdp, dev, pk, pk_src):
         pk_src, fused, prepare_bytes(1, T, M, H, G, P, N, False))
     out["tokens"] = T
     return out
+
+
+def run_ungated(args, gdp, dev, pk, pk_src, pf):
+    """The headline workload's chunked forward without decay (g = None, the pages'
+    USE_G = false), on the q, k, v, beta the prepare step produced."""
+    w = WORKLOAD
+    q, k, v, beta, _ = pf.pre
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(gdp.GDP_STAGE_EVENTS)]
+
+    def step():
+        gdp.gdp_chunk_fwd(q, k, v, beta, None, chunk_size=w["BT"], num_householder=w["M"],
+                          use_qk_l2norm=True, workspace=pf.ws, out=(pf.o, pf.fs))
+
+    gdp.gdp_set_stage_events(stage)
+    times = _time_chunk_steps(gdp, step, stage, L2Flush(dev), max(5, min(args.steps, 20)), 3)
+    gdp.gdp_set_stage_events(None)
+    alg = method_work(w["B"] * w["T"], w["B"], w["H"], w["HV"], w["K"], w["V"], w["M"], w["BT"],
+                      pf.fused)
+    alg["bytes"] = {n: b - w["B"] * w["T"] * w["HV"] * 4 if n != "h" else b
+                    for n, b in alg["bytes"].items()}  # no g is read
+    alg["chunk_bytes"] -= w["B"] * w["T"] * w["HV"] * 4
+    return _workload_summary("prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64, ungated "
+                             "(g = None; chunk_fwd only)", times, alg, pk["bf16_tflops"],
+                             pk["hbm_gbs"], pk_src, pf.fused)
 
 
 def run_gva(args, gdp, dev, pk, pk_src):

@@ -937,7 +937,9 @@ __device__ bool solve_tril128(float* LA, float* scratch, uint32_t tmem, uint64_t
 // and v are loaded once the previous item's stores have read shared memory.
 // In both modes warp 15, idle in the second tile build, stages the next
 // item's beta and decay and takes their compensated prefix there.
-template <int V>
+// G = false is the ungated form (no decay, g = None on the pages): the decay
+// prefixes stay zero and no exponential is taken.
+template <int V, bool G>
 __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
     const __grid_constant__ CUtensorMap map_whs, const __grid_constant__ CUtensorMap map_wls,
@@ -1020,10 +1022,17 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     issue_v(x);
   }
   if (tid < 128) gates(x, tid, sarr[tid], sarr[128 + tid]);
+  if (!G) {  // both parities' decay prefixes (hi, lo; base e and base 2) stay zero
+    for (int i = tid; i < 2 * 128; i += 512) {
+      const int par = i >> 7, j = i & 127;
+      float* sp = sarr + par * 896;
+      sp[128 + j] = sp[256 + j] = sp[640 + j] = sp[768 + j] = 0.f;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) comp_prefix128_warp(sarr + 128, sarr + 256, lane);
+  if (G && warp == 0) comp_prefix128_warp(sarr + 128, sarr + 256, lane);
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   uint32_t mma_phase = 0;
@@ -1069,10 +1078,14 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 16384 + tid * 128, tid);
       const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
       srk[tid] = r;
-      sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
-      const float2 g2 = log2e_pair(sgh[tid], sgl[tid]);
-      s2h[tid] = g2.x;
-      s2l[tid] = g2.y;
+      if (G) {
+        sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
+        const float2 g2 = log2e_pair(sgh[tid], sgl[tid]);
+        s2h[tid] = g2.x;
+        s2l[tid] = g2.y;
+      } else {
+        sco[tid] = sb[tid] * r;
+      }
     }
     fence_async_smem();  // the k buffer's generic reads end before the next k load
     if (kPipe && tid == 0) tma_store_wait_read();  // the previous item's stores have read LA, tiles
@@ -1098,9 +1111,14 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
           const f2 ih = *reinterpret_cast<const f2*>(s2h + i);
           const f2 il = *reinterpret_cast<const f2*>(s2l + i);
           const f2 rk = *reinterpret_cast<const f2*>(srk + i);
-          const float2 d = upk2(add2(sub2(ph2, ih), sub2(pl2, il)));  // Gam_p - Gam_i, base 2
-          const float2 v = upk2(mul2(mul2(bp2, pk2(ex2_approx(d.x), ex2_approx(d.y))),
-                                     mul2(rk, pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])))));
+          const f2 kk = mul2(rk, pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])));
+          float2 v;
+          if (G) {
+            const float2 d = upk2(add2(sub2(ph2, ih), sub2(pl2, il)));  // Gam_p - Gam_i, base 2
+            v = upk2(mul2(mul2(bp2, pk2(ex2_approx(d.x), ex2_approx(d.y))), kk));
+          } else {
+            v = upk2(mul2(bp2, kk));
+          }
           LA[p * 129 + i] = (i < p) ? v.x : 0.f;
           LA[p * 129 + i + 1] = (i + 1 < p) ? v.y : 0.f;
         }
@@ -1152,9 +1170,11 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         }
       } else if (warp == 15 && has_next) {
         *reinterpret_cast<float4*>(nsb + 4 * lane) = make_float4(pb[0], pb[1], pb[2], pb[3]);
-        *reinterpret_cast<float4*>(nsb + 128 + 4 * lane) = make_float4(pg[0], pg[1], pg[2], pg[3]);
-        __syncwarp();
-        comp_prefix128_warp(nsb + 128, nsb + 256, lane);
+        if (G) {
+          *reinterpret_cast<float4*>(nsb + 128 + 4 * lane) = make_float4(pg[0], pg[1], pg[2], pg[3]);
+          __syncwarp();
+          comp_prefix128_warp(nsb + 128, nsb + 256, lane);
+        }
       }
       fence_async_smem();
       tc_fence_before();
@@ -1614,6 +1634,7 @@ __device__ __forceinline__ bool group_and(uint32_t id, uint32_t count, bool pred
   return r != 0;
 }
 
+template <bool G>
 __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
@@ -1747,7 +1768,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       {  // value phase: position p = row, columns cb .. cb + 15
         const int p = row;
         const float4 gp = gk[p];
-        const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
+        const float sc = (p < n) ? (G ? expf((glast.x - gp.x) + (glast.y - gp.y)) : 1.f) * gp.z : 0.f;
         ok = mbar_wait(&bars[FB_P1], ph, status, kDevTimeout) && ok;
         tc_fence_after();
         if (tid == 0 && ok && j + 1 < nb) load_w(R + 128);
@@ -1845,7 +1866,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         GDP_TMEM_LD16(tmem + lane_base + TD2 + cb, r0);
         GDP_TMEM_LD16(tmem + lane_base + TD2 + 32 + cb, r1);
         tmem_wait_ld();
-        const float dl = expf(glast.x + glast.y);
+        const float dl = G ? expf(glast.x + glast.y) : 1.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + (__uint_as_float(r0[c]) + __uint_as_float(r1[c]));
       }
@@ -1887,7 +1908,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       const uint8_t* qt = sm + F_Q;
       const float ss = row_sumsq(qt + t * 128, t) + row_sumsq(qt + 8192 + t * 128, t);
       const float4 rt = reinterpret_cast<const float4*>(sm + F_OG + (jb & 1) * 2048)[2 * t + 1];
-      const float2 g2 = log2e_pair(rt.x, rt.y);
+      const float2 g2 = G ? log2e_pair(rt.x, rt.y) : make_float2(0.f, 0.f);
       dst[t] = g2.x;
       dst[64 + t] = g2.y;
       dst[128 + t] = f.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
@@ -1934,9 +1955,14 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
           const int t = 32 * cgrp + i;
           const f2 th = *reinterpret_cast<const f2*>(stok + t);
           const f2 tl = *reinterpret_cast<const f2*>(stok + 64 + t);
-          const float2 d = upk2(add2(sub2(th, rh), sub2(tl, rl)));  // Gam_t - Gam_e, base 2
-          const float2 x = upk2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                     pk2(ex2_approx(d.x), ex2_approx(d.y))));
+          float2 x;
+          if (G) {
+            const float2 d = upk2(add2(sub2(th, rh), sub2(tl, rl)));  // Gam_t - Gam_e, base 2
+            x = upk2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                          pk2(ex2_approx(d.x), ex2_approx(d.y))));
+          } else {
+            x = make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          }
           r[i] = __float_as_uint((e < n && s <= t && t < nt) ? x.x : 0.f);
           r[i + 1] = __float_as_uint((e < n && s <= t + 1 && t + 1 < nt) ? x.y : 0.f);
         }
@@ -1984,7 +2010,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         GDP_TMEM_LD16(tmem + lane_base + TQH + 64 * cs + 32 + cb, rq2);
         tmem_wait_ld();
         if (t < nt && ok) {
-          const float qs = ex2_approx(stok[t] + stok[64 + t]), rqn = stok[128 + t];  // o = scale |q|^-1 (e^Gam Qh + O)
+          const float qs = G ? ex2_approx(stok[t] + stok[64 + t]) : 1.f, rqn = stok[128 + t];  // o = scale |q|^-1 (e^Gam Qh + O)
           float4* dst = reinterpret_cast<float4*>(f.o + ((T0 + t) * HVn + hv) * V + v0 + cb);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -2276,7 +2302,7 @@ cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
   return cudaGetLastError();
 }
 
-template <int V>
+template <int V, bool G>
 cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   const int64_t Te = (int64_t)p.B * p.T * p.M;
   CUtensorMap mk, mv, mwh, mwl, mu;
@@ -2286,14 +2312,14 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
       !map3(&mwl, a.w_lo, BF, 2, kK, p.HV, Te, 64, 128, true) ||
       !map3(&mu, a.u, F32, 4, V, p.HV, Te, 32, 128, true))
     return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(wy128_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(wy128_tc_kernel<V, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
   const int64_t NB = block128_bound(p.B, p.T, p.N_seq, p.M);
   const int64_t items = NB * p.HV;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = (int)std::min<int64_t>(items, sm_count());  // persistent, one CTA per SM
-  wy128_tc_kernel<V><<<grid, 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a, (int)NB);
+  wy128_tc_kernel<V, G><<<grid, 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a, (int)NB);
   return cudaGetLastError();
 }
 
@@ -2371,10 +2397,11 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
              w_hi, w_lo, u, gk, status, 0};
     if ((p.M % 2) == 0) a.fault = g_wy_fault.exchange(0);  // one-shot test hook
     const bool blk128 = (p.M % 2) == 0;
+    const bool G = p.g != nullptr;
     switch (p.V) {
-      case 64: e = blk128 ? run_wy128<64>(p, a) : run_wy<64>(p, a); break;
-      case 128: e = blk128 ? run_wy128<128>(p, a) : run_wy<128>(p, a); break;
-      default: e = blk128 ? run_wy128<256>(p, a) : run_wy<256>(p, a); break;
+      case 64: e = !blk128 ? run_wy<64>(p, a) : G ? run_wy128<64, true>(p, a) : run_wy128<64, false>(p, a); break;
+      case 128: e = !blk128 ? run_wy<128>(p, a) : G ? run_wy128<128, true>(p, a) : run_wy128<128, false>(p, a); break;
+      default: e = !blk128 ? run_wy<256>(p, a) : G ? run_wy128<256, true>(p, a) : run_wy128<256, false>(p, a); break;
     }
     if (e != cudaSuccess) return e;
   }
@@ -2399,9 +2426,10 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       if (!map3(&mq, p.q ? p.q : w_hi, BF, 2, kK, p.H, Tt > 0 ? Tt : 1, 64, 64, true))
         return cudaErrorInvalidValue;
       HOArgs fa{a, p.H, p.l2norm, p.scale, p.o};
-      e = cudaFuncSetAttribute(ho128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+      auto kern = p.g ? ho128_tc_kernel<true> : ho128_tc_kernel<false>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
       if (e != cudaSuccess) return e;
-      ho128_tc_kernel<<<grid, 512, F_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, mq, fa);
+      kern<<<grid, 512, F_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, mq, fa);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       record_stage(3, p.stream);
       record_stage(4, p.stream);
