@@ -330,14 +330,16 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // memory. Row R's 16-byte chunk c lands at chunk c ^ (2 (R / 32)): the four
 // row groups a warp reads at once then fall on distinct banks. Columns past V
 // are zero-filled.
+// srh: the item's state-row block (slot * HV + hv); SLOTS: srh < 0 means the
+// item has no state, every chunk is zero-filled and nothing is read.
+template <bool SLOTS>
 __device__ __forceinline__ void prefetch_state(float* sst, const float* state, int it, int ncs,
                                                int V, int64_t srh) {
-  const int rh = it / ncs, cs = it - rh * ncs;
-  (void)rh;
+  const int cs = it % ncs;
   const int tid = threadIdx.x, c16 = tid & 15;
-  // srh < 0 (no state for this item): every chunk is zero-filled, nothing is read
-  const int valid = (srh >= 0 && cs * kSliceCols + 4 * c16 < V) ? 16 : 0;
-  const float* src = state + (srh >= 0 ? srh : 0) * 128 * V + cs * kSliceCols + (valid ? 4 * c16 : 0);
+  const bool has = !SLOTS || srh >= 0;
+  const int valid = (has && cs * kSliceCols + 4 * c16 < V) ? 16 : 0;
+  const float* src = state + (has ? srh : 0) * 128 * V + cs * kSliceCols + (valid ? 4 * c16 : 0);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int row = (tid >> 4) + 16 * i;
@@ -355,15 +357,18 @@ __device__ __forceinline__ float* state_ptr(float* state, int it, int ncs, int V
 }
 
 // State-row block (slot * HV + hv) of item `it`, or -1 when the item's request
-// has no state (padding or a rejected slot).
+// has no state (padding or a rejected slot). Without slots it is request * HV + hv.
+template <bool SLOTS>
 __device__ __forceinline__ int64_t item_srh(int it, int ncs, int HV, const int* slot, int n,
                                             int n_slots, int* status) {
-  const int rh = it / ncs, r = rh / HV, hv = rh - r * HV;
+  const int rh = it / ncs;
+  if (!SLOTS) return rh;
+  const int r = rh / HV, hv = rh - r * HV;
   const int sl = resolve_slot(slot, n, n_slots, r, status);
   return sl < 0 ? -1 : (int64_t)sl * HV + hv;
 }
 
-template <typename Tin>
+template <typename Tin, bool SLOTS>
 __global__ void __launch_bounds__(256, 2)
 recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                     const Tin* __restrict__ v, const float* __restrict__ beta,
@@ -383,17 +388,17 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
   int it = blockIdx.x;
   if (it >= n_items) return;
   Batch<Tin> pf;
-  int64_t srh = item_srh(it, ncs, HV, slot, n, n_slots, status);
-  prefetch_state(sst, state, it, ncs, V, srh);
+  int64_t srh = item_srh<SLOTS>(it, ncs, HV, slot, n, n_slots, status);
+  prefetch_state<SLOTS>(sst, state, it, ncs, V, srh);
   load_batch(pf, q, k, v, beta, g, it, 0, L, H, HV, V, ncs);
   for (; it < n_items; it += gridDim.x) {
     const int rh = it / ncs, cs = it - rh * ncs;
     const int r = rh / HV, hv = rh - r * HV;
     const int col = cs * kSliceCols + cw;
     const bool active = col < V;
-    const bool live = srh >= 0;  // false: padding or rejected slot (no state, zero o rows)
+    const bool live = !SLOTS || srh >= 0;  // false: padding or rejected slot (zero o rows)
     const int nx = it + gridDim.x;
-    int64_t srh_nx = -1;
+    int64_t srh_nx = SLOTS ? -1 : (int64_t)(nx / ncs);
     cp_async_wait_all();
     __syncthreads();  // this item's state is in shared memory
     f2 h[16];  // rows (2i, 2i + 1) of this thread's 32, packed
@@ -439,8 +444,8 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
       // the state buffer has been read (barrier above): the next item's state
       // streams in behind this item's steps
       if (e0 == 0 && nx < n_items) {
-        srh_nx = item_srh(nx, ncs, HV, slot, n, n_slots, status);
-        prefetch_state(sst, state, nx, ncs, V, srh_nx);
+        srh_nx = item_srh<SLOTS>(nx, ncs, HV, slot, n, n_slots, status);
+        prefetch_state<SLOTS>(sst, state, nx, ncs, V, srh_nx);
       }
       if (e0 + kB < L)
         load_batch(pf, q, k, v, beta, g, it, e0 + kB, L, H, HV, V, ncs);
@@ -503,10 +508,10 @@ cudaError_t launch_k128(const void* q, const void* k, const void* v, const float
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = (int)std::min<int64_t>(items, (int64_t)sm_count() * 2);  // 2 resident CTAs / SM
   constexpr int smem = 128 * kSliceCols * 4;
-  cudaError_t e = cudaFuncSetAttribute(recurrent128_kernel<Tin>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = sa.slot ? recurrent128_kernel<Tin, true> : recurrent128_kernel<Tin, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  recurrent128_kernel<Tin><<<grid, 256, smem, s>>>(
+  kern<<<grid, 256, smem, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), beta,
       g, state, (int)items, L, H, HV, V, ncs, scale, l2norm, o, sa.slot, sa.n, sa.n_slots,
       sa.status);

@@ -129,3 +129,19 @@ def test_deterministic(gdp):
     b = gdp.gdp_prefill_prepare(*args)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+@pytest.mark.parametrize("M,H,G,P,N", [(3, 16, 4, 128, 128), (2, 32, 8, 128, 128),
+                                       (5, 8, 8, 64, 128)])
+def test_prepare_long_rows_in_segments(gdp, decode, M, H, G, P, N):
+    """Rows of 1.4-3k 16-byte vectors: the row kernel cuts them into several
+    segments (the last one shorter), over strided rows."""
+    n, T = 2, 7
+    d = si.prepare_inputs(n, T, M, H, G, P, N, seed=M + H)
+    D = d["x"].shape[-1]
+    big = torch.zeros(n, T, D + 64, dtype=torch.bfloat16)
+    big[:, :, 64:] = d["x"]
+    x = big.to(DEV)[:, :, 64:]
+    assert not x.is_contiguous()
+    _check(gdp, x, d["ba"], d["A_log"], d["dt_bias"], M, H, G, P, N, decode)
