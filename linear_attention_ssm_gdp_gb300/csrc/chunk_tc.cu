@@ -599,8 +599,12 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
   const int quarter = warp & 3, chalf = warp >> 2;
   const int row = quarter * 32 + lane;          // state row kf / position p
   const int cb = chalf * kHCols;                // first of this thread's 16 columns
-  const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
-  const int v0 = blockIdx.z * kHBV;
+  // blockIdx.x = sequence * (V / 32) + value slice: the slices of one
+  // (sequence, head), which read the same w and k tiles, run side by side and
+  // share those tiles through L2
+  const int nsl = a.V / kHBV;
+  const int seq = blockIdx.x / nsl, hv = blockIdx.y, kh = hv / (a.HV / H);
+  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
   const int V = a.V, M = a.M;
   const int4 si = a.seq_info[seq];
   const int ne = (int)cdiv((int64_t)si.y * M, kBT);
@@ -1382,8 +1386,12 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   const int row = quarter * 32 + lane;          // state row kf / position p
   constexpr int NC = 16;                        // value columns per thread
   const int cb = cgrp * NC;
-  const int seq = blockIdx.x, hv = blockIdx.y, kh = hv / (a.HV / H);
-  const int v0 = blockIdx.z * kHBV;
+  // blockIdx.x = sequence * (V / 32) + value slice: the slices of one
+  // (sequence, head), which read the same w and k tiles, run side by side and
+  // share those tiles through L2
+  const int nsl = a.V / kHBV;
+  const int seq = blockIdx.x / nsl, hv = blockIdx.y, kh = hv / (a.HV / H);
+  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
   const int V = a.V, M = a.M;
   const int4 si = a.seq_info[seq];
   const int nb = (int)cdiv((int64_t)si.y * M, 128);
@@ -1648,10 +1656,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   const int row = quarter * 32 + lane;
   constexpr int NC = 16;
   const int cb = cgrp * NC;
-  const int seq = blockIdx.x, hv = blockIdx.y;
   const int HVn = f.h.HV, V = f.h.V;
+  // blockIdx.x = sequence * (V / 32) + value slice (slices of one head side by side)
+  const int nsl = V / kHBV;
+  const int seq = blockIdx.x / nsl, hv = blockIdx.y;
   const int kh = hv / (HVn / f.H);
-  const int v0 = blockIdx.z * kHBV;
+  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
   const int4 si = f.h.seq_info[seq];
   const int nb = (int)cdiv((int64_t)si.y * 2, 128);
   int* status = f.h.status;
@@ -2069,12 +2079,16 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int2 tab = a.tok_tab[blockIdx.x];
+  // blockIdx.x = token chunk * (V / 64) + value slice: the slices of one chunk,
+  // which read the same q and k tiles, run side by side
+  const int nsl = a.V / kOBV;
+  const int tc = blockIdx.x / nsl;
+  const int2 tab = a.tok_tab[tc];
   if (tab.x < 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
-  const int v0 = blockIdx.z * kOBV;
+  const int v0 = (blockIdx.x - tc * nsl) * kOBV;
   const int4 si = a.seq_info[tab.x];
   const int t_start = tab.y * kBT;
   const int nt = min(kBT, si.y - t_start);
@@ -2333,7 +2347,7 @@ cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi
   const int smem = o_smem(M);
   cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  o_tc_kernel<M><<<dim3((unsigned)p.NT_max, p.HV, (unsigned)(p.V / kOBV)), 512, smem, p.stream>>>(
+  o_tc_kernel<M><<<dim3((unsigned)(p.NT_max * (p.V / kOBV)), p.HV), 512, smem, p.stream>>>(
       mq, mk, mhhi, mhlo, mvhi, mvlo, a);
   return cudaGetLastError();
 }
@@ -2419,7 +2433,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
         !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, rows, false))
       return cudaErrorInvalidValue;
     HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
-    const dim3 grid(p.N_seq, p.HV, (unsigned)(p.V / kHBV));
+    const dim3 grid((unsigned)((int64_t)p.N_seq * (p.V / kHBV)), p.HV);
     if (p.M == 2) {  // state recurrence and output fused
       CUtensorMap mq;
       const int64_t Tt = (int64_t)p.B * p.T;
