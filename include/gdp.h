@@ -99,6 +99,70 @@ gdp_status gdp_decode_prepare(const void* x, int64_t x_sn, int64_t x_st, const v
                               float* g, cudaStream_t stream);
 
 /*
+ * gdp_prefill_conv_prepare - the short causal conv that precedes prepare in
+ * the layer, fused with gdp_prefill_prepare (prepare page, module overview:
+ * prepare consumes the conv's output, and padding is handled by that conv).
+ * The pages name the conv but not its form; this call takes the usual
+ * depthwise causal short conv with SiLU:
+ *   z[t, c] = conv_b[c] + sum_{i<W} conv_w[c, i] * xin[t - (W-1) + i, c]
+ *   x[t, c] = z / (1 + exp(-z)), rounded to dtype `dt`,
+ * in fp32, one operation at a time (no fused multiply-add), and then applies
+ * exactly the map of gdp_prefill_prepare to x. The conv output never reaches
+ * memory.
+ *   xp        [n, T, C] pre-conv activations, C = M*H*P + M*G*N + G*N (the
+ *             channel layout of prepare's x), strides xp_sn, xp_st.
+ *   conv_w    [C, W] fp32, tap i multiplies input t - (W-1) + i; W in 1..4.
+ *   conv_b    [C] fp32 or NULL (no bias).
+ *   conv_state_in  [N_seq, C, W-1] (dtype dt) or NULL (zeros): per sequence,
+ *             the W-1 inputs before its first token, oldest first.
+ *   conv_state_out [N_seq, C, W-1] (dtype dt) or NULL: per sequence, the last
+ *             W-1 inputs of (conv_state_in ++ its tokens), for the next call.
+ *             Must not alias conv_state_in.
+ *   cu_seqlens [N_seq + 1] int32 token offsets (device) with n == 1, or NULL
+ *             (then N_seq == n and each batch row is one sequence); the conv
+ *             does not cross a sequence start. Rows past cu_seqlens[N_seq]
+ *             are not written.
+ * ba, A_log, dt_bias, the sizes and the outputs q, k, v, beta, g are those of
+ * gdp_prefill_prepare. Requires 16-byte channel vectors: P and N times the
+ * element size multiples of 16 bytes, 16-byte aligned xp, q, k, v and row
+ * strides (else GDP_ERR_UNSUPPORTED).
+ */
+gdp_status gdp_prefill_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
+                                    const float* conv_w, const float* conv_b, int W,
+                                    const void* conv_state_in, void* conv_state_out,
+                                    const int32_t* cu_seqlens, int N_seq, const void* ba,
+                                    int64_t ba_sn, int64_t ba_st, const float* A_log,
+                                    const float* dt_bias, int n, int T, int M, int H, int G,
+                                    int P, int N, gdp_dtype dt, void* q, void* k, void* v,
+                                    float* beta, float* g, cudaStream_t stream);
+
+/*
+ * gdp_decode_conv_prepare - the conv of gdp_prefill_conv_prepare fused with
+ * gdp_decode_prepare for one decode step of S tokens per request, with the
+ * conv states in a pool indexed by request (prepare page, module overview: "a
+ * -1 slot zeroes its conv output, which propagates here"):
+ *   conv_state_pool [n_slots, C, W-1] (dtype dt), read and updated in place
+ *             at the entries the slots name (the new state is the last W-1
+ *             inputs of entry ++ the request's S tokens);
+ *   conv_slot [n] int32 (device): the request's pool entry, or -1 for a
+ *             padding request, whose q, k and v are written as zeros and which
+ *             touches no state (beta and g still come from ba);
+ *   status    (device, nullable) int32 set to 1 when a slot is outside
+ *             [-1, n_slots) or named by two requests; those requests are
+ *             treated as padding. The call never clears it.
+ * Other arguments and outputs as gdp_decode_prepare (S in 1..16) and
+ * gdp_prefill_conv_prepare. No host synchronisation; graph-capturable.
+ */
+gdp_status gdp_decode_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
+                                   const float* conv_w, const float* conv_b, int W,
+                                   void* conv_state_pool, const int32_t* conv_slot, int n_slots,
+                                   const void* ba, int64_t ba_sn, int64_t ba_st,
+                                   const float* A_log, const float* dt_bias, int n, int S, int M,
+                                   int H, int G, int P, int N, gdp_dtype dt, void* q, void* k,
+                                   void* v, float* beta, float* g, int32_t* status,
+                                   cudaStream_t stream);
+
+/*
  * gdp_chunk_fwd_workspace_size - bytes of device workspace gdp_chunk_fwd
  * needs for these sizes (pure host arithmetic; 0 if the sizes are invalid).
  * N_seq is the number of packed sequences when cu_seqlens is used, else B.

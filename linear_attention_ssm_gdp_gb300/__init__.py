@@ -20,7 +20,8 @@ __all__ = [
     "load", "GDPError", "gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
     "gdp_chunk_fwd_workspace_size", "gdp_chunk_fwd_stage_offsets", "gdp_recurrent_update",
     "gdp_read_status", "gdp_version", "gdp_set_stage_events", "gdp_chunk_fwd_noalloc",
-    "gdp_recurrent_update_slots", "gdp_debug_wait_fault",
+    "gdp_recurrent_update_slots", "gdp_debug_wait_fault", "gdp_prefill_conv_prepare",
+    "gdp_decode_conv_prepare",
     "LIB_PATH",
 ]
 
@@ -53,6 +54,10 @@ def load() -> ctypes.CDLL:
             prep = [P, I64, I64, P, I64, I64, P, P] + [I] * 7 + [I] + [P] * 5 + [P]
             lib.gdp_prefill_prepare.argtypes = prep
             lib.gdp_decode_prepare.argtypes = prep
+            lib.gdp_prefill_conv_prepare.argtypes = ([P, I64, I64, P, P, I, P, P, P, I, P, I64, I64,
+                                                      P, P] + [I] * 8 + [P] * 6)
+            lib.gdp_decode_conv_prepare.argtypes = ([P, I64, I64, P, P, I, P, P, I, P, I64, I64, P,
+                                                     P] + [I] * 8 + [P] * 7)
             lib.gdp_chunk_fwd_workspace_size.argtypes = [I] * 9 + [I]
             lib.gdp_chunk_fwd_workspace_size.restype = SZ
             lib.gdp_chunk_fwd_stage_offsets.argtypes = [I] * 9 + [I, P]
@@ -70,6 +75,7 @@ def load() -> ctypes.CDLL:
             lib.gdp_status_string.restype = ctypes.c_char_p
             lib.gdp_version.argtypes = []
             for f in ("gdp_prefill_prepare", "gdp_decode_prepare", "gdp_chunk_fwd",
+                      "gdp_prefill_conv_prepare", "gdp_decode_conv_prepare",
                       "gdp_recurrent_update", "gdp_recurrent_update_slots", "gdp_read_status",
                       "gdp_chunk_fwd_stage_offsets",
                       "gdp_version"):
@@ -347,3 +353,89 @@ def gdp_debug_wait_fault(arm: bool, budget_seconds: float = 0.0):
     the wait budget (<= 0: the default 2 s)."""
     _check("gdp_debug_wait_fault", load().gdp_debug_wait_fault(1 if arm else 0,
                                                                 float(budget_seconds)))
+
+
+def _conv_common(xp, conv_w, conv_b, ba, A_log, dt_bias, M, H, G, P, N):
+    _need_cuda(xp, conv_w, conv_b, ba, A_log, dt_bias)
+    if xp.dtype not in _DTYPE or ba.dtype != xp.dtype:
+        raise ValueError("xp and ba must share a dtype in {bf16, fp16, fp32}")
+    if xp.dim() != 3 or ba.dim() != 3 or xp.stride(-1) != 1 or ba.stride(-1) != 1:
+        raise ValueError("xp and ba must be [n, T, D] with a contiguous last dimension")
+    n, T, C = xp.shape
+    if C != M * H * P + M * G * N + G * N or tuple(ba.shape) != (n, T, M * H + H):
+        raise ValueError("xp/ba last dimensions do not match M, H, G, P, N")
+    if conv_w.dim() != 2 or conv_w.shape[0] != C:
+        raise ValueError("conv_w must be [C, W]")
+    W = conv_w.shape[1]
+    conv_w = conv_w.to(torch.float32).contiguous()
+    conv_b = None if conv_b is None else conv_b.to(torch.float32).contiguous()
+    return n, T, C, W, conv_w, conv_b, A_log.to(torch.float32).contiguous(), \
+        dt_bias.to(torch.float32).contiguous()
+
+
+def gdp_prefill_conv_prepare(xp, conv_w, conv_b, ba, A_log, dt_bias, num_householder: int,
+                             num_heads: int, num_groups: int, head_dim: int, state_dim: int,
+                             conv_state=None, cu_seqlens=None, return_conv_state=True,
+                             out=None):
+    """Short causal conv (+ SiLU) fused with the prefill prepare. Returns
+    (q, k, v, beta, g, conv_state_out or None); conv_state_out [N, C, W-1]."""
+    M, H, G, P, N = num_householder, num_heads, num_groups, head_dim, state_dim
+    n, T, C, W, conv_w, conv_b, A_log, dt_bias = _conv_common(xp, conv_w, conv_b, ba, A_log,
+                                                              dt_bias, M, H, G, P, N)
+    NS = n if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    if conv_state is not None and (tuple(conv_state.shape) != (NS, C, W - 1)
+                                   or conv_state.dtype != xp.dtype
+                                   or not conv_state.is_contiguous()):
+        raise ValueError("conv_state must be [N, C, W-1] in xp's dtype")
+    dev = xp.device
+    if out is None:
+        out = (torch.empty((n, T, H, N), dtype=xp.dtype, device=dev),
+               torch.empty((n, T * M, H, N), dtype=xp.dtype, device=dev),
+               torch.empty((n, T * M, H, P), dtype=xp.dtype, device=dev),
+               torch.empty((n, T * M, H), dtype=torch.float32, device=dev),
+               torch.empty((n, T, H), dtype=torch.float32, device=dev))
+    q, k, v, beta, g = out
+    st_out = (torch.empty((NS, C, W - 1), dtype=xp.dtype, device=dev)
+              if return_conv_state else None)
+    st = load().gdp_prefill_conv_prepare(
+        _p(xp), xp.stride(0), xp.stride(1), _p(conv_w), _p(conv_b), W, _p(conv_state),
+        _p(st_out), _p(cu_seqlens), NS, _p(ba), ba.stride(0), ba.stride(1), _p(A_log),
+        _p(dt_bias), n, T, M, H, G, P, N, _DTYPE[xp.dtype], _p(q), _p(k), _p(v), _p(beta),
+        _p(g), _stream(dev))
+    _check("gdp_prefill_conv_prepare", st)
+    return q, k, v, beta, g, st_out
+
+
+def gdp_decode_conv_prepare(xp, conv_w, conv_b, ba, A_log, dt_bias, num_householder: int,
+                            num_heads: int, num_groups: int, head_dim: int, state_dim: int,
+                            conv_state_pool, conv_slot, status=None, out=None):
+    """Short causal conv (+ SiLU) fused with the decode prepare; conv states live in
+    ``conv_state_pool`` [n_slots, C, W-1] (updated in place), ``conv_slot`` int32 [n]
+    names each request's entry (-1: padding, zero q/k/v). Returns (q, k, v, beta, g)."""
+    M, H, G, P, N = num_householder, num_heads, num_groups, head_dim, state_dim
+    n, S, C, W, conv_w, conv_b, A_log, dt_bias = _conv_common(xp, conv_w, conv_b, ba, A_log,
+                                                              dt_bias, M, H, G, P, N)
+    _need_cuda(conv_state_pool, conv_slot, status)
+    if (conv_state_pool.dim() != 3 or tuple(conv_state_pool.shape[1:]) != (C, W - 1)
+            or conv_state_pool.dtype != xp.dtype or not conv_state_pool.is_contiguous()):
+        raise ValueError("conv_state_pool must be [n_slots, C, W-1] in xp's dtype")
+    if tuple(conv_slot.shape) != (n,) or conv_slot.dtype != torch.int32:
+        raise ValueError("conv_slot must be int32 [n]")
+    dev = xp.device
+    L = S * M
+    if out is None:
+        out = (torch.empty((n, L, H, N), dtype=xp.dtype, device=dev),
+               torch.empty((n, L, H, N), dtype=xp.dtype, device=dev),
+               torch.empty((n, L, H, P), dtype=xp.dtype, device=dev),
+               torch.empty((n, L, H), dtype=torch.float32, device=dev),
+               torch.empty((n, L, H), dtype=torch.float32, device=dev))
+    q, k, v, beta, g = out
+    st = load().gdp_decode_conv_prepare(
+        _p(xp), xp.stride(0), xp.stride(1), _p(conv_w), _p(conv_b), W, _p(conv_state_pool),
+        _p(conv_slot), conv_state_pool.shape[0], _p(ba), ba.stride(0), ba.stride(1), _p(A_log),
+        _p(dt_bias), n, S, M, H, G, P, N, _DTYPE[xp.dtype], _p(q), _p(k), _p(v), _p(beta),
+        _p(g), _p(status), _stream(dev))
+    _check("gdp_decode_conv_prepare", st)
+    return q, k, v, beta, g

@@ -131,6 +131,79 @@ gdp_status gdp_decode_prepare(const void* x, int64_t x_sn, int64_t x_st, const v
   return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The fused conv + prepare calls need 16-byte channel vectors: every head
+// size a multiple of 16 bytes, 16-byte aligned bases and row strides.
+gdp_status check_conv(const void* xp, int64_t xp_sn, int64_t xp_st, const float* w, int W, int P,
+                      int N, gdp_dtype dt, const void* q, const void* k, const void* v) {
+  if (W < 1 || W > 4 || !w) return W < 1 || !w ? GDP_ERR_INVALID_ARG : GDP_ERR_UNSUPPORTED;
+  const int64_t es = dt == GDP_F32 ? 4 : 2;
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if ((P * es) % 16 || (N * es) % 16 || (xp_sn * es) % 16 || (xp_st * es) % 16 || !al(xp) ||
+      !al(q) || !al(k) || !al(v))
+    return GDP_ERR_UNSUPPORTED;
+  return GDP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdp_status gdp_prefill_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
+                                    const float* conv_w, const float* conv_b, int W,
+                                    const void* conv_state_in, void* conv_state_out,
+                                    const int32_t* cu_seqlens, int N_seq, const void* ba,
+                                    int64_t ba_sn, int64_t ba_st, const float* A_log,
+                                    const float* dt_bias, int n, int T, int M, int H, int G,
+                                    int P, int N, gdp_dtype dt, void* q, void* k, void* v,
+                                    float* beta, float* g, cudaStream_t stream) {
+  gdp_status s = check_prepare(xp, xp_sn, xp_st, ba, ba_sn, ba_st, A_log, dt_bias, n, T, M, H,
+                               G, P, N, dt, q, k, v, beta, g);
+  if (s != GDP_OK) return s;
+  if (cu_seqlens ? (n != 1 || N_seq < 0) : (N_seq != n)) return GDP_ERR_INVALID_ARG;
+  if (conv_state_in && conv_state_in == conv_state_out) return GDP_ERR_INVALID_ARG;
+  if (W < 1 || !conv_w) return GDP_ERR_INVALID_ARG;
+  if ((int64_t)n * T == 0) {  // no tokens: every sequence keeps its initial state
+    if (!conv_state_out || W == 1 || N_seq == 0) return GDP_OK;
+    const size_t bytes = (size_t)N_seq * ((size_t)M * H * P + (size_t)M * G * N + (size_t)G * N) *
+                         (size_t)(W - 1) * (dt == GDP_F32 ? 4 : 2);
+    const cudaError_t e = conv_state_in ? cudaMemcpyAsync(conv_state_out, conv_state_in, bytes,
+                                                          cudaMemcpyDeviceToDevice, stream)
+                                        : cudaMemsetAsync(conv_state_out, 0, bytes, stream);
+    return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
+  }
+  if ((s = check_conv(xp, xp_sn, xp_st, conv_w, W, P, N, dt, q, k, v)) != GDP_OK) return s;
+  const cudaError_t e = launch_conv_prepare(
+      xp, xp_sn, xp_st, conv_w, conv_b, W, conv_state_in, conv_state_out, cu_seqlens, N_seq,
+      nullptr, 0, nullptr, ba, ba_sn, ba_st, A_log, dt_bias, n, T, M, H, G, P, N, dt, false, q,
+      k, v, beta, g, stream);
+  return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
+}
+
+gdp_status gdp_decode_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
+                                   const float* conv_w, const float* conv_b, int W,
+                                   void* conv_state_pool, const int32_t* conv_slot, int n_slots,
+                                   const void* ba, int64_t ba_sn, int64_t ba_st,
+                                   const float* A_log, const float* dt_bias, int n, int S, int M,
+                                   int H, int G, int P, int N, gdp_dtype dt, void* q, void* k,
+                                   void* v, float* beta, float* g, int32_t* status,
+                                   cudaStream_t stream) {
+  if (S < 1 || S > 16 || n_slots < 0) return GDP_ERR_INVALID_ARG;
+  gdp_status s = check_prepare(xp, xp_sn, xp_st, ba, ba_sn, ba_st, A_log, dt_bias, n, S, M, H,
+                               G, P, N, dt, q, k, v, beta, g);
+  if (s != GDP_OK || n == 0) return s;
+  if (!conv_slot || (W > 1 && n_slots > 0 && !conv_state_pool)) return GDP_ERR_INVALID_ARG;
+  if ((s = check_conv(xp, xp_sn, xp_st, conv_w, W, P, N, dt, q, k, v)) != GDP_OK) return s;
+  const cudaError_t e = launch_conv_prepare(
+      xp, xp_sn, xp_st, conv_w, conv_b, W, conv_state_pool, conv_state_pool, nullptr, n,
+      conv_slot, n_slots, status, ba, ba_sn, ba_st, A_log, dt_bias, n, S, M, H, G, P, N, dt,
+      true, q, k, v, beta, g, stream);
+  return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
+}
+
 size_t gdp_chunk_fwd_workspace_size(int B, int T, int N_seq, int H, int HV, int K, int V, int M,
                                     int chunk_size, gdp_dtype dt) {
   if (!sizes_valid(B, T, N_seq, H, HV, K, V, M, chunk_size) || !dtype_ok(dt)) return 0;

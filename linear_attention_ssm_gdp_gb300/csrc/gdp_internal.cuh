@@ -81,6 +81,17 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
                            int N, gdp_dtype dt, bool decode, void* q, void* k, void* v,
                            float* beta, float* g, cudaStream_t stream);
 
+// Short causal conv fused with prepare (prepare.cu). Prefill: st_in/st_out are
+// per-sequence conv states (nullable), cu the varlen offsets (nullable). Decode:
+// st_in == st_out is the state pool, slot the per-request pool entries.
+cudaError_t launch_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st, const float* w,
+                                const float* bias, int W, const void* st_in, void* st_out,
+                                const int32_t* cu, int N_seq, const int32_t* slot, int n_slots,
+                                int32_t* status, const void* ba, int64_t ba_sn, int64_t ba_st,
+                                const float* A_log, const float* dt_bias, int n, int T, int M,
+                                int H, int G, int P, int N, gdp_dtype dt, bool decode, void* q,
+                                void* k, void* v, float* beta, float* g, cudaStream_t stream);
+
 cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
 cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);
 cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* ws);

@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "gdp_internal.cuh"
 
 namespace gdp {
@@ -264,6 +266,310 @@ __global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Short causal conv fused with prepare. The step before prepare in the layer
+// (the prepare page's module overview: "padding handled by the conv kernel
+// upstream (a -1 slot zeroes its conv output, which propagates here)") is a
+// depthwise causal conv of width W over the pre-conv activations xp [n, T, C]
+// (C = M*H*P + M*G*N + G*N, the channel layout prepare splits), followed by
+// SiLU:  z = bias[c] + sum_i w[c][i] xin[t - (W-1) + i][c],  y = z / (1 + e^-z),
+// rounded to the activation dtype. Each sequence continues from its conv state
+// (the last W-1 inputs before it, oldest first, [.., C, W-1] in the activation
+// dtype; zeros without one). Here the conv output never reaches HBM: each
+// thread keeps a sliding window of W-1 inputs for 16 bytes of channels, walks a
+// tile of consecutive tokens, and writes the SiLU outputs straight to their
+// q/k/v destinations (group expansion and copy placement as prepare_kernel).
+// CTAs of channel segment 0 also compute the gates of their rows.
+struct ConvArgs {
+  PrepArgs pa;               // x = xp (pre-conv), strides in bytes
+  const float* w;            // [C][W]
+  const float* bias;         // [C] or null
+  int W, C, RT;              // taps, channels, token rows per tile (prefill)
+  const uint8_t* st_in;      // prefill: [N_seq][C][W-1] or null; decode: the pool
+  uint8_t* st_out;           // prefill: [N_seq][C][W-1] or null; decode: the pool
+  const int* cu;             // prefill varlen offsets [N_seq + 1] (n == 1) or null
+  int N_seq;
+  const int* slot;           // decode: [n] pool entries (-1 padding)
+  int n_slots;
+  int* status;               // decode: set to 1 for an out-of-range or repeated slot
+};
+
+template <typename T>
+__device__ __forceinline__ float cv_ld(const uint8_t* p) {
+  return to_f32(p, 0, sizeof(T) == 4 ? GDP_F32 : (std::is_same<T, __half>::value ? GDP_F16 : GDP_BF16));
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void cv_unpack(uint4 u, float* f) {
+  if constexpr (VE == 4) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  } else {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (std::is_same<T, __half>::value) {
+        f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xffffu)));
+        f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+      } else {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    }
+  }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ uint4 cv_pack(const float* f) {
+  if constexpr (VE == 4) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      unsigned short a, b;
+      if constexpr (std::is_same<T, __half>::value) {
+        a = __half_as_ushort(__float2half_rn(f[2 * i]));
+        b = __half_as_ushort(__float2half_rn(f[2 * i + 1]));
+      } else {
+        a = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i]));
+        b = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i + 1]));
+      }
+      w[i] = (uint32_t)a | ((uint32_t)b << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Writes one 16-byte vector of post-conv channels c0.. (within one head) of
+// token row `row` to its q/k/v destinations (prepare's map).
+template <bool DECODE>
+__device__ __forceinline__ void cv_scatter(const PrepArgs& a, int64_t row, int c0, uint4 val) {
+  const int es = a.es, hpg = a.H / a.G;
+  const int KB = a.M * a.H * a.P, QB = KB + a.M * a.G * a.N;
+  if (c0 < KB) {
+    const int j = c0 / (a.H * a.P), rem = c0 - j * a.H * a.P, h = rem / a.P, p = rem - h * a.P;
+    __stcs(reinterpret_cast<uint4*>(a.v + ((((row * a.M + j) * a.H + h) * a.P + p) * es)), val);
+  } else if (c0 < QB) {
+    const int c1 = c0 - KB, j = c1 / (a.G * a.N), rem = c1 - j * a.G * a.N;
+    const int gi = rem / a.N, nn = rem - gi * a.N;
+    for (int hh = gi * hpg; hh < gi * hpg + hpg; ++hh)
+      __stcs(reinterpret_cast<uint4*>(a.k + ((((row * a.M + j) * a.H + hh) * a.N + nn) * es)), val);
+  } else {
+    const int c2 = c0 - QB, gi = c2 / a.N, nn = c2 - gi * a.N;
+    for (int hh = gi * hpg; hh < gi * hpg + hpg; ++hh) {
+      if (DECODE) {
+        for (int j = 0; j < a.M; ++j)
+          __stcs(reinterpret_cast<uint4*>(a.q + ((((row * a.M + j) * a.H + hh) * a.N + nn) * es)),
+                 j == a.M - 1 ? val : make_uint4(0u, 0u, 0u, 0u));
+      } else {
+        __stcs(reinterpret_cast<uint4*>(a.q + (((row * a.H + hh) * a.N + nn) * es)), val);
+      }
+    }
+  }
+}
+
+// The gates of one token row (prepare's fp32 operations).
+template <bool DECODE>
+__device__ __forceinline__ void cv_gates(const PrepArgs& a, int64_t r, int i) {
+  const int64_t in = r / a.T, t = r - in * a.T;
+  const int64_t bar = in * a.ba_sn + t * a.ba_st;
+  const int MH = a.M * a.H;
+  if (i < MH) a.beta[r * MH + i] = 1.0f / (1.0f + expf(-to_f32(a.ba, bar + i, a.dt)));
+  const int ng = DECODE ? MH : a.H;
+  if (i < ng) {
+    const int j = DECODE ? i / a.H : 0;
+    const int h = DECODE ? i - j * a.H : i;
+    float gv = 0.0f;
+    if (j == 0) {
+      const float sp = softplus_page(to_f32(a.ba, bar + MH + h, a.dt) + a.dt_bias[h]);
+      gv = -(expf(a.A_log[h]) * sp);
+    }
+    a.g[r * ng + i] = gv;
+  }
+}
+
+// Grid: x = token tile (prefill: RT rows of one batch row; decode: the S rows of
+// one request), y = segment of 256 channel vectors. 256 threads, one 16-byte
+// channel vector each.
+template <typename T, int W, bool DECODE>
+__global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
+  constexpr int VE = 16 / sizeof(T);  // channels per vector
+  const PrepArgs& a = ca.pa;
+  const int es = a.es;
+  const int nvec = ca.C / VE;
+  const int tiles_per_row = DECODE ? 1 : (a.T + ca.RT - 1) / ca.RT;
+  const int in = blockIdx.x / tiles_per_row;
+  const int t0 = DECODE ? 0 : (blockIdx.x - in * tiles_per_row) * ca.RT;
+  const int t1 = DECODE ? a.T : min(a.T, t0 + ca.RT);
+  // decode: this request's pool entry (-1: padding or rejected)
+  int sl = 0;
+  if (DECODE) {
+    sl = ca.slot[in];
+    if (sl != -1) {
+      int bad = sl < -1 || sl >= ca.n_slots;
+      if (!bad) {
+        int dup = 0;
+        for (int i = threadIdx.x; i < a.n; i += blockDim.x) dup |= (i != in) & (ca.slot[i] == sl);
+        bad = __syncthreads_or(dup);
+      }
+      if (bad) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && ca.status) atomicExch(ca.status, 1);
+        sl = -1;
+      }
+    }
+  }
+  if (blockIdx.y == 0) {  // gates of this tile's rows
+    const int ng = a.M * a.H;
+    for (int idx = threadIdx.x; idx < (t1 - t0) * ng; idx += blockDim.x) {
+      const int tt = idx / ng;
+      cv_gates<DECODE>(a, (int64_t)in * a.T + t0 + tt, idx - tt * ng);
+    }
+  }
+  const int cv = blockIdx.y * 256 + threadIdx.x;
+  if (cv >= nvec || t0 >= t1) return;
+  const int c0 = cv * VE;
+  float wv[W][VE], bv[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) wv[i][e] = ca.w[(int64_t)(c0 + e) * W + i];
+    bv[e] = ca.bias ? ca.bias[c0 + e] : 0.f;
+  }
+  const uint8_t* xrow0 = a.x + (int64_t)in * a.x_sn_b;
+  if (DECODE && sl < 0) {  // padding request: zero conv output, no state access
+    for (int t = t0; t < t1; ++t) cv_scatter<DECODE>(a, (int64_t)in * a.T + t, c0, make_uint4(0u, 0u, 0u, 0u));
+    return;
+  }
+  const int64_t sC = (int64_t)ca.C * (W - 1);  // state entries per sequence
+  // the sequence of row t0 (varlen) and its bounds; offsets are clamped to
+  // [0, T] so that no list, however malformed, moves a read outside the rows
+  int seq = in, s_start = 0, s_end = a.T;
+  auto bounds = [&](int sq) {
+    s_start = sq < ca.N_seq ? min(max(ca.cu[sq], 0), a.T) : a.T;
+    s_end = sq < ca.N_seq ? min(max(ca.cu[sq + 1], s_start), a.T) : a.T;
+  };
+  if (!DECODE && ca.cu) {
+    int lo = 0, hi = ca.N_seq;  // largest s < N_seq with cu[s] <= t0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ca.cu[mid] <= t0) lo = mid; else hi = mid;
+    }
+    seq = lo;
+    bounds(seq);
+    while (seq < ca.N_seq && s_end <= t0) bounds(++seq);  // skip sequences ending before t0
+    if (t0 == 0 && ca.st_out && W > 1) {
+      // empty sequences keep their initial state: the first tile's threads copy it
+      for (int sq = 0; sq < ca.N_seq; ++sq) {
+        const int b0 = min(max(ca.cu[sq], 0), a.T), b1 = min(max(ca.cu[sq + 1], b0), a.T);
+        if (b1 > b0) continue;
+        for (int e = 0; e < VE; ++e)
+          for (int i = 0; i < W - 1; ++i) {
+            const int64_t off = ((int64_t)sq * sC + (int64_t)(c0 + e) * (W - 1) + i) * es;
+            for (int bb = 0; bb < es; ++bb) ca.st_out[off + bb] = ca.st_in ? ca.st_in[off + bb] : 0;
+          }
+      }
+    }
+  }
+  float win[W > 1 ? W - 1 : 1][VE];
+  // window for row t: inputs t-(W-1) .. t-1 of its sequence, from rows or the state
+  auto fill = [&](int t) {
+#pragma unroll
+    for (int i = 0; i < W - 1; ++i) {
+      const int src = t - (W - 1) + i;
+      if (src >= s_start) {
+        cv_unpack<T, VE>(__ldcs(reinterpret_cast<const uint4*>(xrow0 + (int64_t)src * a.x_st_b + (int64_t)c0 * es)), win[i]);
+      } else {
+        const int si = (W - 1) - (s_start - src);  // state index (oldest first)
+        const uint8_t* sb = DECODE ? ca.st_in + (int64_t)sl * sC * es
+                                   : (ca.st_in ? ca.st_in + (int64_t)seq * sC * es : nullptr);
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+          win[i][e] = (sb && si >= 0) ? cv_ld<T>(sb + ((int64_t)(c0 + e) * (W - 1) + si) * es) : 0.f;
+      }
+    }
+  };
+  auto put_state = [&](uint8_t* base) {  // the window after the last row: the new state
+#pragma unroll
+    for (int e = 0; e < VE; ++e)
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) {
+        float f[VE];
+#pragma unroll
+        for (int z = 0; z < VE; ++z) f[z] = win[i][z];
+        const uint4 pk = cv_pack<T, VE>(f);
+        const uint8_t* pb = reinterpret_cast<const uint8_t*>(&pk);
+        uint8_t* d = base + ((int64_t)(c0 + e) * (W - 1) + i) * es;
+        for (int bb = 0; bb < es; ++bb) d[bb] = pb[e * es + bb];
+      }
+  };
+  fill(t0);
+  auto ldrow = [&](int t) {
+    return __ldcs(reinterpret_cast<const uint4*>(xrow0 + (int64_t)t * a.x_st_b + (int64_t)c0 * es));
+  };
+  uint4 nxt = ldrow(t0);  // one row of lookahead keeps two loads in flight per thread
+  for (int t = t0; t < t1; ++t) {
+    const uint4 cur = nxt;
+    if (t + 1 < t1) nxt = ldrow(t + 1);
+    if (!DECODE && ca.cu) {
+      bool moved = false;
+      while (t >= s_end && seq < ca.N_seq) {  // crossed into the next sequence
+        bounds(++seq);
+        moved = true;
+      }
+      if (seq >= ca.N_seq) break;  // rows past the last sequence are not outputs
+      if (moved) fill(t);
+    }
+    float x[VE], y[VE];
+    cv_unpack<T, VE>(cur, x);
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      float z = bv[e];
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) z = z + wv[i][e] * win[i][e];
+      z = z + wv[W - 1][e] * x[e];
+      y[e] = z / (1.0f + expf(-z));
+    }
+#pragma unroll
+    for (int i = 0; i + 1 < W - 1; ++i)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) win[i][e] = win[i + 1][e];
+    if (W > 1) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) win[W > 1 ? W - 2 : 0][e] = x[e];
+    }
+    cv_scatter<DECODE>(a, (int64_t)in * a.T + t, c0, cv_pack<T, VE>(y));
+    if (!DECODE && ca.st_out && W > 1 && t == s_end - 1)
+      put_state(ca.st_out + (int64_t)(ca.cu ? seq : in) * sC * es);
+  }
+  if (DECODE && W > 1) put_state(ca.st_out + (int64_t)sl * sC * es);
+  // prefill: a sequence with no rows in this batch keeps its state only if its
+  // (empty) range starts in this tile; the host launches cover that case
+}
+
+template <typename T, int W>
+cudaError_t launch_conv_w(const ConvArgs& ca, bool decode, cudaStream_t s) {
+  const int nvec = ca.C / (16 / (int)sizeof(T));
+  const int tiles = decode ? 1 : (ca.pa.T + ca.RT - 1) / ca.RT;
+  const dim3 grid((unsigned)((int64_t)ca.pa.n * tiles), (unsigned)((nvec + 255) / 256));
+  if (decode)
+    conv_prepare_kernel<T, W, true><<<grid, 256, 0, s>>>(ca);
+  else
+    conv_prepare_kernel<T, W, false><<<grid, 256, 0, s>>>(ca);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_conv_t(const ConvArgs& ca, bool decode, cudaStream_t s) {
+  switch (ca.W) {
+    case 1: return launch_conv_w<T, 1>(ca, decode, s);
+    case 2: return launch_conv_w<T, 2>(ca, decode, s);
+    case 3: return launch_conv_w<T, 3>(ca, decode, s);
+    default: return launch_conv_w<T, 4>(ca, decode, s);
+  }
+}
+
 template <int VB>
 cudaError_t launch_vb(const PrepArgs& a, bool decode, cudaStream_t s) {
   const int64_t rows = (int64_t)a.n * a.T;
@@ -325,6 +631,50 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
   }
   if (a.es == 4) return launch_vb<4>(a, decode, stream);
   return launch_vb<2>(a, decode, stream);
+}
+
+cudaError_t launch_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st, const float* w,
+                                const float* bias, int W, const void* st_in, void* st_out,
+                                const int32_t* cu, int N_seq, const int32_t* slot, int n_slots,
+                                int32_t* status, const void* ba, int64_t ba_sn, int64_t ba_st,
+                                const float* A_log, const float* dt_bias, int n, int T, int M,
+                                int H, int G, int P, int N, gdp_dtype dt, bool decode, void* q,
+                                void* k, void* v, float* beta, float* g, cudaStream_t stream) {
+  if ((int64_t)n * T == 0) return cudaSuccess;
+  ConvArgs ca;
+  PrepArgs& a = ca.pa;
+  a.es = dt == GDP_F32 ? 4 : 2;
+  a.x = static_cast<const uint8_t*>(xp);
+  a.x_sn_b = xp_sn * a.es;
+  a.x_st_b = xp_st * a.es;
+  a.ba = ba;
+  a.ba_sn = ba_sn;
+  a.ba_st = ba_st;
+  a.A_log = A_log;
+  a.dt_bias = dt_bias;
+  a.n = n; a.T = T; a.M = M; a.H = H; a.G = G; a.P = P; a.N = N; a.dt = (int)dt;
+  a.q = static_cast<uint8_t*>(q);
+  a.k = static_cast<uint8_t*>(k);
+  a.v = static_cast<uint8_t*>(v);
+  a.beta = beta;
+  a.g = g;
+  ca.w = w;
+  ca.bias = bias;
+  ca.W = W;
+  ca.C = M * H * P + M * G * N + G * N;
+  ca.RT = 32;
+  ca.st_in = static_cast<const uint8_t*>(st_in);
+  ca.st_out = static_cast<uint8_t*>(st_out);
+  ca.cu = cu;
+  ca.N_seq = N_seq;
+  ca.slot = slot;
+  ca.n_slots = n_slots;
+  ca.status = status;
+  switch (dt) {
+    case GDP_BF16: return launch_conv_t<__nv_bfloat16>(ca, decode, stream);
+    case GDP_F16: return launch_conv_t<__half>(ca, decode, stream);
+    default: return launch_conv_t<float>(ca, decode, stream);
+  }
 }
 
 }  // namespace gdp

@@ -65,8 +65,9 @@ def _load():
             lib.oracle_prepare.argtypes = [P, I64, I64, P, I64, I64, P, P] + [I] * 9 + [P] * 5
             lib.oracle_gdp_walk.argtypes = [P] * 7 + [I] * 8 + [D, I, I, P, P]
             lib.oracle_gdp_recurrent.argtypes = [P] * 6 + [I] * 6 + [D, I, I, P]
+            lib.oracle_conv.argtypes = ([P, I64, I64, P, P, I, P, P, P, I, P, I] + [I] * 5 + [P])
             lib.oracle_max_threads.argtypes = []
-            for f in ("oracle_gate_map", "oracle_prepare", "oracle_gdp_walk",
+            for f in ("oracle_gate_map", "oracle_prepare", "oracle_gdp_walk", "oracle_conv",
                       "oracle_gdp_recurrent", "oracle_max_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -130,6 +131,44 @@ def prepare(x: torch.Tensor, ba: torch.Tensor, A_log: torch.Tensor, dt_bias: tor
     if rc:
         raise ValueError("oracle_prepare: bad arguments")
     return q, k, v, beta, g
+
+
+def conv(xp: torch.Tensor, w: torch.Tensor, b, state=None, cu_seqlens=None, slot=None):
+    """The short causal conv + SiLU before prepare (depthwise, width W = w.shape[1]),
+    fp32 one operation at a time, output in xp's dtype (bf16 or fp32).
+
+    Prefill (slot None): state [N, C, W-1] or None; returns (x [n,T,C], new_state
+    [N, C, W-1]). Decode (slot int32 [n]): state is the pool [n_slots, C, W-1];
+    returns (x, new_pool) with padding requests (slot -1, out of range, repeated)
+    zero and their entries untouched.
+    """
+    assert xp.dtype in (torch.bfloat16, torch.float32) and xp.stride(-1) == 1
+    n, T, C = xp.shape
+    W = w.shape[1]
+    xc = xp.cpu()
+    wf = w.detach().to(torch.float32).contiguous().cpu()
+    bf = None if b is None else b.detach().to(torch.float32).contiguous().cpu()
+    out = torch.zeros((n, T, C), dtype=xp.dtype)
+    decode = slot is not None
+    if decode:
+        pool = state.detach().cpu().contiguous().clone()
+        sl = slot.detach().cpu().to(torch.int32).contiguous()
+        rc = _load().oracle_conv(ctypes.c_void_p(xc.data_ptr()), xc.stride(0), xc.stride(1),
+                                 _ptr(wf), _ptr(bf), W, _ptr(pool), _ptr(pool), None, n,
+                                 _ptr(sl), pool.shape[0], n, T, C, _DT[xp.dtype], 1, _ptr(out))
+        if rc:
+            raise ValueError("oracle_conv: bad arguments")
+        return out, pool
+    cu = None if cu_seqlens is None else cu_seqlens.detach().cpu().to(torch.int32).contiguous()
+    N = n if cu is None else cu.numel() - 1
+    st_in = None if state is None else state.detach().cpu().contiguous()
+    st_out = torch.zeros((N, C, max(W - 1, 0)), dtype=xp.dtype)
+    rc = _load().oracle_conv(ctypes.c_void_p(xc.data_ptr()), xc.stride(0), xc.stride(1),
+                             _ptr(wf), _ptr(bf), W, _ptr(st_in), _ptr(st_out), _ptr(cu), N, None,
+                             0, n, T, C, _DT[xp.dtype], 0, _ptr(out))
+    if rc:
+        raise ValueError("oracle_conv: bad arguments")
+    return out, st_out
 
 
 # --------------------------------------------------------------------------------------

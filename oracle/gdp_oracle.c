@@ -181,6 +181,105 @@ int oracle_prepare(const void* x, int64_t x_sn, int64_t x_st, const void* ba, in
   return 0;
 }
 
+/* fp32 -> bf16, round to nearest even (NaN kept quiet). */
+static uint16_t or_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static void or_store(void* base, int64_t idx, int dtype, float v) {
+  if (dtype == OR_F32)
+    ((float*)base)[idx] = v;
+  else
+    ((uint16_t*)base)[idx] = or_f32_to_bf16(v);
+}
+
+/*
+ * The short causal conv that precedes prepare (prepare page, module overview:
+ * prepare reads the conv's output; "a -1 slot zeroes its conv output"). The
+ * pages do not spell the conv out; this is the depthwise causal short conv
+ * with SiLU, written from its definition, per channel c of a sequence:
+ *     xin(t) = the sequence's input at t, or for t < 0 its state entry
+ *              W-1+t (the W-1 inputs before the sequence, oldest first), or 0
+ *              without a state;
+ *     z = b[c];  z = z + w[c][i] * xin(t - (W-1) + i)   for i = 0 .. W-1;
+ *     y = z / (1 + exp(-z)),  stored in `dtype` (bf16 rounds to nearest even).
+ * Evaluated in fp32 one operation at a time (no contraction) with host libm.
+ *   xp     [n, T, C] dtype, strides xp_sn, xp_st (elements)
+ *   w      [C, W] fp32; b [C] fp32 or NULL
+ *   decode = 0: sequences are the batch rows, or (n == 1) the cu [N_seq + 1]
+ *            ranges; st_in [N_seq, C, W-1] or NULL, st_out [N_seq, C, W-1]
+ *            or NULL receives the last W-1 inputs of state ++ tokens. Rows
+ *            outside every sequence are left as they are in x_out.
+ *   decode = 1: request r's S = T tokens continue from pool entry slot[r]
+ *            (st_in == st_out, [n_slots, C, W-1], updated in place); slot -1,
+ *            a slot outside [-1, n_slots) or one named twice makes the request
+ *            padding: zero output rows, no state touched.
+ *   x_out  [n, T, C] dtype (contiguous).
+ * dtype: OR_BF16 or OR_F32. Returns 0, or 1 on a bad argument.
+ */
+int oracle_conv(const void* xp, int64_t xp_sn, int64_t xp_st, const float* w, const float* b,
+                int W, const void* st_in, void* st_out, const int32_t* cu, int N_seq,
+                const int32_t* slot, int n_slots, int n, int T, int C, int dtype, int decode,
+                void* x_out) {
+  if (n < 0 || T < 0 || C <= 0 || W < 1 || W > 64 || (dtype != OR_BF16 && dtype != OR_F32))
+    return 1;
+  const int nseq = decode ? n : (cu ? N_seq : n);
+  float* win = (float*)malloc(sizeof(float) * (size_t)(W + T));
+  if (!win) return 1;
+  for (int s = 0; s < nseq; ++s) {
+    int in = s, t0 = 0, t1 = T;
+    const void* sin = st_in;
+    void* sout = st_out;
+    int64_t sidx = s;
+    if (!decode && cu) {
+      in = 0;
+      t0 = cu[s];
+      t1 = cu[s + 1];
+      if (t0 < 0 || t1 < t0 || t1 > T) { free(win); return 1; }
+    }
+    if (decode) {
+      int sl = slot[s];
+      int pad = sl < 0 || sl >= n_slots;
+      for (int r = 0; r < n && !pad; ++r)
+        if (r != s && slot[r] == sl) pad = 1;
+      if (pad) {
+        for (int t = 0; t < T; ++t)
+          for (int c = 0; c < C; ++c) or_store(x_out, ((int64_t)s * T + t) * C + c, dtype, 0.0f);
+        continue;
+      }
+      sidx = sl;
+    }
+    const int len = t1 - t0;
+    for (int c = 0; c < C; ++c) {
+      /* win[0 .. W-2]: the state; win[W-1 + j]: token t0 + j */
+      for (int i = 0; i < W - 1; ++i)
+        win[i] = sin ? or_load(sin, (sidx * C + c) * (int64_t)(W - 1) + i, dtype) : 0.0f;
+      for (int j = 0; j < len; ++j)
+        win[W - 1 + j] = or_load(xp, (int64_t)in * xp_sn + (int64_t)(t0 + j) * xp_st + c, dtype);
+      for (int j = 0; j < len; ++j) {
+        float z = b ? b[c] : 0.0f;
+        for (int i = 0; i < W; ++i) z = z + w[(int64_t)c * W + i] * win[j + i];
+        const float y = z / (1.0f + expf(-z));
+        or_store(x_out, ((int64_t)in * T + t0 + j) * C + c, dtype, y);
+      }
+      if (sout)
+        for (int i = 0; i < W - 1; ++i) {
+          const float v = win[len + i]; /* the last W-1 entries of state ++ tokens */
+          if (dtype == OR_F32)
+            ((float*)sout)[(sidx * C + c) * (int64_t)(W - 1) + i] = v;
+          else
+            ((uint16_t*)sout)[(sidx * C + c) * (int64_t)(W - 1) + i] = or_f32_to_bf16(v);
+        }
+    }
+  }
+  free(win);
+  return 0;
+}
+
 /* One gated-delta step on the V x K state S (row-major, S[i*K + c]):
  *   S <- eg * S * (I - b kk kk^T) + b vv kk^T.   sk: V-sized scratch for S kk. */
 static void or_step(double* S, int K, int V, const double* kk, const double* vv, double b,

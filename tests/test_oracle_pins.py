@@ -405,3 +405,96 @@ def test_prepare_bf16_copies_are_bit_moves():
     assert q.dtype == torch.bfloat16 and k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16
     assert beta.dtype == torch.float32 and g.dtype == torch.float32
     assert torch.equal(v.view(2, 5, -1), d["x"][..., :M * H * P])
+
+
+# ---------------------------------------------------------------------------------
+# the short causal conv before prepare (oracle.conv): pins against library
+# routines and the conv's invariants
+# ---------------------------------------------------------------------------------
+def _conv_inputs(n, T, C, W, seed, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, T, C, generator=g).to(dtype)
+    w = torch.randn(C, W, generator=g) * 0.5
+    b = torch.randn(C, generator=g) * 0.1
+    return x, w, b
+
+
+def test_conv_width_one_is_silu():
+    x, _, _ = _conv_inputs(2, 9, 16, 1, 1)
+    y, st = oracle.conv(x, torch.ones(16, 1), None)
+    ref = torch.nn.functional.silu(x)  # library SiLU
+    assert st.shape == (2, 16, 0)
+    assert (y - ref).abs().max() <= 4e-7 * ref.abs().max()
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+def test_conv_matches_numpy_correlation(W):
+    """z = b + sum_i w[i] x[t-(W-1)+i] with zeros before the sequence is a valid
+    cross-correlation of the zero-padded input with the taps (numpy's routine)."""
+    n, T, C = 2, 11, 6
+    x, w, b = _conv_inputs(n, T, C, W, W)
+    y, _ = oracle.conv(x, w, b)
+    xd = x.double().numpy()
+    for r in range(n):
+        for c in range(C):
+            xpad = np.concatenate([np.zeros(W - 1), xd[r, :, c]])
+            z = np.correlate(xpad, w[c].double().numpy(), "valid") + float(b[c])
+            ref = z / (1.0 + np.exp(-z))
+            assert np.abs(y[r, :, c].double().numpy() - ref).max() <= 2e-6 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("tap", [0, 1, 3])
+def test_conv_one_hot_tap_shifts_and_reads_the_state_oldest_first(tap):
+    """With w = e_tap and no bias, y[t] = silu(xin[t - 3 + tap]); positions before
+    the sequence come from the state, entry W-1+t (oldest first)."""
+    W, T, C = 4, 6, 5
+    x, _, _ = _conv_inputs(1, T, C, W, 10 + tap)
+    state = torch.randn(1, C, W - 1, generator=torch.Generator().manual_seed(3))
+    w = torch.zeros(C, W)
+    w[:, tap] = 1.0
+    y, st = oracle.conv(x, w, None, state=state)
+    full = torch.cat([state[0].t(), x[0]], 0)  # [W-1+T, C]: state entries, then tokens
+    want = torch.nn.functional.silu(full[tap:tap + T])
+    assert (y[0] - want).abs().max() <= 4e-7 * want.abs().max()
+    assert torch.equal(st[0], full[-(W - 1):].t())  # last W-1 inputs, oldest first
+
+
+def test_conv_chained_calls_equal_one_call_and_varlen_equals_separate():
+    W, C = 4, 8
+    x, w, b = _conv_inputs(1, 20, C, W, 21, dtype=torch.bfloat16)
+    y, st = oracle.conv(x, w, b)
+    y1, s1 = oracle.conv(x[:, :2], w, b)            # shorter than W - 1
+    y2, s2 = oracle.conv(x[:, 2:13], w, b, state=s1)
+    y3, s3 = oracle.conv(x[:, 13:], w, b, state=s2)
+    assert torch.equal(torch.cat([y1, y2, y3], 1), y) and torch.equal(s3, st)
+    cu = torch.tensor([0, 2, 2, 13, 20], dtype=torch.int32)  # with an empty sequence
+    h0 = torch.randn(4, C, W - 1).to(torch.bfloat16)
+    yv, sv = oracle.conv(x, w, b, state=h0, cu_seqlens=cu)
+    for i in range(4):
+        t0, t1 = int(cu[i]), int(cu[i + 1])
+        yi, si = oracle.conv(x[:, t0:t1], w, b, state=h0[i:i + 1])
+        assert torch.equal(yv[:, t0:t1], yi) and torch.equal(sv[i], si[0])
+    assert torch.equal(sv[1], h0[1])  # empty sequence keeps its state
+
+
+def test_conv_decode_pool_padding_and_continuation():
+    W, C, n, S, n_slots = 3, 8, 4, 2, 6
+    x, w, b = _conv_inputs(n, 5 + S, C, W, 31, dtype=torch.bfloat16)
+    # continuation: prefill of 5 tokens, then a decode step of S from its state
+    yp, sp = oracle.conv(x[:, :5], w, b)
+    pool = torch.zeros(n_slots, C, W - 1, dtype=torch.bfloat16)
+    slots = torch.tensor([4, -1, 0, 2], dtype=torch.int32)
+    for r in range(n):
+        if slots[r] >= 0:
+            pool[slots[r]] = sp[r]
+    yd, new_pool = oracle.conv(x[:, 5:], w, b, state=pool, slot=slots)
+    yfull, sfull = oracle.conv(x, w, b)
+    for r in (0, 2, 3):
+        assert torch.equal(yd[r], yfull[r, 5:]) and torch.equal(new_pool[slots[r]], sfull[r])
+    assert torch.count_nonzero(yd[1]) == 0
+    untouched = [1, 3, 5]
+    assert torch.equal(new_pool[untouched], pool[untouched])
+    # a slot named twice makes both requests padding
+    yd2, pool2 = oracle.conv(x[:, 5:], w, b, state=pool, slot=torch.tensor([4, 4, 0, 2],
+                                                                         dtype=torch.int32))
+    assert torch.count_nonzero(yd2[:2]) == 0 and torch.equal(pool2[4], pool[4])
