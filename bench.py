@@ -556,7 +556,11 @@ def run_decode(args, gdp, dev, pk):
                  + n * L * H * P * 4)
     mp, mr = statistics.mean(tp), statistics.mean(tr)
     hbm = pk["hbm_gbs"]
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    conv = time_conv_prepare(gdp, dev, x, ba, A_log, dt_bias, M, H, G, P, N, None, outs,
+                             prep_bytes, hbm, decode=True, slots=slots)
     return {"workload": "decode n256 S4 M2 H32 G8 P128 N128 (fp32 state)",
+            "conv_prepare": conv,
             "prepare_us": mp * 1e3, "prepare_GBps": prep_bytes / (mp * 1e-3) / 1e9,
             "prepare_hbm_frac": prep_bytes / (mp * 1e-3) / 1e9 / hbm,
             "update_us": mr * 1e3, "update_GBps": rec_bytes / (mr * 1e-3) / 1e9,
@@ -657,6 +661,8 @@ def run_varlen(args, gdp, dev, pk, pk_src):
     times = _time_chunk_steps(gdp, step, stage, L2Flush(dev), max(3, min(args.steps, 10)), 3,
                               prep_ev)
     gdp.gdp_set_stage_events(None)
+    conv = time_conv_prepare(gdp, dev, x, ba, A_log, dt_bias, M, H, G, P, N, cu, pre,
+                             prepare_bytes(1, T, M, H, G, P, N, False), pk["hbm_gbs"])
     fused = off[7] == 1
     alg = method_work(T, nseq, H, H, N, P, M, BT, fused)
     out = _workload_summary(
@@ -664,7 +670,48 @@ def run_varlen(args, gdp, dev, pk, pk_src):
         "(prepare + chunk_fwd with cu_seqlens)", times, alg, pk["bf16_tflops"], pk["hbm_gbs"],
         pk_src, fused, prepare_bytes(1, T, M, H, G, P, N, False))
     out["tokens"] = T
+    out["conv_prepare"] = conv
     return out
+
+
+def time_conv_prepare(gdp, dev, x, ba, A_log, dt_bias, M, H, G, P, N, cu, pre, prep_bytes, hbm,
+                      W=4, decode=False, slots=None):
+    """The short causal conv (width W, SiLU) fused into prepare on the same workload:
+    x stands in for the pre-conv activations; conv weights and states are synthetic
+    (seeded). Bytes: prepare's plus the conv states read and written."""
+    C = x.shape[-1]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    w = torch.randn(C, W, device=dev, generator=gen) * 0.5
+    b = torch.randn(C, device=dev, generator=gen) * 0.1
+    nst = (cu.numel() - 1) if cu is not None else x.shape[0]
+    if decode:
+        pool = torch.randn(slots.numel() * 2, C, W - 1, device=dev, generator=gen).to(x.dtype)
+        st_bytes = 2 * slots.numel() * C * (W - 1) * x.element_size()
+        fn = lambda: gdp.gdp_decode_conv_prepare(x, w, b, ba, A_log, dt_bias, M, H, G, P, N,
+                                                 pool, slots, out=pre)
+    else:
+        st0 = torch.randn(nst, C, W - 1, device=dev, generator=gen).to(x.dtype)
+        st_bytes = 2 * nst * C * (W - 1) * x.element_size()
+        fn = lambda: gdp.gdp_prefill_conv_prepare(x, w, b, ba, A_log, dt_bias, M, H, G, P, N,
+                                                  conv_state=st0, cu_seqlens=cu, out=pre)
+    flush = L2Flush(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(10):
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        ev[0].record()
+        fn()
+        ev[1].record()
+        torch.cuda.synchronize()
+        ts.append(ev[0].elapsed_time(ev[1]))
+    us = statistics.mean(ts) * 1e3
+    nbytes = prep_bytes + st_bytes
+    return {"W": W, "us": us, "bytes": nbytes, "GBps": nbytes / (us * 1e-6) / 1e9,
+            "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm}
 
 
 def run_ungated(args, gdp, dev, pk, pk_src, pf):

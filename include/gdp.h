@@ -124,8 +124,8 @@ gdp_status gdp_decode_prepare(const void* x, int64_t x_sn, int64_t x_st, const v
  *             are not written.
  * ba, A_log, dt_bias, the sizes and the outputs q, k, v, beta, g are those of
  * gdp_prefill_prepare. Requires 16-byte channel vectors: P and N times the
- * element size multiples of 16 bytes, 16-byte aligned xp, q, k, v and row
- * strides (else GDP_ERR_UNSUPPORTED).
+ * element size multiples of 16 bytes, 16-byte aligned xp, q, k, v, conv
+ * states and row strides (else GDP_ERR_UNSUPPORTED).
  */
 gdp_status gdp_prefill_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
                                     const float* conv_w, const float* conv_b, int W,

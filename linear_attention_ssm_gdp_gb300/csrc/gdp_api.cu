@@ -176,6 +176,8 @@ gdp_status gdp_prefill_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st
     return e == cudaSuccess ? GDP_OK : GDP_ERR_CUDA;
   }
   if ((s = check_conv(xp, xp_sn, xp_st, conv_w, W, P, N, dt, q, k, v)) != GDP_OK) return s;
+  if ((reinterpret_cast<uintptr_t>(conv_state_in) | reinterpret_cast<uintptr_t>(conv_state_out)) % 16)
+    return GDP_ERR_UNSUPPORTED;
   const cudaError_t e = launch_conv_prepare(
       xp, xp_sn, xp_st, conv_w, conv_b, W, conv_state_in, conv_state_out, cu_seqlens, N_seq,
       nullptr, 0, nullptr, ba, ba_sn, ba_st, A_log, dt_bias, n, T, M, H, G, P, N, dt, false, q,
@@ -197,6 +199,7 @@ gdp_status gdp_decode_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st,
   if (s != GDP_OK || n == 0) return s;
   if (!conv_slot || (W > 1 && n_slots > 0 && !conv_state_pool)) return GDP_ERR_INVALID_ARG;
   if ((s = check_conv(xp, xp_sn, xp_st, conv_w, W, P, N, dt, q, k, v)) != GDP_OK) return s;
+  if (reinterpret_cast<uintptr_t>(conv_state_pool) % 16) return GDP_ERR_UNSUPPORTED;
   const cudaError_t e = launch_conv_prepare(
       xp, xp_sn, xp_st, conv_w, conv_b, W, conv_state_pool, conv_state_pool, nullptr, n,
       conv_slot, n_slots, status, ba, ba_sn, ba_st, A_log, dt_bias, n, S, M, H, G, P, N, dt,

@@ -45,6 +45,26 @@ __device__ __forceinline__ float softplus_page(float x) {
   return x > 20.0f ? x : log1pf(expf(x));
 }
 
+// Division of non-negative ints below 2^31 by a divisor fixed for the launch,
+// as a multiply-high, an add and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994: with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (umulhi(m, n) + n) >> s). The
+// prepare kernels' index arithmetic (vectors per head, heads, heads per
+// group) would otherwise be a chain of 32-bit divisions per 16-byte vector.
+struct FastDiv {
+  uint32_t d, m, s;
+  __host__ __device__ FastDiv() : d(1), m(1), s(0) {}
+  __host__ explicit FastDiv(uint32_t div) : d(div) {
+    s = 0;
+    while ((1ull << s) < div) ++s;
+    m = (uint32_t)(((1ull << 32) * ((1ull << s) - div)) / div + 1);
+  }
+  __device__ __forceinline__ int div(int n) const {
+    const uint32_t un = (uint32_t)n;
+    return (int)((__umulhi(m, un) + un) >> s);
+  }
+};
+
 struct PrepArgs {
   const uint8_t* x;
   int64_t x_sn_b, x_st_b;  // byte strides
@@ -58,6 +78,7 @@ struct PrepArgs {
   uint8_t* v;
   float* beta;
   float* g;
+  FastDiv fd_H, fd_hpg, fd_hv;  // by H, H / G, and the vectors per key/query head
 };
 
 // VB: bytes moved per vector access (16, or the element size when the
@@ -96,18 +117,18 @@ __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
           buf[u] = __ldcs(reinterpret_cast<const VT*>(xr) + c);
         } else if (c < nv + nk) {  // key: output head (j, h) reads group (j, h / hpg)
           const int ck = c - nv;
-          const int jh = ck / head_v, w = ck - jh * head_v;
-          const int j = jh / a.H, h = jh - j * a.H;
+          const int jh = a.fd_hv.div(ck), w = ck - jh * head_v;
+          const int j = a.fd_H.div(jh), h = jh - j * a.H;
           buf[u] = __ldcs(reinterpret_cast<const VT*>(
-                              xr + kbase_b + ((int64_t)j * a.G + h / hpg) * head_kb) + w);
+                              xr + kbase_b + ((int64_t)j * a.G + a.fd_hpg.div(h)) * head_kb) + w);
         } else if (c < ntot) {  // query: prefill one row per token; decode the last copy
           const int cq = c - nv - nk;
-          const int jh = cq / head_v, w = cq - jh * head_v;
-          const int j = DECODE ? jh / a.H : a.M - 1;
+          const int jh = a.fd_hv.div(cq), w = cq - jh * head_v;
+          const int j = DECODE ? a.fd_H.div(jh) : a.M - 1;
           const int h = DECODE ? jh - j * a.H : jh;
           if (j == a.M - 1)
             buf[u] = __ldcs(reinterpret_cast<const VT*>(xr + qbase_b +
-                                                        (int64_t)(h / hpg) * head_kb) + w);
+                                                        (int64_t)a.fd_hpg.div(h) * head_kb) + w);
           else
             buf[u] = VT{};  // +0.0 in every dtype
         }
@@ -342,31 +363,64 @@ __device__ __forceinline__ uint4 cv_pack(const float* f) {
   }
 }
 
-// Writes one 16-byte vector of post-conv channels c0.. (within one head) of
-// token row `row` to its q/k/v destinations (prepare's map).
+// Where one 16-byte vector of post-conv channels c0.. (within one head) goes,
+// worked out once per thread: element offset of its first destination inside
+// a token row's block of the output, the row stride of that output, and the
+// number of destinations (the heads of a key/query group) spaced N apart.
+struct CvDst {
+  uint8_t* base;   // v, k or q
+  int64_t off;     // elements, first destination in row 0
+  int64_t rstride; // elements per token row
+  int count;       // destinations (1 for values, H/G for keys and queries)
+  int zcopies;     // decode queries: copies j < M-1 per destination get zeros
+};
+
 template <bool DECODE>
-__device__ __forceinline__ void cv_scatter(const PrepArgs& a, int64_t row, int c0, uint4 val) {
-  const int es = a.es, hpg = a.H / a.G;
+__device__ __forceinline__ CvDst cv_plan(const PrepArgs& a, int c0) {
+  const int hpg = a.H / a.G;
   const int KB = a.M * a.H * a.P, QB = KB + a.M * a.G * a.N;
+  CvDst d;
+  d.zcopies = 0;
   if (c0 < KB) {
     const int j = c0 / (a.H * a.P), rem = c0 - j * a.H * a.P, h = rem / a.P, p = rem - h * a.P;
-    __stcs(reinterpret_cast<uint4*>(a.v + ((((row * a.M + j) * a.H + h) * a.P + p) * es)), val);
+    d.base = a.v;
+    d.off = ((int64_t)j * a.H + h) * a.P + p;
+    d.rstride = (int64_t)a.M * a.H * a.P;
+    d.count = 1;
   } else if (c0 < QB) {
     const int c1 = c0 - KB, j = c1 / (a.G * a.N), rem = c1 - j * a.G * a.N;
     const int gi = rem / a.N, nn = rem - gi * a.N;
-    for (int hh = gi * hpg; hh < gi * hpg + hpg; ++hh)
-      __stcs(reinterpret_cast<uint4*>(a.k + ((((row * a.M + j) * a.H + hh) * a.N + nn) * es)), val);
+    d.base = a.k;
+    d.off = ((int64_t)j * a.H + gi * hpg) * a.N + nn;
+    d.rstride = (int64_t)a.M * a.H * a.N;
+    d.count = hpg;
   } else {
     const int c2 = c0 - QB, gi = c2 / a.N, nn = c2 - gi * a.N;
-    for (int hh = gi * hpg; hh < gi * hpg + hpg; ++hh) {
-      if (DECODE) {
-        for (int j = 0; j < a.M; ++j)
-          __stcs(reinterpret_cast<uint4*>(a.q + ((((row * a.M + j) * a.H + hh) * a.N + nn) * es)),
-                 j == a.M - 1 ? val : make_uint4(0u, 0u, 0u, 0u));
-      } else {
-        __stcs(reinterpret_cast<uint4*>(a.q + (((row * a.H + hh) * a.N + nn) * es)), val);
-      }
+    d.base = a.q;
+    d.count = hpg;
+    if (DECODE) {  // the last copy carries the query
+      d.off = ((int64_t)(a.M - 1) * a.H + gi * hpg) * a.N + nn;
+      d.rstride = (int64_t)a.M * a.H * a.N;
+      d.zcopies = a.M - 1;
+    } else {
+      d.off = (int64_t)gi * hpg * a.N + nn;
+      d.rstride = (int64_t)a.H * a.N;
     }
+  }
+  return d;
+}
+
+__device__ __forceinline__ void cv_scatter(const PrepArgs& a, const CvDst& d, int64_t row,
+                                           uint4 val) {
+  const int es = a.es;
+  const int64_t hstride = (int64_t)a.N * es;
+  uint8_t* p = d.base + (row * d.rstride + d.off) * es;
+  for (int i = 0; i < d.count; ++i) __stcs(reinterpret_cast<uint4*>(p + i * hstride), val);
+  if (d.zcopies) {  // decode queries: +0 on the other copies of this token
+    const int64_t cstride = (int64_t)a.H * a.N * es;
+    for (int j = 1; j <= d.zcopies; ++j)
+      for (int i = 0; i < d.count; ++i)
+        __stcs(reinterpret_cast<uint4*>(p - j * cstride + i * hstride), make_uint4(0u, 0u, 0u, 0u));
   }
 }
 
@@ -392,10 +446,30 @@ __device__ __forceinline__ void cv_gates(const PrepArgs& a, int64_t r, int i) {
 
 // Grid: x = token tile (prefill: RT rows of one batch row; decode: the S rows of
 // one request), y = segment of 256 channel vectors. 256 threads, one 16-byte
-// channel vector each.
+// channel vector each; its conv taps (loaded as contiguous 16-byte vectors)
+// stay in registers for the tile. The thread streams its column of the tile's
+// input rows (and the W-1 rows before it) through a private ring of kConvD
+// slots in shared memory with cp.async, one commit group per row, so kConvD
+// loads are in flight without holding registers; it reads back only its own
+// slots (no block barrier). The last W-1 raw rows stay in registers; for a row
+// near the start of its sequence the entries before the start are taken from
+// the sequence's conv state instead. Conv states move as whole 16-byte vectors:
+// a thread's VE channels x (W-1) entries are contiguous in [.., C, W-1].
+constexpr int kConvRT = 64;  // prefill token rows per tile
+constexpr int kConvD = 8;    // rows in flight per thread
+
+__device__ __forceinline__ void cp16(void* dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   (unsigned)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+
 template <typename T, int W, bool DECODE>
-__global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
+__global__ void __launch_bounds__(256, 2) conv_prepare_kernel(ConvArgs ca) {
   constexpr int VE = 16 / sizeof(T);  // channels per vector
+  constexpr int WS = W > 1 ? W - 1 : 1;
+  __shared__ uint4 ring[kConvD][256];
   const PrepArgs& a = ca.pa;
   const int es = a.es;
   const int nvec = ca.C / VE;
@@ -403,6 +477,20 @@ __global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
   const int in = blockIdx.x / tiles_per_row;
   const int t0 = DECODE ? 0 : (blockIdx.x - in * tiles_per_row) * ca.RT;
   const int t1 = DECODE ? a.T : min(a.T, t0 + ca.RT);
+  const int cv = blockIdx.y * 256 + threadIdx.x;
+  const int c0 = cv * VE;
+  const bool has = cv < nvec;
+  const uint8_t* xrow0 = a.x + (int64_t)in * a.x_sn_b;
+  const int nrows = t1 - t0 + W - 1;  // rows streamed: t0-(W-1) .. t1-1
+  auto issue = [&](int rr) {          // row t0-(W-1)+rr into its ring slot (before row 0: zeros)
+    const int row = t0 - (W - 1) + rr;
+    if (rr < nrows)
+      cp16(&ring[rr % kConvD][threadIdx.x],
+           xrow0 + (int64_t)(row >= 0 ? row : 0) * a.x_st_b + (int64_t)c0 * es, row >= 0 ? 16 : 0);
+    asm volatile("cp.async.commit_group;" ::: "memory");  // one group per row (possibly empty)
+  };
+  if (has)
+    for (int rr = 0; rr < kConvD; ++rr) issue(rr);
   // decode: this request's pool entry (-1: padding or rejected)
   int sl = 0;
   if (DECODE) {
@@ -427,22 +515,85 @@ __global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
       cv_gates<DECODE>(a, (int64_t)in * a.T + t0 + tt, idx - tt * ng);
     }
   }
-  const int cv = blockIdx.y * 256 + threadIdx.x;
-  if (cv >= nvec || t0 >= t1) return;
-  const int c0 = cv * VE;
+  if (!has) return;
   float wv[W][VE], bv[VE];
+  {
+    float wr[W * VE];  // channel-major taps: wr[e * W + i] = w[c0 + e][i]
+    const float4* wp = reinterpret_cast<const float4*>(ca.w + (int64_t)c0 * W);
 #pragma unroll
-  for (int e = 0; e < VE; ++e) {
+    for (int i = 0; i < W * VE / 4; ++i) {
+      const float4 f = __ldg(wp + i);
+      wr[4 * i] = f.x; wr[4 * i + 1] = f.y; wr[4 * i + 2] = f.z; wr[4 * i + 3] = f.w;
+    }
 #pragma unroll
-    for (int i = 0; i < W; ++i) wv[i][e] = ca.w[(int64_t)(c0 + e) * W + i];
-    bv[e] = ca.bias ? ca.bias[c0 + e] : 0.f;
+    for (int e = 0; e < VE; ++e)
+#pragma unroll
+      for (int i = 0; i < W; ++i) wv[i][e] = wr[e * W + i];
+    if (ca.bias) {
+      const float4* bp = reinterpret_cast<const float4*>(ca.bias + c0);
+#pragma unroll
+      for (int i = 0; i < VE / 4; ++i) {
+        const float4 f = __ldg(bp + i);
+        bv[4 * i] = f.x; bv[4 * i + 1] = f.y; bv[4 * i + 2] = f.z; bv[4 * i + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) bv[e] = 0.f;
+    }
   }
-  const uint8_t* xrow0 = a.x + (int64_t)in * a.x_sn_b;
+  const CvDst dst = cv_plan<DECODE>(a, c0);
   if (DECODE && sl < 0) {  // padding request: zero conv output, no state access
-    for (int t = t0; t < t1; ++t) cv_scatter<DECODE>(a, (int64_t)in * a.T + t, c0, make_uint4(0u, 0u, 0u, 0u));
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    for (int t = t0; t < t1; ++t) cv_scatter(a, dst, (int64_t)in * a.T + t, make_uint4(0u, 0u, 0u, 0u));
     return;
   }
   const int64_t sC = (int64_t)ca.C * (W - 1);  // state entries per sequence
+  auto st_ptr = [&](const uint8_t* base, int64_t sq) {
+    return base + (sq * sC + (int64_t)c0 * (W - 1)) * es;
+  };
+  float sw[WS][VE];  // the current sequence's state, [entry][channel]
+  auto load_state = [&](const uint8_t* base, int64_t sq) {
+#pragma unroll
+    for (int i = 0; i < WS; ++i)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) sw[i][e] = 0.f;
+    if (!base || W == 1) return;
+    float raw[WS * VE];
+    const uint4* p = reinterpret_cast<const uint4*>(st_ptr(base, sq));
+#pragma unroll
+    for (int i = 0; i < WS; ++i) cv_unpack<T, VE>(p[i], raw + i * VE);
+#pragma unroll
+    for (int e = 0; e < VE; ++e)
+#pragma unroll
+      for (int i = 0; i < WS; ++i) sw[i][e] = raw[e * (W - 1) + i];
+  };
+  // sw[si][e] for a runtime si (0 .. W-2, else 0) by unrolled selects, so the
+  // state stays in registers
+  auto sw_at = [&](int si, int e) {
+    float r = 0.f;
+#pragma unroll
+    for (int j = 0; j < WS; ++j) r = (si == j) ? sw[j][e] : r;
+    return r;
+  };
+  float win[WS][VE];  // raw inputs of rows t-(W-1) .. t-1
+  auto store_state = [&](uint8_t* base, int64_t sq, int t_last, int s0) {
+    // the last W-1 inputs of (state ++ sequence rows up to t_last), oldest first
+    if (W == 1) return;
+    float raw[WS * VE];
+#pragma unroll
+    for (int i = 0; i < WS; ++i) {
+      const int src = t_last - (W - 2) + i;  // entry i of the new state
+      const int si = (W - 1) - (s0 - src);   // its place in the old state, if before s0
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        // rows t_last-(W-2) .. t_last: win holds t_last-(W-2) .. t_last after the shift
+        raw[e * (W - 1) + i] = src >= s0 ? win[i][e] : sw_at(si, e);
+      }
+    }
+    uint4* p = reinterpret_cast<uint4*>(const_cast<uint8_t*>(st_ptr(base, sq)));
+#pragma unroll
+    for (int i = 0; i < WS; ++i) p[i] = cv_pack<T, VE>(raw + i * VE);
+  };
   // the sequence of row t0 (varlen) and its bounds; offsets are clamped to
   // [0, T] so that no list, however malformed, moves a read outside the rows
   int seq = in, s_start = 0, s_end = a.T;
@@ -459,77 +610,47 @@ __global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
     seq = lo;
     bounds(seq);
     while (seq < ca.N_seq && s_end <= t0) bounds(++seq);  // skip sequences ending before t0
-    if (t0 == 0 && ca.st_out && W > 1) {
-      // empty sequences keep their initial state: the first tile's threads copy it
+    if (t0 == 0 && ca.st_out && W > 1) {  // empty sequences keep their initial state
       for (int sq = 0; sq < ca.N_seq; ++sq) {
         const int b0 = min(max(ca.cu[sq], 0), a.T), b1 = min(max(ca.cu[sq + 1], b0), a.T);
         if (b1 > b0) continue;
-        for (int e = 0; e < VE; ++e)
-          for (int i = 0; i < W - 1; ++i) {
-            const int64_t off = ((int64_t)sq * sC + (int64_t)(c0 + e) * (W - 1) + i) * es;
-            for (int bb = 0; bb < es; ++bb) ca.st_out[off + bb] = ca.st_in ? ca.st_in[off + bb] : 0;
-          }
+        const uint4* src = ca.st_in ? reinterpret_cast<const uint4*>(st_ptr(ca.st_in, sq)) : nullptr;
+        uint4* d = reinterpret_cast<uint4*>(const_cast<uint8_t*>(st_ptr(ca.st_out, sq)));
+        for (int i = 0; i < W - 1; ++i) d[i] = src ? src[i] : make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
-  float win[W > 1 ? W - 1 : 1][VE];
-  // window for row t: inputs t-(W-1) .. t-1 of its sequence, from rows or the state
-  auto fill = [&](int t) {
-#pragma unroll
-    for (int i = 0; i < W - 1; ++i) {
-      const int src = t - (W - 1) + i;
-      if (src >= s_start) {
-        cv_unpack<T, VE>(__ldcs(reinterpret_cast<const uint4*>(xrow0 + (int64_t)src * a.x_st_b + (int64_t)c0 * es)), win[i]);
-      } else {
-        const int si = (W - 1) - (s_start - src);  // state index (oldest first)
-        const uint8_t* sb = DECODE ? ca.st_in + (int64_t)sl * sC * es
-                                   : (ca.st_in ? ca.st_in + (int64_t)seq * sC * es : nullptr);
-#pragma unroll
-        for (int e = 0; e < VE; ++e)
-          win[i][e] = (sb && si >= 0) ? cv_ld<T>(sb + ((int64_t)(c0 + e) * (W - 1) + si) * es) : 0.f;
+  load_state(ca.st_in, DECODE ? (int64_t)sl : (int64_t)seq);
+  for (int rr = 0; rr < nrows; ++rr) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kConvD - 1) : "memory");
+    float x[VE];
+    cv_unpack<T, VE>(ring[rr % kConvD][threadIdx.x], x);
+    issue(rr + kConvD);  // the slot is free again: the row kConvD ahead goes in
+    const int t = t0 - (W - 1) + rr;
+    if (rr >= W - 1) {
+      if (!DECODE && ca.cu && t >= s_end) {
+        while (t >= s_end && seq < ca.N_seq) bounds(++seq);  // crossed into the next sequence
+        if (seq >= ca.N_seq) break;  // rows past the last sequence are not outputs
+        load_state(ca.st_in, seq);
       }
-    }
-  };
-  auto put_state = [&](uint8_t* base) {  // the window after the last row: the new state
+      float y[VE];
+      const bool near = t - s_start < W - 1;  // some window entries precede the sequence
 #pragma unroll
-    for (int e = 0; e < VE; ++e)
+      for (int e = 0; e < VE; ++e) {
+        float z = bv[e];
 #pragma unroll
-      for (int i = 0; i < W - 1; ++i) {
-        float f[VE];
-#pragma unroll
-        for (int z = 0; z < VE; ++z) f[z] = win[i][z];
-        const uint4 pk = cv_pack<T, VE>(f);
-        const uint8_t* pb = reinterpret_cast<const uint8_t*>(&pk);
-        uint8_t* d = base + ((int64_t)(c0 + e) * (W - 1) + i) * es;
-        for (int bb = 0; bb < es; ++bb) d[bb] = pb[e * es + bb];
+        for (int i = 0; i < W - 1; ++i) {
+          float xi = win[i][e];
+          if (near) {
+            const int src = t - (W - 1) + i, si = (W - 1) - (s_start - src);
+            if (src < s_start) xi = sw_at(si, e);
+          }
+          z = z + wv[i][e] * xi;
+        }
+        z = z + wv[W - 1][e] * x[e];
+        y[e] = z / (1.0f + expf(-z));
       }
-  };
-  fill(t0);
-  auto ldrow = [&](int t) {
-    return __ldcs(reinterpret_cast<const uint4*>(xrow0 + (int64_t)t * a.x_st_b + (int64_t)c0 * es));
-  };
-  uint4 nxt = ldrow(t0);  // one row of lookahead keeps two loads in flight per thread
-  for (int t = t0; t < t1; ++t) {
-    const uint4 cur = nxt;
-    if (t + 1 < t1) nxt = ldrow(t + 1);
-    if (!DECODE && ca.cu) {
-      bool moved = false;
-      while (t >= s_end && seq < ca.N_seq) {  // crossed into the next sequence
-        bounds(++seq);
-        moved = true;
-      }
-      if (seq >= ca.N_seq) break;  // rows past the last sequence are not outputs
-      if (moved) fill(t);
-    }
-    float x[VE], y[VE];
-    cv_unpack<T, VE>(cur, x);
-#pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      float z = bv[e];
-#pragma unroll
-      for (int i = 0; i < W - 1; ++i) z = z + wv[i][e] * win[i][e];
-      z = z + wv[W - 1][e] * x[e];
-      y[e] = z / (1.0f + expf(-z));
+      cv_scatter(a, dst, (int64_t)in * a.T + t, cv_pack<T, VE>(y));
     }
 #pragma unroll
     for (int i = 0; i + 1 < W - 1; ++i)
@@ -537,26 +658,21 @@ __global__ void __launch_bounds__(256) conv_prepare_kernel(ConvArgs ca) {
       for (int e = 0; e < VE; ++e) win[i][e] = win[i + 1][e];
     if (W > 1) {
 #pragma unroll
-      for (int e = 0; e < VE; ++e) win[W > 1 ? W - 2 : 0][e] = x[e];
+      for (int e = 0; e < VE; ++e) win[WS - 1][e] = x[e];
     }
-    cv_scatter<DECODE>(a, (int64_t)in * a.T + t, c0, cv_pack<T, VE>(y));
-    if (!DECODE && ca.st_out && W > 1 && t == s_end - 1)
-      put_state(ca.st_out + (int64_t)(ca.cu ? seq : in) * sC * es);
+    if (rr >= W - 1 && ca.st_out && W > 1 && (DECODE ? t == t1 - 1 : t == s_end - 1))
+      store_state(ca.st_out, DECODE ? (int64_t)sl : (int64_t)(ca.cu ? seq : in), t, s_start);
   }
-  if (DECODE && W > 1) put_state(ca.st_out + (int64_t)sl * sC * es);
-  // prefill: a sequence with no rows in this batch keeps its state only if its
-  // (empty) range starts in this tile; the host launches cover that case
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <typename T, int W>
 cudaError_t launch_conv_w(const ConvArgs& ca, bool decode, cudaStream_t s) {
   const int nvec = ca.C / (16 / (int)sizeof(T));
-  const int tiles = decode ? 1 : (ca.pa.T + ca.RT - 1) / ca.RT;
-  const dim3 grid((unsigned)((int64_t)ca.pa.n * tiles), (unsigned)((nvec + 255) / 256));
-  if (decode)
-    conv_prepare_kernel<T, W, true><<<grid, 256, 0, s>>>(ca);
-  else
-    conv_prepare_kernel<T, W, false><<<grid, 256, 0, s>>>(ca);
+  const int64_t gx = decode ? ca.pa.n : (int64_t)ca.pa.n * ((ca.pa.T + ca.RT - 1) / ca.RT);
+  const dim3 grid((unsigned)gx, (unsigned)((nvec + 255) / 256));
+  auto kern = decode ? conv_prepare_kernel<T, W, true> : conv_prepare_kernel<T, W, false>;
+  kern<<<grid, 256, 0, s>>>(ca);
   return cudaGetLastError();
 }
 
@@ -571,7 +687,8 @@ cudaError_t launch_conv_t(const ConvArgs& ca, bool decode, cudaStream_t s) {
 }
 
 template <int VB>
-cudaError_t launch_vb(const PrepArgs& a, bool decode, cudaStream_t s) {
+cudaError_t launch_vb(PrepArgs a, bool decode, cudaStream_t s) {
+  a.fd_hv = FastDiv((uint32_t)((int64_t)a.N * a.es / VB));
   const int64_t rows = (int64_t)a.n * a.T;
   const int64_t cap = (int64_t)sm_count() * 8;  // 8 resident 256-thread CTAs per SM
   const int grid = (int)(rows < cap ? rows : cap);
@@ -606,6 +723,8 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
   a.v = static_cast<uint8_t*>(v);
   a.beta = beta;
   a.g = g;
+  a.fd_H = FastDiv((uint32_t)H);
+  a.fd_hpg = FastDiv((uint32_t)(H / G));
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec16 = al16(x) && al16(q) && al16(k) && al16(v) && (a.x_sn_b % 16 == 0) &&
                      (a.x_st_b % 16 == 0) && ((int64_t)P * a.es % 16 == 0) &&
@@ -662,7 +781,7 @@ cudaError_t launch_conv_prepare(const void* xp, int64_t xp_sn, int64_t xp_st, co
   ca.bias = bias;
   ca.W = W;
   ca.C = M * H * P + M * G * N + G * N;
-  ca.RT = 32;
+  ca.RT = kConvRT;
   ca.st_in = static_cast<const uint8_t*>(st_in);
   ca.st_out = static_cast<uint8_t*>(st_out);
   ca.cu = cu;
