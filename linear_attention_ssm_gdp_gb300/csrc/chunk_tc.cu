@@ -430,11 +430,8 @@ __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ C
   if (tid == 0) {  // Gram matrix k k^T: M = 128 (rows 64.. unused), N = 64, K = 128
     const uint32_t kb = smem_u32(kbuf);
     const uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-      mma_bf16(tmem, d, d, id, kk > 0);
-    }
+    const uint64_t d0 = sdesc_sw128(kb, 16, 1024);
+    mma_run<8, false, 8192, 32, 8192, 32>(tmem, d0, d0, id);
     mma_commit(&bars[1]);
   }
   if (tid < kBT) {
@@ -484,22 +481,12 @@ __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ C
     const uint32_t ab = smem_u32(atile), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
     const uint32_t idw = idesc_bf16(128, 128, false, true);
     const uint32_t idu = idesc_bf16(128, V, false, true);
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {  // K = 64 positions
-        const uint64_t ad = sdesc_sw128(ab + pass * 8192 + kk * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(kb + kk * 2048, 8192, 1024);
-        mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
-      }
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = sdesc_sw128(ab + (2 + pass) * 8192 + kk * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(vb + kk * 2048, 8192, 1024);
-        mma_bf16(tmem + 128, ad, bd, idu, (pass | kk) != 0);
-      }
+    const uint64_t kd = sdesc_sw128(kb, 8192, 1024), vd = sdesc_sw128(vb, 8192, 1024);
+    // K = 64 positions: hi pass, then lo pass into the same accumulator
+    mma_run<4, false, 0, 32, 0, 2048>(tmem, sdesc_sw128(ab, 16, 1024), kd, idw);
+    mma_run<4, true, 0, 32, 0, 2048>(tmem, sdesc_sw128(ab + 8192, 16, 1024), kd, idw);
+    mma_run<4, false, 0, 32, 0, 2048>(tmem + 128, sdesc_sw128(ab + 2 * 8192, 16, 1024), vd, idu);
+    mma_run<4, true, 0, 32, 0, 2048>(tmem + 128, sdesc_sw128(ab + 3 * 8192, 16, 1024), vd, idu);
     mma_commit(&bars[1]);
   }
   ok = mbar_wait(&bars[1], 1, a.status, kDevTimeout);
@@ -683,17 +670,10 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {  // product 1: D1 = w h  (rows = positions)
       const uint32_t whi = smem_u32(st), wlo = smem_u32(st + 16384), hb = smem_u32(ht);
-#pragma unroll
-      for (int pass = 0; pass < 3; ++pass) {
-        const uint32_t A = pass == 2 ? wlo : whi;
-        const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
-          mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
-        }
-      }
+      // w_hi h_hi + w_hi h_lo + w_lo h_hi
+      mma_run<8, false, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
+      mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
+      mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
       mma_commit(&bars[2]);
     }
     const float4* gk = reinterpret_cast<const float4*>(st + 57344);
@@ -745,14 +725,9 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     tc_fence_after();
     if (tid == 0) {  // product 2: D2 = k^T v'  (rows = state rows kf)
       const uint32_t kb = smem_u32(st + 32768), vb = smem_u32(vp);
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sdesc_sw128(kb + kk * 2048, 8192, 1024);
-          const uint64_t bd = sdesc_sw64(vb + pass * 4096 + kk * 1024, 4096, 512);
-          mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
-        }
+      const uint64_t kd = sdesc_sw128(kb, 8192, 1024);
+      mma_run<4, false, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb, 4096, 512), id2);
+      mma_run<4, true, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb + 4096, 4096, 512), id2);
       mma_commit(&bars[3]);
     }
     ok = mbar_wait(&bars[3], j & 1, a.status, kDevTimeout);
@@ -836,14 +811,9 @@ __device__ bool merge64_tc(float* LA, uint8_t* tiles, uint32_t tmem, uint64_t* b
   auto issue = [&](uint32_t dcol) {  // D[dcol..] = A B over K = 64
     const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi);
     const uint32_t idw = idesc_bf16(128, 128, false, true), idn = idesc_bf16(128, 64, false, true);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tmem + dcol, sdesc_sw128(ah + kk * 32, 16, 1024), sdesc_sw128(bh + kk * 2048, 8192, 1024),
-               idw, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tmem + dcol, sdesc_sw128(al + kk * 32, 16, 1024), sdesc_sw128(bh + kk * 2048, 8192, 1024),
-               idn, true);
+    const uint64_t bd = sdesc_sw128(bh, 8192, 1024);
+    mma_run<4, false, 0, 32, 0, 2048>(tmem + dcol, sdesc_sw128(ah, 16, 1024), bd, idw);
+    mma_run<4, true, 0, 32, 0, 2048>(tmem + dcol, sdesc_sw128(al, 16, 1024), bd, idn);
     mma_commit(bar);
   };
   float x[16];
@@ -1071,11 +1041,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (tid == 128 && !(a.fault && blockIdx.x == 0 && c == 0)) {  // Gram k k^T, 128 x 128, issued beside the row norms of tid < 128
       const uint32_t kb = smem_u32(kbuf);
       const uint32_t id = idesc_bf16(128, 128, false, false);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t d = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        mma_bf16(tmem, d, d, id, kk > 0);
-      }
+      const uint64_t d0 = sdesc_sw128(kb, 16, 1024);
+      mma_run<8, false, 16384, 32, 16384, 32>(tmem, d0, d0, id);
       mma_commit(&bars[1]);
     }
     if (tid < 128) {
@@ -1189,14 +1156,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (tid == 0) {  // w = A' k: M = 128 positions, N = 128, K = 128 positions
       const uint32_t tb = smem_u32(tiles), kb = smem_u32(kbuf);
       const uint32_t idw = idesc_bf16(128, 128, false, true);
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kb + kk * 2048, 16384, 1024);
-          mma_bf16(tmem, ad, bd, idw, (pass | kk) != 0);
-        }
+      const uint64_t kd = sdesc_sw128(kb, 16384, 1024);
+      mma_run<8, false, 16384, 32, 8192, 2048>(tmem, sdesc_sw128(tb, 16, 1024), kd, idw);
+      mma_run<8, true, 16384, 32, 8192, 2048>(tmem, sdesc_sw128(tb + 32768, 16, 1024), kd, idw);
       mma_commit(&bars[1]);
     }
     ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
@@ -1214,14 +1176,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     auto issue_u = [&](int round) {
       const uint32_t tb = smem_u32(tiles), vb = smem_u32(vbuf);
       const uint32_t idu = idesc_bf16(128, VR, false, true);
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(tb + pass * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-          mma_bf16(tmem + 128 + round * VR, ad, bd, idu, (pass | kk) != 0);
-        }
+      const uint64_t vd = sdesc_sw128(vb, 16384, 1024);
+      mma_run<8, false, 16384, 32, 8192, 2048>(tmem + 128 + round * VR, sdesc_sw128(tb, 16, 1024), vd, idu);
+      mma_run<8, true, 16384, 32, 8192, 2048>(tmem + 128 + round * VR, sdesc_sw128(tb + 32768, 16, 1024), vd, idu);
       mma_commit(&bars[1]);
     };
     if (tid == 0) issue_u(0);
@@ -1484,17 +1441,10 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
     if (!__syncthreads_and(ok)) break;
     if (tid == 0) {  // product 1: D1 = w h (rows = 128 positions)
       const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO), hb = smem_u32(ht);
-#pragma unroll
-      for (int pass = 0; pass < 3; ++pass) {
-        const uint32_t A = pass == 2 ? wlo : whi;
-        const uint32_t Bm = hb + (pass == 1 ? 8192 : 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw64(Bm + kk * 1024, 8192, 512);
-          mma_bf16(tmem, ad, bd, id1, (pass | kk) != 0);
-        }
-      }
+      // w_hi h_hi + w_hi h_lo + w_lo h_hi
+      mma_run<8, false, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
+      mma_run<8, true, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
+      mma_run<8, true, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
       mma_commit(&bars[3]);
     }
     ok = mbar_wait(&bars[1], ph, a.status, kDevTimeout);
@@ -1551,14 +1501,9 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
       ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout);
       if (ok) {  // product 2: D2 = k^T v' (rows = state rows kf), K = 128 positions
         const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
-            const uint64_t bd = sdesc_sw64(vb + pass * 8192 + kk * 1024, 8192, 512);
-            mma_bf16(tmem + 32, ad, bd, id2, (pass | kk) != 0);
-          }
+        const uint64_t kd = sdesc_sw128(kb, 16384, 1024);
+        mma_run<8, false, 8192, 2048, 4096, 1024>(tmem + 32, kd, sdesc_sw64(vb, 8192, 512), id2);
+        mma_run<8, true, 8192, 2048, 4096, 1024>(tmem + 32, kd, sdesc_sw64(vb + 8192, 8192, 512), id2);
         mma_commit(&bars[4]);
       }
     }
@@ -1756,19 +1701,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         if (ok) {
           const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO);
           const uint32_t hb = smem_u32(ht);
-          if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // w_hi [h_hi | h_lo]
-              const uint64_t ad = sdesc_sw128(whi + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + TD1, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // w_lo h_hi, its own accumulator
-              const uint64_t ad = sdesc_sw128(wlo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + TD1B, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1, kk > 0);
-            }
-          }
+          if (tid == 0)  // w_hi [h_hi | h_lo]
+            mma_run<8, false, 16384, 32, 4096, 1024>(tmem + TD1, sdesc_sw128(whi, 16, 1024),
+                                                     sdesc_sw64(hb, 8192, 512), id1w);
+          else  // w_lo h_hi, its own accumulator
+            mma_run<8, false, 16384, 32, 4096, 1024>(tmem + TD1B, sdesc_sw128(wlo, 16, 1024),
+                                                     sdesc_sw64(hb, 8192, 512), id1);
           mma_commit(&bars[FB_P1]);
         }
       }
@@ -1836,11 +1774,9 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         ok = mbar_wait(&bars[FB_K], ph, status, kDevTimeout);
         if (ok) {  // product 2: D2 = k^T v', K = 128 positions
           const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // k^T [v'_hi | v'_lo]
-            const uint64_t ad = sdesc_sw128(kb + kk * 2048, 16384, 1024);
-            mma_bf16(tmem + TD2, ad, sdesc_sw64(vb + kk * 1024, 8192, 512), id2w, kk > 0);
-          }
+          // k^T [v'_hi | v'_lo]
+          mma_run<8, false, 8192, 2048, 4096, 1024>(tmem + TD2, sdesc_sw128(kb, 16384, 1024),
+                                                    sdesc_sw64(vb, 8192, 512), id2w);
           mma_commit(&bars[FB_P2]);
         }
       } else if (tid == 32 || tid == 64) {  // Qh (tid 32) and S (tid 64) beside product 2
@@ -1852,19 +1788,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         if (ok) {
           const uint32_t qb = smem_u32(sm + F_Q), kb = smem_u32(sm + S8_K), hb = smem_u32(ht);
           if (tid == 32) {  // Qh = q [h_hi | h_lo]: rows = tokens (64.. unused)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + TQH + 64 * cs, ad, sdesc_sw64(hb + kk * 1024, 8192, 512), id1w, kk > 0);
-            }
+            mma_run<8, false, 8192, 32, 4096, 1024>(tmem + TQH + 64 * cs, sdesc_sw128(qb, 16, 1024),
+                                                    sdesc_sw64(hb, 8192, 512), id1w);
             mma_commit(&bars[FB_QH0 + cs]);
           } else {  // S^T = k q^T: rows = the block's 128 positions, columns = 64 tokens
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = sdesc_sw128(kb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-              mma_bf16(tmem + TS + 64 * cs, ad, bd, ids, kk > 0);
-            }
+            mma_run<8, false, 16384, 32, 8192, 32>(tmem + TS + 64 * cs, sdesc_sw128(kb, 16, 1024),
+                                                   sdesc_sw128(qb, 16, 1024), ids);
             mma_commit(&bars[FB_S0 + cs]);
           }
         }
@@ -1993,17 +1922,12 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
         ok = mbar_wait(&bars[FB_VN], ph, status, kDevTimeout);
         if (ok) {
           const uint32_t pb = smem_u32(pt), vv = smem_u32(vnt);
-          if (otid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // P_hi [vn_hi | vn_lo]
-              mma_bf16(tmem + TO, sdesc_sw128(pb + kk * 2048, 0, 1024),
-                       sdesc_sw64(vv + kk * 1024, 8192, 512), idow, kk > 0);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // P_lo vn_hi, its own accumulator
-              mma_bf16(tmem + TOB, sdesc_sw128(pb + 16384 + kk * 2048, 0, 1024),
-                       sdesc_sw64(vv + kk * 1024, 8192, 512), ido, kk > 0);
-          }
+          if (otid == 0)  // P_hi [vn_hi | vn_lo]
+            mma_run<8, false, 8192, 2048, 4096, 1024>(tmem + TO, sdesc_sw128(pb, 0, 1024),
+                                                      sdesc_sw64(vv, 8192, 512), idow);
+          else  // P_lo vn_hi, its own accumulator
+            mma_run<8, false, 8192, 2048, 4096, 1024>(tmem + TOB, sdesc_sw128(pb + 16384, 0, 1024),
+                                                      sdesc_sw64(vv, 8192, 512), ido);
           mma_commit(&bars[FB_O]);
         }
       }
@@ -2140,20 +2064,12 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
     const uint32_t ids = idesc_bf16(128, NE, false, false);
     const uint32_t idh = idesc_bf16(128, kOBV, false, true);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {  // scores S = q k^T: N = 64 M positions
-      const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-      const uint64_t bd = sdesc_sw128(k0 + (kk >> 2) * (NE * 128) + (kk & 3) * 32, 16, 1024);
-      mma_bf16(tmem, ad, bd, ids, kk > 0);
-    }
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass)  // q h (h hi then lo), N = 64 columns
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(h0 + pass * 16384 + kk * 2048, 16384, 1024);
-        mma_bf16(tmem + NE, ad, bd, idh, (pass | kk) != 0);
-      }
+    const uint64_t qd = sdesc_sw128(q0, 16, 1024);
+    // scores S = q k^T: N = 64 M positions
+    mma_run<8, false, 8192, 32, NE * 128, 32>(tmem, qd, sdesc_sw128(k0, 16, 1024), ids);
+    // q h (h hi then lo), N = 64 columns
+    mma_run<8, false, 8192, 32, 8192, 2048>(tmem + NE, qd, sdesc_sw128(h0, 16384, 1024), idh);
+    mma_run<8, true, 8192, 32, 8192, 2048>(tmem + NE, qd, sdesc_sw128(h0 + 16384, 16384, 1024), idh);
     mma_commit(&bars[1]);
   }
   // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
@@ -2206,17 +2122,10 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     // A = P, MN-major with M = 128: the second 64-token atom is never written and
     // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
     const uint32_t ido = idesc_bf16(128, kOBV, true, true);
-#pragma unroll
-    for (int pass = 0; pass < 3; ++pass) {
-      const uint32_t A = p0 + (pass == 2 ? M * 8192 : 0);
-      const uint32_t Bm = vv + (pass == 1 ? NE * 128 : 0);
-#pragma unroll
-      for (int kk = 0; kk < 4 * M; ++kk) {
-        const uint64_t ad = sdesc_sw128(A + kk * 2048, 0, 1024);
-        const uint64_t bd = sdesc_sw128(Bm + kk * 2048, NE * 128, 1024);
-        mma_bf16(tmem, ad, bd, ido, (pass | kk) != 0);
-      }
-    }
+    // P_hi v_hi + P_hi v_lo + P_lo v_hi
+    mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024), sdesc_sw128(vv, NE * 128, 1024), ido);
+    mma_run<4 * M, true, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024), sdesc_sw128(vv + NE * 128, NE * 128, 1024), ido);
+    mma_run<4 * M, true, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0 + M * 8192, 0, 1024), sdesc_sw128(vv, NE * 128, 1024), ido);
     mma_commit(&bars[2]);
   }
   if (quarter < 2) {

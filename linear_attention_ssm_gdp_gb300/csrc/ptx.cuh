@@ -151,6 +151,34 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// The same MMA with the accumulate flag as an immediate (ACC: add to D).
+template <bool ACC>
+__device__ __forceinline__ void mma_bf16_i(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
+// NK MMAs along K into one accumulator, D (+)= sum_k A_k B_k, from the base
+// descriptors of A_0 and B_0: step k moves A by (k / 4) A_HI + (k % 4) A_LO bytes
+// and B by (k / 4) B_HI + (k % 4) B_LO bytes (a 128-byte swizzle atom holds four
+// 16-element K steps). The steps are added to the descriptors' address field
+// (no carry out of it: shared addresses stay below 256 KB), so each MMA costs one
+// 64-bit add per operand instead of building its descriptors from scratch; the
+// first MMA overwrites D unless ACC0.
+template <int NK, bool ACC0, int A_HI, int A_LO, int B_HI, int B_LO>
+__device__ __forceinline__ void mma_run(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+  mma_bf16_i<ACC0>(d_tmem, a0, b0, idesc);
+#pragma unroll
+  for (int kk = 1; kk < NK; ++kk)
+    mma_bf16_i<true>(d_tmem, a0 + (uint64_t)((((kk >> 2) * A_HI) + (kk & 3) * A_LO) >> 4),
+                     b0 + (uint64_t)((((kk >> 2) * B_HI) + (kk & 3) * B_LO) >> 4), idesc);
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
