@@ -61,7 +61,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ------------------------------------------------------------------------------------
 __global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M, int BT,
                               int64_t NE_max, int64_t NT_max, int4* seq_info, int2* exp_tab,
-                              int2* tok_tab, int2* blk_tab, int64_t NB_max, int* status) {
+                              int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status) {
   __shared__ int s_bad;
   __shared__ int s_ne, s_nt;
   if (threadIdx.x == 0) {
@@ -109,17 +109,21 @@ __global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M,
   }
   for (int64_t c = ne + threadIdx.x; c < NE_max; c += blockDim.x) exp_tab[c] = make_int2(-1, 0);
   for (int64_t c = nt + threadIdx.x; c < NT_max; c += blockDim.x) tok_tab[c] = make_int2(-1, 0);
-  if (blk_tab) {  // 128-position blocks: (sequence, index of the block's first 64-chunk)
+  // 128-position blocks: (sequence, index of the block's first 64-chunk, the
+  // sequence's first token, its length), so that a block's reader needs one load
+  if (blk_tab) {
     int64_t nb = 0;
     if (!s_bad) {
       for (int i = 0; i < N_seq; ++i) {
         const int4 si = seq_info[i];
         const int nbi = (int)cdiv((int64_t)si.y * M, 128);
-        for (int c = threadIdx.x; c < nbi; c += blockDim.x) blk_tab[nb + c] = make_int2(i, 2 * c);
+        for (int c = threadIdx.x; c < nbi; c += blockDim.x)
+          blk_tab[nb + c] = make_int4(i, 2 * c, si.x, si.y);
         nb += nbi;
       }
     }
-    for (int64_t c = nb + threadIdx.x; c < NB_max; c += blockDim.x) blk_tab[c] = make_int2(-1, 0);
+    for (int64_t c = nb + threadIdx.x; c < NB_max; c += blockDim.x)
+      blk_tab[c] = make_int4(-1, 0, 0, 0);
   }
 }
 
@@ -562,7 +566,7 @@ cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws)
       p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT, p.NE_max, p.NT_max,
       reinterpret_cast<int4*>(ws + L.seq_info), reinterpret_cast<int2*>(ws + L.exp_tab),
       reinterpret_cast<int2*>(ws + L.tok_tab),
-      L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int2*>(ws + L.blk_tab),
+      L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int4*>(ws + L.blk_tab),
       block128_bound(p.B, p.T, p.N_seq, p.M), reinterpret_cast<int*>(ws + L.status));
   return cudaGetLastError();
 }

@@ -230,7 +230,8 @@ struct WyArgs {
   const float* g;
   const int4* seq_info;
   const int2* exp_tab;
-  const int2* blk_tab;  // 128-position blocks (wy128 only)
+  const int4* blk_tab;  // 128-position blocks (wy128 only): sequence, first 64-chunk,
+                        // sequence's first token, its length; sequence -1 past the end
   bf16* w_hi;
   bf16* w_lo;
   float* u;
@@ -928,30 +929,29 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   const int M = a.M;
   const int n_items = NB * a.HV;
-  auto valid = [&](int it) { return a.blk_tab[it % NB].x >= 0; };
-  auto next_valid = [&](int it) {
-    do it += gridDim.x; while (it < n_items && !valid(it));
-    return it;
-  };
+  // a block's record (one 16-byte load); items past the end read as invalid
+  auto tab_of = [&](int i) { return i < n_items ? a.blk_tab[i % NB] : make_int4(-1, 0, 0, 0); };
   int it = blockIdx.x;
-  if (it < n_items && !valid(it)) it = next_valid(it);
+  int4 tab = tab_of(it);
+  while (it < n_items && tab.x < 0) tab = tab_of(it += gridDim.x);  // only the padded tail
   if (it >= n_items) return;
   struct Item {
     int hv, kh, n, b_start, t0;
     int64_t R0;
   };
-  auto item = [&](int i) {
+  auto item = [&](int i, int4 tb) {
     Item x;
-    const int2 tab = a.blk_tab[i % NB];  // (sequence, first of the block's two 64-chunks)
-    const int4 si = a.seq_info[tab.x];
     x.hv = i / NB;
     x.kh = x.hv / (a.HV / a.H);
-    x.b_start = tab.y * kBT;
-    x.n = min(128, si.y * M - x.b_start);
-    x.t0 = si.x;
-    x.R0 = (int64_t)si.x * M + x.b_start;
+    x.b_start = tb.y * kBT;
+    x.n = min(128, tb.w * M - x.b_start);
+    x.t0 = tb.z;
+    x.R0 = (int64_t)tb.z * M + x.b_start;
     return x;
   };
+  // the next item's record is loaded one item ahead, so no item waits on it
+  int nx = it + gridDim.x;
+  int4 ntab = tab_of(nx);
   // beta and the decay (on a token's first copy) of position p of item x
   auto gates = [&](const Item& x, int p, float& b, float& gl) {
     b = 0.f;
@@ -988,7 +988,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
-  Item x = item(it);
+  Item x = item(it, tab);
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
@@ -1023,9 +1023,11 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     float* s2h = sco + 128;
     float* s2l = s2h + 128;
     float* nsb = sarr + (par ^ 1) * 896;  // the next item's beta and decay
-    const int nx = next_valid(it);
+    while (nx < n_items && ntab.x < 0) ntab = tab_of(nx += gridDim.x);  // only the padded tail
     const bool has_next = nx < n_items;
-    const Item y = has_next ? item(nx) : x;
+    const Item y = has_next ? item(nx, ntab) : x;
+    const int nnx = nx + gridDim.x;
+    const int4 nntab = tab_of(nnx);  // used by the next iteration
     float pb[4], pg[4];  // warp 15: the next item's gate inputs (positions 4 lane + i)
     if (warp == 15 && has_next) {
 #pragma unroll
@@ -1059,7 +1061,10 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       }
     }
     fence_async_smem();  // the k buffer's generic reads end before the next k load
-    if (kPipe && tid == 0) tma_store_wait_read();  // the previous item's stores have read LA, tiles
+    // The previous item's w stores (staged in LA, which the L build overwrites)
+    // must have read shared memory; its u stores (staged in the operand tiles,
+    // the solve's scratch) may go on reading until just before the solve.
+    if (kPipe && tid == 0) tma_store_wait_read_but_last();
     ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
     mma_phase ^= 1;
     tc_fence_after();
@@ -1095,6 +1100,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         }
       }
     }
+    if (kPipe && tid == 0) tma_store_wait_read();  // the u stores have read the operand tiles
     tc_fence_before();
     __syncthreads();
     ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
@@ -1302,6 +1308,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (!has_next) break;
     it = nx;
     x = y;
+    nx = nnx;
+    ntab = nntab;
   }
   if (tid == 0) {  // nothing may still write or read shared memory when the CTA leaves
     bool w = true;
@@ -2282,7 +2290,7 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.seq_info = take(sizeof(int4) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.exp_tab = take(sizeof(int2) * (size_t)NE);
   L.tok_tab = take(sizeof(int2) * (size_t)NT);
-  if (M % 2 == 0) L.blk_tab = take(sizeof(int2) * (size_t)block128_bound(B, T, N_seq, M));
+  if (M % 2 == 0) L.blk_tab = take(sizeof(int4) * (size_t)block128_bound(B, T, N_seq, M));
   L.w_hi = take(2 * Te * HV * K);
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
@@ -2316,7 +2324,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
   if (p.NE_max > 0 && Te > 0) {
     WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
              reinterpret_cast<const int2*>(ws + L.exp_tab),
-             L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<const int2*>(ws + L.blk_tab),
+             L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<const int4*>(ws + L.blk_tab),
              w_hi, w_lo, u, gk, status, 0};
     if ((p.M % 2) == 0) a.fault = g_wy_fault.exchange(0);  // one-shot test hook
     const bool blk128 = (p.M % 2) == 0;
