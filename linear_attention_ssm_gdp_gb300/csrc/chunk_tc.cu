@@ -774,7 +774,11 @@ constexpr int W8_V = 32768;
 constexpr int W8_T = 65536;
 constexpr int W8_LA = W8_T + 65536;
 constexpr int W8_S = W8_LA + 128 * 129 * 4;
-constexpr int W8_SMEM = W8_S + 2 * 7 * 128 * 4 + 64 + 1024;
+// aligned copy of L's four 32x32 diagonal blocks ([4][32][32], 16-byte chunks
+// swizzled by row), read by the diagonal-block forward substitution
+constexpr int W8_LD = 204800;
+static_assert(W8_LD >= W8_S + 2 * 7 * 128 * 4 + 64, "diagonal-block copy overlaps");
+constexpr int W8_SMEM = W8_LD + 4 * 32 * 32 * 4 + 1024;
 
 // Top merge of the 128x128 inverse on the tensor cores: X = L10 A00, then
 // A10 = -A11 X, each as x_hi [y_hi | y_lo] (one N = 128 MMA per k-step) plus
@@ -867,37 +871,98 @@ __device__ bool merge64_tc(float* LA, uint8_t* tiles, uint32_t tmem, uint64_t* b
 
 // In-place inverse of the unit lower-triangular 128x128 matrix I + L held
 // strictly lower in LA (row stride 129, zeros on and above the diagonal):
-// 16x16 diagonal blocks by forward substitution (results staged in scratch,
-// then copied back), then merges A10 = -A11 (L10 A00) at sizes 16 and 32 on
-// the CUDA cores and 64 on the tensor cores (merge64_tc). scratch: the 64 KB
-// operand-tile region; TMEM columns [0, 256) and `bar` (phases 0, 1) are used.
-// 512 threads. Returns false if a bounded wait gave up.
-__device__ bool solve_tril128(float* LA, float* scratch, uint32_t tmem, uint64_t* bar, int* status) {
-  const int tid = threadIdx.x;
-  if (tid < 128) {
-    const int b = tid >> 4, cl = tid & 15;
-    const float* Lb = LA + (b * 16) * 129 + b * 16;
-    float col[16];
+//  * the four 32x32 diagonal blocks by forward substitution, warp b (0..3) on
+//    block b, lane c on its column c, the column in registers; L's diagonal
+//    blocks come from Ld (an aligned copy, [4][32][32] with row r's 16-byte
+//    chunk q at chunk q ^ (r & 7), so a row is eight broadcast vector loads);
+//    the inverse blocks go to LA and to an aligned copy Ad [4][32][36];
+//  * the 32 merges A10 = -A11 (L10 A00) of the two 64 blocks on the CUDA cores,
+//    their A00 / A11 / X operands read as vectors from Ad and the scratch Xs;
+//  * the 64 merge on the tensor cores (merge64_tc).
+// Both CUDA-core stages are bound by shared-memory load issue (one load a clock
+// for the whole SM), which the vector loads cut. scratch: the 64 KB operand-tile
+// region; TMEM columns [0, 256) and `bar` (phases 0, 1) are used. 512 threads.
+// Returns false if a bounded wait gave up.
+__device__ bool solve_tril128(float* LA, const float* Ld, float* scratch, uint32_t tmem,
+                              uint64_t* bar, int* status) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* Ad = scratch;            // [4][32][36]
+  float* Xs = scratch + 4 * 1152; // [2][32][36]
+  if (warp < 4) {
+    const float* Lb = Ld + warp * 1024;
+    float col[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) col[i] = (i == cl) ? 1.f : 0.f;
+    for (int i = 0; i < 32; ++i) col[i] = (i == lane) ? 1.f : 0.f;
 #pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      float s = 0.f;
+    for (int r = 1; r < 32; ++r) {
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < r; ++i) s += Lb[r * 129 + i] * col[i];  // col[i] = 0 for i < cl
-      if (r > cl) col[r] = -s;
+      for (int q = 0; q < (r + 3) / 4; ++q) {
+        const float4 l = *reinterpret_cast<const float4*>(Lb + r * 32 + ((q ^ (r & 7)) << 2));
+        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * q + e < r) s4[e] = fmaf(lv[e], col[4 * q + e], s4[e]);  // col[i] = 0 for i < lane
+      }
+      if (r > lane) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
     }
+    float* la = LA + (warp * 32) * 129 + warp * 32 + lane;
+    float* ad = Ad + warp * 1152 + lane;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) scratch[(b * 16 + i) * 16 + cl] = col[i];
+    for (int i = 0; i < 32; ++i) {
+      la[i * 129] = col[i];
+      ad[i * 36] = col[i];
+    }
   }
   __syncthreads();
-  for (int idx = tid; idx < 128 * 16; idx += 512) {
-    const int row = idx >> 4, cl = idx & 15;
-    LA[row * 129 + (row & ~15) + cl] = scratch[idx];
+  {  // 32 merges of the two 64 blocks, 4 outputs a thread
+    const int pair = tid >> 8, rem = tid & 255;
+    const int base = pair * 64;
+    const float* A00 = Ad + (2 * pair) * 1152;
+    const float* A11 = Ad + (2 * pair + 1) * 1152;
+    float* X = Xs + pair * 1152;
+    // warps of a pair take their column (row) blocks in the order 0 1 2 3 7 6 5 4, so
+    // that warps sharing an SM sub-partition get a heavy and a light block
+    const int wip = rem >> 5, li = rem & 31;
+    const int mw = ((wip >> 2) & 1) ? (wip | 3) - (wip & 3) : wip;
+    float acc[4];
+    {  // X = L10 A00, A00 lower triangular: i >= c0
+      const int r = li, c0 = mw * 4;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) acc[cc] = 0.f;
+      const float* lrow = LA + (base + 32 + r) * 129 + base;
+#pragma unroll 4
+      for (int i = c0; i < 32; ++i) {
+        const float av = lrow[i];
+        const float4 b = *reinterpret_cast<const float4*>(A00 + i * 36 + c0);
+        acc[0] = fmaf(av, b.x, acc[0]);
+        acc[1] = fmaf(av, b.y, acc[1]);
+        acc[2] = fmaf(av, b.z, acc[2]);
+        acc[3] = fmaf(av, b.w, acc[3]);
+      }
+      *reinterpret_cast<float4*>(X + r * 36 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    __syncthreads();
+    {  // A10 = -A11 X, A11 lower triangular: i <= r0
+      const int r0 = mw * 4 + (li >> 3), c0 = (li & 7) * 4;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) acc[cc] = 0.f;
+      const float* arow = A11 + r0 * 36;
+#pragma unroll 4
+      for (int i = 0; i <= r0; ++i) {
+        const float av = arow[i];
+        const float4 b = *reinterpret_cast<const float4*>(X + i * 36 + c0);
+        acc[0] = fmaf(av, b.x, acc[0]);
+        acc[1] = fmaf(av, b.y, acc[1]);
+        acc[2] = fmaf(av, b.z, acc[2]);
+        acc[3] = fmaf(av, b.w, acc[3]);
+      }
+      float* dst = LA + (base + 32 + r0) * 129 + base + c0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) dst[cc] = -acc[cc];
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  merge_level<16, 4, 512>(LA, 129, scratch);
-  merge_level<32, 2, 512>(LA, 129, scratch);
   return merge64_tc(LA, reinterpret_cast<uint8_t*>(scratch), tmem, bar, status);
 }
 
@@ -966,6 +1031,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   uint8_t* vbuf = sm + W8_V;
   uint8_t* tiles = sm + W8_T;
   float* LA = reinterpret_cast<float*>(sm + W8_LA);
+  float* Ld = reinterpret_cast<float*>(sm + W8_LD);
   float* scratch = reinterpret_cast<float*>(tiles);
   // [2][7][128] by item parity: beta, Gam hi, Gam lo, 1/|k|, column scale,
   // Gam hi and lo in base 2
@@ -1095,15 +1161,25 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
           } else {
             v = upk2(mul2(bp2, kk));
           }
-          LA[p * 129 + i] = (i < p) ? v.x : 0.f;
-          LA[p * 129 + i + 1] = (i + 1 < p) ? v.y : 0.f;
+          // (the register array r now carries this row's L values)
+          r[j] = __float_as_uint((i < p) ? v.x : 0.f);
+          r[j + 1] = __float_as_uint((i + 1 < p) ? v.y : 0.f);
+          LA[p * 129 + i] = __uint_as_float(r[j]);
+          LA[p * 129 + i + 1] = __uint_as_float(r[j + 1]);
+        }
+        if (cq == quarter) {  // a diagonal block: also its aligned, swizzled copy
+          float* ld = Ld + quarter * 1024 + lane * 32;
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq)
+            *reinterpret_cast<uint4*>(ld + ((qq ^ (lane & 7)) << 2)) =
+                make_uint4(r[4 * qq], r[4 * qq + 1], r[4 * qq + 2], r[4 * qq + 3]);
         }
       }
     }
     if (kPipe && tid == 0) tma_store_wait_read();  // the u stores have read the operand tiles
     tc_fence_before();
     __syncthreads();
-    ok = solve_tril128(LA, scratch, tmem, &bars[3], a.status);
+    ok = solve_tril128(LA, Ld, scratch, tmem, &bars[3], a.status);
     if (!ok) break;
     // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
     // Warp w builds one 32 x 32 chunk (row block R, column block C) of A, lane =
