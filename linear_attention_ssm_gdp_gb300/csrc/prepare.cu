@@ -18,7 +18,10 @@
 // kernel is a pure HBM stream. When a row fits one pass of the block
 // (prepare_rows_kernel, the prefill rows of the usual head sizes) each CTA
 // already has the next row's loads in flight while it stores the current one;
-// longer rows go through prepare_kernel, a row at a time. The gates use
+// longer rows (the decode rows among them) stream through a shared-memory ring
+// of raw rows filled by cp.async (prepare_ring_kernel), and rows too long for
+// that ring, or not 16-byte aligned, go through prepare_kernel, a row at a
+// time. The gates use
 // the CUDA math library's expf/log1pf and IEEE division, one fp32 operation at
 // a time; this translation unit is compiled with --fmad=false so no
 // multiply-add is contracted, which keeps beta and g bitwise equal to the
@@ -163,6 +166,14 @@ __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
   }
 }
 
+// Asynchronous 16-byte global -> shared copy (zero-filled when bytes is 0).
+__device__ __forceinline__ void cp16(void* dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   (unsigned)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+
 // Rows that fit one pass of the block (at most 256 x kPU 16-byte vectors, at
 // most 256 gate columns): each CTA loads row r + gridDim.x, gate inputs
 // included, before it stores row r, so every thread keeps a row of loads in
@@ -284,6 +295,85 @@ __global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
     if (rn < rows) load_row<DECODE>(a, g, rn, nxt);
     store_row<DECODE>(a, g, r, cur);
     cur = nxt;
+  }
+}
+
+// Long rows (beyond one pass of prepare_rows_kernel: the decode rows, where q
+// has a row per copy, and prefill rows with many heads). Each CTA walks rows
+// blockIdx.x + i * gridDim.x; the raw x row streams into a ring of kRing
+// row buffers in shared memory with cp.async (one commit group per row), so
+// the next kRing - 1 rows are in flight without holding registers while the
+// threads store the current one: v as a contiguous copy, k and q as one
+// 16-byte shared-memory read per output vector (group expansion and decode
+// copy placement as prepare_kernel). Same fp32 gate operations.
+constexpr int kRing = 3;
+
+template <bool DECODE>
+__global__ void __launch_bounds__(512, 3) prepare_ring_kernel(PrepArgs a, int xrow_v) {
+  extern __shared__ uint4 ring[];  // [kRing][xrow_v]
+  const int64_t rows = (int64_t)a.n * a.T;
+  const RowGeo g = row_geo(a, DECODE);
+  const int tid = threadIdx.x;
+  const int mine = (int)((rows - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  const int ntot = g.nv + g.nk + g.nq;
+  const int kb_v = (int)(g.kbase_b / 16), qb_v = (int)(g.qbase_b / 16);
+  auto fetch = [&](int i) {  // row i of this CTA into slot i % kRing (always one group)
+    if (i < mine) {
+      const int64_t r = blockIdx.x + (int64_t)i * gridDim.x;
+      const int64_t in = r / a.T, t = r - in * a.T;
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + in * a.x_sn_b + t * a.x_st_b);
+      uint4* dst = ring + (i % kRing) * xrow_v;
+      for (int c = tid; c < xrow_v; c += blockDim.x) cp16(dst + c, src + c, 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) fetch(i);
+  for (int i = 0; i < mine; ++i) {
+    fetch(i + kRing - 1);  // into the slot row i - 1 used (freed by the barrier below)
+    const int64_t r = blockIdx.x + (int64_t)i * gridDim.x;
+    const int64_t in = r / a.T, t = r - in * a.T;
+    const int64_t bar = in * a.ba_sn + t * a.ba_st;
+    uint32_t b = 0, av = 0;
+    if (tid < g.MH) b = raw_ld(a.ba, bar + tid, a.dt);
+    if (tid < a.H) av = raw_ld(a.ba, bar + g.MH + tid, a.dt);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+    __syncthreads();  // row i is in its slot
+    const uint4* s = ring + (i % kRing) * xrow_v;
+    uint4* vdst = reinterpret_cast<uint4*>(a.v + r * g.vrow_b);
+    uint4* kdst = reinterpret_cast<uint4*>(a.k + r * g.krow_b);
+    uint4* qdst = reinterpret_cast<uint4*>(a.q + r * g.qrow_b);
+    for (int c = tid; c < ntot; c += blockDim.x) {
+      if (c < g.nv) {  // value: contiguous copy of the row's value block
+        __stcs(vdst + c, s[c]);
+      } else if (c < g.nv + g.nk) {  // key: output head (j, h) reads group (j, h / hpg)
+        const int ck = c - g.nv;
+        const int jh = a.fd_hv.div(ck), w = ck - jh * g.head_v;
+        const int j = a.fd_H.div(jh), h = jh - j * a.H;
+        __stcs(kdst + ck, s[kb_v + (j * a.G + a.fd_hpg.div(h)) * g.head_v + w]);
+      } else {  // query: prefill one row per token; decode the last copy, +0 elsewhere
+        const int cq = c - g.nv - g.nk;
+        const int jh = a.fd_hv.div(cq), w = cq - jh * g.head_v;
+        const int j = DECODE ? a.fd_H.div(jh) : a.M - 1;
+        const int h = DECODE ? jh - j * a.H : jh;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (j == a.M - 1) val = s[qb_v + a.fd_hpg.div(h) * g.head_v + w];
+        __stcs(qdst + cq, val);
+      }
+    }
+    if (tid < g.MH) a.beta[r * g.MH + tid] = 1.0f / (1.0f + expf(-raw_f32(b, a.dt)));
+    const int ng = DECODE ? g.MH : a.H;
+    if (tid < ng) {
+      const int j = DECODE ? tid / a.H : 0;
+      const int h = DECODE ? tid - j * a.H : tid;
+      float gv = 0.0f;
+      if (j == 0) {
+        const float sp = softplus_page(raw_f32(av, a.dt) + a.dt_bias[h]);
+        gv = -(expf(a.A_log[h]) * sp);
+      }
+      a.g[r * ng + tid] = gv;
+    }
+    __syncthreads();  // slot i % kRing is read: row i + kRing may land there
   }
 }
 
@@ -457,13 +547,6 @@ __device__ __forceinline__ void cv_gates(const PrepArgs& a, int64_t r, int i) {
 // a thread's VE channels x (W-1) entries are contiguous in [.., C, W-1].
 constexpr int kConvRT = 64;  // prefill token rows per tile
 constexpr int kConvD = 8;    // rows in flight per thread
-
-__device__ __forceinline__ void cp16(void* dst, const void* src, int bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                   (unsigned)__cvta_generic_to_shared(dst)),
-               "l"(src), "r"(bytes)
-               : "memory");
-}
 
 template <typename T, int W, bool DECODE>
 __global__ void __launch_bounds__(256, 2) conv_prepare_kernel(ConvArgs ca) {
@@ -744,6 +827,23 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
         prepare_rows_kernel<true><<<grid, 256, 0, stream>>>(a);
       else
         prepare_rows_kernel<false><<<grid, 256, 0, stream>>>(a);
+      return cudaGetLastError();
+    }
+    const int64_t xrow_b = (int64_t)(M * H * P + M * G * N + G * N) * a.es;
+    const int64_t ring_b = kRing * xrow_b;
+    if (ring_b <= 200 * 1024 && M * H <= 512) {
+      a.fd_hv = FastDiv((uint32_t)((int64_t)N * a.es / 16));
+      auto kern = decode ? prepare_ring_kernel<true> : prepare_ring_kernel<false>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)ring_b);
+      if (e != cudaSuccess) return e;
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 512, (size_t)ring_b);
+      if (e != cudaSuccess) return e;
+      const int64_t rows = (int64_t)n * T;
+      const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+      const int grid = (int)(rows < cap ? rows : cap);
+      kern<<<grid, 512, (size_t)ring_b, stream>>>(a, (int)(xrow_b / 16));
       return cudaGetLastError();
     }
     return launch_vb<16>(a, decode, stream);

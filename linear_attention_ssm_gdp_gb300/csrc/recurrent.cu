@@ -451,9 +451,13 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         load_batch(pf, q, k, v, beta, g, it, e0 + kB, L, H, HV, V, ncs);
       else if (nx < n_items)
         load_batch(pf, q, k, v, beta, g, nx, 0, L, H, HV, V, ncs);
-      for (int e = 0; e < lc; ++e) {
-        const ulonglong2* kr = reinterpret_cast<const ulonglong2*>(kn + e * kRowPad + grp * kGrpPad);
-        const ulonglong2* qr = reinterpret_cast<const ulonglong2*>(qn + e * kRowPad + grp * kGrpPad);
+      // one step: decay, k^T h, the rank-1 update and o = scale h^T q
+      float* ob = o + (re0 * HV + hv) * V + col;  // this thread's o entry of step e0
+      const float* kg = kn + grp * kGrpPad;
+      const float* qg = qn + grp * kGrpPad;
+      auto step = [&](int e) {
+        const ulonglong2* kr = reinterpret_cast<const ulonglong2*>(kg + e * kRowPad);
+        const ulonglong2* qr = reinterpret_cast<const ulonglong2*>(qg + e * kRowPad);
         const f2 d2 = pk2(eg[e], eg[e]);
         f2 pa = pk2(0.f, 0.f), pb = pa;
 #pragma unroll
@@ -470,20 +474,26 @@ recurrent128_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
         p += __shfl_xor_sync(0xffffffffu, p, 16);
         const float delta = bt[e] * (vs[e * kSliceCols + cw] - p);
         const f2 dl2 = pk2(delta, delta);
-        f2 oa = pk2(0.f, 0.f), ob = oa;
+        f2 oa = pk2(0.f, 0.f), obb = oa;
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const ulonglong2 kk = kr[i4], qq = qr[i4];
           h[2 * i4] = fma2(kk.x, dl2, h[2 * i4]);
           h[2 * i4 + 1] = fma2(kk.y, dl2, h[2 * i4 + 1]);
           oa = fma2(h[2 * i4], qq.x, oa);
-          ob = fma2(h[2 * i4 + 1], qq.y, ob);
+          obb = fma2(h[2 * i4 + 1], qq.y, obb);
         }
-        const float2 oav = upk2(oa), obv = upk2(ob);
+        const float2 oav = upk2(oa), obv = upk2(obb);
         float po = (oav.x + oav.y) + (obv.x + obv.y);
         po += __shfl_xor_sync(0xffffffffu, po, 8);
         po += __shfl_xor_sync(0xffffffffu, po, 16);
-        if (grp == 0 && active) o[((re0 + e) * HV + hv) * V + col] = live ? scale * po : 0.f;
+        if (grp == 0 && active) ob[(int64_t)e * HV * V] = live ? scale * po : 0.f;
+      };
+      if (lc == kB) {  // a full batch: straight-line steps
+#pragma unroll
+        for (int e = 0; e < kB; ++e) step(e);
+      } else {
+        for (int e = 0; e < lc; ++e) step(e);
       }
     }
     if (active && live) {

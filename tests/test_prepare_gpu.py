@@ -132,12 +132,16 @@ def test_deterministic(gdp):
 
 
 @pytest.mark.parametrize("decode", [False, True])
-@pytest.mark.parametrize("M,H,G,P,N", [(3, 16, 4, 128, 128), (2, 32, 8, 128, 128),
-                                       (5, 8, 8, 64, 128)])
-def test_prepare_long_rows_in_segments(gdp, decode, M, H, G, P, N):
-    """Rows of 1.4-3k 16-byte vectors: the row kernel cuts them into several
-    segments (the last one shorter), over strided rows."""
-    n, T = 2, 7
+@pytest.mark.parametrize("M,H,G,P,N,n,T", [
+    (3, 16, 4, 128, 128, 2, 7), (2, 32, 8, 128, 128, 2, 7), (5, 8, 8, 64, 128, 2, 7),
+    (2, 32, 8, 128, 128, 100, 16),  # several rows per resident CTA: the ring wraps
+    (4, 64, 8, 128, 128, 2, 3),     # 76 KB rows: past the ring, one row at a time
+])
+def test_prepare_long_rows(gdp, decode, M, H, G, P, N, n, T):
+    """Rows of 1.4-5k 16-byte vectors, beyond one pass of the row kernel: the
+    shared-memory ring of raw rows (several rows per CTA when there are more
+    rows than resident CTAs) and, for rows too long for the ring, the
+    row-at-a-time kernel; over strided rows."""
     d = si.prepare_inputs(n, T, M, H, G, P, N, seed=M + H)
     D = d["x"].shape[-1]
     big = torch.zeros(n, T, D + 64, dtype=torch.bfloat16)

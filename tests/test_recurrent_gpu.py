@@ -56,6 +56,38 @@ def test_recurrent_small(gdp, n, L, H, HV, K, V, dtype, l2):
     assert rel_err(sd, rs) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_recurrent_extreme_decays_and_zero_queries(gdp, dtype):
+    """K = 128 kernel: decays strong enough that the running product of a call's
+    decays leaves the fp32 range (g = -200 underflows e^g to 0; runs of -30 cross
+    2^-40 several times), g = 0 steps, and all-zero query rows (their o rows are
+    exact zeros), over two staged batches of steps."""
+    n, L, H, HV, K, V = 3, 13, 2, 4, 128, 72
+    gen = torch.Generator().manual_seed(11)
+    q = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    q[:, 0::2] = 0          # every other step has no query (the decode copy layout)
+    q[1, 5] = 0
+    k = torch.randn(n, L, H, K, generator=gen).to(dtype)
+    v = torch.randn(n, L, HV, V, generator=gen).to(dtype)
+    beta = torch.rand(n, L, HV, generator=gen)
+    g = -torch.rand(n, L, HV, generator=gen)
+    g[0, :, :] = -30.0
+    g[1, 3, :] = -200.0
+    g[1, 7:, 1] = -45.0
+    g[2, :, 2] = 0.0
+    state = torch.randn(n, HV, K, V, generator=gen) * 0.1
+    ro, rs = oracle.recurrent(q, k, v, beta, g, state, K ** -0.5, l2norm=True)
+    sd = state.to(DEV)
+    o = gdp.gdp_recurrent_update(*to(DEV, q, k, v, beta, g), sd, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert rel_err(o, ro) <= TOL[dtype]
+    assert rel_err(sd, rs) <= TOL[dtype]
+    zero_rows = (q.float().abs().sum(-1) == 0)            # [n, L, H]
+    hv_to_h = torch.arange(HV) // (HV // H)
+    oz = o.cpu()[zero_rows[:, :, hv_to_h]]
+    assert torch.count_nonzero(oz) == 0
+
+
 @pytest.mark.parametrize("K", [64, 128])
 def test_recurrent_matches_chunked_prefill(gdp, K):
     """Walking a prefill's copies one step at a time (q on the last copy, g on the
