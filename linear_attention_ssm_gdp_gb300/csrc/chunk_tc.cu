@@ -545,28 +545,20 @@ struct HArgs {
   int* status;
 };
 
-// Per stage: w_hi (16 KB) | w_lo (16 KB) | k (16 KB) | u fp32 64x32 (8 KB) | gk 64x16 B (1 KB)
-constexpr int H_STAGE = 16384 * 3 + 8192 + 1024;          // 58 KB
-constexpr int H_HT = 2 * H_STAGE;                         // h^T hi (8 KB) | lo (8 KB)
-constexpr int H_VP = H_HT + 16384;                        // v'^T hi (4 KB) | lo (4 KB)
+// Shared memory: w_hi (16 KB) | w_lo (16 KB) | k (16 KB) | u fp32 64x32 (8 KB) | gk
+// 64x16 B (1 KB) | h^T hi | lo (16 KB) | v'^T hi | lo (8 KB) | barriers: 82 KB, so two
+// CTAs share an SM. Each operand has one buffer and its own barrier; the next
+// chunk's tile is requested as soon as this chunk's last reader of that buffer
+// is done (w after product 1, u and the records after the value phase, k after
+// product 2), so each load streams in behind the rest of the step.
+constexpr int H_W = 0;
+constexpr int H_K = 32768;
+constexpr int H_U = 49152;
+constexpr int H_G = 57344;
+constexpr int H_HT = 58368;                               // 1024-aligned
+constexpr int H_VP = H_HT + 16384;
 constexpr int H_BAR = H_VP + 8192;
 constexpr int H_SMEM = H_BAR + 64 + 1024;
-
-__device__ __forceinline__ void h_issue_loads(uint8_t* st, const CUtensorMap* mw_hi,
-                                              const CUtensorMap* mw_lo, const CUtensorMap* mk,
-                                              const CUtensorMap* mu, const CUtensorMap* mgk, int kh,
-                                              int hv, int v0, int64_t R, int64_t gk_row,
-                                              uint64_t* bar) {
-  mbar_expect_tx(bar, 6 * 8192 + 8192 + 1024);
-  tma_load_3d(st, mw_hi, 0, hv, (int)R, bar);
-  tma_load_3d(st + 8192, mw_hi, 64, hv, (int)R, bar);
-  tma_load_3d(st + 16384, mw_lo, 0, hv, (int)R, bar);
-  tma_load_3d(st + 24576, mw_lo, 64, hv, (int)R, bar);
-  tma_load_3d(st + 32768, mk, 0, kh, (int)R, bar);
-  tma_load_3d(st + 40960, mk, 64, kh, (int)R, bar);
-  tma_load_3d(st + 49152, mu, v0, hv, (int)R, bar);
-  tma_load_2d(st + 57344, mgk, 0, (int)gk_row, bar);
-}
 
 // 256 threads: thread (warp w, lane l) owns state row kf = 32 (w % 4) + l (the
 // TMEM lane quarter its warp may access) and the 16 value columns
@@ -576,7 +568,7 @@ __device__ __forceinline__ void h_issue_loads(uint8_t* st, const CUtensorMap* mw
 // per-thread work on the sequential critical path.
 constexpr int kHCols = kHBV / 2;
 
-__global__ void __launch_bounds__(256, 1) h_tc_kernel(
+__global__ void __launch_bounds__(256, 2) h_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
@@ -598,8 +590,9 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
   const int ne = (int)cdiv((int64_t)si.y * M, kBT);
   uint8_t* ht = sm + H_HT;
   uint8_t* vp = sm + H_VP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + H_BAR);  // [0,1] stage full, [2] p1, [3] p2
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+  // [0] w full, [1] k full, [2] u and records full, [3] product 1, [4] product 2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + H_BAR);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
   const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
@@ -608,7 +601,7 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   // The B operands h (rows kf) and v' (rows p) are MN-major tiles with 64-byte
@@ -626,15 +619,32 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int64_t Rseq = (int64_t)si.x * M;
+  const int64_t gk0 = (int64_t)hv * a.Te + Rseq;
+  auto load_w = [&](int64_t R) {
+    mbar_expect_tx(&bars[0], 32768);
+    tma_load_3d(sm + H_W, &map_whi, 0, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + H_W + 8192, &map_whi, 64, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + H_W + 16384, &map_wlo, 0, hv, (int)R, &bars[0]);
+    tma_load_3d(sm + H_W + 24576, &map_wlo, 64, hv, (int)R, &bars[0]);
+  };
+  auto load_k = [&](int64_t R) {
+    mbar_expect_tx(&bars[1], 16384);
+    tma_load_3d(sm + H_K, &map_k, 0, kh, (int)R, &bars[1]);
+    tma_load_3d(sm + H_K + 8192, &map_k, 64, kh, (int)R, &bars[1]);
+  };
+  auto load_ug = [&](int64_t R, int64_t G) {
+    mbar_expect_tx(&bars[2], 8192 + 1024);
+    tma_load_3d(sm + H_U, &map_u, v0, hv, (int)R, &bars[2]);
+    tma_load_2d(sm + H_G, &map_gk, 0, (int)G, &bars[2]);
+  };
   if (tid == 0 && ne > 0) {
-    h_issue_loads(sm, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0, Rseq,
-                  (int64_t)hv * a.Te + Rseq, &bars[0]);
-    if (ne > 1)
-      h_issue_loads(sm + H_STAGE, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0,
-                    Rseq + kBT, (int64_t)hv * a.Te + Rseq + kBT, &bars[1]);
+    load_w(Rseq);
+    load_k(Rseq);
+    load_ug(Rseq, gk0);
   }
   const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
   const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+  const float4* gk = reinterpret_cast<const float4*>(sm + H_G);
   for (int j = 0; j <= ne; ++j) {
     // publish the state at the start of chunk j (operand h^T, and for chunk_o at token-chunk starts)
     {
@@ -663,47 +673,51 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const int s = j & 1;
-    uint8_t* st = sm + s * H_STAGE;
+    const uint32_t ph = j & 1;
     const int n = min(kBT, si.y * M - j * kBT);
     const int64_t R = Rseq + (int64_t)j * kBT;
-    bool ok = mbar_wait(&bars[s], (j >> 1) & 1, a.status, kDevTimeout);
-    if (!__syncthreads_and(ok)) break;
+    bool ok = true;
     if (tid == 0) {  // product 1: D1 = w h  (rows = positions)
-      const uint32_t whi = smem_u32(st), wlo = smem_u32(st + 16384), hb = smem_u32(ht);
-      // w_hi h_hi + w_hi h_lo + w_lo h_hi
-      mma_run<8, false, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
-      mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
-      mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
-      mma_commit(&bars[2]);
+      ok = mbar_wait(&bars[0], ph, a.status, kDevTimeout);
+      if (ok) {
+        const uint32_t whi = smem_u32(sm + H_W), wlo = smem_u32(sm + H_W + 16384), hb = smem_u32(ht);
+        // w_hi h_hi + w_hi h_lo + w_lo h_hi
+        mma_run<8, false, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
+        mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
+        mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
+        mma_commit(&bars[3]);
+      }
     }
-    const float4* gk = reinterpret_cast<const float4*>(st + 57344);
+    // every thread reads the chunk's last decay record (the state update needs it)
+    ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout) && ok;
     const float4 glast = gk[n - 1];
     if (quarter < 2) {  // positions p = row, columns cb .. cb + 15
       const int p = row;
-      ok = mbar_wait(&bars[2], j & 1, a.status, kDevTimeout);
+      ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout) && ok;
       tc_fence_after();
+      // product 1 has read w: the next chunk's w streams in behind this step
+      if (tid == 0 && ok && j + 1 < ne) load_w(R + kBT);
       uint32_t r[16];
       GDP_TMEM_LD16(tmem + lane_base + cb, r);
       tmem_wait_ld();
-      const uint8_t* urow = st + 49152 + p * 128;  // u row p, 128B-swizzled 16-byte chunks
+      const uint8_t* urow = sm + H_U + p * 128;  // u row p, 128B-swizzled 16-byte chunks
       float us[kHCols];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v4 = *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + j) ^ (p & 7)) << 4));
-        us[4 * j] = v4.x; us[4 * j + 1] = v4.y; us[4 * j + 2] = v4.z; us[4 * j + 3] = v4.w;
+      for (int q = 0; q < 4; ++q) {
+        const float4 v4 = *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + q) ^ (p & 7)) << 4));
+        us[4 * q] = v4.x; us[4 * q + 1] = v4.y; us[4 * q + 2] = v4.z; us[4 * q + 3] = v4.w;
       }
       const float4 gp = gk[p];
       const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
       __align__(16) bf16 vh[kHCols];
       __align__(16) bf16 vl[kHCols];
-      __align__(16) bf16 ph[kHCols];
-      __align__(16) bf16 pl[kHCols];
+      __align__(16) bf16 pvh[kHCols];
+      __align__(16) bf16 pvl[kHCols];
 #pragma unroll
       for (int c = 0; c < kHCols; ++c) {
         const float vn = us[c] - __uint_as_float(r[c]);
         split_bf16(vn, vh[c], vl[c]);
-        split_bf16(p < n ? vn * sc : 0.f, ph[c], pl[c]);
+        split_bf16(p < n ? vn * sc : 0.f, pvh[c], pvl[c]);
       }
       if (p < n) {
         const int64_t rowg = (R + p) * a.HV * V + (int64_t)hv * V + v0 + cb;
@@ -714,25 +728,34 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
         dl[0] = reinterpret_cast<const uint4*>(vl)[0];
         dl[1] = reinterpret_cast<const uint4*>(vl)[1];
       }
-      *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(ph)[0];
-      *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(ph)[1];
-      *reinterpret_cast<uint4*>(vp + 4096 + off_r0) = reinterpret_cast<const uint4*>(pl)[0];
-      *reinterpret_cast<uint4*>(vp + 4096 + off_r1) = reinterpret_cast<const uint4*>(pl)[1];
+      *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(pvh)[0];
+      *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(pvh)[1];
+      *reinterpret_cast<uint4*>(vp + 4096 + off_r0) = reinterpret_cast<const uint4*>(pvl)[0];
+      *reinterpret_cast<uint4*>(vp + 4096 + off_r1) = reinterpret_cast<const uint4*>(pvl)[1];
       fence_async_smem();
       tc_fence_before();
+    } else {
+      fence_async_smem();  // the record reads end before the next records load
     }
     ok = __syncthreads_and(ok);
     if (!ok) break;
     tc_fence_after();
-    if (tid == 0) {  // product 2: D2 = k^T v'  (rows = state rows kf)
-      const uint32_t kb = smem_u32(st + 32768), vb = smem_u32(vp);
-      const uint64_t kd = sdesc_sw128(kb, 8192, 1024);
-      mma_run<4, false, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb, 4096, 512), id2);
-      mma_run<4, true, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb + 4096, 4096, 512), id2);
-      mma_commit(&bars[3]);
+    if (tid == 0) {
+      // u and the records have been read: the next chunk's stream in
+      if (j + 1 < ne) load_ug(R + kBT, gk0 + (int64_t)(j + 1) * kBT);
+      ok = mbar_wait(&bars[1], ph, a.status, kDevTimeout);
+      if (ok) {  // product 2: D2 = k^T v'  (rows = state rows kf)
+        const uint32_t kb = smem_u32(sm + H_K), vb = smem_u32(vp);
+        const uint64_t kd = sdesc_sw128(kb, 8192, 1024);
+        mma_run<4, false, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb, 4096, 512), id2);
+        mma_run<4, true, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb + 4096, 4096, 512), id2);
+        mma_commit(&bars[4]);
+      }
     }
-    ok = mbar_wait(&bars[3], j & 1, a.status, kDevTimeout);
+    ok = mbar_wait(&bars[4], ph, a.status, kDevTimeout) && ok;
     tc_fence_after();
+    // product 2 has read k: the next chunk's k streams in
+    if (tid == 0 && ok && j + 1 < ne) load_k(R + kBT);
     {
       uint32_t r[16];
       GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
@@ -743,10 +766,6 @@ __global__ void __launch_bounds__(256, 1) h_tc_kernel(
     }
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
-    // stage s is free again: prefetch chunk j + 2
-    if (tid == 0 && j + 2 < ne)
-      h_issue_loads(st, &map_whi, &map_wlo, &map_k, &map_u, &map_gk, kh, hv, v0, R + 2 * kBT,
-                    (int64_t)hv * a.Te + R + 2 * kBT, &bars[s]);
   }
   if (a.hT) {
     float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
@@ -1742,10 +1761,10 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       tma_load_3d(sm + S8_WLO, &map_wlo, 0, hv, (int)R, &bars[FB_W]);
       tma_load_3d(sm + S8_WLO + 16384, &map_wlo, 64, hv, (int)R, &bars[FB_W]);
     };
-    auto load_ug = [&](int64_t R, int64_t G) {
+    auto load_ug = [&](int64_t R, int64_t grow) {
       mbar_expect_tx(&bars[FB_UG], 16384 + 2048);
       tma_load_3d(sm + S8_U, &map_u, v0, hv, (int)R, &bars[FB_UG]);
-      tma_load_2d(sm + S8_G, &map_gk, 0, (int)G, &bars[FB_UG]);
+      tma_load_2d(sm + S8_G, &map_gk, 0, (int)grow, &bars[FB_UG]);
     };
     if (tid == 0 && nb > 0) {
       load_w(Rseq);
@@ -1913,9 +1932,9 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
       tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[FB_K]);
       tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[FB_K]);
     };
-    auto load_og = [&](int b, int64_t G) {
+    auto load_og = [&](int b, int64_t grow) {
       mbar_expect_tx(&bars[FB_OG0 + b], 2048);
-      tma_load_2d(sm + F_OG + b * 2048, &map_gk, 0, (int)G, &bars[FB_OG0 + b]);
+      tma_load_2d(sm + F_OG + b * 2048, &map_gk, 0, (int)grow, &bars[FB_OG0 + b]);
     };
     if (otid == 0 && nb > 0) {
       load_k(Rseq);
