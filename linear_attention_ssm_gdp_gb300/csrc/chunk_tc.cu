@@ -2123,6 +2123,8 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   const int64_t T0 = (int64_t)si.x + t_start, E0 = T0 * M;
   const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * kK;  // first of K rows
   constexpr int NE = 64 * M;  // expanded positions in a full token chunk
+  constexpr int NMMA = (NE + 127) / 128;  // score MMAs of 128 positions
+  constexpr uint32_t TQH = 64 * NMMA;     // TMEM columns of q h
   uint8_t* qb = sm;
   uint8_t* kb = sm + o_k_off();
   uint8_t* hb = sm + o_h_off(M);
@@ -2134,7 +2136,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   float* srk = srq + 64;     // [64 M]
   uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);  // [0] tma [1] mma1 [2] mma2
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
-  constexpr uint32_t kCols = (NE + 64) <= 128 ? 128 : 256;
+  constexpr uint32_t kCols = (TQH + 64) <= 128 ? 128 : 256;
 
   if (warp == 0) {
     tmem_alloc(s_tmem, kCols);
@@ -2165,14 +2167,19 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
   if (tid == 0) {
     const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
-    const uint32_t ids = idesc_bf16(128, NE, false, false);
+    const uint32_t ids = idesc_bf16(128, 64, false, false);
     const uint32_t idh = idesc_bf16(128, kOBV, false, true);
     const uint64_t qd = sdesc_sw128(q0, 16, 1024);
-    // scores S = q k^T: N = 64 M positions
-    mma_run<8, false, 8192, 32, NE * 128, 32>(tmem, qd, sdesc_sw128(k0, 16, 1024), ids);
+    // scores S^T = k q^T, rows = positions, N = 64 tokens: one MMA per 128 positions
+    // into columns [64 m, 64 m + 64) (rows past the chunk's 64 M positions read the
+    // buffers behind k and feed accumulator rows that are never read)
+#pragma unroll
+    for (int m = 0; m < NMMA; ++m)
+      mma_run<8, false, NE * 128, 32, 8192, 32>(tmem + 64 * m, sdesc_sw128(k0 + 16384 * m, 16, 1024),
+                                                qd, ids);
     // q h (h hi then lo), N = 64 columns
-    mma_run<8, false, 8192, 32, 8192, 2048>(tmem + NE, qd, sdesc_sw128(h0, 16384, 1024), idh);
-    mma_run<8, true, 8192, 32, 8192, 2048>(tmem + NE, qd, sdesc_sw128(h0 + 16384, 16384, 1024), idh);
+    mma_run<8, false, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
+    mma_run<8, true, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0 + 16384, 16384, 1024), idh);
     mma_commit(&bars[1]);
   }
   // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
@@ -2192,26 +2199,32 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   }
   fence_async_smem();
   __syncthreads();
-  if (quarter < 2) {  // P rows t, this warp's quarter of the N = 64 M columns
-    const int t = quarter * 32 + lane;
+  {  // P^T rows e (positions), this warp's 16 of the 64 tokens: every warp builds rows
     ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
     tc_fence_after();
-    const float rt = srq[t];
-#pragma unroll 1
-    for (int c0 = cq * (NE / 4); c0 < (cq + 1) * (NE / 4); c0 += 16) {
-      uint32_t r[16];
-      GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + c0, r);
-      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {  // branch-free, so that the iterations interleave
-        const int e = c0 + j, s = e / M;
-        const float x = __uint_as_float(r[j]) * rt * srk[e] * __expf(gam_diff4(sgh, sgl, t, s));
-        bf16 ph, pl;
-        split_bf16((e < ne && s <= t && t < nt) ? x : 0.f, ph, pl);
-        // MN-major operand: row e (K), column t (M); a warp writes 64 contiguous bytes of a row
-        const uint32_t off = sw128_offset(e, t * 2);
-        *reinterpret_cast<bf16*>(pb + off) = ph;
-        *reinterpret_cast<bf16*>(pb + M * 8192 + off) = pl;
+    for (int m = 0; m < NMMA; ++m) {
+      if (128 * m + quarter * 32 < NE) {  // warp-uniform
+        const int e = 128 * m + quarter * 32 + lane, s = e / M;
+        uint32_t r[16];
+        GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + 64 * m + 16 * cq, r);
+        tmem_wait_ld();
+        const float rk = srk[e];
+        __align__(16) bf16 ph[16];
+        __align__(16) bf16 pl[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {  // branch-free, so that the iterations interleave
+          const int t = 16 * cq + j;
+          const float x = __uint_as_float(r[j]) * rk * __expf(gam_diff4(sgh, sgl, t, s));
+          split_bf16((e < ne && s <= t && t < nt) ? x : 0.f, ph[j], pl[j]);
+        }
+        // MN-major operand: row e (K), 64 tokens (M) of 128 bytes; two 16-byte chunks
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t off = (uint32_t)e * 128u + ((((uint32_t)(2 * cq + c)) ^ (e & 7u)) << 4);
+          *reinterpret_cast<uint4*>(pb + off) = reinterpret_cast<const uint4*>(ph)[c];
+          *reinterpret_cast<uint4*>(pb + M * 8192 + off) = reinterpret_cast<const uint4*>(pl)[c];
+        }
       }
     }
     fence_async_smem();
@@ -2235,13 +2248,13 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const int t = quarter * 32 + lane;
     ok = mbar_wait(&bars[2], 0, a.status, kDevTimeout);
     tc_fence_after();
-    const float qs = expf(sgh[t] + sgl[t]) * srq[t];
+    const float rq = srq[t], qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
     const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
     {
       const int c0 = cq * 16;
       uint32_t ro[16], rh[16];
       GDP_TMEM_LD16(la + c0, ro);
-      GDP_TMEM_LD16(la + NE + c0, rh);
+      GDP_TMEM_LD16(la + TQH + c0, rh);
       tmem_wait_ld();
       if (t < nt && ok) {
         float4* dst = reinterpret_cast<float4*>(a.o + ((T0 + t) * a.HV + hv) * a.V + v0 + c0);
@@ -2250,7 +2263,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
           float x[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            x[q] = a.scale * (qs * __uint_as_float(rh[4 * j + q]) + __uint_as_float(ro[4 * j + q]));
+            x[q] = a.scale * (qs * __uint_as_float(rh[4 * j + q]) + rq * __uint_as_float(ro[4 * j + q]));
           dst[j] = make_float4(x[0], x[1], x[2], x[3]);
         }
       }
