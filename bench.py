@@ -304,22 +304,33 @@ def run_ours(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # the timed steps: only the two step events in the stream, no stage events between
+    # the kernels (each event record is one more stream operation between launches)
+    gdp.gdp_set_stage_events(None)
     for _ in range(args.steps):
         flush()
         torch.cuda._sleep(HOST_LEAD_CYCLES)  # the host queues the whole step meanwhile
         step_ev[0].record()
-        pf.step(prep_ev)
+        pf.step()
         step_ev[1].record()
         torch.cuda.synchronize()
         times["step"].append(step_ev[0].elapsed_time(step_ev[1]))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    # per-kernel breakdown: the same steps again with events at the stage boundaries
+    gdp.gdp_set_stage_events(stage)
+    for _ in range(max(5, min(args.steps, 20))):
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        pf.step(prep_ev)
+        torch.cuda.synchronize()
         times["prepare"].append(prep_ev[0].elapsed_time(prep_ev[1]))
         times["tables"].append(stage[0].elapsed_time(stage[1]))
         times["wy"].append(stage[1].elapsed_time(stage[2]))
         times["h"].append(stage[2].elapsed_time(stage[3]))
         times["o"].append(stage[3].elapsed_time(stage[4]))
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     # keep the GPU busy a little longer so the sampler sees load, then stop
     extra_t0 = time.time()
     while time.time() - extra_t0 < 0.5:
@@ -581,6 +592,8 @@ def _time_chunk_steps(gdp, step, stage, flush, steps, warmup, prep_ev=None):
         step()
     torch.cuda.synchronize()
     times = {"step": [], "prepare": [], "tables": [], "wy": [], "h": [], "o": []}
+    # whole steps without the library's stage events, then the per-stage breakdown
+    gdp.gdp_set_stage_events(None)
     for _ in range(steps):
         flush()
         torch.cuda._sleep(HOST_LEAD_CYCLES)
@@ -589,6 +602,12 @@ def _time_chunk_steps(gdp, step, stage, flush, steps, warmup, prep_ev=None):
         step_ev[1].record()
         torch.cuda.synchronize()
         times["step"].append(step_ev[0].elapsed_time(step_ev[1]))
+    gdp.gdp_set_stage_events(stage)
+    for _ in range(steps):
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        step()
+        torch.cuda.synchronize()
         if prep_ev is not None:
             times["prepare"].append(prep_ev[0].elapsed_time(prep_ev[1]))
         times["tables"].append(stage[0].elapsed_time(stage[1]))

@@ -62,6 +62,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 __global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M, int BT,
                               int64_t NE_max, int64_t NT_max, int4* seq_info, int2* exp_tab,
                               int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status) {
+  pdl_wait();
   __shared__ int s_bad;
   __shared__ int s_ne, s_nt;
   if (threadIdx.x == 0) {
@@ -562,13 +563,12 @@ WsLayout generic_layout(int B, int T, int N_seq, int H, int HV, int K, int V, in
 }
 
 cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {
-  tables_kernel<<<1, 512, 0, p.stream>>>(
-      p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT, p.NE_max, p.NT_max,
-      reinterpret_cast<int4*>(ws + L.seq_info), reinterpret_cast<int2*>(ws + L.exp_tab),
-      reinterpret_cast<int2*>(ws + L.tok_tab),
+  return launch_pdl(
+      tables_kernel, dim3(1), dim3(512), 0, p.stream, p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT,
+      p.NE_max, p.NT_max, reinterpret_cast<int4*>(ws + L.seq_info),
+      reinterpret_cast<int2*>(ws + L.exp_tab), reinterpret_cast<int2*>(ws + L.tok_tab),
       L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int4*>(ws + L.blk_tab),
       block128_bound(p.B, p.T, p.N_seq, p.M), reinterpret_cast<int*>(ws + L.status));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {

@@ -367,6 +367,7 @@ template <int V>
 __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ CUtensorMap map_k,
                                                        const __grid_constant__ CUtensorMap map_v,
                                                        WyArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -572,6 +573,7 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -1003,6 +1005,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
     const __grid_constant__ CUtensorMap map_whs, const __grid_constant__ CUtensorMap map_wls,
     const __grid_constant__ CUtensorMap map_us, WyArgs a, int NB) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -1438,6 +1441,7 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -1696,6 +1700,7 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, const __grid_constant__ CUtensorMap map_q,
     HOArgs f) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -2103,6 +2108,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const __grid_constant__ CUtensorMap map_hhi, const __grid_constant__ CUtensorMap map_hlo,
     const __grid_constant__ CUtensorMap map_vhi, const __grid_constant__ CUtensorMap map_vlo,
     OArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -2337,8 +2343,8 @@ cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
   const int smem = wy_smem(V);
   cudaError_t e = cudaFuncSetAttribute(wy_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  wy_tc_kernel<V><<<dim3((unsigned)p.NE_max, p.HV), 256, smem, p.stream>>>(mk, mv, a);
-  return cudaGetLastError();
+  return launch_pdl(wy_tc_kernel<V>, dim3((unsigned)p.NE_max, p.HV), dim3(256), smem, p.stream,
+                    mk, mv, a);
 }
 
 template <int V, bool G>
@@ -2358,8 +2364,8 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   const int64_t items = NB * p.HV;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = (int)std::min<int64_t>(items, sm_count());  // persistent, one CTA per SM
-  wy128_tc_kernel<V, G><<<grid, 512, W8_SMEM, p.stream>>>(mk, mv, mwh, mwl, mu, a, (int)NB);
-  return cudaGetLastError();
+  return launch_pdl(wy128_tc_kernel<V, G>, dim3(grid), dim3(512), W8_SMEM, p.stream, mk, mv, mwh,
+                    mwl, mu, a, (int)NB);
 }
 
 template <int M>
@@ -2372,9 +2378,8 @@ cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi
   const int smem = o_smem(M);
   cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  o_tc_kernel<M><<<dim3((unsigned)(p.NT_max * (p.V / kOBV)), p.HV), 512, smem, p.stream>>>(
-      mq, mk, mhhi, mhlo, mvhi, mvlo, a);
-  return cudaGetLastError();
+  return launch_pdl(o_tc_kernel<M>, dim3((unsigned)(p.NT_max * (p.V / kOBV)), p.HV), dim3(512),
+                    smem, p.stream, mq, mk, mhhi, mhlo, mvhi, mvlo, a);
 }
 
 }  // namespace
@@ -2468,8 +2473,9 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       auto kern = p.g ? ho128_tc_kernel<true> : ho128_tc_kernel<false>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
       if (e != cudaSuccess) return e;
-      kern<<<grid, 512, F_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, mq, fa);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = launch_pdl(kern, grid, dim3(512), F_SMEM, p.stream, mwh, mwl, mk, mu, mg, mq, fa)) !=
+          cudaSuccess)
+        return e;
       record_stage(3, p.stream);
       record_stage(4, p.stream);
       return cudaSuccess;
@@ -2477,13 +2483,13 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
     if (blk128) {
       e = cudaFuncSetAttribute(h128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S8_SMEM);
       if (e != cudaSuccess) return e;
-      h128_tc_kernel<<<grid, 256, S8_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, a, p.H);
+      e = launch_pdl(h128_tc_kernel, grid, dim3(256), S8_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
     } else {
       e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
       if (e != cudaSuccess) return e;
-      h_tc_kernel<<<grid, 256, H_SMEM, p.stream>>>(mwh, mwl, mk, mu, mg, a, p.H);
+      e = launch_pdl(h_tc_kernel, grid, dim3(256), H_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
   record_stage(3, p.stream);
   // output

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gdp.h"
 
 namespace gdp {
@@ -106,6 +108,31 @@ cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const 
                              cudaStream_t stream);
 
 int sm_count();  // multiprocessors on the current device (cached per device)
+
+// Programmatic dependent launch. A kernel launched with launch_pdl is launched
+// as soon as the kernel before it in the stream completes, while that kernel's
+// writes are still being made visible, so the launch overlaps the flush; it
+// calls pdl_wait() before its first global-memory access, which returns once
+// every earlier kernel of the stream has completed and its writes are visible.
+// No kernel triggers its dependents early: with an early trigger the fused scan's
+// CTAs were placed on SMs as WY-128's CTAs drained and the prefill step took
+// 0.541 ms instead of 0.482 ms.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Records stage-boundary event i (gdp_set_stage_events) on `s`; no-op when off.
 // Slots: 0 entry, 1 after the chunk tables, 2 after the WY stage (transition

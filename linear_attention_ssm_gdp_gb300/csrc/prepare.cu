@@ -88,6 +88,7 @@ struct PrepArgs {
 // alignment of some pointer/stride/head size forbids 16-byte vectors).
 template <int VB, bool DECODE>
 __global__ void __launch_bounds__(256) prepare_kernel(PrepArgs a) {
+  pdl_wait();
   using VT = typename std::conditional<VB == 16, uint4,
              typename std::conditional<VB == 4, uint32_t, uint16_t>::type>::type;
   constexpr int U = 8;  // vectors in flight per thread
@@ -283,6 +284,7 @@ __device__ __forceinline__ void store_row(const PrepArgs& a, const RowGeo& g, in
 
 template <bool DECODE>
 __global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
+  pdl_wait();
   const int64_t rows = (int64_t)a.n * a.T;
   const RowGeo g = row_geo(a, DECODE);
   int64_t r = blockIdx.x;
@@ -310,6 +312,7 @@ constexpr int kRing = 3;
 
 template <bool DECODE>
 __global__ void __launch_bounds__(512, 3) prepare_ring_kernel(PrepArgs a, int xrow_v) {
+  pdl_wait();
   extern __shared__ uint4 ring[];  // [kRing][xrow_v]
   const int64_t rows = (int64_t)a.n * a.T;
   const RowGeo g = row_geo(a, DECODE);
@@ -775,11 +778,8 @@ cudaError_t launch_vb(PrepArgs a, bool decode, cudaStream_t s) {
   const int64_t rows = (int64_t)a.n * a.T;
   const int64_t cap = (int64_t)sm_count() * 8;  // 8 resident 256-thread CTAs per SM
   const int grid = (int)(rows < cap ? rows : cap);
-  if (decode)
-    prepare_kernel<VB, true><<<grid, 256, 0, s>>>(a);
-  else
-    prepare_kernel<VB, false><<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(decode ? prepare_kernel<VB, true> : prepare_kernel<VB, false>, dim3(grid),
+                    dim3(256), 0, s, a);
 }
 
 }  // namespace
@@ -823,11 +823,8 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
       if (e != cudaSuccess) return e;
       const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
       const int grid = (int)(rows < cap ? rows : cap);
-      if (decode)
-        prepare_rows_kernel<true><<<grid, 256, 0, stream>>>(a);
-      else
-        prepare_rows_kernel<false><<<grid, 256, 0, stream>>>(a);
-      return cudaGetLastError();
+      return launch_pdl(decode ? prepare_rows_kernel<true> : prepare_rows_kernel<false>,
+                        dim3(grid), dim3(256), 0, stream, a);
     }
     const int64_t xrow_b = (int64_t)(M * H * P + M * G * N + G * N) * a.es;
     const int64_t ring_b = kRing * xrow_b;
@@ -843,8 +840,8 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
       const int64_t rows = (int64_t)n * T;
       const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
       const int grid = (int)(rows < cap ? rows : cap);
-      kern<<<grid, 512, (size_t)ring_b, stream>>>(a, (int)(xrow_b / 16));
-      return cudaGetLastError();
+      return launch_pdl(kern, dim3(grid), dim3(512), (size_t)ring_b, stream, a,
+                        (int)(xrow_b / 16));
     }
     return launch_vb<16>(a, decode, stream);
   }
