@@ -91,7 +91,7 @@ __global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M,
     s_bad = bad;
     s_ne = bad ? 0 : (int)eoff;
     s_nt = bad ? 0 : (int)toff;
-    if (bad) atomicExch(status, kDevBadSeqlens);
+    *status = bad ? kDevBadSeqlens : kDevOk;  // the call's status word starts here
   }
   __syncthreads();
   // A bad list leaves every sequence with a zero-length record: the state

@@ -253,12 +253,15 @@ gdp_status gdp_chunk_fwd(const void* q, const void* k, const void* v, const floa
   p.o = o; p.hT = final_state; p.stream = stream;
   chunk_bounds(B, T, N_seq, M, chunk_size, &p.NE_max, &p.NT_max);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws + L.status, 0, kAlign, stream) != cudaSuccess) return GDP_ERR_CUDA;
   record_stage(0, stream);
   if (N_seq == 0) {
+    if (cudaMemsetAsync(ws + L.status, 0, sizeof(int32_t), stream) != cudaSuccess)
+      return GDP_ERR_CUDA;
     for (int i = 1; i < GDP_STAGE_EVENTS; ++i) record_stage(i, stream);
     return GDP_OK;
   }
+  // the chunk-table kernel, first of the call, writes the status word (0 or the
+  // bad-offsets code); later kernels only ever record errors in it
   if (launch_tables(p, L, ws) != cudaSuccess) return GDP_ERR_CUDA;
   record_stage(1, stream);
   const cudaError_t e = L.path == 1 ? launch_chunk_tc(p, L, ws) : launch_chunk_generic(p, L, ws);
