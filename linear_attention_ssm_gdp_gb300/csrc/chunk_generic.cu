@@ -59,73 +59,148 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ------------------------------------------------------------------------------------
 // chunk tables
 // ------------------------------------------------------------------------------------
-__global__ void tables_kernel(const int32_t* cu, int N_seq, int B, int T, int M, int BT,
-                              int64_t NE_max, int64_t NT_max, int4* seq_info, int2* exp_tab,
-                              int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status) {
+// One CTA of kTabThreads threads. The sequences are taken kTabThreads at a time:
+// each thread loads its sequence's offsets, checks them and counts its chunks,
+// and a block-wide scan turns the counts into the sequence's first chunk
+// indices (no thread walks the list alone). Records and chunk counts of the
+// first kTabSmem sequences stay in shared memory for the table fill, so the
+// fill takes no division (chunk sizes are powers of two: counts are shifts).
+constexpr int kTabThreads = 512;
+constexpr int kTabSmem = 1024;
+
+// Exclusive block-wide scan of three counts (all threads of the block call it);
+// returns the block's totals in tot.
+__device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_t* sw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NW = kTabThreads / 32;
+  int64_t inc[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    inc[j] = x[j];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, inc[j], o);
+      if (lane >= o) inc[j] += y;
+    }
+  }
+  if (lane == 31)
+#pragma unroll
+    for (int j = 0; j < 3; ++j) sw[warp * 3 + j] = inc[j];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      int64_t w = lane < NW ? sw[lane * 3 + j] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < NW) sw[lane * 3 + j] = w;  // inclusive warp prefix
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int64_t before = warp > 0 ? sw[(warp - 1) * 3 + j] : 0;
+    x[j] = before + inc[j] - x[j];
+    tot[j] = sw[(NW - 1) * 3 + j];
+  }
+  __syncthreads();  // sw is reused by the next call
+}
+
+__global__ void __launch_bounds__(kTabThreads) tables_kernel(
+    const int32_t* cu, int N_seq, int B, int T, int M, int BT, int64_t NE_max, int64_t NT_max,
+    int4* seq_info, int2* exp_tab, int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status) {
   pdl_wait();
+  __shared__ int4 s_info[kTabSmem];     // (first token, length, first exp chunk, first token chunk)
+  __shared__ int4 s_cnt[kTabSmem];      // (exp chunks, token chunks, 128-position blocks, first block)
+  __shared__ int64_t s_scan[3 * (kTabThreads / 32)];
   __shared__ int s_bad;
-  __shared__ int s_ne, s_nt;
-  if (threadIdx.x == 0) {
-    int bad = 0;
-    int64_t eoff = 0, toff = 0;
-    int prev = 0;
-    for (int i = 0; i < N_seq; ++i) {
-      int t0, len;
+  const int tid = threadIdx.x;
+  const int sh = __ffs(BT) - 1;  // BT = 2^sh
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  int64_t carry[3] = {0, 0, 0};  // expanded chunks, token chunks, 128-position blocks so far
+  for (int base = 0; base < N_seq; base += kTabThreads) {
+    const int i = base + tid;
+    int t0 = 0, len = 0;
+    bool bad = false;
+    if (i < N_seq) {
       if (cu) {
         t0 = cu[i];
         const int t1 = cu[i + 1];
-        if (i == 0 && t0 != 0) bad = 1;
-        if (t0 < prev || t1 < t0 || t1 > (int64_t)B * T) bad = 1;
-        prev = t1;
+        // cu[0] = 0, non-decreasing, within B*T: each sequence checks its own pair
+        bad = (i == 0 && t0 != 0) || t1 < t0 || (int64_t)t1 > (int64_t)B * T;
         len = t1 - t0;
       } else {
         t0 = i * T;
         len = T;
       }
-      if (bad) break;
-      seq_info[i] = make_int4(t0, len, (int)eoff, (int)toff);
-      eoff += cdiv((int64_t)len * M, BT);
-      toff += cdiv((int64_t)len, BT);
     }
-    if (eoff > NE_max || toff > NT_max) bad = 1;
-    s_bad = bad;
-    s_ne = bad ? 0 : (int)eoff;
-    s_nt = bad ? 0 : (int)toff;
-    *status = bad ? kDevBadSeqlens : kDevOk;  // the call's status word starts here
+    if (bad) s_bad = 1;
+    int64_t cnt[3] = {0, 0, 0}, tot[3];
+    int c3[3] = {0, 0, 0};
+    if (i < N_seq && !bad) {
+      c3[0] = (int)((((int64_t)len * M) + BT - 1) >> sh);
+      c3[1] = (int)((((int64_t)len) + BT - 1) >> sh);
+      c3[2] = (int)((((int64_t)len * M) + 127) >> 7);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) cnt[j] = c3[j];
+    scan3(cnt, tot, s_scan);
+    if (i < N_seq) {
+      const int4 rec = make_int4(t0, len, (int)(carry[0] + cnt[0]), (int)(carry[1] + cnt[1]));
+      seq_info[i] = rec;
+      if (i < kTabSmem) {
+        s_info[i] = rec;
+        s_cnt[i] = make_int4(c3[0], c3[1], c3[2], (int)(carry[2] + cnt[2]));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) carry[j] += tot[j];
   }
   __syncthreads();
+  const bool bad = s_bad || carry[0] > NE_max || carry[1] > NT_max;
+  if (tid == 0) *status = bad ? kDevBadSeqlens : kDevOk;  // the call's status word starts here
   // A bad list leaves every sequence with a zero-length record: the state
   // kernels, which launch one CTA row per sequence, then read no input rows,
   // write no output rows and only pass the initial state through.
-  if (s_bad)
-    for (int i = threadIdx.x; i < N_seq; i += blockDim.x) seq_info[i] = make_int4(0, 0, 0, 0);
-  const int ne = s_ne, nt = s_nt;
-  if (!s_bad) {
-    for (int i = 0; i < N_seq; ++i) {
+  if (bad)
+    for (int i = tid; i < N_seq; i += kTabThreads) seq_info[i] = make_int4(0, 0, 0, 0);
+  const int64_t ne = bad ? 0 : carry[0], nt = bad ? 0 : carry[1], nb = bad ? 0 : carry[2];
+  if (!bad) {
+    // one warp per sequence over the shared records, lanes over its chunks
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ns = N_seq < kTabSmem ? N_seq : kTabSmem;
+    for (int i = warp; i < ns; i += kTabThreads / 32) {
+      const int4 si = s_info[i], cn = s_cnt[i];
+      for (int c = lane; c < cn.x; c += 32) exp_tab[si.z + c] = make_int2(i, c);
+      for (int c = lane; c < cn.y; c += 32) tok_tab[si.w + c] = make_int2(i, c);
+      if (blk_tab)
+        // 128-position blocks: (sequence, index of the block's first 64-chunk, the
+        // sequence's first token, its length), so that a block's reader needs one load
+        for (int c = lane; c < cn.z; c += 32) blk_tab[cn.w + c] = make_int4(i, 2 * c, si.x, si.y);
+    }
+    // sequences past the shared records: all threads, one sequence at a time
+    int64_t b_run = ns > 0 ? (int64_t)s_cnt[ns - 1].w + s_cnt[ns - 1].z : 0;
+    for (int i = kTabSmem; i < N_seq; ++i) {
       const int4 si = seq_info[i];
-      const int nei = (int)cdiv((int64_t)si.y * M, BT), nti = (int)cdiv((int64_t)si.y, BT);
-      for (int c = threadIdx.x; c < nei; c += blockDim.x) exp_tab[si.z + c] = make_int2(i, c);
-      for (int c = threadIdx.x; c < nti; c += blockDim.x) tok_tab[si.w + c] = make_int2(i, c);
+      const int nei = (int)((((int64_t)si.y * M) + BT - 1) >> sh);
+      const int nti = (int)((((int64_t)si.y) + BT - 1) >> sh);
+      const int nbi = (int)((((int64_t)si.y * M) + 127) >> 7);
+      for (int c = tid; c < nei; c += kTabThreads) exp_tab[si.z + c] = make_int2(i, c);
+      for (int c = tid; c < nti; c += kTabThreads) tok_tab[si.w + c] = make_int2(i, c);
+      if (blk_tab)
+        for (int c = tid; c < nbi; c += kTabThreads)
+          blk_tab[b_run + c] = make_int4(i, 2 * c, si.x, si.y);
+      b_run += nbi;
     }
   }
-  for (int64_t c = ne + threadIdx.x; c < NE_max; c += blockDim.x) exp_tab[c] = make_int2(-1, 0);
-  for (int64_t c = nt + threadIdx.x; c < NT_max; c += blockDim.x) tok_tab[c] = make_int2(-1, 0);
-  // 128-position blocks: (sequence, index of the block's first 64-chunk, the
-  // sequence's first token, its length), so that a block's reader needs one load
-  if (blk_tab) {
-    int64_t nb = 0;
-    if (!s_bad) {
-      for (int i = 0; i < N_seq; ++i) {
-        const int4 si = seq_info[i];
-        const int nbi = (int)cdiv((int64_t)si.y * M, 128);
-        for (int c = threadIdx.x; c < nbi; c += blockDim.x)
-          blk_tab[nb + c] = make_int4(i, 2 * c, si.x, si.y);
-        nb += nbi;
-      }
-    }
-    for (int64_t c = nb + threadIdx.x; c < NB_max; c += blockDim.x)
-      blk_tab[c] = make_int4(-1, 0, 0, 0);
-  }
+  for (int64_t c = ne + tid; c < NE_max; c += kTabThreads) exp_tab[c] = make_int2(-1, 0);
+  for (int64_t c = nt + tid; c < NT_max; c += kTabThreads) tok_tab[c] = make_int2(-1, 0);
+  if (blk_tab)
+    for (int64_t c = nb + tid; c < NB_max; c += kTabThreads) blk_tab[c] = make_int4(-1, 0, 0, 0);
 }
 
 // ------------------------------------------------------------------------------------
@@ -564,7 +639,7 @@ WsLayout generic_layout(int B, int T, int N_seq, int H, int HV, int K, int V, in
 
 cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {
   return launch_pdl(
-      tables_kernel, dim3(1), dim3(512), 0, p.stream, p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT,
+      tables_kernel, dim3(1), dim3(kTabThreads), 0, p.stream, p.cu_seqlens, p.N_seq, p.B, p.T, p.M, p.BT,
       p.NE_max, p.NT_max, reinterpret_cast<int4*>(ws + L.seq_info),
       reinterpret_cast<int2*>(ws + L.exp_tab), reinterpret_cast<int2*>(ws + L.tok_tab),
       L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int4*>(ws + L.blk_tab),

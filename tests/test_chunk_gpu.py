@@ -74,6 +74,23 @@ def test_varlen_with_ragged_and_empty_sequences(gdp, K, V, M):
     assert torch.equal(fs[5], h0[5])
 
 
+@pytest.mark.parametrize("M", [2, 3])
+def test_varlen_many_sequences(gdp, M):
+    """More sequences than the chunk-table kernel keeps in shared memory (1024):
+    the table fill for the ones past it takes its other branch. Short ragged
+    lengths, empty ones among them, on the tensor-core path."""
+    gen = torch.Generator().manual_seed(21)
+    lens = torch.randint(0, 5, (1100,), generator=gen).tolist()
+    lens[1050] = 70  # one sequence past the shared records spans two 64-token chunks
+    cu = si.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    q, k, v, beta, g = chunk_case(1, T, 1, 1, 128, 128, M, seed=22)
+    o, fs = _run(gdp, q, k, v, beta, g, M, 64, True, cu=cu)
+    ro, rfs = oracle.walk(q, k, v, beta, g, M, 128 ** -0.5, cu_seqlens=cu, l2norm=True)
+    assert rel_err(o, ro) <= 2e-3
+    assert rel_err(fs, rfs) <= 2e-3
+
+
 def test_varlen_equals_separate_calls(gdp):
     lens = [70, 129, 5]
     cu = si.cu_seqlens_of(lens)
