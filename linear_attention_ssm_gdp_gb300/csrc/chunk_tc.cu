@@ -463,17 +463,27 @@ __global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ C
   solve_tril64(Ls, As, X);
   // A' = A diag(beta e^Gam / |k|), A'' = A diag(beta), split into bf16 hi + lo,
   // written as K-major operand tiles (row p, column i) with the 128B swizzle
-  for (int idx = tid; idx < 64 * 64; idx += 256) {
-    const int p = idx >> 6, i = idx & 63;
-    const float av = As[p * 65 + i];
-    bf16 h1, l1, h2, l2;
-    split_bf16(av * sco[i], h1, l1);
-    split_bf16(av * sb[i], h2, l2);
-    const uint32_t off = sw128_offset(p, i * 2);
-    *reinterpret_cast<bf16*>(atile + 0 * 8192 + off) = h1;
-    *reinterpret_cast<bf16*>(atile + 1 * 8192 + off) = l1;
-    *reinterpret_cast<bf16*>(atile + 2 * 8192 + off) = h2;
-    *reinterpret_cast<bf16*>(atile + 3 * 8192 + off) = l2;
+  // (a thread takes 8 consecutive columns of a row: four 16-byte stores)
+  for (int idx = tid; idx < 64 * 8; idx += 256) {
+    const int p = idx >> 3, q = idx & 7;
+    float v1[8], v2[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float av = As[p * 65 + 8 * q + e];
+      v1[e] = av * sco[8 * q + e];
+      v2[e] = av * sb[8 * q + e];
+    }
+    __align__(16) bf16 h1[8];
+    __align__(16) bf16 l1[8];
+    __align__(16) bf16 h2[8];
+    __align__(16) bf16 l2[8];
+    split_bf16_n<8>(v1, h1, l1);
+    split_bf16_n<8>(v2, h2, l2);
+    const uint32_t off = (uint32_t)p * 128u + (((uint32_t)q ^ (p & 7u)) << 4);
+    *reinterpret_cast<uint4*>(atile + 0 * 8192 + off) = *reinterpret_cast<const uint4*>(h1);
+    *reinterpret_cast<uint4*>(atile + 1 * 8192 + off) = *reinterpret_cast<const uint4*>(l1);
+    *reinterpret_cast<uint4*>(atile + 2 * 8192 + off) = *reinterpret_cast<const uint4*>(h2);
+    *reinterpret_cast<uint4*>(atile + 3 * 8192 + off) = *reinterpret_cast<const uint4*>(l2);
   }
   fence_async_smem();
   tc_fence_before();
