@@ -1110,6 +1110,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   uint32_t mma_phase = 0;
   // k / v loads issued and consumed so far: load i completes phase i of bars[0] / bars[4]
   int k_iss = 1, k_got = 0, v_iss = 1, v_got = 0;
+  int r_iss = 0, r_got = 0;  // V = 256: loads of the second value round (bars[2])
   bool ok = true;
   for (int c = 0;; ++c) {
     const int par = c & 1;
@@ -1161,8 +1162,14 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     fence_async_smem();  // the k buffer's generic reads end before the next k load
     // The previous item's w stores (staged in LA, which the L build overwrites)
     // must have read shared memory; its u stores (staged in the operand tiles,
-    // the solve's scratch) may go on reading until just before the solve.
-    if (kPipe && tid == 0) tma_store_wait_read_but_last();
+    // the solve's scratch, and for V = 256 also in LA) may go on reading until
+    // just before the solve (V = 256: the L build).
+    if (tid == 0) {
+      if (kPipe)
+        tma_store_wait_read_but_last();
+      else
+        tma_store_wait_read();
+    }
     ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
     mma_phase ^= 1;
     tc_fence_after();
@@ -1208,7 +1215,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         }
       }
     }
-    if (kPipe && tid == 0) tma_store_wait_read();  // the u stores have read the operand tiles
+    if (tid == 0) tma_store_wait_read();  // the u stores have read the operand tiles
     tc_fence_before();
     __syncthreads();
     ok = solve_tril128(LA, Ld, scratch, tmem, &bars[3], a.status);
@@ -1283,12 +1290,19 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       if (tid == 0) issue_k(y);
       ++k_iss;
     }
+    if (!kPipe && tid == 0) {  // V = 256: the value columns of round 1 go to the k buffer
+      mbar_expect_tx(&bars[2], (VR / 64) * 16384);
+#pragma unroll
+      for (int c2 = 0; c2 < VR / 64; ++c2)
+        tma_load_3d(kbuf + c2 * 16384, &map_v, VR + 64 * c2, x.hv, (int)x.R0, &bars[2]);
+    }
+    if (!kPipe) ++r_iss;
     build_tiles(1);
     ok = mbar_wait(&bars[4], v_got & 1, a.status, kDevTimeout);
     if (ok) ++v_got;
     if (!__syncthreads_and(ok)) break;
     auto issue_u = [&](int round) {
-      const uint32_t tb = smem_u32(tiles), vb = smem_u32(vbuf);
+      const uint32_t tb = smem_u32(tiles), vb = smem_u32(round == 0 ? vbuf : kbuf);
       const uint32_t idu = idesc_bf16(128, VR, false, true);
       const uint64_t vd = sdesc_sw128(vb, 16384, 1024);
       mma_run<8, false, 16384, 32, 8192, 2048>(tmem + 128 + round * VR, sdesc_sw128(tb, 16, 1024), vd, idu);
@@ -1301,10 +1315,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     // partial block is written row by row, so that no store reaches the rows of
     // the next sequence.
     const bool full = n == 128;
-    // w staging, two 64-column boxes per array: pipelined, w_hi and w_lo in
-    // LA; otherwise w_hi in the k buffer and w_lo in LA
-    uint8_t* whs = kPipe ? reinterpret_cast<uint8_t*>(LA) : kbuf;
-    uint8_t* wls = reinterpret_cast<uint8_t*>(LA) + (kPipe ? 32768 : 0);
+    // w staging, two 64-column boxes per array, w_hi and w_lo in LA
+    uint8_t* whs = reinterpret_cast<uint8_t*>(LA);
+    uint8_t* wls = reinterpret_cast<uint8_t*>(LA) + 32768;
     {  // w epilogue (overlaps the u MMAs): row p, 32 of the 128 columns per thread
       const int p = quarter * 32 + lane;
       const int c0 = cq * 32;
@@ -1345,13 +1358,13 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
       mma_phase ^= 1;
       if (!__syncthreads_and(ok)) break;
-      if (tid == 0) {
-        mbar_expect_tx(&bars[2], (VR / 64) * 16384);
-#pragma unroll
-        for (int c2 = 0; c2 < VR / 64; ++c2)
-          tma_load_3d(vbuf + c2 * 16384, &map_v, round * VR + 64 * c2, hv, (int)R0, &bars[2]);
+      if (has_next) {  // U round 0 was the v buffer's last reader
+        if (tid == 0) issue_v(y);
+        ++v_iss;
       }
+      // round 1's columns were requested into the k buffer after the W product
       ok = mbar_wait(&bars[2], (c * (NR - 1) + round - 1) & 1, a.status, kDevTimeout);
+      if (ok) ++r_got;
       if (!__syncthreads_and(ok)) break;
       if (tid == 0) issue_u(round);
     }
@@ -1359,17 +1372,22 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
     mma_phase ^= 1;
     tc_fence_after();
+    // V = 256: u boxes 4-7 go to LA, which the w stores must have read
+    if (!kPipe && tid == 0) tma_store_wait_read();
     if (!__syncthreads_and(ok)) break;
-    if (kPipe && has_next) {  // the U product was the v buffer's last reader
-      if (tid == 0) issue_v(y);
-      ++v_iss;
+    if (has_next) {
+      if (kPipe) {  // the U product was the v buffer's last reader
+        if (tid == 0) issue_v(y);
+        ++v_iss;
+      } else {  // U round 1 was the k buffer's last reader
+        if (tid == 0) issue_k(y);
+        ++k_iss;
+      }
     }
-    // u staging: 32-column boxes, 0-3 in the operand tiles, 4-5 in the upper
-    // half of LA, 6-7 in the v buffer (V = 256; all released by the u MMAs)
+    // u staging: 32-column boxes, 0-3 in the operand tiles, 4-7 (V = 256) in LA;
+    // the loads of the next item use neither
     auto ustage = [&](int cc) -> uint8_t* {
-      return cc < 4 ? tiles + cc * 16384
-                    : cc < 6 ? reinterpret_cast<uint8_t*>(LA) + 32768 + (cc - 4) * 16384
-                             : vbuf + (cc - 6) * 16384;
+      return cc < 4 ? tiles + cc * 16384 : reinterpret_cast<uint8_t*>(LA) + (cc - 4) * 16384;
     };
     {  // u epilogue: row p, V / 4 columns per thread
       const int p = quarter * 32 + lane;
@@ -1406,13 +1424,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         for (int cc = 0; cc < V / 32; ++cc) tma_store_3d(&map_us, ustage(cc), 32 * cc, hv, (int)R0);
         tma_store_commit();
       }
-      if (!kPipe && has_next) {  // the next item's loads reuse the staging buffers
-        tma_store_wait_read();
-        issue_k(y);
-        issue_v(y);
-      }
     }
-    if (!kPipe && has_next) ++k_iss, ++v_iss;
     if (!has_next) break;
     it = nx;
     x = y;
@@ -1423,6 +1435,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     bool w = true;
     for (; w && k_got < k_iss; ++k_got) w = mbar_wait(&bars[0], k_got & 1, nullptr, 0);
     for (; w && v_got < v_iss; ++v_got) w = mbar_wait(&bars[4], v_got & 1, nullptr, 0);
+    for (; w && r_got < r_iss; ++r_got) w = mbar_wait(&bars[2], r_got & 1, nullptr, 0);
     tma_store_wait_read();
   }
   tc_fence_before();

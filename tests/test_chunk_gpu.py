@@ -245,11 +245,14 @@ def test_prefill_bf16_workload(gdp):
     _check_all(o, fs, q, k, v, beta, g, w["M"])
 
 
-def test_persistent_wy_loop_many_items_per_cta(gdp):
-    """B1 T4096 H=HV=8 K=V=128 M=2: 520 (128-position block, head) items, more than
-    twice the persistent WY grid, so every CTA runs the next-item loads, the buffer
-    reuse and the next item's decay prefix several times."""
-    q, k, v, beta, g = chunk_case(1, 4096, 8, 8, 128, 128, 2, seed=12)
+@pytest.mark.parametrize("T,H,HV,V", [(4096, 8, 8, 128), (2100, 2, 8, 256)])
+def test_persistent_wy_loop_many_items_per_cta(gdp, T, H, HV, V):
+    """M=2, K=128: 520 (V = 128) or 264 (V = 256, GVA, a partial last block per
+    head) (128-position block, head) items, more than the persistent WY grid, so
+    every CTA runs the next-item loads (for V = 256 also the second value round
+    through the k buffer), the buffer reuse and the next item's decay prefix
+    more than once."""
+    q, k, v, beta, g = chunk_case(1, T, H, HV, 128, V, 2, seed=12)
     o, fs = _run(gdp, q, k, v, beta, g, 2, 64, True)
     _check_all(o, fs, q, k, v, beta, g, 2)
 
