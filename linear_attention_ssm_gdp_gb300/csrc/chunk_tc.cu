@@ -608,12 +608,15 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
   const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
+  // TMEM columns: D1 = w_hi [h_hi | h_lo] [0, 64), D1B = w_lo h_hi [64, 96),
+  // D2 = k^T [v'_hi | v'_lo] [128, 192); a product is the sum of its halves
+  constexpr uint32_t TD1 = 0, TD1B = 64, TD2 = 128;
   if (warp == 0) {
-    tmem_alloc(s_tmem, 64);
+    tmem_alloc(s_tmem, 256);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);  // product 1: two issuers
     fence_mbar_init();
   }
   // The B operands h (rows kf) and v' (rows p) are MN-major tiles with 64-byte
@@ -655,7 +658,8 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     load_ug(Rseq, gk0);
   }
   const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
-  const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
+  const uint32_t id1w = idesc_bf16(128, 2 * kHBV, false, true);
+  const uint32_t id2w = idesc_bf16(128, 2 * kHBV, true, true);
   const float4* gk = reinterpret_cast<const float4*>(sm + H_G);
   for (int j = 0; j <= ne; ++j) {
     // publish the state at the start of chunk j (operand h^T, and for chunk_o at token-chunk starts)
@@ -689,14 +693,16 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     const int n = min(kBT, si.y * M - j * kBT);
     const int64_t R = Rseq + (int64_t)j * kBT;
     bool ok = true;
-    if (tid == 0) {  // product 1: D1 = w h  (rows = positions)
+    if (tid == 0 || tid == 32) {  // product 1: D1 = w h (rows = positions), two issuers
       ok = mbar_wait(&bars[0], ph, a.status, kDevTimeout);
       if (ok) {
         const uint32_t whi = smem_u32(sm + H_W), wlo = smem_u32(sm + H_W + 16384), hb = smem_u32(ht);
-        // w_hi h_hi + w_hi h_lo + w_lo h_hi
-        mma_run<8, false, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
-        mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
-        mma_run<8, true, 8192, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
+        if (tid == 0)  // w_hi [h_hi | h_lo]: the lo tile is the next 32-column group (LBO)
+          mma_run<8, false, 8192, 32, 4096, 1024>(tmem + TD1, sdesc_sw128(whi, 16, 1024),
+                                                  sdesc_sw64(hb, 8192, 512), id1w);
+        else  // w_lo h_hi
+          mma_run<8, false, 8192, 32, 4096, 1024>(tmem + TD1B, sdesc_sw128(wlo, 16, 1024),
+                                                  sdesc_sw64(hb, 8192, 512), id1);
         mma_commit(&bars[3]);
       }
     }
@@ -709,9 +715,14 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
       tc_fence_after();
       // product 1 has read w: the next chunk's w streams in behind this step
       if (tid == 0 && ok && j + 1 < ne) load_w(R + kBT);
-      uint32_t r[16];
-      GDP_TMEM_LD16(tmem + lane_base + cb, r);
+      uint32_t r[16], r1[16], r2[16];
+      GDP_TMEM_LD16(tmem + lane_base + TD1 + cb, r);
+      GDP_TMEM_LD16(tmem + lane_base + TD1 + 32 + cb, r1);
+      GDP_TMEM_LD16(tmem + lane_base + TD1B + cb, r2);
       tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < kHCols; ++c)
+        r[c] = __float_as_uint((__uint_as_float(r[c]) + __uint_as_float(r2[c])) + __uint_as_float(r1[c]));
       const uint8_t* urow = sm + H_U + p * 128;  // u row p, 128B-swizzled 16-byte chunks
       float us[kHCols];
 #pragma unroll
@@ -759,8 +770,8 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
       if (ok) {  // product 2: D2 = k^T v'  (rows = state rows kf)
         const uint32_t kb = smem_u32(sm + H_K), vb = smem_u32(vp);
         const uint64_t kd = sdesc_sw128(kb, 8192, 1024);
-        mma_run<4, false, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb, 4096, 512), id2);
-        mma_run<4, true, 0, 2048, 0, 1024>(tmem + 32, kd, sdesc_sw64(vb + 4096, 4096, 512), id2);
+        // k^T [v'_hi | v'_lo]: the lo tile is the next 32-column group (LBO)
+        mma_run<4, false, 0, 2048, 0, 1024>(tmem + TD2, kd, sdesc_sw64(vb, 4096, 512), id2w);
         mma_commit(&bars[4]);
       }
     }
@@ -769,12 +780,14 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     // product 2 has read k: the next chunk's k streams in
     if (tid == 0 && ok && j + 1 < ne) load_k(R + kBT);
     {
-      uint32_t r[16];
-      GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
+      uint32_t r[16], r1[16];
+      GDP_TMEM_LD16(tmem + lane_base + TD2 + cb, r);
+      GDP_TMEM_LD16(tmem + lane_base + TD2 + 32 + cb, r1);
       tmem_wait_ld();
       const float dl = expf(glast.x + glast.y);
 #pragma unroll
-      for (int c = 0; c < kHCols; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
+      for (int c = 0; c < kHCols; ++c)
+        h[c] = dl * h[c] + (__uint_as_float(r[c]) + __uint_as_float(r1[c]));
     }
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
@@ -785,7 +798,7 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     for (int c = 0; c < kHCols; c += 4)
       *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
   }
-  tmem_release(tmem, 64);
+  tmem_release(tmem, 256);
 }
 
 // ============================================================================ wy, 128-position blocks
