@@ -2166,7 +2166,10 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * kK;  // first of K rows
   constexpr int NE = 64 * M;  // expanded positions in a full token chunk
   constexpr int NMMA = (NE + 127) / 128;  // score MMAs of 128 positions
-  constexpr uint32_t TQH = 64 * NMMA;     // TMEM columns of q h
+  // TMEM columns: S^T [0, 64 NMMA) (then O = P_hi [v_hi | v_lo] in [0, 128)),
+  // q [h_hi | h_lo] [128, 256), P_lo v_hi [256, 320); a product is the sum of its
+  // 64-column halves
+  constexpr uint32_t TQH = 128, TOB = 256;
   uint8_t* qb = sm;
   uint8_t* kb = sm + o_k_off();
   uint8_t* hb = sm + o_h_off(M);
@@ -2178,14 +2181,14 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   float* srk = srq + 64;     // [64 M]
   uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);  // [0] tma [1] mma1 [2] mma2
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
-  constexpr uint32_t kCols = (TQH + 64) <= 128 ? 128 : 256;
+  constexpr uint32_t kCols = 512;
 
   if (warp == 0) {
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], i == 2 ? 2 : 1);  // O: two issuers
     fence_mbar_init();
   }
   if (tid < kBT) sgh[tid] = (tid < nt && a.g) ? a.g[(T0 + tid) * a.HV + hv] : 0.f;
@@ -2210,7 +2213,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   if (tid == 0) {
     const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
     const uint32_t ids = idesc_bf16(128, 64, false, false);
-    const uint32_t idh = idesc_bf16(128, kOBV, false, true);
+    const uint32_t idh = idesc_bf16(128, 2 * kOBV, false, true);
     const uint64_t qd = sdesc_sw128(q0, 16, 1024);
     // scores S^T = k q^T, rows = positions, N = 64 tokens: one MMA per 128 positions
     // into columns [64 m, 64 m + 64) (rows past the chunk's 64 M positions read the
@@ -2219,9 +2222,8 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     for (int m = 0; m < NMMA; ++m)
       mma_run<8, false, NE * 128, 32, 8192, 32>(tmem + 64 * m, sdesc_sw128(k0 + 16384 * m, 16, 1024),
                                                 qd, ids);
-    // q h (h hi then lo), N = 64 columns
+    // q [h_hi | h_lo], N = 128: the lo tile is the next 64-column group (LBO)
     mma_run<8, false, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
-    mma_run<8, true, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0 + 16384, 16384, 1024), idh);
     mma_commit(&bars[1]);
   }
   // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
@@ -2275,15 +2277,18 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   ok = __syncthreads_and(ok);
   tc_fence_after();
   if (!ok) { tmem_release(tmem, kCols); return; }
-  if (tid == 0) {  // O = P v_new (3 passes), into the score columns (consumed)
+  if (tid == 0 || tid == 32) {  // O = P v_new, into the score columns (consumed)
     const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
     // A = P, MN-major with M = 128: the second 64-token atom is never written and
     // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
-    const uint32_t ido = idesc_bf16(128, kOBV, true, true);
-    // P_hi v_hi + P_hi v_lo + P_lo v_hi
-    mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024), sdesc_sw128(vv, NE * 128, 1024), ido);
-    mma_run<4 * M, true, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024), sdesc_sw128(vv + NE * 128, NE * 128, 1024), ido);
-    mma_run<4 * M, true, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0 + M * 8192, 0, 1024), sdesc_sw128(vv, NE * 128, 1024), ido);
+    if (tid == 0)  // P_hi [v_hi | v_lo], N = 128: the lo tile is the next 64-column group
+      mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024),
+                                                    sdesc_sw128(vv, NE * 128, 1024),
+                                                    idesc_bf16(128, 2 * kOBV, true, true));
+    else  // P_lo v_hi
+      mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + TOB, sdesc_sw128(p0 + M * 8192, 0, 1024),
+                                                    sdesc_sw128(vv, NE * 128, 1024),
+                                                    idesc_bf16(128, kOBV, true, true));
     mma_commit(&bars[2]);
   }
   if (quarter < 2) {
@@ -2294,10 +2299,22 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
     {
       const int c0 = cq * 16;
-      uint32_t ro[16], rh[16];
+      uint32_t ro[16], rh[16], t16[16];
       GDP_TMEM_LD16(la + c0, ro);
       GDP_TMEM_LD16(la + TQH + c0, rh);
       tmem_wait_ld();
+      GDP_TMEM_LD16(la + 64 + c0, t16);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ro[j] = __float_as_uint(__uint_as_float(ro[j]) + __uint_as_float(t16[j]));
+      GDP_TMEM_LD16(la + TOB + c0, t16);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ro[j] = __float_as_uint(__uint_as_float(ro[j]) + __uint_as_float(t16[j]));
+      GDP_TMEM_LD16(la + TQH + 64 + c0, t16);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) rh[j] = __float_as_uint(__uint_as_float(rh[j]) + __uint_as_float(t16[j]));
       if (t < nt && ok) {
         float4* dst = reinterpret_cast<float4*>(a.o + ((T0 + t) * a.HV + hv) * a.V + v0 + c0);
 #pragma unroll
