@@ -18,7 +18,11 @@
  *   - Every call is asynchronous on `stream`, performs no host
  *     synchronisation (except gdp_read_status, which is for debugging) and
  *     validates all scalar arguments before launching anything. On a
- *     validation error nothing is launched.
+ *     validation error nothing is launched. Work is ordered on `stream` as
+ *     usual: the prepare and chunk kernels are launched with programmatic
+ *     dependent launch, so each may be scheduled while the work before it is
+ *     finishing, but none touches global memory before everything earlier on
+ *     the stream has completed and its writes are visible.
  *   - Tensors are row-major with the shapes given; strides, where a call takes
  *     them, are in elements. Only x and ba may be strided (rows), and their
  *     last dimension must be contiguous.
