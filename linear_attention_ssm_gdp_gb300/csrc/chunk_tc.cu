@@ -17,14 +17,15 @@
 // about 2^-9 of the output RMS per element.
 //
 // Kernels (one launch each):
-//   wy / wy128  grid (64-position block, HV) / persistent, one CTA per SM over
-//       (128-position block, HV) items: Gram matrix k k^T (MMA), transition
-//       block L and its inverse A = (I+L)^-1 (blocked: forward substitution and
-//       small merges in fp32 on CUDA cores, the 128 block's top merge on the
-//       tensor cores), then w = (A diag(beta e^Gam/|k|)) k and
-//       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32 (128-position
-//       blocks leave through TMA bulk stores while the next item's k and v
-//       load).
+//   wy128  persistent, one CTA per SM over (128-position block, HV) items: Gram
+//       matrix k k^T (MMA), transition block L and its inverse A = (I+L)^-1
+//       (blocked: forward substitution and 32 merges in fp32 on CUDA cores, the
+//       top merge on the tensor cores), then w = (A diag(beta e^Gam/|k|)) k and
+//       u = (A diag(beta)) v (MMAs) -> w as bf16 hi/lo, u fp32 (whole blocks
+//       leave through TMA bulk stores while the next item's k and v load). For
+//       odd M an item is two 64-position chunks with their own inverses and
+//       decay prefixes (no top merge), the factors the 64-position state
+//       recurrence steps with.
 //   ho128 (M = 2) grid (sequence, HV, 32-column slice of V): the sequential
 //       state recurrence and the chunk output in one kernel (a 128-position
 //       block is one 64-token output chunk); a chain warp group and an output
@@ -34,9 +35,9 @@
 //       state row), per block v_new = u - w h and h <- e^Gam_last h +
 //       k^T (e^(Gam_last - Gam)/|k| v_new); writes v_new (hi/lo) and the state
 //       at every token-chunk start (hi/lo).
-//   o   (other M) grid (token chunk, HV, 64-column slice): scores q k^T (MMA),
-//       q h, P = masked decayed scores (fp32 -> hi/lo), P v_new,
-//       o = scale (e^Gt |q|^-1 q h + P v_new).
+//   o   (other M) grid (token chunk, HV, 64-column slice): scores k q^T (MMA),
+//       q h, P^T = masked decayed scores (fp32 -> hi/lo), P v_new,
+//       o = scale |q|^-1 (e^Gt q h + P v_new).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -89,7 +90,9 @@ __device__ __forceinline__ float two_sum(float a, float b, float& e) {
 // across the warp as (sum, correction) pairs combined by TwoSum, and each
 // lane re-adds its exclusive prefix. hi[p] + lo[p] carries the prefix to about
 // twice fp32 precision, like the serial Neumaier form, in 4 + 5 + 4 steps
-// instead of 128.
+// instead of 128. SPLIT: two independent prefixes, positions 0..63 and
+// 64..127 (lanes 0-15 and 16-31), for two 64-position chunks.
+template <bool SPLIT>
 __device__ __forceinline__ void comp_prefix128_warp(float* hi, float* lo, int lane) {
   float s[4], c[4];
   const float4 x = *reinterpret_cast<const float4*>(hi + 4 * lane);
@@ -103,11 +106,12 @@ __device__ __forceinline__ void comp_prefix128_warp(float* hi, float* lo, int la
     c[i] = __fadd_rn(c[i - 1], e);
   }
   float S = s[3], C = c[3];  // inclusive scan of the lane totals
+  const int sl = SPLIT ? (lane & 15) : lane;  // lane within its scan
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
+  for (int off = 1; off < (SPLIT ? 16 : 32); off <<= 1) {
     const float S2 = __shfl_up_sync(0xffffffffu, S, off);
     const float C2 = __shfl_up_sync(0xffffffffu, C, off);
-    if (lane >= off) {
+    if (sl >= off) {
       float e;
       const float t = two_sum(S2, S, e);
       C = __fadd_rn(__fadd_rn(C2, C), e);
@@ -115,7 +119,7 @@ __device__ __forceinline__ void comp_prefix128_warp(float* hi, float* lo, int la
     }
   }
   float ES = __shfl_up_sync(0xffffffffu, S, 1), EC = __shfl_up_sync(0xffffffffu, C, 1);
-  if (lane == 0) ES = EC = 0.f;
+  if (sl == 0) ES = EC = 0.f;
   float oh[4], ol[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -229,8 +233,7 @@ struct WyArgs {
   const float* beta;
   const float* g;
   const int4* seq_info;
-  const int2* exp_tab;
-  const int4* blk_tab;  // 128-position blocks (wy128 only): sequence, first 64-chunk,
+  const int4* blk_tab;  // 128-position blocks: sequence, first 64-chunk, the
                         // sequence's first token, its length; sequence -1 past the end
   bf16* w_hi;
   bf16* w_lo;
@@ -239,306 +242,6 @@ struct WyArgs {
   int* status;
   int fault;   // test hook (gdp_debug_wait_fault): CTA 0 skips its first Gram product
 };
-
-// Shared memory (offsets from a 1024-aligned base). Operand tiles hold 64
-// rows of 128 bytes (one 128B-swizzle row each); MMA views with M = 128 read
-// 128 rows, i.e. 8 KB past a tile, which always lands on other live data and
-// only feeds accumulator rows 64..127 that are never read.
-constexpr int WY_K = 0;                     // k: 2 K-halves at stride 8 KB (+8 KB view)
-constexpr int WY_V = 24576;                 // v: V/64 column chunks of 8 KB
-constexpr int wy_a_off(int V) { return WY_V + (V / 64) * 8192; }   // A'hi A'lo A''hi A''lo
-constexpr int wy_l_off(int V) { return wy_a_off(V) + 4 * 8192; }   // L fp32 [64][65]
-constexpr int wy_i_off(int V) { return wy_l_off(V) + 64 * 65 * 4; }  // A fp32 [64][65]
-constexpr int wy_s_off(int V) { return wy_i_off(V) + 64 * 65 * 4; }  // small arrays
-constexpr int wy_smem(int V) { return wy_s_off(V) + 6 * 64 * 4 + 64 + 1024; }
-
-// One merge level of the blocked triangular inverse, for NP independent pairs
-// of SZ x SZ blocks along the diagonal of the in-place matrix LA (row stride
-// lda): X = L10 A00, then A10 = -A11 X written over L10. Register-tiled: each
-// of the NT threads owns a TR x TC tile of outputs with independent
-// accumulators. Both products skip the zero triangles of A00 / A11; the
-// thread-to-tile maps put threads sharing a loop bound in the same warp (a
-// column block for X = L10 A00, where i runs from the tile's first column; a
-// row block for A10 = -A11 X, where i runs up to the tile's last row).
-template <int SZ, int NP, int NT>
-__device__ __forceinline__ void merge_level(float* LA, int lda, float* X) {
-  constexpr int E = NP * SZ * SZ / NT;
-  constexpr int TC = E >= 4 ? 4 : E;
-  constexpr int TR = E / TC;
-  constexpr int NCB = SZ / TC, NRB = SZ / TR;
-  constexpr int XS = SZ + 4;
-  const int t = threadIdx.x;
-  const int pair = t / (NRB * NCB), rem = t - pair * (NRB * NCB);
-  const int base = pair * 2 * SZ;
-  float* Xp = X + pair * SZ * XS;
-  // Warps of a pair take their column (row) blocks in the order 0 1 2 3 7 6 5 4
-  // 8 9 10 11 15 14 13 12 ..., so that the warps sharing an SM sub-partition
-  // (w, w + 4, ...) get a heavy and a light block of the triangular loops.
-  const int wip = rem >> 5, li = rem & 31;
-  const int mw = ((wip >> 2) & 1) ? (wip | 3) - (wip & 3) : wip;
-  float acc[TR][TC];
-  {  // X = L10 A00, A00 lower triangular: i >= c0
-    const int r0 = (NRB == 32 ? li : rem % NRB) * TR, c0 = (NRB == 32 ? mw : rem / NRB) * TC;
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
-#pragma unroll 4
-    for (int i = c0; i < SZ; ++i) {
-      float av[TR], bv[TC];
-#pragma unroll
-      for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + i];
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) bv[cc] = LA[(base + i) * lda + base + c0 + cc];
-#pragma unroll
-      for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-        for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
-    }
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) Xp[(r0 + rr) * XS + c0 + cc] = acc[rr][cc];
-  }
-  __syncthreads();
-  {  // A10 = -A11 X, A11 lower triangular: i <= r0 + TR - 1
-    const int r0 = (32 % NCB == 0 ? mw * (32 / NCB) + li / NCB : rem / NCB) * TR;
-    const int c0 = (rem % NCB) * TC;
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < r0 + TR; ++i) {
-      float av[TR], bv[TC];
-#pragma unroll
-      for (int rr = 0; rr < TR; ++rr) av[rr] = LA[(base + SZ + r0 + rr) * lda + base + SZ + i];
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) bv[cc] = Xp[i * XS + c0 + cc];
-#pragma unroll
-      for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-        for (int cc = 0; cc < TC; ++cc) acc[rr][cc] += av[rr] * bv[cc];
-    }
-#pragma unroll
-    for (int rr = 0; rr < TR; ++rr)
-#pragma unroll
-      for (int cc = 0; cc < TC; ++cc) LA[(base + SZ + r0 + rr) * lda + base + c0 + cc] = -acc[rr][cc];
-  }
-  __syncthreads();
-}
-
-// Blocked inversion of the unit lower-triangular 64x64 matrix I + L (L strictly
-// lower, row stride 65) into A (row stride 65): 16x16 diagonal blocks by
-// column-parallel forward substitution, then two merge levels
-// A10 = -A11 (L10 A00). X is a scratch of at least 32 x 36 floats. 256 threads.
-__device__ void solve_tril64(const float* Ls, float* As, float* X) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < 64 * 65; i += 256) As[i] = 0.f;
-  __syncthreads();
-  if (tid < 64) {  // level 0: block b, column c = 16 b + cl; fully unrolled, column in registers
-    const int b = tid >> 4, cl = tid & 15, c = tid;
-    const float* Lb = Ls + (b * 16) * 65 + b * 16;
-    float col[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) col[i] = (i == cl) ? 1.f : 0.f;
-#pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < r; ++i) s += Lb[r * 65 + i] * col[i];  // col[i] = 0 for i < cl
-      if (r > cl) col[r] = -s;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) As[(b * 16 + i) * 65 + c] = col[i];
-  }
-  __syncthreads();
-  // below the diagonal blocks, As takes L (the merges read L10 there and overwrite it)
-  for (int i = tid; i < 64 * 64; i += 256) {
-    const int r = i >> 6, c = i & 63;
-    if ((r >> 4) > (c >> 4)) As[r * 65 + c] = Ls[r * 65 + c];
-  }
-  __syncthreads();
-  merge_level<16, 2, 256>(As, 65, X);
-  merge_level<32, 1, 256>(As, 65, X);
-}
-
-template <int V>
-__global__ void __launch_bounds__(256, 2) wy_tc_kernel(const __grid_constant__ CUtensorMap map_k,
-                                                       const __grid_constant__ CUtensorMap map_v,
-                                                       WyArgs a) {
-  pdl_wait();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
-  const int2 tab = a.exp_tab[blockIdx.x];
-  if (tab.x < 0) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
-  const int4 si = a.seq_info[tab.x];
-  const int M = a.M;
-  const int e_start = tab.y * kBT;
-  const int n = min(kBT, si.y * M - e_start);
-  const int64_t R0 = (int64_t)si.x * M + e_start;
-
-  uint8_t* kbuf = sm + WY_K;
-  uint8_t* vbuf = sm + WY_V;
-  uint8_t* atile = sm + wy_a_off(V);
-  float* Ls = reinterpret_cast<float*>(sm + wy_l_off(V));
-  float* As = reinterpret_cast<float*>(sm + wy_i_off(V));
-  float* X = reinterpret_cast<float*>(atile);  // solve scratch, dead before the A tiles
-  float* sb = reinterpret_cast<float*>(sm + wy_s_off(V));
-  float* sgh = sb + 64;
-  float* sgl = sgh + 64;
-  float* srk = sgl + 64;
-  float* sco = srk + 64;   // beta e^Gam / |k|
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sco + 64);  // [0] tma, [1] mma
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2);
-  constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
-
-  if (warp == 0) {
-    tmem_alloc(s_tmem, kCols);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
-  }
-  if (tid < kBT) {
-    float b = 0.f, gl = 0.f;
-    if (tid < n) {
-      const int e = e_start + tid, t = e / M;
-      b = a.beta[(R0 + tid) * a.HV + hv];
-      if (a.g && e - t * M == 0) gl = a.g[((int64_t)si.x + t) * a.HV + hv];
-    }
-    sb[tid] = b;
-    sgh[tid] = gl;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-  if (tid == 0) {
-    mbar_expect_tx(&bars[0], 2 * 8192 + (V / 64) * 8192);
-    tma_load_3d(kbuf, &map_k, 0, kh, (int)R0, &bars[0]);
-    tma_load_3d(kbuf + 8192, &map_k, 64, kh, (int)R0, &bars[0]);
-#pragma unroll
-    for (int c = 0; c < V / 64; ++c) tma_load_3d(vbuf + c * 8192, &map_v, 64 * c, hv, (int)R0, &bars[0]);
-    comp_prefix(sgh, sgl, kBT);
-  }
-  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  if (tid == 0) {  // Gram matrix k k^T: M = 128 (rows 64.. unused), N = 64, K = 128
-    const uint32_t kb = smem_u32(kbuf);
-    const uint32_t id = idesc_bf16(128, 64, false, false);
-    const uint64_t d0 = sdesc_sw128(kb, 16, 1024);
-    mma_run<8, false, 8192, 32, 8192, 32>(tmem, d0, d0, id);
-    mma_commit(&bars[1]);
-  }
-  if (tid < kBT) {
-    const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 8192 + tid * 128, tid);
-    const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    srk[tid] = r;
-    sco[tid] = sb[tid] * expf(sgh[tid] + sgl[tid]) * r;
-  }
-  ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
-  tc_fence_after();
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  // transition block L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|), i < p
-  if ((warp & 3) < 2) {
-    const int p = (warp & 3) * 32 + lane, c0 = (warp >> 2) * 32;
-    uint32_t r[32];
-    GDP_TMEM_LD32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0, r);
-    tmem_wait_ld();
-    const float bp = sb[p] * srk[p];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {  // branch-free, so that the iterations interleave
-      const int i = c0 + j;
-      const float x = bp * __expf(gam_diff4(sgh, sgl, p, i)) * srk[i] * __uint_as_float(r[j]);
-      Ls[p * 65 + i] = (i < p) ? x : 0.f;
-    }
-  }
-  __syncthreads();
-  solve_tril64(Ls, As, X);
-  // A' = A diag(beta e^Gam / |k|), A'' = A diag(beta), split into bf16 hi + lo,
-  // written as K-major operand tiles (row p, column i) with the 128B swizzle
-  // (a thread takes 8 consecutive columns of a row: four 16-byte stores)
-  for (int idx = tid; idx < 64 * 8; idx += 256) {
-    const int p = idx >> 3, q = idx & 7;
-    float v1[8], v2[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float av = As[p * 65 + 8 * q + e];
-      v1[e] = av * sco[8 * q + e];
-      v2[e] = av * sb[8 * q + e];
-    }
-    __align__(16) bf16 h1[8];
-    __align__(16) bf16 l1[8];
-    __align__(16) bf16 h2[8];
-    __align__(16) bf16 l2[8];
-    split_bf16_n<8>(v1, h1, l1);
-    split_bf16_n<8>(v2, h2, l2);
-    const uint32_t off = (uint32_t)p * 128u + (((uint32_t)q ^ (p & 7u)) << 4);
-    *reinterpret_cast<uint4*>(atile + 0 * 8192 + off) = *reinterpret_cast<const uint4*>(h1);
-    *reinterpret_cast<uint4*>(atile + 1 * 8192 + off) = *reinterpret_cast<const uint4*>(l1);
-    *reinterpret_cast<uint4*>(atile + 2 * 8192 + off) = *reinterpret_cast<const uint4*>(h2);
-    *reinterpret_cast<uint4*>(atile + 3 * 8192 + off) = *reinterpret_cast<const uint4*>(l2);
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) {
-    const uint32_t ab = smem_u32(atile), kb = smem_u32(kbuf), vb = smem_u32(vbuf);
-    const uint32_t idw = idesc_bf16(128, 128, false, true);
-    const uint32_t idu = idesc_bf16(128, V, false, true);
-    const uint64_t kd = sdesc_sw128(kb, 8192, 1024), vd = sdesc_sw128(vb, 8192, 1024);
-    // K = 64 positions: hi pass, then lo pass into the same accumulator
-    mma_run<4, false, 0, 32, 0, 2048>(tmem, sdesc_sw128(ab, 16, 1024), kd, idw);
-    mma_run<4, true, 0, 32, 0, 2048>(tmem, sdesc_sw128(ab + 8192, 16, 1024), kd, idw);
-    mma_run<4, false, 0, 32, 0, 2048>(tmem + 128, sdesc_sw128(ab + 2 * 8192, 16, 1024), vd, idu);
-    mma_run<4, true, 0, 32, 0, 2048>(tmem + 128, sdesc_sw128(ab + 3 * 8192, 16, 1024), vd, idu);
-    mma_commit(&bars[1]);
-  }
-  ok = mbar_wait(&bars[1], 1, a.status, kDevTimeout);
-  tc_fence_after();
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  if ((warp & 3) < 2) {
-    const int p = (warp & 3) * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    if (warp < 4) {  // w: 128 columns -> bf16 hi/lo
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t r[32];
-        GDP_TMEM_LD32(lane_addr + c0, r);
-        tmem_wait_ld();
-        if (p < n) {
-          bf16 hi[32], lo[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) split_bf16(__uint_as_float(r[j]), hi[j], lo[j]);
-          const int64_t row = ((R0 + p) * a.HV + hv) * kK + c0;
-          store_bf16x32(a.w_hi + row, hi);
-          store_bf16x32(a.w_lo + row, lo);
-        }
-      }
-      if (p < n) a.gk[(int64_t)hv * a.Te + R0 + p] = make_float4(sgh[p], sgl[p], srk[p], 0.f);
-    } else {  // u: V columns fp32
-      for (int c0 = 0; c0 < V; c0 += 32) {
-        uint32_t r[32];
-        GDP_TMEM_LD32(lane_addr + 128 + c0, r);
-        tmem_wait_ld();
-        if (p < n) {
-          float4* dst = reinterpret_cast<float4*>(a.u + ((R0 + p) * a.HV + hv) * V + c0);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
-      }
-    }
-  }
-  tmem_release(tmem, kCols);
-}
 
 // ============================================================================ chunk_h
 struct HArgs {
@@ -927,6 +630,7 @@ __device__ bool merge64_tc(float* LA, uint8_t* tiles, uint32_t tmem, uint64_t* b
 // for the whole SM), which the vector loads cut. scratch: the 64 KB operand-tile
 // region; TMEM columns [0, 256) and `bar` (phases 0, 1) are used. 512 threads.
 // Returns false if a bounded wait gave up.
+template <bool C64>
 __device__ bool solve_tril128(float* LA, const float* Ld, float* scratch, uint32_t tmem,
                               uint64_t* bar, int* status) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1007,23 +711,31 @@ __device__ bool solve_tril128(float* LA, const float* Ld, float* scratch, uint32
     }
     __syncthreads();
   }
-  return merge64_tc(LA, reinterpret_cast<uint8_t*>(scratch), tmem, bar, status);
+  // C64: two 64-position chunks, L10 = 0 and so A10 = 0: no top merge
+  return C64 ? true : merge64_tc(LA, reinterpret_cast<uint8_t*>(scratch), tmem, bar, status);
 }
 
 // Persistent: one CTA per SM walks (128-position block, value head) items,
 // item = head * NB + block, skipping the block list's unused tail entries.
-// TMEM, barriers and tensor maps are set up once per CTA. For V <= 128 the
-// items are pipelined: w (hi, lo) is staged in LA and u in the operand tiles,
-// so the k and v buffers are free as soon as the W and U products have read
-// them, and the next item's k and v stream in behind this item's epilogues;
-// the bulk stores only have to have read their staging before the next item
-// writes LA. For V = 256 the u staging needs the v buffer, so each item's k
-// and v are loaded once the previous item's stores have read shared memory.
-// In both modes warp 15, idle in the second tile build, stages the next
-// item's beta and decay and takes their compensated prefix there.
+// TMEM, barriers and tensor maps are set up once per CTA. The items are
+// pipelined: w (hi, lo) is staged in LA and u in the operand tiles (V = 256:
+// and in LA), so the k and v buffers are free as soon as the products have
+// read them. For V <= 128 the next item's k and v stream in behind this item's
+// epilogues; for V = 256 the second round of value columns streams into the k
+// buffer once the W product has read it, the next item's first round into the
+// v buffer after the first U product and its k after the second. The bulk
+// stores only have to have read their staging before the next item writes LA
+// (or, for the operand tiles, before its solve). Warp 15, idle in the second
+// tile build, stages the next item's beta and decay and takes their
+// compensated prefix there.
 // G = false is the ungated form (no decay, g = None on the pages): the decay
 // prefixes stay zero and no exponential is taken.
-template <int V, bool G>
+// C64: the item is two of the pages' 64-position chunks, each with its own
+// transition block, inverse and decay prefix (odd M, whose state recurrence
+// steps 64 positions): the L block coupling the two is zero, the prefix
+// restarts at position 64, and the inverse skips its top merge (A10 = 0), so
+// w, u and the decay records are those of the 64-position chunks.
+template <int V, bool G, bool C64>
 __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
     const __grid_constant__ CUtensorMap map_whs, const __grid_constant__ CUtensorMap map_wls,
@@ -1117,7 +829,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (G && warp == 0) comp_prefix128_warp(sarr + 128, sarr + 256, lane);
+  if (G && warp == 0) comp_prefix128_warp<C64>(sarr + 128, sarr + 256, lane);
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   uint32_t mma_phase = 0;
@@ -1191,7 +903,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       const int p = quarter * 32 + lane;
       const float bp = sb[p] * srk[p];
       const int c0 = cq * 32;
-      if (cq > quarter) {  // block entirely on or above the diagonal: zeros
+      // blocks on or above the diagonal, and for C64 the block coupling the two chunks: zeros
+      if (cq > quarter || (C64 && quarter >= 2 && cq < 2)) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) LA[p * 129 + c0 + j] = 0.f;
       } else {
@@ -1231,7 +944,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (tid == 0) tma_store_wait_read();  // the u stores have read the operand tiles
     tc_fence_before();
     __syncthreads();
-    ok = solve_tril128(LA, Ld, scratch, tmem, &bars[3], a.status);
+    ok = solve_tril128<C64>(LA, Ld, scratch, tmem, &bars[3], a.status);
     if (!ok) break;
     // operand tiles for pass `which`: 0 -> A diag(beta e^Gam/|k|) (for w), 1 -> A diag(beta) (for u).
     // Warp w builds one 32 x 32 chunk (row block R, column block C) of A, lane =
@@ -1278,7 +991,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         if (G) {
           *reinterpret_cast<float4*>(nsb + 128 + 4 * lane) = make_float4(pg[0], pg[1], pg[2], pg[3]);
           __syncwarp();
-          comp_prefix128_warp(nsb + 128, nsb + 256, lane);
+          comp_prefix128_warp<C64>(nsb + 128, nsb + 256, lane);
         }
       }
       fence_async_smem();
@@ -2387,20 +2100,8 @@ bool map2(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esz
 constexpr CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 constexpr CUtensorMapDataType F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 
-template <int V>
-cudaError_t run_wy(const ChunkProblem& p, const WyArgs& a) {
-  const int64_t Te = (int64_t)p.B * p.T * p.M;
-  CUtensorMap mk, mv;
-  if (!map3(&mk, p.k, BF, 2, kK, p.H, Te, 64, 64, true)) return cudaErrorInvalidValue;
-  if (!map3(&mv, p.v, BF, 2, V, p.HV, Te, 64, 64, true)) return cudaErrorInvalidValue;
-  const int smem = wy_smem(V);
-  cudaError_t e = cudaFuncSetAttribute(wy_tc_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(wy_tc_kernel<V>, dim3((unsigned)p.NE_max, p.HV), dim3(256), smem, p.stream,
-                    mk, mv, a);
-}
 
-template <int V, bool G>
+template <int V, bool G, bool C64>
 cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
   const int64_t Te = (int64_t)p.B * p.T * p.M;
   CUtensorMap mk, mv, mwh, mwl, mu;
@@ -2410,14 +2111,14 @@ cudaError_t run_wy128(const ChunkProblem& p, const WyArgs& a) {
       !map3(&mwl, a.w_lo, BF, 2, kK, p.HV, Te, 64, 128, true) ||
       !map3(&mu, a.u, F32, 4, V, p.HV, Te, 32, 128, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(wy128_tc_kernel<V, G>,
+  cudaError_t e = cudaFuncSetAttribute(wy128_tc_kernel<V, G, C64>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, W8_SMEM);
   if (e != cudaSuccess) return e;
   const int64_t NB = block128_bound(p.B, p.T, p.N_seq, p.M);
   const int64_t items = NB * p.HV;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const int grid = (int)std::min<int64_t>(items, sm_count());  // persistent, one CTA per SM
-  return launch_pdl(wy128_tc_kernel<V, G>, dim3(grid), dim3(512), W8_SMEM, p.stream, mk, mv, mwh,
+  return launch_pdl(wy128_tc_kernel<V, G, C64>, dim3(grid), dim3(512), W8_SMEM, p.stream, mk, mv, mwh,
                     mwl, mu, a, (int)NB);
 }
 
@@ -2456,7 +2157,8 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.seq_info = take(sizeof(int4) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.exp_tab = take(sizeof(int2) * (size_t)NE);
   L.tok_tab = take(sizeof(int2) * (size_t)NT);
-  if (M % 2 == 0) L.blk_tab = take(sizeof(int4) * (size_t)block128_bound(B, T, N_seq, M));
+  // 128-position blocks: WY-128 for every M (odd M in its two-chunk form)
+  L.blk_tab = take(sizeof(int4) * (size_t)block128_bound(B, T, N_seq, M));
   L.w_hi = take(2 * Te * HV * K);
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
@@ -2489,16 +2191,25 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
   // WY stage
   if (p.NE_max > 0 && Te > 0) {
     WyArgs a{p.H, p.HV, p.V, p.M, p.l2norm, Te, p.beta, p.g, seq_info,
-             reinterpret_cast<const int2*>(ws + L.exp_tab),
-             L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<const int4*>(ws + L.blk_tab),
-             w_hi, w_lo, u, gk, status, 0};
+             reinterpret_cast<const int4*>(ws + L.blk_tab), w_hi, w_lo, u, gk, status, 0};
     if ((p.M % 2) == 0) a.fault = g_wy_fault.exchange(0);  // one-shot test hook
-    const bool blk128 = (p.M % 2) == 0;
+    // even M: 128-position blocks; odd M: the same kernel on pairs of 64-position
+    // chunks (the state recurrence steps 64 positions)
+    const bool c64 = (p.M % 2) != 0;
     const bool G = p.g != nullptr;
     switch (p.V) {
-      case 64: e = !blk128 ? run_wy<64>(p, a) : G ? run_wy128<64, true>(p, a) : run_wy128<64, false>(p, a); break;
-      case 128: e = !blk128 ? run_wy<128>(p, a) : G ? run_wy128<128, true>(p, a) : run_wy128<128, false>(p, a); break;
-      default: e = !blk128 ? run_wy<256>(p, a) : G ? run_wy128<256, true>(p, a) : run_wy128<256, false>(p, a); break;
+      case 64:
+        e = c64 ? (G ? run_wy128<64, true, true>(p, a) : run_wy128<64, false, true>(p, a))
+                : (G ? run_wy128<64, true, false>(p, a) : run_wy128<64, false, false>(p, a));
+        break;
+      case 128:
+        e = c64 ? (G ? run_wy128<128, true, true>(p, a) : run_wy128<128, false, true>(p, a))
+                : (G ? run_wy128<128, true, false>(p, a) : run_wy128<128, false, false>(p, a));
+        break;
+      default:
+        e = c64 ? (G ? run_wy128<256, true, true>(p, a) : run_wy128<256, false, true>(p, a))
+                : (G ? run_wy128<256, true, false>(p, a) : run_wy128<256, false, false>(p, a));
+        break;
     }
     if (e != cudaSuccess) return e;
   }
