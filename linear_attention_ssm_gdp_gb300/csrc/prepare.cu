@@ -15,13 +15,13 @@
 // GB300 design: a persistent grid (a multiple of the SM count) walks token
 // rows with 16-byte vector loads/stores (the row's value block maps onto the
 // output contiguously, key/query heads are 16-byte-aligned runs), so the
-// kernel is a pure HBM stream. When a row fits one pass of the block
-// (prepare_rows_kernel, the prefill rows of the usual head sizes) each CTA
-// already has the next row's loads in flight while it stores the current one;
-// longer rows (the decode rows among them) stream through a shared-memory ring
-// of raw rows filled by cp.async (prepare_ring_kernel), and rows too long for
-// that ring, or not 16-byte aligned, go through prepare_kernel, a row at a
-// time. The gates use
+// kernel is a pure HBM stream. Prefill rows, and decode rows longer than one
+// pass of a 256-thread block, stream through a shared-memory ring of raw rows
+// filled by cp.async (prepare_ring_kernel: each CTA has its next two rows in
+// flight without holding registers while it stores the current one); shorter
+// decode rows take prepare_rows_kernel, which keeps the next row's loads in
+// registers; rows too long for the ring, or not 16-byte aligned, go through
+// prepare_kernel, a row at a time. The gates use
 // the CUDA math library's expf/log1pf and IEEE division, one fp32 operation at
 // a time; this translation unit is compiled with --fmad=false so no
 // multiply-add is contracted, which keeps beta and g bitwise equal to the
@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
 // copy placement as prepare_kernel). Same fp32 gate operations.
 constexpr int kRing = 3;
 
-template <bool DECODE>
-__global__ void __launch_bounds__(512, 3) prepare_ring_kernel(PrepArgs a, int xrow_v) {
+template <bool DECODE, int NT>
+__global__ void __launch_bounds__(NT, 3) prepare_ring_kernel(PrepArgs a, int xrow_v) {
   pdl_wait();
   extern __shared__ uint4 ring[];  // [kRing][xrow_v]
   const int64_t rows = (int64_t)a.n * a.T;
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(512, 3) prepare_ring_kernel(PrepArgs a, int xr
       const int64_t in = r / a.T, t = r - in * a.T;
       const uint4* src = reinterpret_cast<const uint4*>(a.x + in * a.x_sn_b + t * a.x_st_b);
       uint4* dst = ring + (i % kRing) * xrow_v;
-      for (int c = tid; c < xrow_v; c += blockDim.x) cp16(dst + c, src + c, 16);
+      for (int c = tid; c < xrow_v; c += NT) cp16(dst + c, src + c, 16);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(512, 3) prepare_ring_kernel(PrepArgs a, int xr
     uint4* vdst = reinterpret_cast<uint4*>(a.v + r * g.vrow_b);
     uint4* kdst = reinterpret_cast<uint4*>(a.k + r * g.krow_b);
     uint4* qdst = reinterpret_cast<uint4*>(a.q + r * g.qrow_b);
-    for (int c = tid; c < ntot; c += blockDim.x) {
+    for (int c = tid; c < ntot; c += NT) {
       if (c < g.nv) {  // value: contiguous copy of the row's value block
         __stcs(vdst + c, s[c]);
       } else if (c < g.nv + g.nk) {  // key: output head (j, h) reads group (j, h / hpg)
@@ -815,7 +815,15 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
   if (vec16) {
     const int64_t ntot = ((int64_t)M * H * P + (int64_t)(decode ? 2 * M : M + 1) * H * N) *
                          a.es / 16;
-    if (ntot <= 256 * kPU && M * H <= 256) {
+    const int64_t xrow_b = (int64_t)(M * H * P + M * G * N + G * N) * a.es;
+    const int64_t ring_b = kRing * xrow_b;
+    // Prefill rows go through the ring with 256-thread CTAs (measured: 51 us on
+    // the B2 T4096 H16 workload against 55 us for the register-prefetch row
+    // kernel); decode rows that fit one pass of the row kernel stay there, longer
+    // decode rows take the ring with 512-thread CTAs (14.3 against 16.3 us).
+    const int nt = decode ? 512 : 256;
+    const bool ring = ring_b <= 200 * 1024 && M * H <= nt && (!decode || ntot > 256 * kPU);
+    if (!ring && ntot <= 256 * kPU && M * H <= 256) {
       const int64_t rows = (int64_t)n * T;
       int per_sm = 0;
       cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -826,21 +834,19 @@ cudaError_t launch_prepare(const void* x, int64_t x_sn, int64_t x_st, const void
       return launch_pdl(decode ? prepare_rows_kernel<true> : prepare_rows_kernel<false>,
                         dim3(grid), dim3(256), 0, stream, a);
     }
-    const int64_t xrow_b = (int64_t)(M * H * P + M * G * N + G * N) * a.es;
-    const int64_t ring_b = kRing * xrow_b;
-    if (ring_b <= 200 * 1024 && M * H <= 512) {
+    if (ring) {
       a.fd_hv = FastDiv((uint32_t)((int64_t)N * a.es / 16));
-      auto kern = decode ? prepare_ring_kernel<true> : prepare_ring_kernel<false>;
+      auto kern = decode ? prepare_ring_kernel<true, 512> : prepare_ring_kernel<false, 256>;
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)ring_b);
       if (e != cudaSuccess) return e;
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 512, (size_t)ring_b);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nt, (size_t)ring_b);
       if (e != cudaSuccess) return e;
       const int64_t rows = (int64_t)n * T;
       const int64_t cap = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
       const int grid = (int)(rows < cap ? rows : cap);
-      return launch_pdl(kern, dim3(grid), dim3(512), (size_t)ring_b, stream, a,
+      return launch_pdl(kern, dim3(grid), dim3(nt), (size_t)ring_b, stream, a,
                         (int)(xrow_b / 16));
     }
     return launch_vb<16>(a, decode, stream);
