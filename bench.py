@@ -567,6 +567,31 @@ def run_decode(args, gdp, dev, pk):
                  + n * L * H * P * 4)
     mp, mr = statistics.mean(tp), statistics.mean(tr)
     hbm = pk["hbm_gbs"]
+    # the same update through a state pool (decode serving): 2n pool entries,
+    # requests on a seeded permutation of them, every 16th request padding (-1)
+    gen = torch.Generator().manual_seed(3)
+    slot = torch.randperm(2 * n, generator=gen)[:n].to(torch.int32)
+    slot[::16] = -1
+    slot = slot.to(dev)
+    pool = si.decode_state(2 * n, H, N, P).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        gdp.gdp_recurrent_update_slots(*outs, pool, slot, use_qk_l2norm=True, status=status,
+                                       out=o)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(5, min(args.steps, 50))):
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        ev[0].record()
+        gdp.gdp_recurrent_update_slots(*outs, pool, slot, use_qk_l2norm=True, status=status,
+                                       out=o)
+        ev[1].record()
+        torch.cuda.synchronize()
+        ts.append(ev[0].elapsed_time(ev[1]))
+    live = int((slot >= 0).sum())
+    ms_slots = statistics.mean(ts)
+    slot_bytes = rec_bytes - (n - live) * (2 * H * N * P * 4)  # padding moves no state
     slots = torch.arange(n, dtype=torch.int32, device=dev)
     conv = time_conv_prepare(gdp, dev, x, ba, A_log, dt_bias, M, H, G, P, N, None, outs,
                              prep_bytes, hbm, decode=True, slots=slots)
@@ -576,6 +601,10 @@ def run_decode(args, gdp, dev, pk):
             "prepare_hbm_frac": prep_bytes / (mp * 1e-3) / 1e9 / hbm,
             "update_us": mr * 1e3, "update_GBps": rec_bytes / (mr * 1e-3) / 1e9,
             "update_hbm_frac": rec_bytes / (mr * 1e-3) / 1e9 / hbm,
+            "update_slots": {"us": ms_slots * 1e3, "pool_entries": 2 * n, "live_requests": live,
+                             "GBps": slot_bytes / (ms_slots * 1e-3) / 1e9,
+                             "hbm_frac": slot_bytes / (ms_slots * 1e-3) / 1e9 / hbm,
+                             "status": int(status.item())},
             "requests_per_s": n / ((mp + mr) * 1e-3)}
 
 
