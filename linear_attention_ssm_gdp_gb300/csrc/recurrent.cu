@@ -80,7 +80,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 // uses entry r. A slot outside [-1, n_slots) or shared by two requests would
 // make the update ill-defined (two requests racing on one state), so such a
 // request is skipped like padding and *status (if given) is set to 1. Every
-// thread of the block calls this with the same r.
+// thread of the block calls this with the same r; each warp scans the table
+// for repeats on its own (no block barrier) and all reach the same answer.
 __device__ __forceinline__ int resolve_slot(const int* __restrict__ slot, int n, int n_slots,
                                             int r, int* status) {
   if (!slot) return r;
@@ -89,8 +90,8 @@ __device__ __forceinline__ int resolve_slot(const int* __restrict__ slot, int n,
   int bad = s < -1 || s >= n_slots;
   if (!bad) {
     int dup = 0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dup |= (i != r) & (slot[i] == s);
-    bad = __syncthreads_or(dup);
+    for (int i = threadIdx.x & 31; i < n; i += 32) dup |= (i != r) & (slot[i] == s);
+    bad = __any_sync(0xffffffffu, dup);
   }
   if (bad) {
     if (threadIdx.x == 0 && status) atomicExch(status, 1);
