@@ -1856,27 +1856,21 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
     const __grid_constant__ CUtensorMap map_hhi, const __grid_constant__ CUtensorMap map_hlo,
     const __grid_constant__ CUtensorMap map_vhi, const __grid_constant__ CUtensorMap map_vlo,
-    OArgs a) {
+    OArgs a, int n_items) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  // blockIdx.x = token chunk * (V / 64) + value slice: the slices of one chunk,
-  // which read the same q and k tiles, run side by side
+  // Persistent: item = hv * (NT_max * nsl) + token chunk * nsl + value slice, so
+  // the value slices of one chunk, which read the same q and k tiles, are
+  // processed side by side by neighbouring CTAs. Each tile buffer is free well
+  // before the next item needs it: the next item's q, k and h load once this
+  // item's score and q h products and norms have read them, its v once the O
+  // product has.
   const int nsl = a.V / kOBV;
-  const int tc = blockIdx.x / nsl;
-  const int2 tab = a.tok_tab[tc];
-  if (tab.x < 0) return;
+  const int per_hv = n_items / a.HV;  // NT_max * nsl
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
-  const int hv = blockIdx.y, kh = hv / (a.HV / a.H);
-  const int v0 = (blockIdx.x - tc * nsl) * kOBV;
-  const int4 si = a.seq_info[tab.x];
-  const int t_start = tab.y * kBT;
-  const int nt = min(kBT, si.y - t_start);
-  const int ne = nt * M;
-  const int64_t T0 = (int64_t)si.x + t_start, E0 = T0 * M;
-  const int64_t hrow = (((int64_t)si.w + tab.y) * a.HV + hv) * kK;  // first of K rows
   constexpr int NE = 64 * M;  // expanded positions in a full token chunk
   constexpr int NMMA = (NE + 127) / 128;  // score MMAs of 128 positions
   // TMEM columns: S^T [0, 64 NMMA) (then O = P_hi [v_hi | v_lo] in [0, 128)),
@@ -1892,125 +1886,188 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   float* sgl = sgh + 64;
   float* srq = sgl + 64;
   float* srk = srq + 64;     // [64 M]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);  // [0] tma [1] mma1 [2] mma2
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3);
+  // [0] q, k, h loaded, [1] v loaded, [2] scores and q h, [3] O (two issuers)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
   constexpr uint32_t kCols = 512;
 
+  // an item's geometry; tab.x < 0 marks a padding token chunk (no work)
+  struct Item {
+    int2 tab;
+    int hv, kh, v0, nt, ne;
+    int64_t T0, E0, hrow;
+  };
+  auto item = [&](int i) {
+    Item x;
+    x.hv = i / per_hv;
+    const int rem = i - x.hv * per_hv, tc = rem / nsl;
+    x.v0 = (rem - tc * nsl) * kOBV;
+    x.kh = x.hv / (a.HV / a.H);
+    x.tab = a.tok_tab[tc];
+    x.nt = x.ne = 0;
+    x.T0 = x.E0 = x.hrow = 0;
+    if (x.tab.x >= 0) {
+      const int4 si = a.seq_info[x.tab.x];
+      const int t_start = x.tab.y * kBT;
+      x.nt = min(kBT, si.y - t_start);
+      x.ne = x.nt * M;
+      x.T0 = (int64_t)si.x + t_start;
+      x.E0 = x.T0 * M;
+      x.hrow = (((int64_t)si.w + x.tab.y) * a.HV + x.hv) * kK;  // first of K rows
+    }
+    return x;
+  };
+  // the next item with work at or after i (n_items when none)
+  auto next_live = [&](int i) {
+    for (; i < n_items; i += gridDim.x)
+      if (a.tok_tab[(i - (i / per_hv) * per_hv) / nsl].x >= 0) break;
+    return i;
+  };
+  auto load_qkh = [&](const Item& x) {
+    mbar_expect_tx(&bars[0], 2 * 8192 + 2 * NE * 128 + 4 * 8192);
+    tma_load_3d(qb, &map_q, 0, x.kh, (int)x.T0, &bars[0]);
+    tma_load_3d(qb + 8192, &map_q, 64, x.kh, (int)x.T0, &bars[0]);
+    tma_load_3d(kb, &map_k, 0, x.kh, (int)x.E0, &bars[0]);
+    tma_load_3d(kb + NE * 128, &map_k, 64, x.kh, (int)x.E0, &bars[0]);
+    tma_load_2d(hb, &map_hhi, x.v0, (int)x.hrow, &bars[0]);
+    tma_load_2d(hb + 16384, &map_hlo, x.v0, (int)x.hrow, &bars[0]);
+  };
+  auto load_v = [&](const Item& x) {
+    mbar_expect_tx(&bars[1], 2 * NE * 128);
+    tma_load_3d(vb, &map_vhi, x.v0, x.hv, (int)x.E0, &bars[1]);
+    tma_load_3d(vb + NE * 128, &map_vlo, x.v0, x.hv, (int)x.E0, &bars[1]);
+  };
+
+  int it = next_live(blockIdx.x);
+  if (it >= n_items) return;
   if (warp == 0) {
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
+  Item x = item(it);
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], i == 2 ? 2 : 1);  // O: two issuers
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);
     fence_mbar_init();
+    load_qkh(x);
+    load_v(x);
   }
-  if (tid < kBT) sgh[tid] = (tid < nt && a.g) ? a.g[(T0 + tid) * a.HV + hv] : 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  if (tid == 0) {
-    mbar_expect_tx(&bars[0], 2 * 8192 + 2 * NE * 128 + 4 * 8192 + 2 * NE * 128);
-    tma_load_3d(qb, &map_q, 0, kh, (int)T0, &bars[0]);
-    tma_load_3d(qb + 8192, &map_q, 64, kh, (int)T0, &bars[0]);
-    tma_load_3d(kb, &map_k, 0, kh, (int)E0, &bars[0]);
-    tma_load_3d(kb + NE * 128, &map_k, 64, kh, (int)E0, &bars[0]);
-    tma_load_2d(hb, &map_hhi, v0, (int)hrow, &bars[0]);
-    tma_load_2d(hb + 16384, &map_hlo, v0, (int)hrow, &bars[0]);
-    tma_load_3d(vb, &map_vhi, v0, hv, (int)E0, &bars[0]);
-    tma_load_3d(vb + NE * 128, &map_vlo, v0, hv, (int)E0, &bars[0]);
-    comp_prefix(sgh, sgl, kBT);
-  }
-  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
-  if (!__syncthreads_and(ok)) { tmem_release(tmem, kCols); return; }
-  if (tid == 0) {
-    const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
-    const uint32_t ids = idesc_bf16(128, 64, false, false);
-    const uint32_t idh = idesc_bf16(128, 2 * kOBV, false, true);
-    const uint64_t qd = sdesc_sw128(q0, 16, 1024);
-    // scores S^T = k q^T, rows = positions, N = 64 tokens: one MMA per 128 positions
-    // into columns [64 m, 64 m + 64) (rows past the chunk's 64 M positions read the
-    // buffers behind k and feed accumulator rows that are never read)
+  int qkh_iss = 1, qkh_got = 0, v_iss = 1, v_got = 0;  // loads issued / consumed
+  bool ok = true;
+  for (int j = 0;; ++j) {
+    const uint32_t ph = j & 1;
+    const int nx = next_live(it + gridDim.x);
+    const bool has_next = nx < n_items;
+    const Item y = has_next ? item(nx) : x;
+    if (tid < kBT) sgh[tid] = (tid < x.nt && a.g) ? a.g[(x.T0 + tid) * a.HV + x.hv] : 0.f;
+    __syncthreads();
+    if (tid == 0) comp_prefix(sgh, sgl, kBT);
+    ok = mbar_wait(&bars[0], qkh_got & 1, a.status, kDevTimeout);
+    if (ok) ++qkh_got;
+    if (!__syncthreads_and(ok)) break;
+    if (tid == 0) {
+      const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
+      const uint32_t ids = idesc_bf16(128, 64, false, false);
+      const uint32_t idh = idesc_bf16(128, 2 * kOBV, false, true);
+      const uint64_t qd = sdesc_sw128(q0, 16, 1024);
+      // scores S^T = k q^T, rows = positions, N = 64 tokens: one MMA per 128
+      // positions into columns [64 m, 64 m + 64) (rows past the chunk's 64 M
+      // positions read the buffers behind k and feed accumulator rows that are
+      // never read)
 #pragma unroll
-    for (int m = 0; m < NMMA; ++m)
-      mma_run<8, false, NE * 128, 32, 8192, 32>(tmem + 64 * m, sdesc_sw128(k0 + 16384 * m, 16, 1024),
-                                                qd, ids);
-    // q [h_hi | h_lo], N = 128: the lo tile is the next 64-column group (LBO)
-    mma_run<8, false, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
-    mma_commit(&bars[1]);
-  }
-  // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
-  if (tid < kBT) {
-    const float ss = row_sumsq(qb + tid * 128, tid) + row_sumsq(qb + 8192 + tid * 128, tid);
-    srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-  }
-  for (int e = tid; e < NE; e += 512) {
-    const float ss = row_sumsq(kb + e * 128, e) + row_sumsq(kb + NE * 128 + e * 128, e);
-    srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-  }
-  // value rows past the chunk's end may hold anything: zero them (their P is 0)
-  for (int idx = tid; idx < 2 * NE * 8; idx += 512) {
-    const int row = idx >> 3, ch = idx & 7;
-    const int e = row % NE;
-    if (e >= ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
-  }
-  fence_async_smem();
-  __syncthreads();
-  {  // P^T rows e (positions), this warp's 16 of the 64 tokens: every warp builds rows
-    ok = mbar_wait(&bars[1], 0, a.status, kDevTimeout);
+      for (int m = 0; m < NMMA; ++m)
+        mma_run<8, false, NE * 128, 32, 8192, 32>(tmem + 64 * m,
+                                                  sdesc_sw128(k0 + 16384 * m, 16, 1024), qd, ids);
+      // q [h_hi | h_lo], N = 128: the lo tile is the next 64-column group (LBO)
+      mma_run<8, false, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
+      mma_commit(&bars[2]);
+    }
+    // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
+    if (tid < kBT) {
+      const float ss = row_sumsq(qb + tid * 128, tid) + row_sumsq(qb + 8192 + tid * 128, tid);
+      srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+    for (int e = tid; e < NE; e += 512) {
+      const float ss = row_sumsq(kb + e * 128, e) + row_sumsq(kb + NE * 128 + e * 128, e);
+      srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+    fence_async_smem();  // the norms' reads of q and k end before the next item's loads
+    ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout);
     tc_fence_after();
+    ok = mbar_wait(&bars[1], v_got & 1, a.status, kDevTimeout) && ok;
+    if (ok) ++v_got;
+    if (!__syncthreads_and(ok)) break;
+    // the score and q h products and the norms have read q, k and h
+    if (has_next) {
+      if (tid == 0) load_qkh(y);
+      ++qkh_iss;
+    }
+    // value rows past the chunk's end may hold anything: zero them (their P is 0)
+    for (int idx = tid; idx < 2 * NE * 8; idx += 512) {
+      const int row = idx >> 3, ch = idx & 7;
+      const int e = row % NE;
+      if (e >= x.ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
+    }
+    {  // P^T rows e (positions), this warp's 16 of the 64 tokens: every warp builds rows
 #pragma unroll
-    for (int m = 0; m < NMMA; ++m) {
-      if (128 * m + quarter * 32 < NE) {  // warp-uniform
-        const int e = 128 * m + quarter * 32 + lane, s = e / M;
-        uint32_t r[16];
-        GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + 64 * m + 16 * cq, r);
-        tmem_wait_ld();
-        const float rk = srk[e];
-        __align__(16) bf16 ph[16];
-        __align__(16) bf16 pl[16];
+      for (int m = 0; m < NMMA; ++m) {
+        if (128 * m + quarter * 32 < NE) {  // warp-uniform
+          const int e = 128 * m + quarter * 32 + lane, s = e / M;
+          uint32_t r[16];
+          GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + 64 * m + 16 * cq, r);
+          tmem_wait_ld();
+          const float rk = srk[e];
+          __align__(16) bf16 ph_[16];
+          __align__(16) bf16 pl_[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {  // branch-free, so that the iterations interleave
-          const int t = 16 * cq + j;
-          const float x = __uint_as_float(r[j]) * rk * __expf(gam_diff4(sgh, sgl, t, s));
-          split_bf16((e < ne && s <= t && t < nt) ? x : 0.f, ph[j], pl[j]);
-        }
-        // MN-major operand: row e (K), 64 tokens (M) of 128 bytes; two 16-byte chunks
+          for (int jj = 0; jj < 16; ++jj) {  // branch-free, so that the iterations interleave
+            const int t = 16 * cq + jj;
+            const float v = __uint_as_float(r[jj]) * rk * __expf(gam_diff4(sgh, sgl, t, s));
+            split_bf16((e < x.ne && s <= t && t < x.nt) ? v : 0.f, ph_[jj], pl_[jj]);
+          }
+          // MN-major operand: row e (K), 64 tokens (M) of 128 bytes; two 16-byte chunks
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t off = (uint32_t)e * 128u + ((((uint32_t)(2 * cq + c)) ^ (e & 7u)) << 4);
-          *reinterpret_cast<uint4*>(pb + off) = reinterpret_cast<const uint4*>(ph)[c];
-          *reinterpret_cast<uint4*>(pb + M * 8192 + off) = reinterpret_cast<const uint4*>(pl)[c];
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t off = (uint32_t)e * 128u + ((((uint32_t)(2 * cq + c)) ^ (e & 7u)) << 4);
+            *reinterpret_cast<uint4*>(pb + off) = reinterpret_cast<const uint4*>(ph_)[c];
+            *reinterpret_cast<uint4*>(pb + M * 8192 + off) = reinterpret_cast<const uint4*>(pl_)[c];
+          }
         }
       }
+      fence_async_smem();
     }
-    fence_async_smem();
-  }
-  tc_fence_before();
-  ok = __syncthreads_and(ok);
-  tc_fence_after();
-  if (!ok) { tmem_release(tmem, kCols); return; }
-  if (tid == 0 || tid == 32) {  // O = P v_new, into the score columns (consumed)
-    const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
-    // A = P, MN-major with M = 128: the second 64-token atom is never written and
-    // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
-    if (tid == 0)  // P_hi [v_hi | v_lo], N = 128: the lo tile is the next 64-column group
-      mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024),
-                                                    sdesc_sw128(vv, NE * 128, 1024),
-                                                    idesc_bf16(128, 2 * kOBV, true, true));
-    else  // P_lo v_hi
-      mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + TOB, sdesc_sw128(p0 + M * 8192, 0, 1024),
-                                                    sdesc_sw128(vv, NE * 128, 1024),
-                                                    idesc_bf16(128, kOBV, true, true));
-    mma_commit(&bars[2]);
-  }
-  if (quarter < 2) {
-    const int t = quarter * 32 + lane;
-    ok = mbar_wait(&bars[2], 0, a.status, kDevTimeout);
+    tc_fence_before();
+    __syncthreads();
     tc_fence_after();
-    const float rq = srq[t], qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
-    const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
-    {
+    if (tid == 0 || tid == 32) {  // O = P v_new, into the score columns (consumed)
+      const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
+      // A = P, MN-major with M = 128: the second 64-token atom is never written and
+      // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
+      if (tid == 0)  // P_hi [v_hi | v_lo], N = 128: the lo tile is the next 64-column group
+        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024),
+                                                      sdesc_sw128(vv, NE * 128, 1024),
+                                                      idesc_bf16(128, 2 * kOBV, true, true));
+      else  // P_lo v_hi
+        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + TOB,
+                                                      sdesc_sw128(p0 + M * 8192, 0, 1024),
+                                                      sdesc_sw128(vv, NE * 128, 1024),
+                                                      idesc_bf16(128, kOBV, true, true));
+      mma_commit(&bars[3]);
+    }
+    ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout);
+    tc_fence_after();
+    // the O product has read v (and P): the next item's v streams in
+    if (ok && has_next) {
+      if (tid == 0) load_v(y);
+      ++v_iss;
+    }
+    if (quarter < 2) {
+      const int t = quarter * 32 + lane;
+      const float rq = srq[t], qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
+      const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
       const int c0 = cq * 16;
       uint32_t ro[16], rh[16], t16[16];
       GDP_TMEM_LD16(la + c0, ro);
@@ -2019,28 +2076,43 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
       GDP_TMEM_LD16(la + 64 + c0, t16);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ro[j] = __float_as_uint(__uint_as_float(ro[j]) + __uint_as_float(t16[j]));
+      for (int jj = 0; jj < 16; ++jj) ro[jj] = __float_as_uint(__uint_as_float(ro[jj]) + __uint_as_float(t16[jj]));
       GDP_TMEM_LD16(la + TOB + c0, t16);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ro[j] = __float_as_uint(__uint_as_float(ro[j]) + __uint_as_float(t16[j]));
+      for (int jj = 0; jj < 16; ++jj) ro[jj] = __float_as_uint(__uint_as_float(ro[jj]) + __uint_as_float(t16[jj]));
       GDP_TMEM_LD16(la + TQH + 64 + c0, t16);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) rh[j] = __float_as_uint(__uint_as_float(rh[j]) + __uint_as_float(t16[j]));
-      if (t < nt && ok) {
-        float4* dst = reinterpret_cast<float4*>(a.o + ((T0 + t) * a.HV + hv) * a.V + v0 + c0);
+      for (int jj = 0; jj < 16; ++jj) rh[jj] = __float_as_uint(__uint_as_float(rh[jj]) + __uint_as_float(t16[jj]));
+      if (t < x.nt && ok) {
+        float4* dst = reinterpret_cast<float4*>(a.o + ((x.T0 + t) * a.HV + x.hv) * a.V + x.v0 + c0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float x[4];
+        for (int jj = 0; jj < 4; ++jj) {
+          float o4[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            x[q] = a.scale * (qs * __uint_as_float(rh[4 * j + q]) + rq * __uint_as_float(ro[4 * j + q]));
-          dst[j] = make_float4(x[0], x[1], x[2], x[3]);
+            o4[q] = a.scale * (qs * __uint_as_float(rh[4 * jj + q]) + rq * __uint_as_float(ro[4 * jj + q]));
+          dst[jj] = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
       }
     }
+    tc_fence_before();
+    // TMEM, P and the small arrays are free for the next item
+    if (!__syncthreads_and(ok)) break;
+    tc_fence_after();
+    if (!has_next) break;
+    it = nx;
+    x = y;
   }
+  if (tid == 0) {  // nothing may still write shared memory when the CTA leaves
+    bool w = true;
+    for (; w && qkh_got < qkh_iss; ++qkh_got) w = mbar_wait(&bars[0], qkh_got & 1, nullptr, 0);
+    for (; w && v_got < v_iss; ++v_got) w = mbar_wait(&bars[1], v_got & 1, nullptr, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   tmem_release(tmem, kCols);
 }
 
@@ -2132,8 +2204,11 @@ cudaError_t run_o(const ChunkProblem& p, const OArgs& a, const CUtensorMap& mhhi
   const int smem = o_smem(M);
   cudaError_t e = cudaFuncSetAttribute(o_tc_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(o_tc_kernel<M>, dim3((unsigned)(p.NT_max * (p.V / kOBV)), p.HV), dim3(512),
-                    smem, p.stream, mq, mk, mhhi, mhlo, mvhi, mvlo, a);
+  const int64_t items = p.NT_max * (p.V / kOBV) * p.HV;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<int64_t>(items, sm_count());  // persistent, one CTA per SM
+  return launch_pdl(o_tc_kernel<M>, dim3(grid), dim3(512), smem, p.stream, mq, mk, mhhi, mhlo, mvhi,
+                    mvlo, a, (int)items);
 }
 
 }  // namespace
