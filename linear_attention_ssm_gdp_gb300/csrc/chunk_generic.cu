@@ -111,7 +111,8 @@ __device__ __forceinline__ void scan3(int64_t (&x)[3], int64_t (&tot)[3], int64_
 
 __global__ void __launch_bounds__(kTabThreads) tables_kernel(
     const int32_t* cu, int N_seq, int B, int T, int M, int BT, int64_t NE_max, int64_t NT_max,
-    int4* seq_info, int2* exp_tab, int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status) {
+    int4* seq_info, int2* exp_tab, int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status,
+    int* seq_order) {
   pdl_wait();
   __shared__ int4 s_info[kTabSmem];     // (first token, length, first exp chunk, first token chunk)
   __shared__ int4 s_cnt[kTabSmem];      // (exp chunks, token chunks, 128-position blocks, first block)
@@ -168,6 +169,24 @@ __global__ void __launch_bounds__(kTabThreads) tables_kernel(
   // write no output rows and only pass the initial state through.
   if (bad)
     for (int i = tid; i < N_seq; i += kTabThreads) seq_info[i] = make_int4(0, 0, 0, 0);
+  if (seq_order) {
+    // Launch order of the state-scan chains: sequences by length, longest first
+    // (equal lengths by index), so that the CTAs that start last run the shortest
+    // chains; the identity when the records do not all fit in shared memory
+    const bool sort = !bad && N_seq <= kTabSmem;
+    for (int i = tid; i < N_seq; i += kTabThreads) {
+      int r = i;
+      if (sort) {
+        const int li = s_info[i].y;
+        r = 0;
+        for (int j = 0; j < N_seq; ++j) {
+          const int lj = s_info[j].y;
+          r += (lj > li) | (lj == li & j < i);
+        }
+      }
+      seq_order[r] = i;
+    }
+  }
   const int64_t ne = bad ? 0 : carry[0], nt = bad ? 0 : carry[1], nb = bad ? 0 : carry[2];
   if (!bad) {
     // one warp per sequence over the shared records, lanes over its chunks
@@ -643,7 +662,8 @@ cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws)
       p.NE_max, p.NT_max, reinterpret_cast<int4*>(ws + L.seq_info),
       reinterpret_cast<int2*>(ws + L.exp_tab), reinterpret_cast<int2*>(ws + L.tok_tab),
       L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int4*>(ws + L.blk_tab),
-      block128_bound(p.B, p.T, p.N_seq, p.M), reinterpret_cast<int*>(ws + L.status));
+      block128_bound(p.B, p.T, p.N_seq, p.M), reinterpret_cast<int*>(ws + L.status),
+      L.seq_order == SIZE_MAX ? nullptr : reinterpret_cast<int*>(ws + L.seq_order));
 }
 
 cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {

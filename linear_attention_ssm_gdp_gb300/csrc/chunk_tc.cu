@@ -257,7 +257,24 @@ struct HArgs {
   bf16* h_hi;   // [n_tok_chunks][HV][K][V]
   bf16* h_lo;
   int* status;
+  const int* seq_order;  // null: dense launch order (see chain_pos)
 };
+
+// The (sequence, value head, value slice) of a state-scan CTA. The value slices
+// of one (sequence, head), which read the same w, k and q tiles, are always
+// neighbours in launch order. Without an order table the grid is
+// (sequence x slice, head); with one (ragged sequences) the launch order walks
+// the sequences longest first, every head of one sequence before the next, so
+// that the chains that start last are the shortest and the grid ends evenly.
+struct ChainPos {
+  int seq, hv, slice;
+};
+__device__ __forceinline__ ChainPos chain_pos(const int* order, int nsl, int HV) {
+  if (!order) return {(int)blockIdx.x / nsl, (int)blockIdx.y, (int)(blockIdx.x % nsl)};
+  const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x), per = HV * nsl;
+  const int r = lin / per, rem = lin - r * per;
+  return {order[r], rem / nsl, rem % nsl};
+}
 
 // Shared memory: w_hi (16 KB) | w_lo (16 KB) | k (16 KB) | u fp32 64x32 (8 KB) | gk
 // 64x16 B (1 KB) | h^T hi | lo (16 KB) | v'^T hi | lo (8 KB) | barriers: 82 KB, so two
@@ -294,12 +311,10 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
   const int quarter = warp & 3, chalf = warp >> 2;
   const int row = quarter * 32 + lane;          // state row kf / position p
   const int cb = chalf * kHCols;                // first of this thread's 16 columns
-  // blockIdx.x = sequence * (V / 32) + value slice: the slices of one
-  // (sequence, head), which read the same w and k tiles, run side by side and
-  // share those tiles through L2
   const int nsl = a.V / kHBV;
-  const int seq = blockIdx.x / nsl, hv = blockIdx.y, kh = hv / (a.HV / H);
-  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
+  const ChainPos cp = chain_pos(a.seq_order, nsl, a.HV);
+  const int seq = cp.seq, hv = cp.hv, kh = hv / (a.HV / H);
+  const int v0 = cp.slice * kHBV;
   const int V = a.V, M = a.M;
   const int4 si = a.seq_info[seq];
   const int ne = (int)cdiv((int64_t)si.y * M, kBT);
@@ -1199,12 +1214,10 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
   const int row = quarter * 32 + lane;          // state row kf / position p
   constexpr int NC = 16;                        // value columns per thread
   const int cb = cgrp * NC;
-  // blockIdx.x = sequence * (V / 32) + value slice: the slices of one
-  // (sequence, head), which read the same w and k tiles, run side by side and
-  // share those tiles through L2
   const int nsl = a.V / kHBV;
-  const int seq = blockIdx.x / nsl, hv = blockIdx.y, kh = hv / (a.HV / H);
-  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
+  const ChainPos cp = chain_pos(a.seq_order, nsl, a.HV);
+  const int seq = cp.seq, hv = cp.hv, kh = hv / (a.HV / H);
+  const int v0 = cp.slice * kHBV;
   const int V = a.V, M = a.M;
   const int4 si = a.seq_info[seq];
   const int nb = (int)cdiv((int64_t)si.y * M, 128);
@@ -1459,11 +1472,11 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   constexpr int NC = 16;
   const int cb = cgrp * NC;
   const int HVn = f.h.HV, V = f.h.V;
-  // blockIdx.x = sequence * (V / 32) + value slice (slices of one head side by side)
   const int nsl = V / kHBV;
-  const int seq = blockIdx.x / nsl, hv = blockIdx.y;
+  const ChainPos cp = chain_pos(f.h.seq_order, nsl, HVn);
+  const int seq = cp.seq, hv = cp.hv;
   const int kh = hv / (HVn / f.H);
-  const int v0 = (blockIdx.x - seq * nsl) * kHBV;
+  const int v0 = cp.slice * kHBV;
   const int4 si = f.h.seq_info[seq];
   const int nb = (int)cdiv((int64_t)si.y * 2, 128);
   int* status = f.h.status;
@@ -2234,6 +2247,7 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.tok_tab = take(sizeof(int2) * (size_t)NT);
   // 128-position blocks: WY-128 for every M (odd M in its two-chunk form)
   L.blk_tab = take(sizeof(int4) * (size_t)block128_bound(B, T, N_seq, M));
+  L.seq_order = take(sizeof(int32_t) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.w_hi = take(2 * Te * HV * K);
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
@@ -2301,7 +2315,9 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
         !map3(&mu, u, F32, 4, p.V, p.HV, Tr, kHBV, rows, true) ||
         !map2(&mg, gk, F32, 4, 4, (uint64_t)p.HV * Tr, 4, rows, false))
       return cudaErrorInvalidValue;
-    HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
+    // ragged sequences: chains in the tables kernel's longest-first order
+    const int* order = p.cu_seqlens ? reinterpret_cast<const int*>(ws + L.seq_order) : nullptr;
+    HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status, order};
     const dim3 grid((unsigned)((int64_t)p.N_seq * (p.V / kHBV)), p.HV);
     if (p.M == 2) {  // state recurrence and output fused
       CUtensorMap mq;

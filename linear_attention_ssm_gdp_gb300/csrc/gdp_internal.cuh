@@ -48,6 +48,8 @@ struct ChunkProblem {
 // Byte offsets inside a chunk_fwd workspace.
 struct WsLayout {
   size_t status = 0, seq_info = 0, exp_tab = 0, tok_tab = 0;
+  // tensor-core path: launch order of the state-scan chains (sequences by length)
+  size_t seq_order = SIZE_MAX;
   // tensor-core path, even M: list of 128-position blocks (sequence, first 64-chunk)
   size_t blk_tab = SIZE_MAX;
   size_t A = SIZE_MAX, w = SIZE_MAX, u = SIZE_MAX, gexp = SIZE_MAX, v_new = SIZE_MAX,
