@@ -1856,13 +1856,14 @@ struct OArgs {
 };
 
 // q (24 KB incl. view) | k (2 halves of 64M rows, 16M KB) | h hi, lo (16 KB each) |
-// v_new hi, lo (8M KB each) | P hi, lo (MN-major: 64M rows e x 64 tokens t, 8M KB each) | small
+// v_new hi, lo (8M KB each) | P hi, lo (MN-major: 64M rows e x 64 tokens t, 8M KB each) |
+// gate prefixes [2][hi 128 | lo 128] | 1/|q| [64] | 1/|k| [64M] | barriers
 constexpr int o_k_off() { return 24576; }
 constexpr int o_h_off(int M) { return o_k_off() + 16384 * M; }
 constexpr int o_v_off(int M) { return o_h_off(M) + 32768; }
 constexpr int o_p_off(int M) { return o_v_off(M) + 16384 * M; }
 constexpr int o_s_off(int M) { return o_p_off(M) + 2 * M * 8192; }
-constexpr int o_smem(int M) { return o_s_off(M) + (3 * 64 + 64 * M) * 4 + 64 + 1024; }
+constexpr int o_smem(int M) { return o_s_off(M) + (2 * 256 + 64 + 64 * M) * 4 + 64 + 1024; }
 
 template <int M>
 __global__ void __launch_bounds__(512, 1) o_tc_kernel(
@@ -1895,9 +1896,10 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   uint8_t* hb = sm + o_h_off(M);
   uint8_t* vb = sm + o_v_off(M);
   uint8_t* pb = sm + o_p_off(M);
-  float* sgh = reinterpret_cast<float*>(sm + o_s_off(M));
-  float* sgl = sgh + 64;
-  float* srq = sgl + 64;
+  // token gate prefixes, one buffer per item parity: hi [0, 64) and lo [128, 192)
+  // (the second 64 of each half take comp_prefix128_warp's unused second scan)
+  float* sgb = reinterpret_cast<float*>(sm + o_s_off(M));
+  float* srq = sgb + 2 * 256;
   float* srk = srq + 64;     // [64 M]
   // [0] q, k, h loaded, [1] v loaded, [2] scores and q h, [3] O (two issuers)
   uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);
@@ -1957,7 +1959,26 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     tmem_alloc(s_tmem, kCols);
     tmem_relinquish();
   }
+  // An item's gates: warp 2 loads them (lanes 0-15, four tokens each) as soon
+  // as the item is known and builds their compensated prefix while the output
+  // warps run the previous item's epilogue.
+  float gv[4];
+  auto gate_load = [&](const Item& z) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = 4 * lane + i;
+      gv[i] = (lane < 16 && t < z.nt && a.g) ? a.g[(z.T0 + t) * a.HV + z.hv] : 0.f;
+    }
+  };
+  auto gate_prefix = [&](float* buf) {
+    *reinterpret_cast<float4*>(buf + 4 * lane) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+    comp_prefix128_warp<true>(buf, buf + 128, lane);
+  };
   Item x = item(it);
+  if (warp == 2) {
+    gate_load(x);
+    gate_prefix(sgb);
+  }
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);
     fence_mbar_init();
@@ -1975,9 +1996,9 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     const int nx = next_live(it + gridDim.x);
     const bool has_next = nx < n_items;
     const Item y = has_next ? item(nx) : x;
-    if (tid < kBT) sgh[tid] = (tid < x.nt && a.g) ? a.g[(x.T0 + tid) * a.HV + x.hv] : 0.f;
-    __syncthreads();
-    if (tid == 0) comp_prefix(sgh, sgl, kBT);
+    const float* sgh = sgb + ph * 256;
+    const float* sgl = sgh + 128;
+    if (warp == 2 && has_next) gate_load(y);
     ok = mbar_wait(&bars[0], qkh_got & 1, a.status, kDevTimeout);
     if (ok) ++qkh_got;
     if (!__syncthreads_and(ok)) break;
@@ -2077,6 +2098,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
       if (tid == 0) load_v(y);
       ++v_iss;
     }
+    if (warp == 2 && has_next) gate_prefix(sgb + (ph ^ 1) * 256);
     if (quarter < 2) {
       const int t = quarter * 32 + lane;
       const float rq = srq[t], qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
