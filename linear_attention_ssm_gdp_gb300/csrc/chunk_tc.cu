@@ -1857,13 +1857,13 @@ struct OArgs {
 
 // q (24 KB incl. view) | k (2 halves of 64M rows, 16M KB) | h hi, lo (16 KB each) |
 // v_new hi, lo (8M KB each) | P hi, lo (MN-major: 64M rows e x 64 tokens t, 8M KB each) |
-// gate prefixes [2][hi 128 | lo 128] | 1/|q| [64] | 1/|k| [64M] | barriers
+// gate prefixes [2][hi 128 | lo 128] | 1/|q| [2][64] | 1/|k| [64M] | barriers
 constexpr int o_k_off() { return 24576; }
 constexpr int o_h_off(int M) { return o_k_off() + 16384 * M; }
 constexpr int o_v_off(int M) { return o_h_off(M) + 32768; }
 constexpr int o_p_off(int M) { return o_v_off(M) + 16384 * M; }
 constexpr int o_s_off(int M) { return o_p_off(M) + 2 * M * 8192; }
-constexpr int o_smem(int M) { return o_s_off(M) + (2 * 256 + 64 + 64 * M) * 4 + 64 + 1024; }
+constexpr int o_smem(int M) { return o_s_off(M) + (2 * 256 + 2 * 64 + 64 * M) * 4 + 64 + 1024; }
 
 template <int M>
 __global__ void __launch_bounds__(512, 1) o_tc_kernel(
@@ -1877,9 +1877,12 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
                                            ~uintptr_t(1023));
   // Persistent: item = hv * (NT_max * nsl) + token chunk * nsl + value slice, so
   // the value slices of one chunk, which read the same q and k tiles, are
-  // processed side by side by neighbouring CTAs. Each tile buffer is free well
-  // before the next item needs it: the next item's q, k and h load once this
-  // item's score and q h products and norms have read them, its v once the O
+  // processed side by side by neighbouring CTAs. Two items overlap: TMEM holds
+  // two column sets, one per item parity, and while the output warps wait for
+  // item j's O product and store its output, the other warps wait for item
+  // j + 1's q, k and h, issue its score and q h products and compute its row
+  // norms. Each tile buffer is reloaded as soon as its last reader is done: q, k
+  // and h once item j's score and q h products have completed, v once its O
   // product has.
   const int nsl = a.V / kOBV;
   const int per_hv = n_items / a.HV;  // NT_max * nsl
@@ -1887,10 +1890,11 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   const int quarter = warp & 3, cq = warp >> 2;  // TMEM lane quarter, column quarter
   constexpr int NE = 64 * M;  // expanded positions in a full token chunk
   constexpr int NMMA = (NE + 127) / 128;  // score MMAs of 128 positions
-  // TMEM columns: S^T [0, 64 NMMA) (then O = P_hi [v_hi | v_lo] in [0, 128)),
-  // q [h_hi | h_lo] [128, 256), P_lo v_hi [256, 320); a product is the sum of its
-  // 64-column halves
-  constexpr uint32_t TQH = 128, TOB = 256;
+  // TMEM columns of the set at base (0 or 256, by item parity): S^T [base, base +
+  // 64 NMMA), then O = P_hi [v_hi | v_lo] [base, base + 128); q h = q h_hi + q h_lo
+  // [base + 128, +64); P_lo v_hi [base + 192, +64). O is the sum of its three
+  // 64-column parts.
+  constexpr uint32_t TQH = 128, TOB = 192;
   uint8_t* qb = sm;
   uint8_t* kb = sm + o_k_off();
   uint8_t* hb = sm + o_h_off(M);
@@ -1899,11 +1903,12 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   // token gate prefixes, one buffer per item parity: hi [0, 64) and lo [128, 192)
   // (the second 64 of each half take comp_prefix128_warp's unused second scan)
   float* sgb = reinterpret_cast<float*>(sm + o_s_off(M));
-  float* srq = sgb + 2 * 256;
-  float* srk = srq + 64;     // [64 M]
-  // [0] q, k, h loaded, [1] v loaded, [2] scores and q h, [3] O (two issuers)
+  float* srq = sgb + 2 * 256;  // [2][64], by item parity
+  float* srk = srq + 2 * 64;   // [64 M]
+  // [0] q, k, h loaded, [1] v loaded, [2 + b] score and q h products of parity b,
+  // [4 + b] O product of parity b (two issuers)
   uint64_t* bars = reinterpret_cast<uint64_t*>(srk + NE);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 6);
   constexpr uint32_t kCols = 512;
 
   // an item's geometry; tab.x < 0 marks a padding token chunk (no work)
@@ -1952,13 +1957,6 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     tma_load_3d(vb, &map_vhi, x.v0, x.hv, (int)x.E0, &bars[1]);
     tma_load_3d(vb + NE * 128, &map_vlo, x.v0, x.hv, (int)x.E0, &bars[1]);
   };
-
-  int it = next_live(blockIdx.x);
-  if (it >= n_items) return;
-  if (warp == 0) {
-    tmem_alloc(s_tmem, kCols);
-    tmem_relinquish();
-  }
   // An item's gates: warp 2 loads them (lanes 0-15, four tokens each) as soon
   // as the item is known and builds their compensated prefix while the output
   // warps run the previous item's epilogue.
@@ -1974,13 +1972,53 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
     *reinterpret_cast<float4*>(buf + 4 * lane) = make_float4(gv[0], gv[1], gv[2], gv[3]);
     comp_prefix128_warp<true>(buf, buf + 128, lane);
   };
+  // Score and q h products of the item in q, k, h into the column set at base:
+  // S^T = k q^T, rows = positions, N = 64 tokens, one MMA per 128 positions into
+  // columns [64 m, 64 m + 64) (rows past the chunk's 64 M positions read the
+  // buffers behind k and feed accumulator rows that are never read); q h as
+  // q h_hi then q h_lo into one accumulator (N = 64 each).
+  auto issue_sq = [&](uint32_t tm, uint32_t base) {
+    const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
+    const uint32_t ids = idesc_bf16(128, 64, false, false);
+    const uint32_t idh = idesc_bf16(128, kOBV, false, true);
+    const uint64_t qd = sdesc_sw128(q0, 16, 1024);
+#pragma unroll
+    for (int m = 0; m < NMMA; ++m)
+      mma_run<8, false, NE * 128, 32, 8192, 32>(tm + base + 64 * m,
+                                                sdesc_sw128(k0 + 16384 * m, 16, 1024), qd, ids);
+    mma_run<8, false, 8192, 32, 8192, 2048>(tm + base + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
+    mma_run<8, true, 8192, 32, 8192, 2048>(tm + base + TQH, qd,
+                                           sdesc_sw128(h0 + 16384, 16384, 1024), idh);
+  };
+  // Row norms of the staged q and k tiles (swizzle only permutes 16-byte
+  // chunks), one row per thread of the 256 threads of lane quarters 2 and 3.
+  auto norms = [&](float* rq) {
+    const int gi = (warp >> 2) * 64 + (quarter - 2) * 32 + lane;
+    if (gi < kBT) {
+      const float ss = row_sumsq(qb + gi * 128, gi) + row_sumsq(qb + 8192 + gi * 128, gi);
+      rq[gi] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    } else if (gi < kBT + NE) {
+      const int e = gi - kBT;
+      const float ss = row_sumsq(kb + e * 128, e) + row_sumsq(kb + NE * 128 + e * 128, e);
+      srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+    fence_async_smem();  // the reads of q and k end before the next item's loads
+  };
+  static_assert(kBT + NE <= 256, "one norm row per thread of lane quarters 2 and 3");
+
+  int it = next_live(blockIdx.x);
+  if (it >= n_items) return;
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kCols);
+    tmem_relinquish();
+  }
   Item x = item(it);
   if (warp == 2) {
     gate_load(x);
     gate_prefix(sgb);
   }
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], i == 3 ? 2 : 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], i >= 4 ? 2 : 1);
     fence_mbar_init();
     load_qkh(x);
     load_v(x);
@@ -1989,61 +2027,33 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  int qkh_iss = 1, qkh_got = 0, v_iss = 1, v_got = 0;  // loads issued / consumed
-  bool ok = true;
-  for (int j = 0;; ++j) {
-    const uint32_t ph = j & 1;
+  int qkh_iss = 1, qkh_got = 0, v_iss = 1, v_got = 0;  // loads issued / consumed (thread 0's count)
+  // the first item's products and norms
+  bool ok = mbar_wait(&bars[0], 0, a.status, kDevTimeout);
+  if (ok) {
+    qkh_got = 1;
+    if (tid == 64) {
+      issue_sq(tmem, 0);
+      mma_commit(&bars[2]);
+    }
+    if (quarter >= 2) norms(srq);
+  }
+  ok = __syncthreads_and(ok);
+  for (int j = 0; ok; ++j) {
+    const uint32_t b = j & 1, base = 256 * b, ph = (j >> 1) & 1;
     const int nx = next_live(it + gridDim.x);
     const bool has_next = nx < n_items;
     const Item y = has_next ? item(nx) : x;
-    const float* sgh = sgb + ph * 256;
+    const float* sgh = sgb + b * 256;
     const float* sgl = sgh + 128;
     if (warp == 2 && has_next) gate_load(y);
-    ok = mbar_wait(&bars[0], qkh_got & 1, a.status, kDevTimeout);
-    if (ok) ++qkh_got;
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {
-      const uint32_t q0 = smem_u32(qb), k0 = smem_u32(kb), h0 = smem_u32(hb);
-      const uint32_t ids = idesc_bf16(128, 64, false, false);
-      const uint32_t idh = idesc_bf16(128, 2 * kOBV, false, true);
-      const uint64_t qd = sdesc_sw128(q0, 16, 1024);
-      // scores S^T = k q^T, rows = positions, N = 64 tokens: one MMA per 128
-      // positions into columns [64 m, 64 m + 64) (rows past the chunk's 64 M
-      // positions read the buffers behind k and feed accumulator rows that are
-      // never read)
-#pragma unroll
-      for (int m = 0; m < NMMA; ++m)
-        mma_run<8, false, NE * 128, 32, 8192, 32>(tmem + 64 * m,
-                                                  sdesc_sw128(k0 + 16384 * m, 16, 1024), qd, ids);
-      // q [h_hi | h_lo], N = 128: the lo tile is the next 64-column group (LBO)
-      mma_run<8, false, 8192, 32, 8192, 2048>(tmem + TQH, qd, sdesc_sw128(h0, 16384, 1024), idh);
-      mma_commit(&bars[2]);
-    }
-    // norms (rows of the staged q and k tiles; swizzle only permutes 16-byte chunks)
-    if (tid < kBT) {
-      const float ss = row_sumsq(qb + tid * 128, tid) + row_sumsq(qb + 8192 + tid * 128, tid);
-      srq[tid] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    }
-    for (int e = tid; e < NE; e += 512) {
-      const float ss = row_sumsq(kb + e * 128, e) + row_sumsq(kb + NE * 128 + e * 128, e);
-      srk[e] = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    }
-    fence_async_smem();  // the norms' reads of q and k end before the next item's loads
-    ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout);
+    ok = mbar_wait(&bars[2 + b], ph, a.status, kDevTimeout);
     tc_fence_after();
-    ok = mbar_wait(&bars[1], v_got & 1, a.status, kDevTimeout) && ok;
-    if (ok) ++v_got;
     if (!__syncthreads_and(ok)) break;
     // the score and q h products and the norms have read q, k and h
-    if (has_next) {
-      if (tid == 0) load_qkh(y);
+    if (has_next && tid == 0) {
+      load_qkh(y);
       ++qkh_iss;
-    }
-    // value rows past the chunk's end may hold anything: zero them (their P is 0)
-    for (int idx = tid; idx < 2 * NE * 8; idx += 512) {
-      const int row = idx >> 3, ch = idx & 7;
-      const int e = row % NE;
-      if (e >= x.ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
     }
     {  // P^T rows e (positions), this warp's 16 of the 64 tokens: every warp builds rows
 #pragma unroll
@@ -2051,7 +2061,7 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
         if (128 * m + quarter * 32 < NE) {  // warp-uniform
           const int e = 128 * m + quarter * 32 + lane, s = e / M;
           uint32_t r[16];
-          GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + 64 * m + 16 * cq, r);
+          GDP_TMEM_LD16(tmem + ((uint32_t)(quarter * 32) << 16) + base + 64 * m + 16 * cq, r);
           tmem_wait_ld();
           const float rk = srk[e];
           __align__(16) bf16 ph_[16];
@@ -2071,38 +2081,46 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
           }
         }
       }
-      fence_async_smem();
     }
+    ok = mbar_wait(&bars[1], v_got & 1, a.status, kDevTimeout);
+    if (ok) ++v_got;
+    // value rows past the chunk's end may hold anything: zero them (their P is 0)
+    for (int idx = tid; idx < 2 * NE * 8; idx += 512) {
+      const int row = idx >> 3, ch = idx & 7;
+      const int e = row % NE;
+      if (e >= x.ne) reinterpret_cast<uint4*>(vb + row * 128)[ch] = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    if (!__syncthreads_and(ok)) break;
     tc_fence_after();
     if (tid == 0 || tid == 32) {  // O = P v_new, into the score columns (consumed)
       const uint32_t p0 = smem_u32(pb), vv = smem_u32(vb);
       // A = P, MN-major with M = 128: the second 64-token atom is never written and
       // LBO = 0 re-reads the first, which only feeds the unused accumulator rows
       if (tid == 0)  // P_hi [v_hi | v_lo], N = 128: the lo tile is the next 64-column group
-        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem, sdesc_sw128(p0, 0, 1024),
+        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + base, sdesc_sw128(p0, 0, 1024),
                                                       sdesc_sw128(vv, NE * 128, 1024),
                                                       idesc_bf16(128, 2 * kOBV, true, true));
       else  // P_lo v_hi
-        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + TOB,
+        mma_run<4 * M, false, 8192, 2048, 8192, 2048>(tmem + base + TOB,
                                                       sdesc_sw128(p0 + M * 8192, 0, 1024),
                                                       sdesc_sw128(vv, NE * 128, 1024),
                                                       idesc_bf16(128, kOBV, true, true));
-      mma_commit(&bars[3]);
+      mma_commit(&bars[4 + b]);
     }
-    ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout);
-    tc_fence_after();
-    // the O product has read v (and P): the next item's v streams in
-    if (ok && has_next) {
-      if (tid == 0) load_v(y);
-      ++v_iss;
-    }
-    if (warp == 2 && has_next) gate_prefix(sgb + (ph ^ 1) * 256);
-    if (quarter < 2) {
+    if (quarter < 2) {  // the output: wait for O, store o rows
+      ok = mbar_wait(&bars[4 + b], ph, a.status, kDevTimeout);
+      tc_fence_after();
+      // the O product has read v (and P): the next item's v streams in
+      if (ok && has_next && tid == 0) {
+        load_v(y);
+        ++v_iss;
+      }
       const int t = quarter * 32 + lane;
-      const float rq = srq[t], qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
-      const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16);
+      const float rq = srq[64 * b + t];
+      const float qs = expf(sgh[t] + sgl[t]) * rq;  // o = scale |q|^-1 (e^Gam Qh + O)
+      const uint32_t la = tmem + ((uint32_t)(quarter * 32) << 16) + base;
       const int c0 = cq * 16;
       uint32_t ro[16], rh[16], t16[16];
       GDP_TMEM_LD16(la + c0, ro);
@@ -2116,10 +2134,6 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
       tmem_wait_ld();
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) ro[jj] = __float_as_uint(__uint_as_float(ro[jj]) + __uint_as_float(t16[jj]));
-      GDP_TMEM_LD16(la + TQH + 64 + c0, t16);
-      tmem_wait_ld();
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) rh[jj] = __float_as_uint(__uint_as_float(rh[jj]) + __uint_as_float(t16[jj]));
       if (t < x.nt && ok) {
         float4* dst = reinterpret_cast<float4*>(a.o + ((x.T0 + t) * a.HV + x.hv) * a.V + x.v0 + c0);
 #pragma unroll
@@ -2131,12 +2145,24 @@ __global__ void __launch_bounds__(512, 1) o_tc_kernel(
           dst[jj] = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
       }
+    } else if (has_next) {  // the next item: its products into the other column set, its norms
+      ok = mbar_wait(&bars[0], qkh_got & 1, a.status, kDevTimeout);
+      if (ok) {
+        if (tid == 64) {
+          tc_fence_after();
+          issue_sq(tmem, 256 * (b ^ 1));
+          mma_commit(&bars[2 + (b ^ 1)]);
+        }
+        norms(srq + 64 * (b ^ 1));
+      }
+      if (warp == 2) gate_prefix(sgb + (b ^ 1) * 256);
     }
     tc_fence_before();
-    // TMEM, P and the small arrays are free for the next item
+    // TMEM set b, P, the gates and norms of parity b are free for item j + 2
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
     if (!has_next) break;
+    ++qkh_got;
     it = nx;
     x = y;
   }
