@@ -42,6 +42,7 @@ CASES = [
     (1, 65, 1, 1, 256, 64, 1, 64, torch.float32, True, True, False),
     (1, 200, 2, 2, 128, 128, 2, 64, torch.bfloat16, True, False, True),  # tensor-core, ungated
     (1, 150, 2, 2, 128, 64, 3, 64, torch.bfloat16, True, False, False),  # tensor-core, ungated
+    (1, 600, 2, 2, 128, 128, 1, 64, torch.bfloat16, True, True, True),   # tensor-core, M = 1
 ]
 
 
@@ -255,6 +256,20 @@ def test_persistent_wy_loop_many_items_per_cta(gdp, T, H, HV, V):
     q, k, v, beta, g = chunk_case(1, T, H, HV, 128, V, 2, seed=12)
     o, fs = _run(gdp, q, k, v, beta, g, 2, 64, True)
     _check_all(o, fs, q, k, v, beta, g, 2)
+
+
+@pytest.mark.parametrize("M,V", [(1, 128), (3, 128), (3, 256)])
+def test_persistent_output_loop_many_items_per_cta(gdp, M, V):
+    """Odd M, K=128, ragged sequences (one empty, one of a single token): 360
+    (V = 128) or 720 (V = 256) (token chunk, value head, 64-column slice) items
+    for the persistent output kernel, padding chunks among them, so every CTA
+    skips padding, alternates its two TMEM column sets and runs the next-item
+    loads, products and norms more than once."""
+    lens = [700, 0, 1, 1199, 600]
+    cu = si.cu_seqlens_of(lens)
+    q, k, v, beta, g = chunk_case(1, sum(lens), 2, 4, 128, V, M, seed=15)
+    o, fs = _run(gdp, q, k, v, beta, g, M, 64, True, cu=cu)
+    _check_all(o, fs, q, k, v, beta, g, M, cu=cu)
 
 
 @pytest.mark.parametrize("M", [2, 3])
