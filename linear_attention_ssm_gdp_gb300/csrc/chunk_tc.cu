@@ -30,14 +30,16 @@
 //       state recurrence and the chunk output in one kernel (a 128-position
 //       block is one 64-token output chunk); a chain warp group and an output
 //       warp group meeting at mbarriers; states and v_new never reach HBM.
-//   h / h128 (other M) grid (sequence, HV, 32-column slice of V): the
-//       sequential chunk-state recurrence, fp32 state in registers (thread =
-//       state row), per block v_new = u - w h and h <- e^Gam_last h +
-//       k^T (e^(Gam_last - Gam)/|k| v_new); writes v_new (hi/lo) and the state
-//       at every token-chunk start (hi/lo).
-//   o   (other M) grid (token chunk, HV, 64-column slice): scores k q^T (MMA),
-//       q h, P^T = masked decayed scores (fp32 -> hi/lo), P v_new,
-//       o = scale |q|^-1 (e^Gt q h + P v_new).
+//   h   (odd M) grid (sequence, HV, 32-column slice of V), ragged sequences
+//       longest first: the sequential chunk-state recurrence on 64-position
+//       steps, fp32 state in registers (thread = state row), per step
+//       v_new = u - w h and h <- e^Gam_last h + k^T (e^(Gam_last - Gam)/|k| v_new);
+//       writes v_new (hi/lo) and the state at every token-chunk start (hi/lo).
+//   o   (odd M) persistent, one CTA per SM over (token chunk, HV, 64-column
+//       slice) items: scores k q^T and q h (MMA), P^T = masked decayed scores
+//       (fp32 -> hi/lo), P v_new, o = scale |q|^-1 (e^Gt q h + P v_new); two
+//       TMEM column sets, so one item's products and norms overlap the previous
+//       item's O product and stores.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -61,19 +63,6 @@ constexpr int kOBV = 64;   // value columns per chunk_o CTA
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ float gam_diff4(const float* hi, const float* lo, int p, int i) {
   return (hi[p] - hi[i]) + (lo[p] - lo[i]);
-}
-
-// Neumaier-compensated inclusive prefix sum, serial (n <= 64).
-__device__ __forceinline__ void comp_prefix(float* hi, float* lo, int n) {
-  float s = 0.f, c = 0.f;
-  for (int p = 0; p < n; ++p) {
-    const float x = hi[p];
-    const float t = s + x;
-    c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
-    s = t;
-    hi[p] = s;
-    lo[p] = c;
-  }
 }
 
 // Error-free sum (Knuth's TwoSum): a + b = s + e exactly.
@@ -1186,219 +1175,16 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
 }
 
 // ============================================================================ chunk_h, 128-position steps
-// Same recurrence as h_tc_kernel, one 128-position block per step (WY factors
-// from wy128_tc_kernel), every accumulator row in use. Operand buffers are
-// single: each group is refilled for the next block as soon as its last
-// consumer of this block is done (w after product 1, u and the per-position
-// records after the value phase, k after product 2).
+// Shared memory of the state chain on 128-position blocks (the chain warps of
+// ho128_tc_kernel below). Operand buffers are single: each group is refilled
+// for the next block as soon as its last consumer of this block is done (w
+// after product 1, u and the per-position records after the value phase, k
+// after product 2).
 constexpr int S8_WHI = 0;                   // w hi: 2 K-halves x 128 rows x 128 B
 constexpr int S8_WLO = 32768;               // w lo
 constexpr int S8_K = 65536;                 // k: 2 K-halves x 128 rows x 128 B
 constexpr int S8_U = 98304;                 // u fp32 128 x 32
 constexpr int S8_G = 114688;                // (Gam hi, Gam lo, 1/|k|, 0) x 128
-constexpr int S8_HT = 116736;               // h operand hi | lo: 128 rows x 64 B each
-constexpr int S8_VP = S8_HT + 16384;        // v' operand hi | lo: 128 rows x 64 B each
-constexpr int S8_BAR = S8_VP + 16384;
-constexpr int S8_SMEM = S8_BAR + 64 + 1024;
-
-__global__ void __launch_bounds__(256, 1) h128_tc_kernel(
-    const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
-    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
-    const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
-  pdl_wait();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, cgrp = warp >> 2;
-  const int row = quarter * 32 + lane;          // state row kf / position p
-  constexpr int NC = 16;                        // value columns per thread
-  const int cb = cgrp * NC;
-  const int nsl = a.V / kHBV;
-  const ChainPos cp = chain_pos(a.seq_order, nsl, a.HV);
-  const int seq = cp.seq, hv = cp.hv, kh = hv / (a.HV / H);
-  const int v0 = cp.slice * kHBV;
-  const int V = a.V, M = a.M;
-  const int4 si = a.seq_info[seq];
-  const int nb = (int)cdiv((int64_t)si.y * M, 128);
-  const int tok_blocks = M / 2;                 // 128-blocks per token chunk (M even)
-  uint8_t* ht = sm + S8_HT;
-  uint8_t* vp = sm + S8_VP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S8_BAR);  // [0] w [1] u+gk [2] k [3] p1 [4] p2
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
-  const int64_t hoff = ((int64_t)seq * a.HV + hv) * kK * V;
-  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  const int64_t Rseq = (int64_t)si.x * M;
-  const int64_t gk_base = (int64_t)hv * a.Te + Rseq;
-
-  if (warp == 0) {
-    tmem_alloc(s_tmem, 64);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
-    fence_mbar_init();
-  }
-  // this thread's two 16-byte chunks of an operand row
-  const uint32_t off_r0 = sw64_chunk(row, 2 * cgrp), off_r1 = sw64_chunk(row, 2 * cgrp + 1);
-  float h[NC];
-  {
-    const float* src = a.h0 ? a.h0 + hoff + (int64_t)row * V + v0 + cb : nullptr;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) h[c] = src ? src[c] : 0.f;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-  auto load_w = [&](int64_t R) {
-    mbar_expect_tx(&bars[0], 65536);
-    tma_load_3d(sm + S8_WHI, &map_whi, 0, hv, (int)R, &bars[0]);
-    tma_load_3d(sm + S8_WHI + 16384, &map_whi, 64, hv, (int)R, &bars[0]);
-    tma_load_3d(sm + S8_WLO, &map_wlo, 0, hv, (int)R, &bars[0]);
-    tma_load_3d(sm + S8_WLO + 16384, &map_wlo, 64, hv, (int)R, &bars[0]);
-  };
-  auto load_ug = [&](int64_t R, int64_t G) {
-    mbar_expect_tx(&bars[1], 16384 + 2048);
-    tma_load_3d(sm + S8_U, &map_u, v0, hv, (int)R, &bars[1]);
-    tma_load_2d(sm + S8_G, &map_gk, 0, (int)G, &bars[1]);
-  };
-  auto load_k = [&](int64_t R) {
-    mbar_expect_tx(&bars[2], 32768);
-    tma_load_3d(sm + S8_K, &map_k, 0, kh, (int)R, &bars[2]);
-    tma_load_3d(sm + S8_K + 16384, &map_k, 64, kh, (int)R, &bars[2]);
-  };
-  if (tid == 0 && nb > 0) {
-    load_w(Rseq);
-    load_ug(Rseq, gk_base);
-    load_k(Rseq);
-  }
-  const uint32_t id1 = idesc_bf16(128, kHBV, false, true);
-  const uint32_t id2 = idesc_bf16(128, kHBV, true, true);
-  for (int j = 0; j <= nb; ++j) {
-    {  // publish the state at the start of block j
-      __align__(16) bf16 hi[NC];
-      __align__(16) bf16 lo[NC];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) split_bf16(h[c], hi[c], lo[c]);
-      const uint4* h4 = reinterpret_cast<const uint4*>(hi);
-      const uint4* l4 = reinterpret_cast<const uint4*>(lo);
-      *reinterpret_cast<uint4*>(ht + off_r0) = h4[0];
-      *reinterpret_cast<uint4*>(ht + off_r1) = h4[1];
-      *reinterpret_cast<uint4*>(ht + 8192 + off_r0) = l4[0];
-      *reinterpret_cast<uint4*>(ht + 8192 + off_r1) = l4[1];
-      if (j < nb && j % tok_blocks == 0) {
-        const int64_t base =
-            ((((int64_t)si.w + j / tok_blocks) * a.HV + hv) * kK + row) * V + v0 + cb;
-        uint4* dh = reinterpret_cast<uint4*>(a.h_hi + base);
-        uint4* dl = reinterpret_cast<uint4*>(a.h_lo + base);
-        dh[0] = h4[0];
-        dh[1] = h4[1];
-        dl[0] = l4[0];
-        dl[1] = l4[1];
-      }
-    }
-    if (j == nb) break;
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const int n = min(128, si.y * M - j * 128);
-    const int64_t R = Rseq + (int64_t)j * 128;
-    const uint32_t ph = j & 1;
-    bool ok = mbar_wait(&bars[0], ph, a.status, kDevTimeout);
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0) {  // product 1: D1 = w h (rows = 128 positions)
-      const uint32_t whi = smem_u32(sm + S8_WHI), wlo = smem_u32(sm + S8_WLO), hb = smem_u32(ht);
-      // w_hi h_hi + w_hi h_lo + w_lo h_hi
-      mma_run<8, false, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
-      mma_run<8, true, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(whi, 16, 1024), sdesc_sw64(hb + 8192, 8192, 512), id1);
-      mma_run<8, true, 16384, 32, 4096, 1024>(tmem, sdesc_sw128(wlo, 16, 1024), sdesc_sw64(hb, 8192, 512), id1);
-      mma_commit(&bars[3]);
-    }
-    ok = mbar_wait(&bars[1], ph, a.status, kDevTimeout);
-    const float4* gk = reinterpret_cast<const float4*>(sm + S8_G);
-    const float4 glast = gk[n - 1];
-    {  // value phase: position p = row, columns cb .. cb + 15
-      const int p = row;
-      ok = mbar_wait(&bars[3], ph, a.status, kDevTimeout) && ok;
-      tc_fence_after();
-      if (tid == 0 && j + 1 < nb) load_w(R + 128);  // w buffers are free once product 1 is done
-      uint32_t r[NC];
-      GDP_TMEM_LD16(tmem + lane_base + cb, r);
-      tmem_wait_ld();
-      const uint8_t* urow = sm + S8_U + p * 128;  // u row p, 128B-swizzled 16-byte chunks
-      float us[NC];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v4 = *reinterpret_cast<const float4*>(urow + ((((cb >> 2) + j) ^ (p & 7)) << 4));
-        us[4 * j] = v4.x; us[4 * j + 1] = v4.y; us[4 * j + 2] = v4.z; us[4 * j + 3] = v4.w;
-      }
-      const float4 gp = gk[p];
-      const float sc = (p < n) ? expf((glast.x - gp.x) + (glast.y - gp.y)) * gp.z : 0.f;
-      __align__(16) bf16 vh[NC];
-      __align__(16) bf16 vl[NC];
-      __align__(16) bf16 pvh[NC];
-      __align__(16) bf16 pvl[NC];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const float vn = us[c] - __uint_as_float(r[c]);
-        split_bf16(vn, vh[c], vl[c]);
-        split_bf16(p < n ? vn * sc : 0.f, pvh[c], pvl[c]);
-      }
-      if (p < n) {
-        const int64_t rowg = (R + p) * a.HV * V + (int64_t)hv * V + v0 + cb;
-        uint4* dh = reinterpret_cast<uint4*>(a.vn_hi + rowg);
-        uint4* dl = reinterpret_cast<uint4*>(a.vn_lo + rowg);
-        dh[0] = reinterpret_cast<const uint4*>(vh)[0];
-        dh[1] = reinterpret_cast<const uint4*>(vh)[1];
-        dl[0] = reinterpret_cast<const uint4*>(vl)[0];
-        dl[1] = reinterpret_cast<const uint4*>(vl)[1];
-      }
-      *reinterpret_cast<uint4*>(vp + off_r0) = reinterpret_cast<const uint4*>(pvh)[0];
-      *reinterpret_cast<uint4*>(vp + off_r1) = reinterpret_cast<const uint4*>(pvh)[1];
-      *reinterpret_cast<uint4*>(vp + 8192 + off_r0) = reinterpret_cast<const uint4*>(pvl)[0];
-      *reinterpret_cast<uint4*>(vp + 8192 + off_r1) = reinterpret_cast<const uint4*>(pvl)[1];
-      fence_async_smem();
-      tc_fence_before();
-    }
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    tc_fence_after();
-    if (tid == 0) {
-      if (j + 1 < nb) load_ug(R + 128, gk_base + (int64_t)(j + 1) * 128);  // u, records consumed
-      ok = mbar_wait(&bars[2], ph, a.status, kDevTimeout);
-      if (ok) {  // product 2: D2 = k^T v' (rows = state rows kf), K = 128 positions
-        const uint32_t kb = smem_u32(sm + S8_K), vb = smem_u32(vp);
-        const uint64_t kd = sdesc_sw128(kb, 16384, 1024);
-        mma_run<8, false, 8192, 2048, 4096, 1024>(tmem + 32, kd, sdesc_sw64(vb, 8192, 512), id2);
-        mma_run<8, true, 8192, 2048, 4096, 1024>(tmem + 32, kd, sdesc_sw64(vb + 8192, 8192, 512), id2);
-        mma_commit(&bars[4]);
-      }
-    }
-    if (!__syncthreads_and(ok)) break;
-    ok = mbar_wait(&bars[4], ph, a.status, kDevTimeout);
-    tc_fence_after();
-    if (tid == 0 && ok && j + 1 < nb) load_k(R + 128);  // k consumed by product 2
-    {
-      uint32_t r[NC];
-      GDP_TMEM_LD16(tmem + lane_base + 32 + cb, r);
-      tmem_wait_ld();
-      const float dl = expf(glast.x + glast.y);
-#pragma unroll
-      for (int c = 0; c < NC; ++c) h[c] = dl * h[c] + __uint_as_float(r[c]);
-    }
-    tc_fence_before();
-    if (!__syncthreads_and(ok)) break;
-  }
-  if (a.hT) {
-    float* dst = a.hT + hoff + (int64_t)row * V + v0 + cb;
-#pragma unroll
-    for (int c = 0; c < NC; c += 4)
-      *reinterpret_cast<float4*>(dst + c) = make_float4(h[c], h[c + 1], h[c + 2], h[c + 3]);
-  }
-  tmem_release(tmem, 64);
-}
 
 // ============================================================================ chunk_h + chunk_o, M = 2
 // For M = 2 a 128-position block is exactly one 64-token output chunk, so the
@@ -1407,7 +1193,9 @@ __global__ void __launch_bounds__(256, 1) h128_tc_kernel(
 // keys (product 2's k tile) and v_new. Neither states nor v_new go to HBM.
 //
 // Warp roles (512 threads):
-//  * warps 0-7, the chain: the state recurrence of h128_tc_kernel. Thread
+//  * warps 0-7, the chain: the state recurrence of h_tc_kernel, one
+//    128-position block per step (WY factors from wy128_tc_kernel, every
+//    accumulator row in use). Thread
 //    (warp w, lane l) owns state row / position 32 (w % 4) + l and value
 //    columns [16 (w / 4), +16) of the CTA's 32. Besides the v' operand it
 //    writes v_new / |k_p| as the output's operand tile.
@@ -2353,8 +2141,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
   record_stage(2, p.stream);
   // state recurrence: 128-position steps for even M, 64-position steps otherwise
   {
-    const bool blk128 = (p.M % 2) == 0;
-    const uint32_t rows = blk128 ? 128 : 64;
+    const uint32_t rows = p.M == 2 ? 128 : 64;  // M = 2: 128-position steps
     CUtensorMap mwh, mwl, mk, mu, mg;
     const int64_t Tr = Te > 0 ? Te : 1;
     if (!map3(&mwh, w_hi, BF, 2, kK, p.HV, Tr, 64, rows, true) ||
@@ -2383,15 +2170,10 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       record_stage(4, p.stream);
       return cudaSuccess;
     }
-    if (blk128) {
-      e = cudaFuncSetAttribute(h128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S8_SMEM);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(h128_tc_kernel, grid, dim3(256), S8_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
-    } else {
-      e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(h_tc_kernel, grid, dim3(256), H_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
-    }
+    // odd M: 64-position steps (the WY factors are the 64-position chunks')
+    e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(h_tc_kernel, grid, dim3(256), H_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
     if (e != cudaSuccess) return e;
   }
   record_stage(3, p.stream);
