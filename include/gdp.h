@@ -207,7 +207,10 @@ size_t gdp_chunk_fwd_workspace_size(int B, int T, int N_seq, int H, int HV, int 
  * 256-byte aligned; its first 256 bytes hold the device status word that
  * gdp_read_status() reads back. Calls that share a workspace must not overlap
  * on the GPU.
- * Requires HV % H == 0, K <= 256, V <= 1024, M in 1..8.
+ * Requires HV % H == 0, K <= 256, V <= 1024, M in 1..8; GDP_ERR_UNSUPPORTED
+ * when B*T*M*HV, the expanded chunks times chunk_size, or the token chunks
+ * times HV*K reach 2^31 (the kernels' 32-bit row coordinates; such tensors
+ * exceed one GPU's memory).
  * Path: bf16 inputs with K = 128, chunk_size 64, V in {64, 128, 256} and
  * M <= 3 run on the tensor cores (bf16 hi/lo operand splits, fp32
  * accumulation; for M = 2 the output is formed inside the state-scan kernel);

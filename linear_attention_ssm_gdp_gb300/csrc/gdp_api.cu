@@ -69,6 +69,16 @@ gdp_status check_chunk(const void* q, const void* k, const void* v, const float*
   if (cu_seqlens ? (B != 1) : (N_seq != B)) return GDP_ERR_INVALID_ARG;
   if (!(BT == 16 || BT == 32 || BT == 64)) return GDP_ERR_UNSUPPORTED;
   if (K > 256 || V > 1024 || M > 8) return GDP_ERR_UNSUPPORTED;
+  // The kernels address positions, decay-record rows and state rows with 32-bit
+  // tensor-map coordinates and table entries; every one of them stays below
+  // 2^31 for problems whose tensors fit in a GPU's memory, and larger ones are
+  // refused here.
+  {
+    int64_t NE, NT;
+    chunk_bounds(B, T, N_seq, M, BT, &NE, &NT);
+    if ((int64_t)B * T * M * HV > INT32_MAX || NE * BT > INT32_MAX || NT * HV * K > INT32_MAX)
+      return GDP_ERR_UNSUPPORTED;
+  }
   if ((int64_t)B * T > 0 && (!q || !k || !v || !beta || !o)) return GDP_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < need)
     return GDP_ERR_WORKSPACE;

@@ -74,6 +74,8 @@ def _chunk(so, **kw):
     (dict(ws_bytes=1000), 5),        # workspace too small
     (dict(ws=(1 << 20) + 8), 5),     # workspace misaligned
     (dict(dt=7), 2),                 # unknown dtype
+    (dict(B=1, T=1 << 28, N=1, HV=8, H=2), 2),      # positions x heads past 32-bit coordinates
+    (dict(cu=1 << 20, B=1, T=64, N=1 << 27, HV=64, H=2, K=256), 2),  # state rows past 32 bits
 ])
 def test_chunk_fwd_rejects_before_launch(lib, kw, status):
     assert _chunk(lib.load(), **kw) == status
