@@ -257,3 +257,55 @@ def test_recurrent_slots_graph_replay_with_new_slots(gdp):
     torch.cuda.synchronize()
     ro, rpool = _slot_reference(q, k, v, beta, g, pool0, new, K ** -0.5, True)
     assert rel_err(o, ro) <= 2e-3 and rel_err(pd, rpool) <= 2e-3
+
+
+def _draw_decode(seed):
+    import random
+    r = random.Random(seed)
+    H = r.choice([1, 2])
+    return dict(n=r.randint(1, 40), L=r.randint(1, 20), H=H, HV=H * r.choice([1, 2, 4]),
+                K=r.choice([32, 64, 128, 128, 256]),
+                V=r.choice([8, 16, 40, 64, 72, 128, 136, 200, 256]),
+                dtype=r.choice([torch.float32, torch.float16, torch.bfloat16]),
+                l2=r.random() < 0.7, slots=r.random() < 0.4, strong=r.random() < 0.3)
+
+
+@pytest.mark.parametrize("seed", list(range(300, 360)))
+def test_recurrent_shape_sweep(gdp, seed):
+    """Seeded shapes for the decode update, dense or through a slot pool with
+    padding requests: both kernels (K = 128 and the others), ragged value
+    slices, one or two staged step batches, GVA ratios, all input dtypes, the
+    L2 norm on or off, and some calls with decays far below the fp32 range."""
+    c = _draw_decode(seed)
+    n, L, H, HV, K, V, dtype, l2 = (c[x] for x in ("n", "L", "H", "HV", "K", "V", "dtype", "l2"))
+    gen = torch.Generator().manual_seed(seed)
+    sc = 1.0 if l2 else K ** -0.5
+    q = (torch.randn(n, L, H, K, generator=gen) * sc).to(dtype)
+    k = (torch.randn(n, L, H, K, generator=gen) * sc).to(dtype)
+    v = torch.randn(n, L, HV, V, generator=gen).to(dtype)
+    beta = torch.rand(n, L, HV, generator=gen)
+    g = -torch.rand(n, L, HV, generator=gen) * (40.0 if c["strong"] else 1.0)
+    if c["slots"]:
+        n_slots = n + 5
+        pool = torch.randn(n_slots, HV, K, V, generator=gen) * 0.1
+        slots = torch.randperm(n_slots, generator=gen)[:n].to(torch.int32)
+        slots[torch.rand(n, generator=gen) < 0.15] = -1
+        ro, rpool = _slot_reference(q, k, v, beta, g, pool, slots, K ** -0.5, l2)
+        pd = pool.to(DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        o = gdp.gdp_recurrent_update_slots(*to(DEV, q, k, v, beta, g), pd, slots.to(DEV),
+                                           use_qk_l2norm=l2, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert rel_err(o, ro) <= TOL[dtype], (c, rel_err(o, ro))
+        assert rel_err(pd, rpool) <= TOL[dtype], (c, rel_err(pd, rpool))
+        untouched = sorted(set(range(n_slots)) - {int(s) for s in slots if int(s) >= 0})
+        assert torch.equal(pd.cpu()[untouched], pool[untouched])
+    else:
+        state = torch.randn(n, HV, K, V, generator=gen) * 0.1
+        ro, rs = oracle.recurrent(q, k, v, beta, g, state, K ** -0.5, l2norm=l2)
+        sd = state.to(DEV)
+        o = gdp.gdp_recurrent_update(*to(DEV, q, k, v, beta, g), sd, use_qk_l2norm=l2)
+        torch.cuda.synchronize()
+        assert rel_err(o, ro) <= TOL[dtype], (c, rel_err(o, ro))
+        assert rel_err(sd, rs) <= TOL[dtype], (c, rel_err(sd, rs))
