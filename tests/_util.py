@@ -10,6 +10,18 @@ import synth_inputs as si
 # state; tol = 2e-3 for bf16/fp16 inputs and 1e-5 for fp32 inputs.
 TOL = {torch.bfloat16: 2e-3, torch.float16: 2e-3, torch.float32: 1e-5}
 
+# Gates against the host-libm oracle, in ulp. The kernels' gates are bit-exact
+# against the eager composition with CUDA's math library (asserted separately);
+# the oracle calls the host's expf/log1pf. With CUDA's documented maximum errors
+# (expf 2 ulp, log1pf 1 ulp) and the host's (expf 1 ulp, log1pf 2 ulp), the two
+# sides' exp differ by at most 3 ulp and their log1p by at most 3 ulp more:
+#   beta = 1/(1 + e^-b): 3 ulp passed through the sum (condition <= 1) plus the
+#     add's and the division's rounding on each side: <= 5 ulp;
+#   g = -e^A_log softplus(a + dt_bias) = -e^A_log log1p(e^x): 3 ulp (e^A_log) +
+#     3 ulp (e^x, through log1p with condition <= 1) + 3 ulp (log1p) + the
+#     product's rounding on each side: <= 10 ulp.
+GATE_ULP = {"beta": 5, "g": 10}
+
 
 def rel_err(got, want) -> float:
     want = want.detach().cpu().to(torch.float64)

@@ -13,6 +13,7 @@ import torch
 import bench
 import oracle
 import synth_inputs as si
+from _util import GATE_ULP
 
 
 def _ulp(a, b):
@@ -34,4 +35,4 @@ def test_eager_prepare_matches_the_oracle(decode, n, T, M, H, G, P, N):
         assert torch.equal(a.contiguous(), b), name
     for name, a, b in zip(("beta", "g"), got[3:], ref[3:]):
         assert a.dtype == torch.float32 and tuple(a.shape) == tuple(b.shape), name
-        assert int(_ulp(a, b).max()) <= 4, name
+        assert int(_ulp(a, b).max()) <= GATE_ULP[name], name

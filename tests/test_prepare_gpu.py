@@ -4,8 +4,8 @@ composition of the same fp32 operations.
 
 q/k/v and the +0 placements are bit moves: bit-exact against the oracle.
 beta and g are bit-exact against the eager GPU composition (the pages'
-contract, asserted with torch.equal) and within 4 ulp of the oracle, whose host
-libm expf/log1pf are not CUDA's.
+contract, asserted with torch.equal) and within the libm error bound of the
+oracle, whose host expf/log1pf are not CUDA's (GATE_ULP: beta 5, g 10 ulp).
 """
 import pytest
 import torch
@@ -13,6 +13,7 @@ import torch.nn.functional as F
 
 import oracle
 import synth_inputs as si
+from _util import GATE_ULP
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -54,7 +55,7 @@ def _check(gdp, x, ba, A_log, dt_bias, M, H, G, P, N, decode):
     assert torch.equal(out[4], eg), "g differs from the eager composition"
     for nm, a, b in zip(names[3:], out[3:], ref[3:]):
         d = _ulp(a.cpu(), b)
-        assert int(d.max()) <= 4, f"{nm}: {int(d.max())} ulp from the oracle"
+        assert int(d.max()) <= GATE_ULP[nm], f"{nm}: {int(d.max())} ulp from the oracle"
     if decode:
         n, T = x.shape[:2]
         assert torch.count_nonzero(out[0].view(n, T, M, H, N)[:, :, :M - 1]) == 0
@@ -149,3 +150,31 @@ def test_prepare_long_rows(gdp, decode, M, H, G, P, N, n, T):
     x = big.to(DEV)[:, :, 64:]
     assert not x.is_contiguous()
     _check(gdp, x, d["ba"], d["A_log"], d["dt_bias"], M, H, G, P, N, decode)
+
+
+@pytest.mark.parametrize("seed", list(range(500, 540)))
+def test_prepare_shape_sweep(gdp, seed):
+    """Seeded shapes: copies M, heads H over groups G, head sizes P and N (16-byte
+    vector and element paths), all input dtypes, contiguous or strided rows,
+    prefill or decode; row lengths from a few vectors to past the shared-memory
+    ring, row counts below and above the resident CTAs."""
+    import random
+    r = random.Random(seed)
+    decode = r.random() < 0.4
+    dtype = r.choice([torch.bfloat16, torch.bfloat16, torch.float16, torch.float32])
+    M = r.randint(1, 4)
+    G = r.choice([1, 2, 4, 8])
+    H = G * r.choice([1, 2, 4])
+    P = r.choice([3, 5, 8, 16, 24, 64, 128])
+    N = r.choice([4, 8, 16, 32, 64, 128])
+    n = r.randint(1, 64)
+    T = r.randint(1, 16) if decode else r.randint(1, 40)
+    d = si.prepare_inputs(n, T, M, H, G, P, N, seed=seed, dtype=dtype)
+    x, ba = d["x"], d["ba"]
+    if r.random() < 0.5:  # rows inside a wider buffer (a view of a conv output)
+        D = x.shape[-1]
+        pad = r.choice([8, 16, 40])
+        big = torch.zeros(n, T, D + pad, dtype=dtype)
+        big[:, :, pad:] = x
+        x = big.to(DEV)[:, :, pad:]
+    _check(gdp, x, ba, d["A_log"], d["dt_bias"], M, H, G, P, N, decode)
