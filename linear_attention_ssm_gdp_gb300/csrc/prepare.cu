@@ -720,21 +720,27 @@ __global__ void __launch_bounds__(256, 2) conv_prepare_kernel(ConvArgs ca) {
         load_state(ca.st_in, seq);
       }
       float y[VE];
-      const bool near = t - s_start < W - 1;  // some window entries precede the sequence
+      if (t - s_start < W - 1) {  // some window entries precede the sequence: take the state's
 #pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        float z = bv[e];
+        for (int e = 0; e < VE; ++e) {
+          float z = bv[e];
 #pragma unroll
-        for (int i = 0; i < W - 1; ++i) {
-          float xi = win[i][e];
-          if (near) {
+          for (int i = 0; i < W - 1; ++i) {
             const int src = t - (W - 1) + i, si = (W - 1) - (s_start - src);
-            if (src < s_start) xi = sw_at(si, e);
+            z = z + wv[i][e] * (src < s_start ? sw_at(si, e) : win[i][e]);
           }
-          z = z + wv[i][e] * xi;
+          z = z + wv[W - 1][e] * x[e];
+          y[e] = z / (1.0f + expf(-z));
         }
-        z = z + wv[W - 1][e] * x[e];
-        y[e] = z / (1.0f + expf(-z));
+      } else {  // the whole window is inside the sequence
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          float z = bv[e];
+#pragma unroll
+          for (int i = 0; i < W - 1; ++i) z = z + wv[i][e] * win[i][e];
+          z = z + wv[W - 1][e] * x[e];
+          y[e] = z / (1.0f + expf(-z));
+        }
       }
       cv_scatter(a, dst, (int64_t)in * a.T + t, cv_pack<T, VE>(y));
     }
