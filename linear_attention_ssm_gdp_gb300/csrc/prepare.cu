@@ -310,6 +310,16 @@ __global__ void __launch_bounds__(256, 4) prepare_rows_kernel(PrepArgs a) {
 // copy placement as prepare_kernel). Same fp32 gate operations.
 constexpr int kRing = 3;
 
+// Output stores of the ring kernel: streaming (evict-first) for prefill, whose
+// outputs exceed L2; plain for decode, whose outputs stay in L2 for the update.
+template <bool DECODE>
+__device__ __forceinline__ void st_row(uint4* p, uint4 v) {
+  if (DECODE)
+    *p = v;
+  else
+    __stcs(p, v);
+}
+
 template <bool DECODE, int NT>
 __global__ void __launch_bounds__(NT, 3) prepare_ring_kernel(PrepArgs a, int xrow_v) {
   pdl_wait();
@@ -348,12 +358,12 @@ __global__ void __launch_bounds__(NT, 3) prepare_ring_kernel(PrepArgs a, int xro
     uint4* qdst = reinterpret_cast<uint4*>(a.q + r * g.qrow_b);
     for (int c = tid; c < ntot; c += NT) {
       if (c < g.nv) {  // value: contiguous copy of the row's value block
-        __stcs(vdst + c, s[c]);
+        st_row<DECODE>(vdst + c, s[c]);
       } else if (c < g.nv + g.nk) {  // key: output head (j, h) reads group (j, h / hpg)
         const int ck = c - g.nv;
         const int jh = a.fd_hv.div(ck), w = ck - jh * g.head_v;
         const int j = a.fd_H.div(jh), h = jh - j * a.H;
-        __stcs(kdst + ck, s[kb_v + (j * a.G + a.fd_hpg.div(h)) * g.head_v + w]);
+        st_row<DECODE>(kdst + ck, s[kb_v + (j * a.G + a.fd_hpg.div(h)) * g.head_v + w]);
       } else {  // query: prefill one row per token; decode the last copy, +0 elsewhere
         const int cq = c - g.nv - g.nk;
         const int jh = a.fd_hv.div(cq), w = cq - jh * g.head_v;
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(NT, 3) prepare_ring_kernel(PrepArgs a, int xro
         const int h = DECODE ? jh - j * a.H : jh;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (j == a.M - 1) val = s[qb_v + a.fd_hpg.div(h) * g.head_v + w];
-        __stcs(qdst + cq, val);
+        st_row<DECODE>(qdst + cq, val);
       }
     }
     if (tid < g.MH) a.beta[r * g.MH + tid] = 1.0f / (1.0f + expf(-raw_f32(b, a.dt)));
