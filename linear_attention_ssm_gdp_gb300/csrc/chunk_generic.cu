@@ -663,7 +663,8 @@ cudaError_t launch_tables(const ChunkProblem& p, const WsLayout& L, uint8_t* ws)
       reinterpret_cast<int2*>(ws + L.exp_tab), reinterpret_cast<int2*>(ws + L.tok_tab),
       L.blk_tab == SIZE_MAX ? nullptr : reinterpret_cast<int4*>(ws + L.blk_tab),
       block128_bound(p.B, p.T, p.N_seq, p.M), reinterpret_cast<int*>(ws + L.status),
-      L.seq_order == SIZE_MAX ? nullptr : reinterpret_cast<int*>(ws + L.seq_order));
+      // the chain order only matters for ragged sequences
+      (L.seq_order == SIZE_MAX || !p.cu_seqlens) ? nullptr : reinterpret_cast<int*>(ws + L.seq_order));
 }
 
 cudaError_t launch_chunk_generic(const ChunkProblem& p, const WsLayout& L, uint8_t* ws) {

@@ -246,7 +246,6 @@ struct HArgs {
   bf16* h_hi;   // [n_tok_chunks][HV][K][V]
   bf16* h_lo;
   int* status;
-  const int* seq_order;  // null: dense launch order (see chain_pos)
 };
 
 // The (sequence, value head, value slice) of a state-scan CTA. The value slices
@@ -291,7 +290,7 @@ constexpr int kHCols = kHBV / 2;
 __global__ void __launch_bounds__(256, 2) h_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
-    const __grid_constant__ CUtensorMap map_gk, HArgs a, int H) {
+    const __grid_constant__ CUtensorMap map_gk, HArgs a, int H, const int* seq_order) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -301,7 +300,7 @@ __global__ void __launch_bounds__(256, 2) h_tc_kernel(
   const int row = quarter * 32 + lane;          // state row kf / position p
   const int cb = chalf * kHCols;                // first of this thread's 16 columns
   const int nsl = a.V / kHBV;
-  const ChainPos cp = chain_pos(a.seq_order, nsl, a.HV);
+  const ChainPos cp = chain_pos(seq_order, nsl, a.HV);
   const int seq = cp.seq, hv = cp.hv, kh = hv / (a.HV / H);
   const int v0 = cp.slice * kHBV;
   const int V = a.V, M = a.M;
@@ -1244,12 +1243,12 @@ __device__ __forceinline__ bool group_and(uint32_t id, uint32_t count, bool pred
   return r != 0;
 }
 
-template <bool G>
+template <bool G, bool ORD>
 __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
     const __grid_constant__ CUtensorMap map_whi, const __grid_constant__ CUtensorMap map_wlo,
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_u,
     const __grid_constant__ CUtensorMap map_gk, const __grid_constant__ CUtensorMap map_q,
-    HOArgs f) {
+    HOArgs f, const int* seq_order) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1261,10 +1260,20 @@ __global__ void __launch_bounds__(512, 1) ho128_tc_kernel(
   const int cb = cgrp * NC;
   const int HVn = f.h.HV, V = f.h.V;
   const int nsl = V / kHBV;
-  const ChainPos cp = chain_pos(f.h.seq_order, nsl, HVn);
-  const int seq = cp.seq, hv = cp.hv;
+  // ORD: ragged sequences, launched longest first; dense batches: blockIdx.x =
+  // sequence * (V / 32) + value slice (slices of one head side by side)
+  int seq, hv, v0;
+  if (ORD) {
+    const ChainPos cp = chain_pos(seq_order, nsl, HVn);
+    seq = cp.seq;
+    hv = cp.hv;
+    v0 = cp.slice * kHBV;
+  } else {
+    seq = blockIdx.x / nsl;
+    hv = blockIdx.y;
+    v0 = (blockIdx.x - seq * nsl) * kHBV;
+  }
   const int kh = hv / (HVn / f.H);
-  const int v0 = cp.slice * kHBV;
   const int4 si = f.h.seq_info[seq];
   const int nb = (int)cdiv((int64_t)si.y * 2, 128);
   int* status = f.h.status;
@@ -2083,7 +2092,6 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.tok_tab = take(sizeof(int2) * (size_t)NT);
   // 128-position blocks: WY-128 for every M (odd M in its two-chunk form)
   L.blk_tab = take(sizeof(int4) * (size_t)block128_bound(B, T, N_seq, M));
-  L.seq_order = take(sizeof(int32_t) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.w_hi = take(2 * Te * HV * K);
   L.w_lo = take(2 * Te * HV * K);
   L.u = take(4 * Te * HV * V);
@@ -2095,6 +2103,7 @@ WsLayout tc_layout(int B, int T, int N_seq, int H, int HV, int K, int V, int M, 
   L.vn_lo = take(keep * 2 * Te * HV * V);
   L.h_hi = take(keep * 2 * (size_t)NT * HV * V * K);
   L.h_lo = take(keep * 2 * (size_t)NT * HV * V * K);
+  L.seq_order = take(sizeof(int32_t) * (size_t)(N_seq > 0 ? N_seq : 1));
   L.total = off;
   L.path = 1;
   return L;
@@ -2152,7 +2161,7 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       return cudaErrorInvalidValue;
     // ragged sequences: chains in the tables kernel's longest-first order
     const int* order = p.cu_seqlens ? reinterpret_cast<const int*>(ws + L.seq_order) : nullptr;
-    HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status, order};
+    HArgs a{p.HV, p.V, p.M, Te, seq_info, u, gk, p.h0, p.hT, vn_hi, vn_lo, h_hi, h_lo, status};
     const dim3 grid((unsigned)((int64_t)p.N_seq * (p.V / kHBV)), p.HV);
     if (p.M == 2) {  // state recurrence and output fused
       CUtensorMap mq;
@@ -2160,10 +2169,12 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
       if (!map3(&mq, p.q ? p.q : w_hi, BF, 2, kK, p.H, Tt > 0 ? Tt : 1, 64, 64, true))
         return cudaErrorInvalidValue;
       HOArgs fa{a, p.H, p.l2norm, p.scale, p.o};
-      auto kern = p.g ? ho128_tc_kernel<true> : ho128_tc_kernel<false>;
+      auto kern = p.g ? (order ? ho128_tc_kernel<true, true> : ho128_tc_kernel<true, false>)
+                      : (order ? ho128_tc_kernel<false, true> : ho128_tc_kernel<false, false>);
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
       if (e != cudaSuccess) return e;
-      if ((e = launch_pdl(kern, grid, dim3(512), F_SMEM, p.stream, mwh, mwl, mk, mu, mg, mq, fa)) !=
+      if ((e = launch_pdl(kern, grid, dim3(512), F_SMEM, p.stream, mwh, mwl, mk, mu, mg, mq, fa,
+                          order)) !=
           cudaSuccess)
         return e;
       record_stage(3, p.stream);
@@ -2173,7 +2184,8 @@ cudaError_t launch_chunk_tc(const ChunkProblem& p, const WsLayout& L, uint8_t* w
     // odd M: 64-position steps (the WY factors are the 64-position chunks')
     e = cudaFuncSetAttribute(h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, H_SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(h_tc_kernel, grid, dim3(256), H_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H);
+    e = launch_pdl(h_tc_kernel, grid, dim3(256), H_SMEM, p.stream, mwh, mwl, mk, mu, mg, a, p.H,
+                   order);
     if (e != cudaSuccess) return e;
   }
   record_stage(3, p.stream);
