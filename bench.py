@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel at the bench workload, from one `ncu --set full` capture of
 # `bench.py --only prefill --steps 2 --warmup 3`. A kernel's entry is removed
 # whenever the kernel changes after the capture.
-TRAFFIC = {"wy": 351.8e6, "scan_out": 429.1e6, "prepare": 279.0e6}
+TRAFFIC = {"wy": 351.9e6, "scan_out": 429.0e6, "prepare": 279.5e6}
 
 
 def peaks():
