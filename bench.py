@@ -371,14 +371,9 @@ def run_ours(args, rank, world, dev):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations and gate inputs)",
-        "config": {"workload": "prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64 "
-                               "(prepare + chunk_fwd, G=16, in-kernel qk L2 norm)",
-                   "B": w["B"], "T": w["T"], "H": w["H"], "HV": w["HV"], "G": w["G"],
-                   "K": w["K"], "V": w["V"], "M": w["M"], "chunk_size": w["BT"],
-                   "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read)",
-                   "chunk_path": ("tensor-core" if pf.path == 1 else "generic")
-                   + (", scan and output fused" if pf.fused else "")},
+        "config": workload_config(world),
+        "chunk_path": ("tensor-core" if pf.path == 1 else "generic")
+        + (", scan and output fused" if pf.fused else ""),
         "roofline": roof,
         "chunk": {"ms": chunk_ms, "TFLOPs": chunk_tf, "tc_frac": chunk_tf / tc,
                   "GBps_fused_floor": chunk_gbs, "hbm_frac": chunk_gbs / hbm},
@@ -880,6 +875,17 @@ def cpu_baseline(d, min_seconds=10.0, max_seconds=30.0):
                       f"tokens x {w['M']} copies): oracle prepare + fp64 walk, {dt:.1f} s"}
 
 
+def workload_config(world: int) -> dict:
+    """The bench line's `config`, the same for both arms."""
+    w = WORKLOAD
+    return {"workload": "prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64 "
+                        "(prepare + chunk_fwd, G=16, in-kernel qk L2 norm)",
+            "B": w["B"], "T": w["T"], "H": w["H"], "HV": w["HV"], "G": w["G"],
+            "K": w["K"], "V": w["V"], "M": w["M"], "chunk_size": w["BT"],
+            "parallelism": f"replicas x{world} (no collective)",
+            "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read)"}
+
+
 def run_reference(args, rank, world, budget_seconds=150.0):
     """Reference arm: the CPU oracle, rank 0 only. Each step is batch row 0, all heads,
     a token prefix sized so that warm-up + timed steps take about budget_seconds."""
@@ -909,8 +915,7 @@ def run_reference(args, rank, world, budget_seconds=150.0):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "prefill bf16 B2 T4096 H16 HV16 K128 V128 M2 BT64 "
-                                   "(prepare + chunk_fwd, G=16, in-kernel qk L2 norm)"},
+            "config": workload_config(world),
             "impl": "reference",
             "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": value},
             "e2e": {"value": value, "unit": "expanded tokens/s (B*T*M)",
