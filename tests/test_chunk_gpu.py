@@ -273,6 +273,16 @@ def test_persistent_output_loop_many_items_per_cta(gdp, M, V):
 
 
 @pytest.mark.parametrize("M", [2, 3])
+def test_long_single_sequence(gdp, M):
+    """One 32768-token sequence (65536 or 98304 expanded positions): a state chain
+    of 512 (M = 2, 128-position blocks) or 1536 (M = 3, 64-position steps) steps
+    and token / position coordinates far from zero, element by element."""
+    q, k, v, beta, g = chunk_case(1, 32768, 1, 1, 128, 128, M, seed=31)
+    o, fs = _run(gdp, q, k, v, beta, g, M, 64, True)
+    _check_all(o, fs, q, k, v, beta, g, M)
+
+
+@pytest.mark.parametrize("M", [2, 3])
 def test_tensor_core_ungated(gdp, M):
     """g = None on the bf16 tensor-core path (no decay anywhere)."""
     q, k, v, beta, _ = chunk_case(1, 900, 2, 4, 128, 128, M, seed=13)
