@@ -717,6 +717,7 @@ __global__ void __launch_bounds__(256, 2) conv_prepare_kernel(ConvArgs ca) {
     }
   }
   load_state(ca.st_in, DECODE ? (int64_t)sl : (int64_t)seq);
+#pragma unroll(DECODE ? 1 : (W > 1 ? W - 1 : 1))
   for (int rr = 0; rr < nrows; ++rr) {
     asm volatile("cp.async.wait_group %0;" ::"n"(kConvD - 1) : "memory");
     float x[VE];
