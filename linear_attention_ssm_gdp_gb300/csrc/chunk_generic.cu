@@ -59,7 +59,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 // ------------------------------------------------------------------------------------
 // chunk tables
 // ------------------------------------------------------------------------------------
-// One CTA of kTabThreads threads. The sequences are taken kTabThreads at a time:
+// One CTA of kTabThreads threads. A dense batch (no offsets) has every entry in
+// closed form and fills the tables directly. With offsets, the sequences are
+// taken kTabThreads at a time:
 // each thread loads its sequence's offsets, checks them and counts its chunks,
 // and a block-wide scan turns the counts into the sequence's first chunk
 // indices (no thread walks the list alone). Records and chunk counts of the
@@ -114,12 +116,32 @@ __global__ void __launch_bounds__(kTabThreads) tables_kernel(
     int4* seq_info, int2* exp_tab, int2* tok_tab, int4* blk_tab, int64_t NB_max, int* status,
     int* seq_order) {
   pdl_wait();
+  const int sh = __ffs(BT) - 1;  // BT = 2^sh
+  if (!cu) {  // dense batch: B sequences of T tokens, every table entry in closed form
+    const int tid = threadIdx.x;
+    const int ne = (int)((((int64_t)T * M) + BT - 1) >> sh), nt = (T + BT - 1) >> sh;
+    const int nb = (int)((((int64_t)T * M) + 127) >> 7);
+    if (tid == 0) *status = kDevOk;
+    for (int i = tid; i < B; i += kTabThreads) seq_info[i] = make_int4(i * T, T, i * ne, i * nt);
+    for (int64_t c = tid; c < NE_max; c += kTabThreads)
+      exp_tab[c] = c < (int64_t)B * ne ? make_int2((int)(c / ne), (int)(c % ne)) : make_int2(-1, 0);
+    for (int64_t c = tid; c < NT_max; c += kTabThreads)
+      tok_tab[c] = c < (int64_t)B * nt ? make_int2((int)(c / nt), (int)(c % nt)) : make_int2(-1, 0);
+    if (blk_tab)
+      for (int64_t c = tid; c < NB_max; c += kTabThreads) {
+        const int i = nb > 0 ? (int)(c / nb) : 0;
+        blk_tab[c] = c < (int64_t)B * nb ? make_int4(i, (int)(2 * (c - (int64_t)i * nb)), i * T, T)
+                                         : make_int4(-1, 0, 0, 0);
+      }
+    if (seq_order)
+      for (int i = tid; i < B; i += kTabThreads) seq_order[i] = i;
+    return;
+  }
   __shared__ int4 s_info[kTabSmem];     // (first token, length, first exp chunk, first token chunk)
   __shared__ int4 s_cnt[kTabSmem];      // (exp chunks, token chunks, 128-position blocks, first block)
   __shared__ int64_t s_scan[3 * (kTabThreads / 32)];
   __shared__ int s_bad;
   const int tid = threadIdx.x;
-  const int sh = __ffs(BT) - 1;  // BT = 2^sh
   if (tid == 0) s_bad = 0;
   __syncthreads();
   int64_t carry[3] = {0, 0, 0};  // expanded chunks, token chunks, 128-position blocks so far
@@ -128,16 +150,11 @@ __global__ void __launch_bounds__(kTabThreads) tables_kernel(
     int t0 = 0, len = 0;
     bool bad = false;
     if (i < N_seq) {
-      if (cu) {
-        t0 = cu[i];
-        const int t1 = cu[i + 1];
-        // cu[0] = 0, non-decreasing, within B*T: each sequence checks its own pair
-        bad = (i == 0 && t0 != 0) || t1 < t0 || (int64_t)t1 > (int64_t)B * T;
-        len = t1 - t0;
-      } else {
-        t0 = i * T;
-        len = T;
-      }
+      t0 = cu[i];
+      const int t1 = cu[i + 1];
+      // cu[0] = 0, non-decreasing, within B*T: each sequence checks its own pair
+      bad = (i == 0 && t0 != 0) || t1 < t0 || (int64_t)t1 > (int64_t)B * T;
+      len = t1 - t0;
     }
     if (bad) s_bad = 1;
     int64_t cnt[3] = {0, 0, 0}, tot[3];
