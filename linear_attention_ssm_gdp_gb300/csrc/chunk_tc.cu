@@ -796,10 +796,13 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   // [2][7][128] by item parity: beta, Gam hi, Gam lo, 1/|k|, column scale,
   // Gam hi and lo in base 2
   float* sarr = reinterpret_cast<float*>(sm + W8_S);
-  // [0] k, [1] mma, [2] v round, [3] solve MMAs, [4] v
+  // [0] k, [1] mma, [2] v round, [3] solve MMAs, [4] v, [5] the next item's Gram
   uint64_t* bars = reinterpret_cast<uint64_t*>(sarr + 2 * 7 * 128);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 5);
-  constexpr uint32_t kCols = (128 + V) <= 256 ? 256 : 512;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 6);
+  // TMEM: Gram, solve scratch, W [0, 128), U [128, 128 + V); with V <= 128 the
+  // next item's Gram product is issued early, into [TGE, TGE + 128)
+  constexpr uint32_t kCols = 512;
+  constexpr uint32_t TGE = 384;
   auto issue_k = [&](const Item& x) {
     mbar_expect_tx(&bars[0], 32768);
     tma_load_3d(kbuf, &map_k, 0, x.kh, (int)x.R0, &bars[0]);
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   }
   Item x = item(it, tab);
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     issue_k(x);
     issue_v(x);
@@ -839,6 +842,8 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   // k / v loads issued and consumed so far: load i completes phase i of bars[0] / bars[4]
   int k_iss = 1, k_got = 0, v_iss = 1, v_got = 0;
   int r_iss = 0, r_got = 0;  // V = 256: loads of the second value round (bars[2])
+  bool gram_early = false;   // this item's Gram product was issued during the previous item
+  uint32_t ge_phase = 0;     // bars[5] phase
   bool ok = true;
   for (int c = 0;; ++c) {
     const int par = c & 1;
@@ -867,13 +872,16 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (!__syncthreads_and(ok)) break;
     // (the test hook leaves CTA 0's first Gram product, and so its commit, out:
     // every thread's bounded wait below then runs out and the CTA leaves cleanly)
-    if (tid == 128 && !(a.fault && blockIdx.x == 0 && c == 0)) {  // Gram k k^T, 128 x 128, issued beside the row norms of tid < 128
+    // Gram k k^T, 128 x 128: issued beside the row norms of tid < 128, unless the
+    // previous item already issued it into [TGE, TGE + 128)
+    if (!gram_early && tid == 128 && !(a.fault && blockIdx.x == 0 && c == 0)) {
       const uint32_t kb = smem_u32(kbuf);
       const uint32_t id = idesc_bf16(128, 128, false, false);
       const uint64_t d0 = sdesc_sw128(kb, 16, 1024);
       mma_run<8, false, 16384, 32, 16384, 32>(tmem, d0, d0, id);
       mma_commit(&bars[1]);
     }
+    const uint32_t tg = gram_early ? TGE : 0u;  // this item's Gram columns
     if (tid < 128) {
       const float ss = row_sumsq(kbuf + tid * 128, tid) + row_sumsq(kbuf + 16384 + tid * 128, tid);
       const float r = a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
@@ -898,8 +906,13 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       else
         tma_store_wait_read();
     }
-    ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
-    mma_phase ^= 1;
+    if (gram_early) {
+      ok = mbar_wait(&bars[5], ge_phase, a.status, kDevTimeout);
+      ge_phase ^= 1;
+    } else {
+      ok = mbar_wait(&bars[1], mma_phase, a.status, kDevTimeout);
+      mma_phase ^= 1;
+    }
     tc_fence_after();
     if (!__syncthreads_and(ok)) break;
     {  // L[p][i] = beta_p e^(Gam_p - Gam_i) k_p.k_i / (|k_p||k_i|) for i < p
@@ -912,7 +925,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
         for (int j = 0; j < 32; ++j) LA[p * 129 + c0 + j] = 0.f;
       } else {
         uint32_t r[32];
-        GDP_TMEM_LD32(tmem + lane_base + c0, r);
+        GDP_TMEM_LD32(tmem + lane_base + tg + c0, r);
         tmem_wait_ld();
         const f2 ph2 = pk2(s2h[p], s2h[p]), pl2 = pk2(s2l[p], s2l[p]), bp2 = pk2(bp, bp);
 #pragma unroll
@@ -1104,6 +1117,19 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     // V = 256: u boxes 4-7 go to LA, which the w stores must have read
     if (!kPipe && tid == 0) tma_store_wait_read();
     if (!__syncthreads_and(ok)) break;
+    // V <= 128: the next item's k was requested after the W product; its Gram
+    // product goes to the spare columns now, behind this item's u epilogue
+    const bool early_next = kPipe && has_next;
+    if (early_next && tid == 128) {
+      if (mbar_wait(&bars[0], k_got & 1, a.status, kDevTimeout)) {
+        tc_fence_after();
+        const uint32_t kb = smem_u32(kbuf);
+        const uint32_t id = idesc_bf16(128, 128, false, false);
+        const uint64_t d0 = sdesc_sw128(kb, 16, 1024);
+        mma_run<8, false, 16384, 32, 16384, 32>(tmem + TGE, d0, d0, id);
+        mma_commit(&bars[5]);
+      }
+    }
     if (has_next) {
       if (kPipe) {  // the U product was the v buffer's last reader
         if (tid == 0) issue_v(y);
@@ -1155,6 +1181,7 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
       }
     }
     if (!has_next) break;
+    gram_early = early_next;
     it = nx;
     x = y;
     nx = nnx;
