@@ -799,8 +799,9 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
   // [0] k, [1] mma, [2] v round, [3] solve MMAs, [4] v, [5] the next item's Gram
   uint64_t* bars = reinterpret_cast<uint64_t*>(sarr + 2 * 7 * 128);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 6);
-  // TMEM: Gram, solve scratch, W [0, 128), U [128, 128 + V); with V <= 128 the
-  // next item's Gram product is issued early, into [TGE, TGE + 128)
+  // TMEM: Gram, solve scratch, W [0, 128), U [128, 128 + V); with V <= 128 (and
+  // 128-position items) the next item's Gram product is issued early, into
+  // [TGE, TGE + 128)
   constexpr uint32_t kCols = 512;
   constexpr uint32_t TGE = 384;
   auto issue_k = [&](const Item& x) {
@@ -1118,8 +1119,10 @@ __global__ void __launch_bounds__(512, 1) wy128_tc_kernel(
     if (!kPipe && tid == 0) tma_store_wait_read();
     if (!__syncthreads_and(ok)) break;
     // V <= 128: the next item's k was requested after the W product; its Gram
-    // product goes to the spare columns now, behind this item's u epilogue
-    const bool early_next = kPipe && has_next;
+    // product goes to the spare columns now, behind this item's u epilogue (not
+    // for C64, whose shorter items reach this point before that k has landed:
+    // measured slower)
+    const bool early_next = kPipe && !C64 && has_next;
     if (early_next && tid == 128) {
       if (mbar_wait(&bars[0], k_got & 1, a.status, kDevTimeout)) {
         tc_fence_after();
