@@ -272,6 +272,23 @@ def test_persistent_output_loop_many_items_per_cta(gdp, M, V):
     _check_all(o, fs, q, k, v, beta, g, M, cu=cu)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_packed_equal_lengths_equal_dense_batch(gdp, M):
+    """B equal-length sequences packed through cu_seqlens give the dense batch's
+    outputs bit for bit: the device tables (closed form for the dense batch, the
+    offset scan for the packed one) and the scan's launch order (grid order
+    against longest first) change nothing in any sequence's arithmetic."""
+    B, T, H, HV = 3, 333, 2, 4
+    q, k, v, beta, g = chunk_case(B, T, H, HV, 128, 128, M, seed=41)
+    h0 = torch.randn(B, HV, 128, 128, generator=torch.Generator().manual_seed(5))
+    o_d, fs_d = _run(gdp, q, k, v, beta, g, M, 64, True, h0=h0)
+    flat = lambda x: x.reshape(1, -1, *x.shape[2:])
+    cu = torch.arange(0, B * T + 1, T, dtype=torch.int32)
+    o_p, fs_p = _run(gdp, flat(q), flat(k), flat(v), flat(beta), flat(g), M, 64, True, h0=h0, cu=cu)
+    assert torch.equal(o_p.reshape(o_d.shape), o_d)
+    assert torch.equal(fs_p, fs_d)
+
+
 @pytest.mark.parametrize("M", [2, 3])
 def test_long_single_sequence(gdp, M):
     """One 32768-token sequence (65536 or 98304 expanded positions): a state chain
