@@ -289,6 +289,20 @@ def test_packed_equal_lengths_equal_dense_batch(gdp, M):
     assert torch.equal(fs_p, fs_d)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_gva_equals_repeated_key_heads(gdp, M):
+    """HV = 4 H value heads reading key/query head hv / 4 give, bit for bit, the
+    outputs of the same call with the key and query heads repeated to H = HV
+    (wy_fast page, GVA parameters: the kernels only index the key head)."""
+    B, T, H, HV, V = 2, 300, 2, 8, 256
+    q, k, v, beta, g = chunk_case(B, T, H, HV, 128, V, M, seed=43)
+    o_g, fs_g = _run(gdp, q, k, v, beta, g, M, 64, True)
+    rep = lambda x: x.repeat_interleave(HV // H, dim=2)
+    o_r, fs_r = _run(gdp, rep(q), rep(k), v, beta, g, M, 64, True)
+    assert torch.equal(o_g, o_r)
+    assert torch.equal(fs_g, fs_r)
+
+
 @pytest.mark.parametrize("M", [2, 3])
 def test_long_single_sequence(gdp, M):
     """One 32768-token sequence (65536 or 98304 expanded positions): a state chain
