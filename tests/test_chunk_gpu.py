@@ -139,6 +139,23 @@ def test_continuation_through_initial_state(gdp):
     assert rel_err(fb, fs) <= 2e-3
 
 
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_continuation_at_a_chunk_boundary_is_exact(gdp, M):
+    """Tensor-core path: a sequence split at a token-chunk boundary (128 tokens)
+    and continued through initial_state gives the single call's outputs and
+    final state bit for bit (the state crosses the split in fp32, and every WY
+    block and output chunk of the second call is one of the single call's)."""
+    T, T1 = 320, 128
+    q, k, v, beta, g = chunk_case(1, T, 2, 4, 128, 128, M, seed=47)
+    o, fs = _run(gdp, q, k, v, beta, g, M, 64, True)
+    E1 = T1 * M
+    oa, fa = _run(gdp, q[:, :T1], k[:, :E1], v[:, :E1], beta[:, :E1], g[:, :T1], M, 64, True)
+    ob, fb = _run(gdp, q[:, T1:], k[:, E1:], v[:, E1:], beta[:, E1:], g[:, T1:], M, 64, True,
+                  h0=fa)
+    assert torch.equal(torch.cat([oa, ob], 1), o)
+    assert torch.equal(fb, fs)
+
+
 def test_empty_inputs(gdp):
     q, k, v, beta, g = chunk_case(1, 0, 2, 2, 32, 32, 2, seed=1, dtype=torch.float32)
     o, fs = _run(gdp, q, k, v, beta, g, 2, 64, False)
