@@ -201,6 +201,28 @@ def test_recurrent_slots_identity_equals_dense_call(gdp):
     assert torch.equal(o1, o2) and torch.equal(a, b)
 
 
+def test_recurrent_slots_request_order_does_not_matter(gdp):
+    """The same requests in a permuted order, each keeping its pool entry, give
+    every request's o rows and pool entry bit for bit."""
+    n, L, H, HV, K, V, n_slots = 12, 4, 2, 4, 128, 128, 20
+    gen = torch.Generator().manual_seed(17)
+    q, k = (torch.randn(n, L, H, K, generator=gen).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn(n, L, HV, V, generator=gen).to(torch.bfloat16)
+    beta, g = torch.rand(n, L, HV, generator=gen), -torch.rand(n, L, HV, generator=gen)
+    pool = torch.randn(n_slots, HV, K, V, generator=gen) * 0.1
+    slots = torch.randperm(n_slots, generator=gen)[:n].to(torch.int32)
+    slots[3] = -1
+    perm = torch.randperm(n, generator=gen)
+    a, b = pool.to(DEV), pool.to(DEV)
+    o1 = gdp.gdp_recurrent_update_slots(*to(DEV, q, k, v, beta, g), a, slots.to(DEV),
+                                        use_qk_l2norm=True)
+    o2 = gdp.gdp_recurrent_update_slots(*to(DEV, q[perm], k[perm], v[perm], beta[perm], g[perm]), b,
+                                        slots[perm].to(DEV), use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.cpu(), o1.cpu()[perm])
+    assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("bad", ["repeated", "out_of_range"])
 def test_recurrent_slots_rejects_bad_slots_on_device(gdp, bad):
     n, L, H, HV, K, V, n_slots = 6, 2, 2, 2, 128, 64, 8
